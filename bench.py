@@ -1,0 +1,482 @@
+#!/usr/bin/env python3
+"""Benchmark of the chunked Gated DeltaNet prefill on GB300.
+
+One step = one full prefill (prepare + chunk kernel: intra-chunk solve, state
+pass, output, checkpoints) over the benchmark workload, inputs resident in HBM.
+Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--seed S] [--no-cpu-baseline]
+
+* value: tokens/s of the whole job (all ranks), device-timed with CUDA events,
+  L2 flushed (256 MiB write) between steps, outside the timed events.
+* roofline: the chunk kernel (the dominant kernel), timed alone with events on
+  its own stream; algorithmic bytes per launch / its mean duration, against the
+  measured HBM copy bandwidth.
+* e2e: the same metric through the public API with host buffers: pinned-host
+  inputs copied in and results copied out inside the timed region.
+* cpu_baseline: the fp64 oracle (sequential recurrence, all host cores) on a
+  bounded sample of the same workload (a subset of state heads), scaled to
+  tokens/s of the whole workload.
+* --impl reference: the oracle as the reference arm (host cores only).
+
+Multi-GPU: launched by torch.distributed.run, every rank runs its own replica
+of the workload (units are independent: no data-path collective); only a
+barrier and a max-reduction of the step time cross ranks ("scaling": "weak").
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gated_deltanet_chunked_device_gb300 as gdn  # noqa: E402
+from gated_deltanet_chunked_device_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "GDN prefill tokens/s and TFLOP/s as % of GB300 dense BF16 roofline, 1 GPU"
+FLOP_DENSE = 180224       # per token per state head: 10*C*D + 6*D^2, dense 64/128 tiles
+FLOP_TRI = 140630         # per token per state head: triangular-aware count
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["gated_deltanet_chunked_device_gb300/csrc/gdn_chunk_bf16.cu",
+                  "gated_deltanet_chunked_device_gb300/csrc/sm103_ptx.cuh",
+                  "gated_deltanet_chunked_device_gb300/csrc/gdn_internal.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def algorithmic_bytes(w, inp):
+    """Bytes the method must move once: q, k, v read, g and beta read, o written,
+    initial / final states, checkpoints."""
+    T, H, D = inp["T"], inp["H"], 128
+    esz = inp["q"].element_size()
+    b = T * (w.hq + w.hk + w.hv) * D * esz      # q, k, v
+    b += T * H * 4 * 2                          # g, beta (fp32)
+    b += T * H * D * esz                        # output
+    N = len(inp["seq_lens"])
+    state = H * D * D * 4
+    if inp.get("initial_state") is not None:
+        b += N * state                          # rows read (pool: only the indexed rows)
+    if inp["output_final_state"]:
+        b += N * state
+    n = inp.get("checkpoint_every_n_tokens") or 0
+    if n:
+        b += wl.num_checkpoints(inp["seq_lens"], n) * state
+    return b
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:  # noqa: BLE001
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """dram read+write bytes per launch of the chunk kernel from the committed
+    ncu summary, if it was taken on the current kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        e = rec.get(workload)
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"]), e.get("note")
+    except Exception:  # noqa: BLE001
+        pass
+    return None, None
+
+
+class ClockSampler:
+    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = None
+        self.t_start = self.t_end = None
+        try:
+            props = torch.cuda.get_device_properties(device_index)
+            bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+        except Exception:  # noqa: BLE001
+            bus = None
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if bus:
+            cmd += ["-i", bus]
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:  # noqa: BLE001
+            self.proc = None
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:  # noqa: BLE001
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) != len(self.FIELDS):
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[3], parts[5:]))
+                except Exception:  # noqa: BLE001
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        lo, hi = (self.t_start or 0) - 1.0, (self.t_end or 1e30) + 1.0
+        inside = [r for r in rows if lo <= r[0] <= hi] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def make_call(inp, device):
+    """Device buffers and C-ABI arguments for one prefill of `inp`."""
+    d = {k: (v.to(device).contiguous() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    T, H = inp["T"], inp["H"]
+    N = len(inp["seq_lens"])
+    out = torch.empty(T, H, 128, dtype=d["q"].dtype, device=device)
+    fin = torch.empty(N, H, 128, 128, dtype=torch.float32, device=device) if inp["output_final_state"] else None
+    n = inp.get("checkpoint_every_n_tokens") or 0
+    ck = torch.empty(max(wl.num_checkpoints(inp["seq_lens"], n), 1), H, 128, 128, dtype=torch.float32,
+                     device=device) if n else None
+    kw = dict(g=d["g"], beta=d["beta"], scale=inp["scale"], cu_seqlens=d["cu_seqlens"],
+              use_qk_l2norm_in_kernel=inp["use_qk_l2norm_in_kernel"], output=out,
+              initial_state=d.get("initial_state"), output_final_state=inp["output_final_state"], output_state=fin,
+              state_indices=d.get("state_indices"), checkpoint_every_n_tokens=n,
+              checkpoint_cu_starts=d.get("checkpoint_cu_starts"), state_checkpoints=ck)
+    if d.get("state_indices") is not None:
+        kw["output_state"] = d["initial_state"]
+    # One eager call builds the plan and the workspace, and checks the device status.
+    _, plan, ws = gdn.chunk_gated_delta_rule(d["q"], d["k"], d["v"], return_plan=True, **kw)
+    bits = gdn.read_status(plan, ws)
+    if bits:
+        raise RuntimeError(f"device status bits {bits:#x} on the benchmark input")
+    st = inp.get("initial_state")
+    args = gdn.Args(q=d["q"].data_ptr(), k=d["k"].data_ptr(), v=d["v"].data_ptr(), g=d["g"].data_ptr(),
+                    beta=d["beta"].data_ptr(), scale=float(inp["scale"]), cu_seqlens=d["cu_seqlens"].data_ptr(),
+                    num_seqs=N, total_tokens=T, max_seqlen=max(inp["seq_lens"]) if N else 0,
+                    initial_state=d["initial_state"].data_ptr() if st is not None else None,
+                    output_state=(kw["output_state"].data_ptr() if inp["output_final_state"] else None),
+                    n_pool=(st.shape[0] if d.get("state_indices") is not None else 0),
+                    state_indices=d["state_indices"].data_ptr() if d.get("state_indices") is not None else None,
+                    state_checkpoints=ck.data_ptr() if ck is not None else None,
+                    num_checkpoints=ck.shape[0] if ck is not None else 0,
+                    checkpoint_cu_starts=d["checkpoint_cu_starts"].data_ptr() if n else None,
+                    output=out.data_ptr())
+    return {"dev": d, "out": out, "fin": fin, "ck": ck, "plan": plan, "ws": ws, "args": args, "kw": kw}
+
+
+def cpu_baseline(inp, budget_s=15.0):
+    """Time the fp64 oracle on a sample of state heads (all sequences, all tokens)."""
+    import oracle
+    import numpy as np
+
+    H = inp["H"]
+    threads = oracle.default_threads()
+
+    def run_heads(nh):
+        hs = list(range(nh))
+        hq, hk, hv = inp["q"].shape[1], inp["k"].shape[1], inp["v"].shape[1]
+        f64 = lambda t: t.to(torch.float64).numpy()
+        q = f64(inp["q"])[:, [h // (H // hq) for h in hs]]
+        k = f64(inp["k"])[:, [h // (H // hk) for h in hs]]
+        v = f64(inp["v"])[:, [h // (H // hv) for h in hs]]
+        g, b = f64(inp["g"])[:, hs], f64(inp["beta"])[:, hs]
+        s0 = None if inp.get("initial_state") is None else f64(inp["initial_state"])[:, hs]
+        idx = None if inp.get("state_indices") is None else inp["state_indices"].numpy().astype(np.int64)
+        n = inp.get("checkpoint_every_n_tokens") or 0
+        ccs = None if not n else inp["checkpoint_cu_starts"].numpy().astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.gdn_sequential(q, k, v, g, b, inp["cu_seqlens"].numpy().astype(np.int64), scale=inp["scale"],
+                              initial_state=s0, state_indices=idx, output_final_state=inp["output_final_state"],
+                              l2norm=inp["use_qk_l2norm_in_kernel"], checkpoint_every_n_tokens=n,
+                              checkpoint_cu_starts=ccs, threads=threads)
+        return time.perf_counter() - t0
+
+    t1 = run_heads(1)
+    nh = max(1, min(H, int(budget_s / max(t1, 1e-3))))
+    # with one head the work splits only across sequences; more heads spread over the cores
+    t = run_heads(nh)
+    value = inp["T"] * nh / t / H
+    return {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{nh} of {H} state heads, all {len(inp['seq_lens'])} sequences ({inp['T']} tokens), "
+                      f"fp64 sequential recurrence, {t:.1f} s; scaled by {nh}/{H} to whole-workload tokens/s"}
+
+
+def run_reference(args, w, inp):
+    """The oracle as the reference arm: host cores only, bounded samples."""
+    steps, warmup = args.steps, args.warmup
+    H = inp["H"]
+    import oracle
+    import numpy as np
+    threads = oracle.default_threads()
+    hq, hk, hv = inp["q"].shape[1], inp["k"].shape[1], inp["v"].shape[1]
+    f64 = lambda t: t.to(torch.float64).numpy()
+    qa, ka, va, ga, ba = f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["g"]), f64(inp["beta"])
+    n = inp.get("checkpoint_every_n_tokens") or 0
+    ccs = None if not n else inp["checkpoint_cu_starts"].numpy().astype(np.int64)
+    cu = inp["cu_seqlens"].numpy().astype(np.int64)
+
+    def one(nh, h0=0):
+        hs = [(h0 + i) % H for i in range(nh)]
+        t0 = time.perf_counter()
+        oracle.gdn_sequential(qa[:, [h // (H // hq) for h in hs]], ka[:, [h // (H // hk) for h in hs]],
+                              va[:, [h // (H // hv) for h in hs]], ga[:, hs], ba[:, hs], cu, scale=inp["scale"],
+                              output_final_state=inp["output_final_state"], l2norm=inp["use_qk_l2norm_in_kernel"],
+                              checkpoint_every_n_tokens=n, checkpoint_cu_starts=ccs, threads=threads)
+        return time.perf_counter() - t0
+
+    t1 = one(1)
+    budget = float(os.environ.get("GDN_REFERENCE_STEP_SECONDS", "6"))
+    nh = max(1, min(H, int(budget / max(t1, 1e-3))))
+    for i in range(warmup):
+        one(nh, i)
+    times = [one(nh, warmup + i) for i in range(steps)]
+    step_s = sum(times) / len(times)
+    value = inp["T"] * nh / step_s / H
+    sample = f"{nh} of {H} state heads per step, all sequences, fp64 sequential recurrence"
+    line = {"metric": METRIC, "impl": "reference", "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": steps, "warmup": warmup, "ms_per_step": step_s * 1e3 * H / nh, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, inp, args),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, inp, args):
+    return {"workload": w.name, "total_tokens": inp["T"], "num_seqs": len(inp["seq_lens"]),
+            "seq_lens": inp["seq_lens"] if len(inp["seq_lens"]) <= 16 else f"{len(inp['seq_lens'])} sequences",
+            "num_q_heads": w.hq, "num_k_heads": w.hk, "num_v_heads": w.hv, "state_heads": inp["H"],
+            "head_size": 128, "chunk": 64, "checkpoint_every_n_tokens": w.checkpoint_every,
+            "qk_l2norm_in_kernel": w.l2norm_in_kernel, "seed": args.seed,
+            "l2": "flushed between steps (256 MiB write outside the timed events)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.generate(w, seed=args.seed)
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w, inp)
+        return
+
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+        pg = dist
+    gdn.build()
+    call = make_call(inp, device)
+    plan, ws, cargs = call["plan"], call["ws"], call["args"]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+    sp = stream.cuda_stream
+
+    def step(e0=None, e1=None, e2=None):
+        if e0 is not None:
+            e0.record(stream)
+        st = gdn.gdn_prefill_prepare(plan.handle, cargs, ws.data_ptr(), plan.workspace_bytes, sp)
+        if e1 is not None:
+            e1.record(stream)
+        st |= gdn.gdn_prefill_chunks(plan.handle, cargs, ws.data_ptr(), plan.workspace_bytes, sp)
+        if e2 is not None:
+            e2.record(stream)
+        if st:
+            raise RuntimeError(f"gdn_prefill returned {st}")
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            step()
+    torch.cuda.synchronize(device)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(device)
+    if sampler:
+        sampler.mark_start()
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush.fill_(float(i))
+            step(*ev[i])
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - wall0
+    if pg:
+        pg.barrier()
+    if sampler:
+        sampler.mark_end()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    chunk_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    ms_per_step = sum(step_ms) / K
+    chunk_avg_ms = sum(chunk_ms) / K
+    if pg:
+        t = torch.tensor([ms_per_step], device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    bits = gdn.read_status(plan, ws)
+    if bits:
+        raise RuntimeError(f"device status bits {bits:#x} after the timed steps")
+
+    # ---- end to end through the public API, host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: inp[k].pin_memory() for k in ("q", "k", "v", "g", "beta", "cu_seqlens")}
+        if inp.get("checkpoint_cu_starts") is not None:
+            host_in["checkpoint_cu_starts"] = inp["checkpoint_cu_starts"].pin_memory()
+        if inp.get("initial_state") is not None:
+            host_in["initial_state"] = inp["initial_state"].pin_memory()
+        if inp.get("state_indices") is not None:
+            host_in["state_indices"] = inp["state_indices"].pin_memory()
+        host_out = {"output": torch.empty_like(call["out"], device="cpu").pin_memory()}
+        if call["ck"] is not None:
+            host_out["checkpoints"] = torch.empty_like(call["ck"], device="cpu").pin_memory()
+        if call["fin"] is not None or inp.get("state_indices") is not None:
+            src = call["kw"]["output_state"]
+            host_out["final_state"] = torch.empty_like(src, device="cpu").pin_memory()
+        dev_in = {k: call["dev"][k] for k in host_in}
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        Ke = max(3, min(K, 50))
+
+        def e2e_step():
+            for k2, t in host_in.items():
+                dev_in[k2].copy_(t, non_blocking=True)
+            step()
+            host_out["output"].copy_(call["out"], non_blocking=True)
+            if "checkpoints" in host_out:
+                host_out["checkpoints"].copy_(call["ck"], non_blocking=True)
+            if "final_state" in host_out:
+                host_out["final_state"].copy_(call["kw"]["output_state"], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                e2e_step()
+        torch.cuda.synchronize(device)
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            es.record(stream)
+            for _ in range(Ke):
+                e2e_step()
+            ee.record(stream)
+        torch.cuda.synchronize(device)
+        e2e_ms = es.elapsed_time(ee) / Ke
+        if pg:
+            t = torch.tensor([e2e_ms], device=device)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * inp["T"] / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    clocks = sampler.stop() if sampler else None
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+    T, H = inp["T"], inp["H"]
+    hbm, bf16, src = measured_peaks()
+    abytes = algorithmic_bytes(w, inp)
+    achieved = abytes / (chunk_avg_ms / 1e3) / 1e9
+    traffic, tnote = recorded_traffic(w.name)
+    tflops_dense = T * H * FLOP_DENSE / (ms_per_step / 1e3) / 1e12
+    tflops_tri = T * H * FLOP_TRI / (ms_per_step / 1e3) / 1e12
+    roof_time = max(abytes / (hbm * 1e9), T * H * FLOP_DENSE / (bf16 * 1e12))
+    line = {
+        "metric": METRIC, "value": world * T / (ms_per_step / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(w, inp, args),
+        "tflops": {"dense_tile_count": tflops_dense, "triangular_aware": tflops_tri,
+                   "pct_of_bf16_peak": 100 * tflops_dense / bf16, "peak_tflops": bf16, "peak_source": src},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": traffic, "kernel": "gdn_chunk_bf16_kernel", "kernel_ms": chunk_avg_ms,
+                     "algorithmic_bytes": abytes, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if src == "measured" else "fallback 6800 GB/s",
+                     "step_frac_of_roofline_time": roof_time / (ms_per_step / 1e3)},
+        "gpu_launches": 2 * K,
+        "wall_s_timed_region": wall,
+    }
+    if tnote:
+        line["roofline"]["traffic_note"] = tnote
+    if e2e:
+        line["e2e"] = e2e
+    if clocks:
+        line["clocks"] = clocks
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp)
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

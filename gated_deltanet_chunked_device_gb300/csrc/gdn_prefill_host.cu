@@ -1,0 +1,310 @@
+// gdn_prefill_host.cu -- host side of the C ABI declared in include/gdn_prefill.h:
+// plan validation, workspace layout, run-time argument checks, TMA descriptor
+// encoding and kernel launches.  Nothing here synchronises or allocates device
+// memory, and nothing reads device memory except gdn_prefill_read_status.
+//
+// Host checks follow the pages' fail-closed rules ("FlashInfer GDN Prefill
+// 完全指南": head_size 128 on SM100; the legal head mappings; checkpoint interval
+// a multiple of 64; checkpoints and their starts given together; an output
+// state pool is required with state_indices; max_seqlen within
+// [ceil(T/N), T]).
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <cudaTypedefs.h>
+#include <mutex>
+#include <new>
+
+#include "gdn_internal.cuh"
+
+struct gdn_prefill_plan_s {
+    gdn_prefill_desc desc;
+    gdn::WorkspaceLayout ws;
+    int32_t H;
+};
+
+namespace {
+
+constexpr uint32_t kKnownFlags = GDN_FLAG_HAS_G | GDN_FLAG_HAS_BETA | GDN_FLAG_HAS_SCALE | GDN_FLAG_QK_L2NORM |
+                                 GDN_FLAG_HAS_INITIAL_STATE | GDN_FLAG_OUTPUT_FINAL_STATE |
+                                 GDN_FLAG_HAS_STATE_INDICES | GDN_FLAG_CU_SEQLENS_I64 | GDN_FLAG_STATE_INDICES_I64 |
+                                 GDN_FLAG_CHECKPOINT_STARTS_I64;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+gdn::WorkspaceLayout make_layout(const gdn_prefill_desc& d) {
+    gdn::WorkspaceLayout w{};
+    const int64_t max_chunks = (d.max_total_tokens + gdn::kChunk - 1) / gdn::kChunk + d.max_num_seqs;
+    size_t off = 0;
+    w.status = off;
+    off += 16;
+    w.counter = off;
+    off += 16;
+    w.n_chunks = off;
+    off += 16;
+    w.chunk_offsets = off;
+    off = align_up(off + sizeof(int32_t) * (static_cast<size_t>(d.max_num_seqs) + 1), 16);
+    w.chunk_map = off;
+    off = align_up(off + sizeof(int32_t) * 2 * static_cast<size_t>(max_chunks > 0 ? max_chunks : 1), 16);
+    w.seq_order = off;
+    off = align_up(off + sizeof(int32_t) * static_cast<size_t>(d.max_num_seqs > 0 ? d.max_num_seqs : 1), 16);
+    w.pool_bitmap = off;
+    w.bitmap_words = (d.max_pool_rows + 31) / 32;
+    off = align_up(off + sizeof(uint32_t) * static_cast<size_t>(w.bitmap_words > 0 ? w.bitmap_words : 1), 256);
+    w.total = off;
+    w.max_chunks = max_chunks;
+    return w;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [T, heads, 128] bf16 tensor as a 3-D TMA map with 64 x 1 x 64 boxes and the
+// 128-byte swizzle; rows past T read as zeros.
+bool encode_qkv_map(CUtensorMap* map, const void* base, int64_t T, int32_t heads) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(gdn::kHead), static_cast<cuuint64_t>(heads),
+                          static_cast<cuuint64_t>(T)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(gdn::kHead) * 2,
+                             static_cast<cuuint64_t>(heads) * gdn::kHead * 2};
+    cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(gdn::kChunk)};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_prefill_plan(const gdn_prefill_desc* desc, gdn_prefill_plan_t* plan, size_t* workspace_bytes) {
+    if (!desc || !plan || !workspace_bytes) return GDN_ERR_INVALID_ARG;
+    *plan = nullptr;
+    const gdn_prefill_desc& d = *desc;
+    if (d.flags & ~kKnownFlags) return GDN_ERR_INVALID_ARG;
+    if (d.head_size != gdn::kHead) return GDN_ERR_UNSUPPORTED;
+    if (d.num_q_heads <= 0 || d.num_k_heads <= 0 || d.num_v_heads <= 0) return GDN_ERR_INVALID_ARG;
+    const bool gva = d.num_q_heads == d.num_k_heads && d.num_v_heads % d.num_q_heads == 0;
+    const bool gqa = d.num_k_heads == d.num_v_heads && d.num_q_heads % d.num_k_heads == 0;
+    if (!gva && !gqa) return GDN_ERR_INVALID_ARG;
+    if (d.qkv_dtype != GDN_DTYPE_BF16 && d.qkv_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
+    if (d.state_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
+    if (d.checkpoint_every_n_tokens < 0 || d.checkpoint_every_n_tokens % gdn::kChunk != 0)
+        return GDN_ERR_INVALID_ARG;
+    if (d.max_total_tokens < 0 || d.max_num_seqs < 0 || d.max_pool_rows < 0) return GDN_ERR_INVALID_ARG;
+    if (d.max_total_tokens > 0x7fffffffLL - gdn::kChunk) return GDN_ERR_UNSUPPORTED;  // 32-bit TMA coordinates
+    if ((d.flags & GDN_FLAG_HAS_STATE_INDICES) && d.max_pool_rows <= 0) return GDN_ERR_INVALID_ARG;
+    gdn_prefill_plan_s* p = new (std::nothrow) gdn_prefill_plan_s;
+    if (!p) return GDN_ERR_INVALID_ARG;
+    p->desc = d;
+    p->ws = make_layout(d);
+    p->H = d.num_q_heads > d.num_v_heads ? d.num_q_heads : d.num_v_heads;
+    *plan = p;
+    *workspace_bytes = p->ws.total;
+    return GDN_OK;
+}
+
+void gdn_prefill_plan_destroy(gdn_prefill_plan_t plan) { delete plan; }
+
+gdn_status gdn_prefill_workspace_layout(gdn_prefill_plan_t plan, gdn_prefill_layout* layout) {
+    if (!plan || !layout) return GDN_ERR_INVALID_ARG;
+    layout->status = plan->ws.status;
+    layout->n_chunks = plan->ws.n_chunks;
+    layout->chunk_offsets = plan->ws.chunk_offsets;
+    layout->chunk_map = plan->ws.chunk_map;
+    layout->seq_order = plan->ws.seq_order;
+    layout->max_chunks = plan->ws.max_chunks;
+    return GDN_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+enum : int { kStagePrepare = 1, kStageChunks = 2 };
+
+gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, void* workspace,
+                      size_t workspace_bytes, void* stream_ptr, int stages) {
+    if (!plan || !args) return GDN_ERR_INVALID_ARG;
+    const gdn_prefill_desc& d = plan->desc;
+    const gdn_prefill_args& a = *args;
+    const uint32_t f = d.flags;
+    const int32_t N = a.num_seqs;
+    const int64_t T = a.total_tokens;
+    if (N < 0 || N > d.max_num_seqs || T < 0 || T > d.max_total_tokens) return GDN_ERR_INVALID_ARG;
+    if (N == 0) return T == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (!a.cu_seqlens) return GDN_ERR_INVALID_ARG;
+    if (T > 0 && (!a.q || !a.k || !a.v || !a.output)) return GDN_ERR_INVALID_ARG;
+    if (!aligned(a.q, 16) || !aligned(a.k, 16) || !aligned(a.v, 16) || !aligned(a.output, 16))
+        return GDN_ERR_INVALID_ARG;
+    if (((f & GDN_FLAG_HAS_G) && !a.g) || ((f & GDN_FLAG_HAS_BETA) && !a.beta)) return GDN_ERR_INVALID_ARG;
+    if ((f & GDN_FLAG_HAS_INITIAL_STATE) && (!a.initial_state || !aligned(a.initial_state, 16)))
+        return GDN_ERR_INVALID_ARG;
+    if ((f & GDN_FLAG_OUTPUT_FINAL_STATE) && (!a.output_state || !aligned(a.output_state, 16)))
+        return GDN_ERR_INVALID_ARG;
+    if (f & GDN_FLAG_HAS_STATE_INDICES) {
+        if (!a.state_indices || a.n_pool <= 0 || a.n_pool > d.max_pool_rows) return GDN_ERR_INVALID_ARG;
+    }
+    const int32_t n = d.checkpoint_every_n_tokens;
+    if (n > 0) {
+        if (!a.state_checkpoints || !a.checkpoint_cu_starts || a.num_checkpoints < 0 ||
+            !aligned(a.state_checkpoints, 16))
+            return GDN_ERR_INVALID_ARG;
+    } else if (a.state_checkpoints || a.checkpoint_cu_starts) {
+        return GDN_ERR_INVALID_ARG;
+    }
+    if (a.max_seqlen != 0) {
+        const int64_t lo = (T + N - 1) / N;
+        if (a.max_seqlen > T || a.max_seqlen < lo) return GDN_ERR_INVALID_ARG;
+    }
+    if (!workspace || workspace_bytes < plan->ws.total || !aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
+    if (d.qkv_dtype != GDN_DTYPE_BF16) return GDN_ERR_UNSUPPORTED;
+
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int32_t* status = a.device_status ? a.device_status : reinterpret_cast<int32_t*>(ws + plan->ws.status);
+
+    gdn::PrepareParams pp{};
+    pp.cu_seqlens = a.cu_seqlens;
+    pp.cu_i64 = (f & GDN_FLAG_CU_SEQLENS_I64) ? 1 : 0;
+    pp.num_seqs = N;
+    pp.total_tokens = T;
+    pp.max_seqlen = a.max_seqlen;
+    pp.ckpt_n = n;
+    pp.ckpt_cu_starts = a.checkpoint_cu_starts;
+    pp.ckpt_i64 = (f & GDN_FLAG_CHECKPOINT_STARTS_I64) ? 1 : 0;
+    pp.num_checkpoints = a.num_checkpoints;
+    pp.state_indices = (f & GDN_FLAG_HAS_STATE_INDICES) ? a.state_indices : nullptr;
+    pp.idx_i64 = (f & GDN_FLAG_STATE_INDICES_I64) ? 1 : 0;
+    pp.n_pool = a.n_pool;
+    pp.status = status;
+    pp.counter = reinterpret_cast<int32_t*>(ws + plan->ws.counter);
+    pp.n_chunks = reinterpret_cast<int32_t*>(ws + plan->ws.n_chunks);
+    pp.chunk_offsets = reinterpret_cast<int32_t*>(ws + plan->ws.chunk_offsets);
+    pp.chunk_map = reinterpret_cast<int32_t*>(ws + plan->ws.chunk_map);
+    pp.max_chunks = (T + gdn::kChunk - 1) / gdn::kChunk + N;
+    pp.seq_order = reinterpret_cast<int32_t*>(ws + plan->ws.seq_order);
+    pp.pool_bitmap = reinterpret_cast<uint32_t*>(ws + plan->ws.pool_bitmap);
+    pp.bitmap_words = (f & GDN_FLAG_HAS_STATE_INDICES) ? (a.n_pool + 31) / 32 : 0;
+    if ((stages & kStagePrepare) && gdn::launch_prepare(pp, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    if (!(stages & kStageChunks)) return GDN_OK;
+
+    gdn::ChunkParams cp{};
+    cp.q = a.q;
+    cp.k = a.k;
+    cp.v = a.v;
+    cp.g = (f & GDN_FLAG_HAS_G) ? a.g : nullptr;
+    cp.beta = (f & GDN_FLAG_HAS_BETA) ? a.beta : nullptr;
+    cp.scale = (f & GDN_FLAG_HAS_SCALE) ? a.scale : 1.0f / std::sqrt(static_cast<float>(gdn::kHead));
+    cp.hq = d.num_q_heads;
+    cp.hk = d.num_k_heads;
+    cp.hv = d.num_v_heads;
+    cp.H = plan->H;
+    cp.l2norm = (f & GDN_FLAG_QK_L2NORM) ? 1 : 0;
+    cp.cu_seqlens = a.cu_seqlens;
+    cp.cu_i64 = pp.cu_i64;
+    cp.num_seqs = N;
+    cp.initial_state = (f & GDN_FLAG_HAS_INITIAL_STATE) ? a.initial_state : nullptr;
+    cp.output_state = (f & GDN_FLAG_OUTPUT_FINAL_STATE) ? a.output_state : nullptr;
+    cp.state_indices = pp.state_indices;
+    cp.idx_i64 = pp.idx_i64;
+    cp.checkpoints = n > 0 ? a.state_checkpoints : nullptr;
+    cp.ckpt_n = n;
+    cp.ckpt_cu_starts = a.checkpoint_cu_starts;
+    cp.ckpt_i64 = pp.ckpt_i64;
+    cp.output = a.output;
+    cp.status = status;
+    cp.counter = pp.counter;
+    cp.chunk_offsets = pp.chunk_offsets;
+    cp.seq_order = pp.seq_order;
+    cp.intra_g = a.intra_g;
+    cp.intra_w = a.intra_w;
+    cp.intra_u = a.intra_u;
+    cp.has_tokens = T > 0 ? 1 : 0;
+
+    CUtensorMap tq, tk, tv;
+    std::memset(&tq, 0, sizeof(tq));
+    std::memset(&tk, 0, sizeof(tk));
+    std::memset(&tv, 0, sizeof(tv));
+    if (T > 0) {
+        if (!encode_qkv_map(&tq, a.q, T, d.num_q_heads) || !encode_qkv_map(&tk, a.k, T, d.num_k_heads) ||
+            !encode_qkv_map(&tv, a.v, T, d.num_v_heads))
+            return GDN_ERR_CUDA;
+    }
+    const int sms = sm_count();
+    if (sms <= 0) return GDN_ERR_CUDA;
+    const int64_t units = static_cast<int64_t>(N) * plan->H;
+    const int grid = static_cast<int>(units < sms ? units : sms);
+    if (gdn::launch_chunk_bf16(cp, tq, tk, tv, grid, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_prefill_run(gdn_prefill_plan_t plan, const gdn_prefill_args* args, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    return run_stages(plan, args, workspace, workspace_bytes, stream, kStagePrepare | kStageChunks);
+}
+
+gdn_status gdn_prefill_prepare(gdn_prefill_plan_t plan, const gdn_prefill_args* args, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    return run_stages(plan, args, workspace, workspace_bytes, stream, kStagePrepare);
+}
+
+gdn_status gdn_prefill_chunks(gdn_prefill_plan_t plan, const gdn_prefill_args* args, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    return run_stages(plan, args, workspace, workspace_bytes, stream, kStageChunks);
+}
+
+gdn_status gdn_prefill_read_status(gdn_prefill_plan_t plan, const void* workspace, const int32_t* device_status,
+                                   void* stream_ptr, int32_t* bits) {
+    if (!plan || !bits || (!workspace && !device_status)) return GDN_ERR_INVALID_ARG;
+    const int32_t* src = device_status
+                             ? device_status
+                             : reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(workspace) + plan->ws.status);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, src, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GDN_ERR_CUDA;
+    *bits = v;
+    if (v == 0) return GDN_OK;
+    return (v & GDN_DEVICE_ERR_TIMEOUT) ? GDN_ERR_DEVICE_TIMEOUT : GDN_ERR_DEVICE_INPUT;
+}
+
+const char* gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_INVALID_ARG: return "invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "unsupported configuration";
+        case GDN_ERR_CUDA: return "CUDA runtime error";
+        case GDN_ERR_DEVICE_INPUT: return "device-checked input error";
+        case GDN_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

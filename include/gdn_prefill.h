@@ -1,0 +1,191 @@
+/*
+ * gdn_prefill.h -- C ABI of the chunked Gated DeltaNet prefill on one GB300 GPU.
+ *
+ * The operation (north-star form; "FlashInfer GDN Prefill 完全指南", section
+ * "chunk_gated_delta_rule API 全参数解析" gives the arguments, and
+ * "GDN 与 Chunked Prefill", sections "GDN 是什么" and "块内 state 和块间 final
+ * state", the recurrence and the read after the update): for every sequence i
+ * of a packed variable-length batch and every state head h,
+ *
+ *     S_t = alpha_t * S_{t-1} * (I - beta_t k_t k_t^T) + beta_t * v_t k_t^T
+ *     o_t = scale * S_t q_t
+ *
+ * with S a 128 x 128 fp32 matrix laid out [V][K], started from the initial
+ * state (or zero), and computed in 64-token chunks: only each chunk's final
+ * state crosses a chunk boundary ("GDN 与 Chunked Prefill", section "为什么要切成
+ * 64-token chunk").
+ *
+ * Shapes (all tensors dense, row-major, device memory unless stated):
+ *   q [T, HQ, 128], k [T, HK, 128], v [T, HV, 128]  bf16 or fp32
+ *   g, beta          [T, H] fp32, H = max(HQ, HV)   (g is alpha, linear space)
+ *   cu_seqlens       [N+1] int32 or int64, cu_seqlens[0] = 0, cu_seqlens[N] = T;
+ *                    equal neighbours are legal zero-length sequences
+ *   initial_state    [N, H, 128, 128] fp32, or the pool [n_pool, H, 128, 128]
+ *   output_state     same shape; may be the same buffer as initial_state
+ *   state_indices    [N] int32 or int64: sequence i reads and writes pool row
+ *                    state_indices[i] (unique, in [0, n_pool))
+ *   state_checkpoints[sum_i floor(L_i / n), H, 128, 128] fp32: the state after
+ *                    local token p = j * n of sequence i goes to row
+ *                    checkpoint_cu_starts[i] + j - 1
+ *   output           [T, H, 128], dtype of q
+ * Head mapping ("FlashInfer GDN Prefill 完全指南", section on the legal CP
+ * shapes): either HQ == HK and HV % HQ == 0 (GVA) or HK == HV and HQ % HK == 0
+ * (GQA); state head h reads q head h / (H/HQ), k head h / (H/HK) and v head
+ * h / (H/HV); g and beta are indexed by the state head.
+ *
+ * Ownership: the caller owns every tensor and the workspace; the library owns
+ * only the opaque plan (shapes, dtypes, flags; no device pointers), so buffer
+ * addresses may change from run to run.  gdn_prefill_run only enqueues work on
+ * the caller's stream: it never synchronises, never allocates device memory
+ * and never reads device memory on the host.
+ *
+ * Errors: conditions the host can check are returned synchronously and
+ * nothing is launched (fail closed).  Conditions that depend on device data
+ * (cu_seqlens order, checkpoint_cu_starts, state index range and uniqueness,
+ * a sequence longer than max_seqlen, a timed-out wait) set bits of a device
+ * status word, checked without a host round trip as the pages recommend
+ * ("FlashInfer GDN Prefill 完全指南": checkpoint_cu_starts and state_indices are
+ * not validated at launch to avoid a device-to-host sync); when a bit is set
+ * the remaining kernels return early and the outputs are unspecified.  Read
+ * the word with gdn_prefill_read_status, which synchronises the stream.
+ */
+#ifndef GDN_PREFILL_H
+#define GDN_PREFILL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,   /* an argument breaks a documented precondition */
+    GDN_ERR_UNSUPPORTED = 2,   /* legal for the API, outside this library's scope */
+    GDN_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, attribute, ...) */
+    GDN_ERR_DEVICE_INPUT = 4,  /* gdn_prefill_read_status: a device-checked input bit is set */
+    GDN_ERR_DEVICE_TIMEOUT = 5 /* gdn_prefill_read_status: a bounded device wait ran out */
+} gdn_status;
+
+typedef enum gdn_dtype { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 } gdn_dtype;
+
+/* gdn_prefill_desc.flags */
+enum {
+    GDN_FLAG_HAS_G = 1u << 0,              /* g given; else alpha = 1 */
+    GDN_FLAG_HAS_BETA = 1u << 1,           /* beta given; else beta = 1 */
+    GDN_FLAG_HAS_SCALE = 1u << 2,          /* args.scale used; else 1/sqrt(128) */
+    GDN_FLAG_QK_L2NORM = 1u << 3,          /* q, k rows -> x / sqrt(sum x^2 + 1e-6), fp32 sum, back to input dtype */
+    GDN_FLAG_HAS_INITIAL_STATE = 1u << 4,  /* initial_state given; else zero */
+    GDN_FLAG_OUTPUT_FINAL_STATE = 1u << 5, /* write the final state to output_state */
+    GDN_FLAG_HAS_STATE_INDICES = 1u << 6,  /* initial/output state are pools addressed by state_indices */
+    GDN_FLAG_CU_SEQLENS_I64 = 1u << 7,     /* cu_seqlens is int64 (else int32) */
+    GDN_FLAG_STATE_INDICES_I64 = 1u << 8,  /* state_indices is int64 (else int32) */
+    GDN_FLAG_CHECKPOINT_STARTS_I64 = 1u << 9 /* checkpoint_cu_starts is int64 (else int32) */
+};
+
+/* Device status bits (gdn_prefill_read_status). */
+enum {
+    GDN_DEVICE_ERR_CU_SEQLENS = 1u << 0,        /* cu_seqlens[0] != 0, decreasing, or cu_seqlens[N] != T */
+    GDN_DEVICE_ERR_CHECKPOINT_STARTS = 1u << 1, /* checkpoint_cu_starts != [0] + cumsum(L_i // n), or > capacity */
+    GDN_DEVICE_ERR_STATE_INDEX_RANGE = 1u << 2, /* a state index outside [0, n_pool) */
+    GDN_DEVICE_ERR_STATE_INDEX_DUP = 1u << 3,   /* two sequences name the same pool row */
+    GDN_DEVICE_ERR_MAX_SEQLEN = 1u << 4,        /* a sequence longer than args.max_seqlen */
+    GDN_DEVICE_ERR_TIMEOUT = 1u << 5            /* a bounded wait inside a kernel ran out */
+};
+
+/* Plan-time description: everything that selects kernels and sizes the
+ * workspace.  Checked on the host by gdn_prefill_plan (no device needed). */
+typedef struct gdn_prefill_desc {
+    int32_t num_q_heads, num_k_heads, num_v_heads; /* HQ, HK, HV */
+    int32_t head_size;                             /* must be 128 */
+    gdn_dtype qkv_dtype;                           /* q, k, v and output: BF16 or F32 */
+    gdn_dtype state_dtype;                         /* states and checkpoints: F32 */
+    int64_t max_total_tokens;                      /* upper bound of T over the plan's runs */
+    int32_t max_num_seqs;                          /* upper bound of N */
+    int32_t max_pool_rows;                         /* upper bound of n_pool (0 without state_indices) */
+    int32_t checkpoint_every_n_tokens;             /* 0, or a multiple of 64 */
+    uint32_t flags;                                /* GDN_FLAG_* */
+} gdn_prefill_desc;
+
+typedef struct gdn_prefill_plan_s *gdn_prefill_plan_t;
+
+/* Run-time arguments.  Pointers are device addresses; q, k, v and output must
+ * be 16-byte aligned.  Unused optional pointers may be NULL. */
+typedef struct gdn_prefill_args {
+    const void *q, *k, *v;
+    const float *g;               /* [T, H], required with GDN_FLAG_HAS_G */
+    const float *beta;            /* [T, H], required with GDN_FLAG_HAS_BETA */
+    float scale;                  /* used with GDN_FLAG_HAS_SCALE */
+    const void *cu_seqlens;       /* [N+1] */
+    int32_t num_seqs;             /* N >= 0 */
+    int64_t total_tokens;         /* T >= 0 */
+    int64_t max_seqlen;           /* 0 = unknown; else ceil(T/N) <= max_seqlen <= T (upper bound of L_i) */
+    const float *initial_state;   /* required with GDN_FLAG_HAS_INITIAL_STATE */
+    float *output_state;          /* required with GDN_FLAG_OUTPUT_FINAL_STATE */
+    int32_t n_pool;               /* pool rows, with GDN_FLAG_HAS_STATE_INDICES */
+    const void *state_indices;    /* [N], with GDN_FLAG_HAS_STATE_INDICES */
+    float *state_checkpoints;     /* required when checkpoint_every_n_tokens > 0 */
+    int64_t num_checkpoints;      /* rows of state_checkpoints (capacity, checked on the device) */
+    const void *checkpoint_cu_starts; /* [N+1], required when checkpoint_every_n_tokens > 0 */
+    void *output;                 /* [T, H, 128], dtype of q */
+    int32_t *device_status;       /* optional: where to keep the status word (else in the workspace) */
+    /* Optional outputs of the intra-chunk stage, indexed by flat chunk id f
+     * (the order of the chunk map: sequence by sequence, chunk by chunk):
+     * intra_g [F, H, 64] fp32 (G = running sum of log alpha in the chunk),
+     * intra_w and intra_u [F, H, 64, 128] fp32 (W = T diag(beta*gamma) K,
+     * U = T diag(beta) V with T = (I + A)^-1), F = ceil(T/64) + N rows. */
+    float *intra_g, *intra_w, *intra_u;
+} gdn_prefill_args;
+
+/* Validate `desc` and create a plan.  *workspace_bytes receives the device
+ * workspace size gdn_prefill_run needs (16-byte aligned, caller allocated).
+ * Needs no GPU.  Returns GDN_OK, GDN_ERR_INVALID_ARG or GDN_ERR_UNSUPPORTED. */
+gdn_status gdn_prefill_plan(const gdn_prefill_desc *desc, gdn_prefill_plan_t *plan, size_t *workspace_bytes);
+
+/* Enqueue one prefill on `stream` (a cudaStream_t; NULL = legacy default
+ * stream).  Host-checked errors return before anything is launched. */
+gdn_status gdn_prefill_run(gdn_prefill_plan_t plan, const gdn_prefill_args *args, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/* The two halves of gdn_prefill_run, for callers that want to place events
+ * or other work between them (same arguments and checks; the chunk half
+ * must follow the prepare half of the same arguments on the same stream,
+ * with no other run on that workspace in between):
+ *   gdn_prefill_prepare -- the device-side chunk map, validation and work
+ *                          order (one small kernel);
+ *   gdn_prefill_chunks  -- the intra-chunk solve, state pass and output
+ *                          (one persistent kernel). */
+gdn_status gdn_prefill_prepare(gdn_prefill_plan_t plan, const gdn_prefill_args *args, void *workspace,
+                               size_t workspace_bytes, void *stream);
+gdn_status gdn_prefill_chunks(gdn_prefill_plan_t plan, const gdn_prefill_args *args, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
+/* Copy the device status word of the last run on `stream` to *bits
+ * (synchronises `stream`; outside the hot path).  `device_status` is the
+ * pointer given in the run's args, or NULL when the word sits in the
+ * workspace.  Returns GDN_OK when no bit is set, GDN_ERR_DEVICE_TIMEOUT when
+ * the timeout bit is set, GDN_ERR_DEVICE_INPUT for any other bit. */
+gdn_status gdn_prefill_read_status(gdn_prefill_plan_t plan, const void *workspace, const int32_t *device_status,
+                                   void *stream, int32_t *bits);
+
+/* Device buffers written by the prepare step (the chunk map), for callers
+ * and tests: offsets in bytes from the workspace start.  chunk_offsets is
+ * [N+1] int32 (exclusive prefix sum of ceil(L_i/64)), chunk_map is
+ * [max_chunks, 2] int32 (sequence, chunk-in-sequence) padded with -1,
+ * n_chunks is one int32, seq_order is [N] int32 (longest first). */
+typedef struct gdn_prefill_layout {
+    size_t status, n_chunks, chunk_offsets, chunk_map, seq_order;
+    int64_t max_chunks;
+} gdn_prefill_layout;
+gdn_status gdn_prefill_workspace_layout(gdn_prefill_plan_t plan, gdn_prefill_layout *layout);
+
+void gdn_prefill_plan_destroy(gdn_prefill_plan_t plan);
+
+const char *gdn_status_string(gdn_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_PREFILL_H */

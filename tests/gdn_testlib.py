@@ -1,0 +1,124 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI,
+run the fp64 oracle on the same (rounded) inputs, and compare."""
+import numpy as np
+import torch
+
+import oracle
+import gated_deltanet_chunked_device_gb300 as gdn
+from gated_deltanet_chunked_device_gb300 import workloads as wl
+
+# Tolerances of the parity bar: elementwise |gpu - ref| <= tol + tol * |ref|
+TOL = {torch.bfloat16: 2e-2, torch.float32: 1e-3}
+
+
+def to_device(inp, device="cuda"):
+    out = dict(inp)
+    for key in ("q", "k", "v", "g", "beta", "cu_seqlens", "initial_state", "state_indices", "checkpoint_cu_starts"):
+        if out.get(key) is not None:
+            out[key] = out[key].to(device).contiguous()
+    return out
+
+
+def run_gpu(inp, intermediates=None, return_plan=False, **override):
+    """Run the CUDA path on device inputs `inp` (from to_device)."""
+    d = inp["q"].device
+    H = inp["H"]
+    T = inp["T"]
+    lens = inp["seq_lens"]
+    kw = dict(g=inp["g"], beta=inp["beta"], scale=inp["scale"], cu_seqlens=inp["cu_seqlens"],
+              use_qk_l2norm_in_kernel=inp["use_qk_l2norm_in_kernel"], output_final_state=inp["output_final_state"])
+    pool = inp.get("state_indices") is not None
+    if inp.get("initial_state") is not None:
+        st = inp["initial_state"].clone()
+        kw["initial_state"] = st
+        if pool:
+            kw["state_indices"] = inp["state_indices"]
+            kw["output_state"] = st  # in place, as the pages' pool example
+    n = inp.get("checkpoint_every_n_tokens") or 0
+    if n:
+        nck = wl.num_checkpoints(lens, n)
+        kw["checkpoint_every_n_tokens"] = n
+        kw["checkpoint_cu_starts"] = inp["checkpoint_cu_starts"]
+        kw["state_checkpoints"] = torch.full((max(nck, 1), H, 128, 128), float("nan"), device=d)
+    kw.update(override)
+    res = gdn.chunk_gated_delta_rule(inp["q"], inp["k"], inp["v"], intermediates=intermediates,
+                                     return_plan=return_plan, **kw)
+    plan = ws = None
+    if return_plan:
+        res, plan, ws = res
+    if kw.get("output_final_state"):
+        out, fin = res
+    else:
+        out, fin = res, None
+    torch.cuda.synchronize()
+    r = {"output": out, "final_state": fin, "checkpoints": kw.get("state_checkpoints")}
+    if return_plan:
+        r["plan"], r["ws"] = plan, ws
+    return r
+
+
+def _np(t):
+    return None if t is None else t.detach().to("cpu", torch.float64).numpy()
+
+
+def run_oracle(inp, heads=None, threads=None):
+    """fp64 oracle on CPU inputs `inp` (from workloads.generate).  With `heads`
+    (a list of state heads) only those heads are computed, as an equal-head
+    problem on the gathered q/k/v/g/beta heads."""
+    H = inp["H"]
+    hq, hk, hv = inp["q"].shape[1], inp["k"].shape[1], inp["v"].shape[1]
+    q, k, v = _np(inp["q"]), _np(inp["k"]), _np(inp["v"])
+    g, b = _np(inp["g"]), _np(inp["beta"])
+    s0 = _np(inp.get("initial_state"))
+    idx = None if inp.get("state_indices") is None else inp["state_indices"].numpy().astype(np.int64)
+    if heads is not None:
+        hs = list(heads)
+        q = q[:, [h // (H // hq) for h in hs]]
+        k = k[:, [h // (H // hk) for h in hs]]
+        v = v[:, [h // (H // hv) for h in hs]]
+        g, b = g[:, hs], b[:, hs]
+        if s0 is not None:
+            s0 = s0[:, hs]
+    n = inp.get("checkpoint_every_n_tokens") or 0
+    ccs = None if not n else inp["checkpoint_cu_starts"].numpy().astype(np.int64)
+    return oracle.gdn_sequential(q, k, v, g, b, inp["cu_seqlens"].numpy().astype(np.int64), scale=inp["scale"],
+                                 initial_state=s0, state_indices=idx, output_final_state=inp["output_final_state"],
+                                 l2norm=inp["use_qk_l2norm_in_kernel"], checkpoint_every_n_tokens=n,
+                                 checkpoint_cu_starts=ccs, threads=threads)
+
+
+def compare(name, gpu, ref, tol):
+    """Elementwise |gpu - ref| <= tol + tol*|ref|; returns stats, raises on failure."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert gpu.shape == ref.shape, f"{name}: shape {gpu.shape} vs {ref.shape}"
+    assert np.isfinite(gpu).all(), f"{name}: non-finite values from the CUDA path"
+    d = np.abs(gpu - ref)
+    bound = tol + tol * np.abs(ref)
+    bad = d > bound
+    stats = {"max_abs": float(d.max()) if d.size else 0.0,
+             "rel_to_max": float(d.max() / max(np.abs(ref).max(), 1e-30)) if d.size else 0.0,
+             "n_bad": int(bad.sum())}
+    if bad.any():
+        i = np.unravel_index(np.argmax(d - bound), d.shape)
+        raise AssertionError(f"{name}: {stats['n_bad']} of {d.size} elements outside tol {tol}; worst at {i}: "
+                             f"gpu={gpu[i]:.6g} ref={ref[i]:.6g}; max_abs={stats['max_abs']:.3g}")
+    return stats
+
+
+def check_against_oracle(inp_cpu, gpu_res, heads=None, tol=None):
+    """Compare output / final state / checkpoints of a GPU run with the oracle."""
+    tol = tol or TOL[inp_cpu["q"].dtype]
+    ref = run_oracle(inp_cpu, heads=heads)
+    H = inp_cpu["H"]
+    hs = list(range(H)) if heads is None else list(heads)
+    stats = {}
+    stats["output"] = compare("output", _np(gpu_res["output"])[:, hs], ref["output"], tol)
+    if inp_cpu["output_final_state"]:
+        fin = _np(gpu_res["final_state"])[:, hs]
+        stats["final_state"] = compare("final_state", fin, ref["final_state"], tol)
+    if inp_cpu.get("checkpoint_every_n_tokens"):
+        nck = ref["checkpoints"].shape[0]
+        stats["checkpoints"] = compare("checkpoints", _np(gpu_res["checkpoints"])[:nck][:, hs], ref["checkpoints"],
+                                       tol)
+    return stats

@@ -1,0 +1,137 @@
+"""The C ABI on the host: the library loads, exports every declared entry
+point, and rejects host-checkable bad arguments before launching anything.
+None of these tests needs a GPU (every rejection happens before the first
+CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_deltanet_chunked_device_gb300 as gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn_prefill.h")
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def L():
+    gdn.build()
+    return gdn.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert {"gdn_prefill_plan", "gdn_prefill_run", "gdn_prefill_read_status", "gdn_prefill_plan_destroy",
+            "gdn_status_string", "gdn_prefill_workspace_layout"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in gdn_prefill.h but not exported"
+
+
+def _desc(**kw):
+    d = dict(num_q_heads=16, num_k_heads=16, num_v_heads=32, head_size=128, qkv_dtype=gdn.DTYPE_BF16,
+             state_dtype=gdn.DTYPE_F32, max_total_tokens=1 << 16, max_num_seqs=64, max_pool_rows=0,
+             checkpoint_every_n_tokens=0, flags=0)
+    d.update(kw)
+    return gdn.Desc(**d)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    ({}, OK),
+    (dict(head_size=64), UNSUPPORTED),
+    (dict(num_q_heads=4, num_k_heads=2, num_v_heads=8), INVALID),       # neither GQA nor GVA
+    (dict(num_q_heads=32, num_k_heads=16, num_v_heads=16), OK),         # GQA
+    (dict(num_q_heads=6, num_k_heads=4, num_v_heads=4), INVALID),       # hq % hk != 0
+    (dict(num_q_heads=16, num_k_heads=16, num_v_heads=24), INVALID),    # hv % hq != 0
+    (dict(num_q_heads=0), INVALID),
+    (dict(checkpoint_every_n_tokens=100), INVALID),
+    (dict(checkpoint_every_n_tokens=512), OK),
+    (dict(checkpoint_every_n_tokens=-64), INVALID),
+    (dict(state_dtype=gdn.DTYPE_BF16), UNSUPPORTED),
+    (dict(qkv_dtype=7), UNSUPPORTED),
+    (dict(flags=1 << 20), INVALID),
+    (dict(max_total_tokens=-1), INVALID),
+    (dict(max_total_tokens=1 << 31), UNSUPPORTED),
+    (dict(flags=gdn.FLAGS["HAS_STATE_INDICES"], max_pool_rows=0), INVALID),
+    (dict(flags=gdn.FLAGS["HAS_STATE_INDICES"], max_pool_rows=64), OK),
+])
+def test_plan_validation(L, kw, expect):
+    st, plan, nbytes = gdn.gdn_prefill_plan(_desc(**kw))
+    assert st == expect, gdn.STATUS.get(st)
+    if st == OK:
+        assert nbytes > 0 and nbytes % 16 == 0
+        lay = gdn.gdn_prefill_workspace_layout(plan)
+        assert lay.max_chunks == (1 << 16) // 64 + 64
+        gdn.gdn_prefill_plan_destroy(plan)
+    else:
+        assert not plan.value
+
+
+def _valid_args(**kw):
+    # fake, 256-byte aligned device addresses: never dereferenced, because every
+    # case below is rejected (or needs no launch) before the first CUDA call
+    fake = 0x7f0000000000
+    a = dict(q=fake, k=fake + 0x100000, v=fake + 0x200000, g=None, beta=None, scale=0.0, cu_seqlens=fake + 0x300000,
+             num_seqs=2, total_tokens=100, max_seqlen=0, initial_state=None, output_state=None, n_pool=0,
+             state_indices=None, state_checkpoints=None, num_checkpoints=0, checkpoint_cu_starts=None,
+             output=fake + 0x400000, device_status=None)
+    a.update(kw)
+    return gdn.Args(**a)
+
+
+@pytest.mark.parametrize("desc_kw,args_kw,ws,expect", [
+    ({}, dict(q=None), 1 << 20, INVALID),
+    ({}, dict(q=0x7f0000000008), 1 << 20, INVALID),                     # q not 16-byte aligned
+    ({}, dict(num_seqs=65), 1 << 20, INVALID),                          # above max_num_seqs
+    ({}, dict(total_tokens=(1 << 16) + 1), 1 << 20, INVALID),           # above max_total_tokens
+    ({}, dict(num_seqs=0, total_tokens=5), 1 << 20, INVALID),
+    ({}, dict(num_seqs=0, total_tokens=0), 1 << 20, OK),                # nothing to do, nothing launched
+    ({}, dict(cu_seqlens=None), 1 << 20, INVALID),
+    ({}, dict(max_seqlen=101), 1 << 20, INVALID),                       # > T
+    ({}, dict(max_seqlen=49), 1 << 20, INVALID),                        # < ceil(T / N)
+    ({}, {}, 16, INVALID),                                              # workspace too small
+    (dict(flags=gdn.FLAGS["HAS_G"]), {}, 1 << 20, INVALID),             # g flag without g
+    (dict(flags=gdn.FLAGS["HAS_INITIAL_STATE"]), {}, 1 << 20, INVALID),
+    (dict(flags=gdn.FLAGS["OUTPUT_FINAL_STATE"] | gdn.FLAGS["HAS_STATE_INDICES"], max_pool_rows=8),
+     dict(state_indices=0x7f0000500000, n_pool=8), 1 << 20, INVALID),  # pool output required with indices
+    (dict(flags=gdn.FLAGS["HAS_STATE_INDICES"], max_pool_rows=8),
+     dict(state_indices=0x7f0000500000, n_pool=9), 1 << 20, INVALID),  # n_pool above the plan's bound
+    (dict(checkpoint_every_n_tokens=64), dict(state_checkpoints=0x7f0000600000), 1 << 20, INVALID),  # starts missing
+    ({}, dict(checkpoint_cu_starts=0x7f0000600000), 1 << 20, INVALID),  # checkpoints without an interval
+    (dict(qkv_dtype=gdn.DTYPE_F32, num_q_heads=2, num_k_heads=2, num_v_heads=2), dict(q=None), 1 << 20, INVALID),
+])
+def test_run_rejects_before_launch(L, desc_kw, args_kw, ws, expect):
+    st, plan, nbytes = gdn.gdn_prefill_plan(_desc(**desc_kw))
+    assert st == OK
+    try:
+        args = _valid_args(**args_kw)
+        st = gdn.gdn_prefill_run(plan, args, 0x7f0000700000, ws, 0)
+        assert st == expect, gdn.STATUS.get(st)
+    finally:
+        gdn.gdn_prefill_plan_destroy(plan)
+
+
+def test_status_strings(L):
+    for code in range(6):
+        assert gdn.gdn_status_string(code) and gdn.gdn_status_string(code) != "unknown status"
+
+
+def test_python_wrapper_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(4, 1, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        gdn.chunk_gated_delta_rule(q, q, q)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(gdn._build, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(gdn, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        gdn.lib()
