@@ -1,33 +1,42 @@
 // gdn_chunk_bf16.cu -- chunked Gated DeltaNet prefill, bf16 q/k/v, fp32 state,
-// tcgen05 tensor cores with TMEM accumulators and TMA-fed operands (sm_103a).
+// on sm_103a: tcgen05 tensor cores with TMEM accumulators, TMA-fed operands,
+// warp-specialised and pipelined across chunks.
 //
-// One CTA runs one work unit (sequence i, state head h) at a time and walks
-// the sequence's 64-token chunks in order; persistent CTAs take units from an
-// atomic counter in longest-first order.  Per chunk (notation: C = 64 rows,
-// G_r = sum_{m<=r} log alpha_m inside the chunk, gamma_r = exp(G_r)):
+// Per chunk of C = 64 tokens (G_r = sum_{m<=r} log alpha_m inside the chunk,
+// gamma_r = e^{G_r}; n_j, m_i = 1/|k_j|, 1/|q_i| when the L2 norm is on, else 1):
 //
 //   intra-chunk step ("GDN 与 Chunked Prefill": cumsum, triangular solve,
-//   recompute; the 4-token table generalised to the 64 x 64 decay table):
-//     D1 = [K; Q] K^T                                  (tcgen05, M=128 N=64 K=128)
-//     A_ij = beta_i e^{G_i-G_j} (k_i.k_j), j < i      (CUDA cores)
-//     P_ij = e^{G_i-G_j} (q_i.k_j), j <= i            (CUDA cores)
-//     T = (I + A)^-1                                   (blocked forward substitution)
-//     W^T = K^T (T diag(beta gamma))^T,  U^T = V^T (T diag(beta))^T   (tcgen05)
+//   recompute; the 4-token expansion table generalised to a 64 x 64 table):
+//     D1 = [K; Q] K^T                               tcgen05, M=128 N=64 K=128
+//     A_ij = beta_i e^{G_i-G_j} n_i n_j (k_i.k_j), j < i
+//     P_ij = e^{G_i-G_j} m_i n_j (q_i.k_j),       j <= i
+//     T = (I + A)^-1                                blocked substitution, CUDA cores
+//     W^T = K^T (T diag(beta gamma n))^T,  U^T = V^T (T diag(beta))^T   tcgen05
 //   state pass ("块内 state 和块间 final state": only the chunk's last state
 //   crosses the boundary):
-//     Delta^T = U^T - S W^T                            (tcgen05, A negated)
-//     S <- gamma_63 S + (Delta^T diag(e^{G_63-G_j})) K (tcgen05, accumulate in TMEM)
+//     Delta^T = U^T - S W^T                         tcgen05, A negated
+//     S <- gamma_63 S + (Delta^T diag(e^{G_63-G_j} n_j)) K     tcgen05, in TMEM
 //   output ("GDN与线性注意力GPU并行实现" section 3.3: O_init = Q S plus a
 //   triangular-masked product):
-//     O^T = scale (S Q^T diag(gamma) + Delta^T P^T)    (tcgen05, two accumulators)
+//     O^T = scale (S Q^T diag(gamma m) + Delta^T P^T)           tcgen05
 //
-// Operand layouts (all 128-byte swizzled, verified against torch matmul):
-//   K, Q, V tiles arrive by TMA as [64 rows][64 cols] boxes; the same K tile
-//   serves as K-major A/B ([K;Q]K^T), MN-major A (K^T ...) and MN-major B
-//   (... K), so no transposed copy is made.  S, Delta^T, P and T' are written
-//   by threads in K-major form; W^T is written MN-major.
-// TMEM (512 columns): S [0,128), D1 [128,192), W^T [192,256), Delta^T [256,320),
-//   S Q^T [320,384), Delta^T P^T [384,448).  Thread t owns TMEM lane t.
+// The L2 norm of q and k ("FlashInfer GDN Prefill 完全指南", API table) enters
+// only as the per-row factors n and m above, applied in fp32: the same values
+// as normalising the rows first, without re-rounding them to bf16.
+//
+// Roles (384 threads, one work unit = (sequence, state head) at a time,
+// units taken longest first from an atomic counter):
+//   warp 0      TMA: K, Q tiles (2 stages) and V tile; unit scheduler
+//   warp 1      tcgen05 issue for the intra-chunk products (D1, W, U)
+//   warp 2      tcgen05 issue for the state chain (Delta, S Q^T, Delta P^T, S)
+//   warp 3      TMEM allocation
+//   warps 4-7   intra warpgroup: gates, A and P, T, W to shared memory,
+//               one chunk ahead of the state warpgroup
+//   warps 8-11  state warpgroup: Delta epilogue, state epilogue (next S
+//               operand, checkpoints, final state), output epilogue
+// Every wait is bounded; a timeout sets GDN_DEVICE_ERR_TIMEOUT, raises a
+// shared abort flag that every other wait polls, drains the CTA's in-flight
+// copies and tensor-core work, frees TMEM and returns.
 #include <cuda_bf16.h>
 
 #include "gdn_internal.cuh"
@@ -36,51 +45,95 @@
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 512;
+constexpr int kWgThreads = 128;     // state warpgroup
+constexpr int kIntraThreads = 256;  // two intra warpgroups
+constexpr uint32_t kBarIntra = 1, kBarState = 2;  // named barrier ids
 
-// Shared memory map (bytes from a 1024-aligned base).
-constexpr uint32_t kStageBytes = 49152;          // K_h0 | Q_h0 | K_h1 | Q_h1 | V_h0 | V_h1 (8 KB each)
-constexpr uint32_t kOffKQ = 0;                   // inside a stage
-constexpr uint32_t kOffV = 32768;                // inside a stage
-constexpr uint32_t kSmTp = 2 * kStageBytes;      // T diag(beta gamma), bf16 [64 i][64 j] K-major
-constexpr uint32_t kSmTpp = kSmTp + 8192;        // T diag(beta)
-constexpr uint32_t kSmP = kSmTpp + 8192;         // P, bf16 [64 i][64 j] K-major
-constexpr uint32_t kSmWb = kSmP + 8192;          // W^T bf16 MN-major B: [128 k rows][64 i]
-constexpr uint32_t kSmSb = kSmWb + 16384;        // S bf16 K-major: 2 halves of [128 v][64 k]
-constexpr uint32_t kSmDb = kSmSb + 32768;        // Delta^T bf16 K-major [128 v][64 j]; A fp32 before
-constexpr uint32_t kSmDtb = kSmDb + 16384;       // decayed Delta^T; T fp32 before
-constexpr uint32_t kSmSmall = kSmDtb + 16384;
-constexpr uint32_t kSmG = kSmSmall;              // float[64]
-constexpr uint32_t kSmGam = kSmG + 256;          // float[64]
-constexpr uint32_t kSmBeta = kSmGam + 256;       // float[64]
-constexpr uint32_t kSmBar = kSmBeta + 256;       // 3 x uint64 mbarriers: tma[0], tma[1], mma
-constexpr uint32_t kSmMisc = kSmBar + 32;        // tmem base, unit id, abort flag
-constexpr uint32_t kSmemBytes = kSmMisc + 32;
+// ---- shared memory map (bytes from a 1024-aligned base)
+constexpr uint32_t kKQ = 0;           // 2 stages x 32 KB: K_h0 | Q_h0 | K_h1 | Q_h1 (64 rows x 128 B each)
+constexpr uint32_t kKQStage = 32768;
+constexpr uint32_t kV = 65536;        // V_h0 | V_h1
+constexpr uint32_t kTp = 81920;       // T diag(beta gamma n) bf16 [64 i][64 j] K-major
+constexpr uint32_t kTpp = 90112;      // T diag(beta)
+constexpr uint32_t kPb = 98304;       // 2 x P bf16 [64 i][64 j] K-major
+constexpr uint32_t kWb = 114688;      // W^T bf16 as MN-major B: [128 k][64 i]
+constexpr uint32_t kSb = 131072;      // S bf16 K-major: 2 halves of [128 v][64 k]
+constexpr uint32_t kAbuf = 163840;    // A fp32 [64][kLd]
+constexpr uint32_t kTbuf = 181248;    // T fp32 [64][kLd]
+constexpr uint32_t kXs = 198656;      // inverse scratch: [2][16][20] then [32][36] fp32
+constexpr uint32_t kOutT = 205824;    // output tile bf16 [64 i][128 v]
+constexpr uint32_t kGbuf = 222208;    // 2 x 576 floats of per-row / per-column factors (see kG*)
+constexpr uint32_t kBars = 226816;    // 32 mbarriers
+constexpr uint32_t kRing = 227072;    // 2 unit descriptors
+constexpr uint32_t kMisc = 227200;    // tmem base, abort flag
+constexpr uint32_t kSmemBytes = 227264;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
+constexpr int kLd = 68;               // fp32 row stride of A and T (bank-conflict free rows)
 
-constexpr uint32_t kTmS = 0, kTmD1 = 128, kTmW = 192, kTmDelta = 256, kTmO1 = 320, kTmO2 = 384;
+// gbuf field offsets (floats), one 64-vector each, per chunk:
+//   G      running sum of log alpha            gamma  e^G
+//   beta   beta (0 on padded rows)             rn, rm 1/|k_j|, 1/|q_i| (1 without the L2 norm)
+//   cw     beta_j gamma_j rn_j (T' columns)    dec    e^{G_63 - G_j} rn_j (decayed Delta columns)
+//   orow   scale gamma_i rm_i (output rows)    ra     beta_i rn_i (A rows)
+constexpr int kGG = 0, kGGam = 64, kGBeta = 128, kGRn = 192, kGRm = 256, kGCw = 320, kGDec = 384, kGOr = 448,
+              kGRa = 512, kGFloats = 576;
+
+// ---- barriers
+enum {
+    B_KQ_FULL = 0, B_KQ_EMPTY = 2, B_V_FULL = 4, B_V_EMPTY = 5, B_D1_FULL = 6, B_D1_EMPTY = 7, B_T_FULL = 8,
+    B_WU_FULL = 9, B_WB_FULL = 10, B_SB_FULL = 12, B_DELTA_FULL = 14, B_DD_FULL = 16, B_S_FULL = 18,
+    B_O_EMPTY = 20, B_GATES_FULL = 22, B_GATES_EMPTY = 24, B_UNIT_FULL = 26, B_UNIT_EMPTY = 28,
+    B_DRAIN_I = 30, B_DRAIN_S = 31, B_COUNT = 32
+};
+
+// ---- TMEM columns
+constexpr uint32_t kTmS = 0, kTmDelta = 128 /* 2 x 64 */, kTmW = 256, kTmD1 = 320, kTmO1 = 384, kTmO2 = 448;
 constexpr uint32_t kTmCols = 512;
 
-constexpr uint32_t kIdescD1 = idesc_bf16_f32(128, 64);                       // [K;Q] K^T, S Q^T
-constexpr uint32_t kIdescWU = idesc_bf16_f32(128, 64, true, false);          // K^T T'^T, V^T T''^T
-constexpr uint32_t kIdescDelta = idesc_bf16_f32(128, 64, false, true, true); // -S W^T
-constexpr uint32_t kIdescO2 = idesc_bf16_f32(128, 64);                       // Delta^T P^T
-constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, true);          // Delta~^T K
+constexpr uint32_t kIdescD1 = idesc_bf16_f32(128, 64);
+constexpr uint32_t kIdescWU = idesc_bf16_f32(128, 64, true, false);
+constexpr uint32_t kIdescDelta = idesc_bf16_f32(128, 64, false, true, true);
+constexpr uint32_t kIdescO = idesc_bf16_f32(128, 64);
+constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, true);
 
-__device__ __forceinline__ void tmem_ld16_f(uint32_t taddr, float* out) {
-    uint32_t r[16];
-    tmem_ld16(taddr, r);
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                   "+r"(r[15])
-                 :
-                 : "memory");
-#pragma unroll
-    for (int j = 0; j < 16; ++j) out[j] = __uint_as_float(r[j]);
+constexpr long long kWaitCycles = 2000000000LL;  // about one second
+
+struct UnitInfo {
+    int32_t valid, seq, h, nC;
+    int32_t qh, kh, vh, flat0;
+    int64_t t0, L, srow, ckpt_base;
+};
+static_assert(sizeof(UnitInfo) <= 64, "unit descriptor slot");
+
+struct Ctx {
+    uint8_t* sm;
+    uint64_t* bars;
+    volatile int32_t* abort;
+    int32_t* status;
+};
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_bar(const Ctx& cx, int b, uint32_t parity) {
+    uint64_t* bar = cx.bars + b;
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 2000)) return true;
+        if (*cx.abort) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            atomicOr(cx.status, static_cast<int32_t>(GDN_DEVICE_ERR_TIMEOUT));
+            *cx.abort = 1;
+            return false;
+        }
+    }
 }
 
-// Write 8 floats as one bf16 16-byte chunk of a 128B-swizzled row.
+// Bounded wait used while draining (ignores the abort flag).
+__device__ __forceinline__ void drain_bar(const Ctx& cx, int b, uint32_t parity) {
+    if (!mbar_wait(cx.bars + b, parity, kWaitCycles)) atomicOr(cx.status, static_cast<int32_t>(GDN_DEVICE_ERR_TIMEOUT));
+}
+
 __device__ __forceinline__ void st_chunk_bf16(uint8_t* tile, uint32_t row, uint32_t chunk, const float* x) {
     uint4 v;
     v.x = pack_bf16x2(x[0], x[1]);
@@ -99,127 +152,183 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4& v, float* f) {
     }
 }
 
-// A row of 128 bf16 values held as two 64-column swizzled halves 16 KB apart
-// (the stage layout K_h0 | Q_h0 | K_h1 | Q_h1 puts K_h1 16 KB after K_h0).
-// Zero it when `zero`, else L2-normalise it in place when `norm`.
-__device__ __forceinline__ void fix_row(uint8_t* half0, uint32_t half_stride, uint32_t row, bool zero, bool norm) {
-    if (zero) {
-        const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-            *reinterpret_cast<uint4*>(half0 + (c >> 3) * half_stride + sw128_offset(row, c & 7)) = z;
-        return;
-    }
-    if (!norm) return;
-    float ss = 0.f;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        float f[8];
-        bf16x8_to_float(*reinterpret_cast<const uint4*>(half0 + (c >> 3) * half_stride + sw128_offset(row, c & 7)), f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
-    }
-    const float inv = rsqrtf(ss + 1e-6f);
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        uint8_t* p = half0 + (c >> 3) * half_stride + sw128_offset(row, c & 7);
-        float f[8];
-        bf16x8_to_float(*reinterpret_cast<const uint4*>(p), f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] *= inv;
-        st_chunk_bf16(half0 + (c >> 3) * half_stride, row, c & 7, f);
-    }
+__device__ __forceinline__ UnitInfo read_unit(const uint8_t* sm, int slot) {
+    return *reinterpret_cast<const UnitInfo*>(sm + kRing + slot * 64);
 }
 
-// T = (I + A)^-1 for a strictly lower 64 x 64 A (fp32, row-major): 16 x 16
-// diagonal blocks by forward substitution, then the block formula
-// T_ab = -T_aa A_ab T_bb at 16 and at 32 granularity.  Upper-triangular
-// storage of T is used as scratch and is garbage on return.
-__device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ T, int tid) {
-    if (tid < 64) {
-        const int o = (tid >> 4) * 16, col = tid & 15;
+// ===========================================================================
+// Triangular inverse T = (I + A)^-1 of a strictly lower 64 x 64 A (fp32,
+// rows of kLd floats), by the two intra warpgroups (256 threads):
+//   level 0: the four 16 x 16 diagonal blocks by forward substitution, one
+//            column per thread;
+//   level 1: T_ab = -T_aa A_ab T_bb for (a, b) = (1, 0), (3, 2);
+//   level 2: T_21 = -T_22 A_21 T_11 on 32 x 32 blocks.
+// On return T holds the lower triangle including the diagonal; the upper
+// triangle is unspecified.
+// ===========================================================================
+__device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ T, float* __restrict__ X1,
+                               float* __restrict__ X2, int t) {
+    if (t < 64) {
+        const int o = (t >> 4) * 16, col = t & 15;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-            float acc = (r == col) ? 1.f : 0.f;
+            const float* arow = A + (o + r) * kLd + o;
+            float acc0 = (r == col) ? 1.f : 0.f, acc1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < r; ++m) acc -= A[(o + r) * 64 + o + m] * x[m];
-            x[r] = (r < col) ? 0.f : acc;
+            for (int m = 0; m + 1 < r; m += 2) {
+                acc0 -= arow[m] * x[m];
+                acc1 -= arow[m + 1] * x[m + 1];
+            }
+            if (r & 1) acc0 -= arow[r - 1] * x[r - 1];
+            x[r] = (r < col) ? 0.f : acc0 + acc1;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) T[(o + r) * 64 + o + col] = x[r];
+        for (int r = 0; r < 16; ++r) T[(o + r) * kLd + o + col] = x[r];
+    } else if (t < 128) {
+        // zero the upper blocks (0,1) and (2,3) so that T_11, T_22 read as triangular
+        const int idx = t - 64;            // 64 threads x 8 values = 2 blocks x 256
+        const int blk = idx >> 5, r = (idx & 31) >> 1, c0 = (idx & 1) * 8;
+        const int ro = blk * 32, co = blk * 32 + 16;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) T[(ro + r) * kLd + co + c0 + q] = 0.f;
     }
-    __syncthreads();
-    {   // level 1, step 1: X_ab = A_ab T_bb for (a, b) = (1, 0), (3, 2); kept at block (b, a)
-        const int pr = tid >> 6, a = 2 * pr + 1, b = 2 * pr;
-        const int idx = tid & 63, r = idx >> 2, c0 = (idx & 3) * 4;
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
+    named_bar_sync(kBarIntra, kIntraThreads);
+    {   // level 1: 2 blocks x 16 x 16 outputs, 2 per thread
+        const int pr = t >> 7, a = 2 * pr + 1, b = 2 * pr;
+        const int idx = t & 127, r = idx >> 3, c0 = (idx & 7) * 2;
+        float x0 = 0.f, x1 = 0.f;
+        const float* arow = A + (16 * a + r) * kLd + 16 * b;
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
-            const float av = A[(16 * a + r) * 64 + 16 * b + m];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) x[q] += av * T[(16 * b + m) * 64 + 16 * b + c0 + q];
+            const float av = arow[m];
+            const float2 tv = *reinterpret_cast<const float2*>(T + (16 * b + m) * kLd + 16 * b + c0);
+            x0 += av * tv.x;
+            x1 += av * tv.y;
         }
-        __syncthreads();
+        float* xs = X1 + pr * 16 * 20;
+        *reinterpret_cast<float2*>(xs + r * 20 + c0) = make_float2(x0, x1);
+        named_bar_sync(kBarIntra, kIntraThreads);
+        float y0 = 0.f, y1 = 0.f;
+        const float* trow = T + (16 * a + r) * kLd + 16 * a;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) T[(16 * b + r) * 64 + 16 * a + c0 + q] = x[q];
-        __syncthreads();
-        // step 2: T_ab = -T_aa X_ab
+        for (int m = 0; m < 16; ++m) {
+            const float tv = trow[m];  // zero above the diagonal
+            const float2 xv = *reinterpret_cast<const float2*>(xs + m * 20 + c0);
+            y0 += tv * xv.x;
+            y1 += tv * xv.y;
+        }
+        *reinterpret_cast<float2*>(T + (16 * a + r) * kLd + 16 * b + c0) = make_float2(-y0, -y1);
+    }
+    named_bar_sync(kBarIntra, kIntraThreads);
+    {   // level 2: 32 x 32 outputs, 4 per thread
+        const int r = t >> 3, c0 = (t & 7) * 4;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        const float* arow = A + (32 + r) * kLd;
+#pragma unroll 4
+        for (int m = c0; m < 32; ++m) {  // T_11[m][c] = 0 for m < c
+            const float av = arow[m];
+            const float4 tv = *reinterpret_cast<const float4*>(T + m * kLd + c0);
+            x[0] += av * tv.x;
+            x[1] += av * tv.y;
+            x[2] += av * tv.z;
+            x[3] += av * tv.w;
+        }
+        *reinterpret_cast<float4*>(X2 + r * 36 + c0) = make_float4(x[0], x[1], x[2], x[3]);
+        named_bar_sync(kBarIntra, kIntraThreads);
         float y[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int m = 0; m <= r; ++m) {
-            const float tv = T[(16 * a + r) * 64 + 16 * a + m];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) y[q] += tv * T[(16 * b + m) * 64 + 16 * a + c0 + q];
+        const float* trow = T + (32 + r) * kLd + 32;
+#pragma unroll 4
+        for (int m = 0; m <= r; ++m) {  // T_22[r][m] = 0 for m > r
+            const float tv = trow[m];
+            const float4 xv = *reinterpret_cast<const float4*>(X2 + m * 36 + c0);
+            y[0] += tv * xv.x;
+            y[1] += tv * xv.y;
+            y[2] += tv * xv.z;
+            y[3] += tv * xv.w;
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) T[(16 * a + r) * 64 + 16 * b + c0 + q] = -y[q];
+        *reinterpret_cast<float4*>(T + (32 + r) * kLd + c0) = make_float4(-y[0], -y[1], -y[2], -y[3]);
     }
-    __syncthreads();
-    {   // level 2: T_21 = -T_22 A_21 T_11 on 32 x 32 blocks; X kept at rows 0..31, cols 32..63
-        const int r = tid >> 2, c0 = (tid & 3) * 8;
-        float x[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] = 0.f;
-        for (int m = 0; m < 32; ++m) {
-            const float av = A[(32 + r) * 64 + m];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float tv = (m >= c0 + q) ? T[m * 64 + c0 + q] : 0.f;  // T_11 is lower triangular
-                x[q] += av * tv;
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) T[r * 64 + 32 + c0 + q] = x[q];
-        __syncthreads();
-        float y[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) y[q] = 0.f;
-        for (int m = 0; m <= r; ++m) {
-            const float tv = T[(32 + r) * 64 + 32 + m];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) y[q] += tv * T[m * 64 + 32 + c0 + q];
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) T[(32 + r) * 64 + c0 + q] = -y[q];
-    }
-    __syncthreads();
+    named_bar_sync(kBarIntra, kIntraThreads);
 }
 
-struct Bars {
-    uint64_t* tma[2];
-    uint64_t* mma;
+// ===========================================================================
+// Gates of one chunk (one warp; lane l owns rows 2l, 2l+1).  load_gates issues
+// the global loads early (alpha = 1, beta = 0 on padded rows); compute_gates
+// forms G = running sum of log alpha, gamma = e^G and the factor vectors as
+// they are without the L2 norm (rn = rm = 1).
+// ===========================================================================
+struct GatePrefetch {
+    float a0, a1, b0, b1;
 };
 
-__device__ __forceinline__ void issue_chunk_loads(uint8_t* stage, uint64_t* bar, const CUtensorMap* tq,
-                                                  const CUtensorMap* tk, const CUtensorMap* tv, int qh, int kh, int vh,
-                                                  int32_t t) {
-    mbar_arrive_expect_tx(bar, kStageBytes);
-    tma_load_3d(stage + kOffKQ + 0, tk, bar, 0, kh, t);
-    tma_load_3d(stage + kOffKQ + 8192, tq, bar, 0, qh, t);
-    tma_load_3d(stage + kOffKQ + 16384, tk, bar, 64, kh, t);
-    tma_load_3d(stage + kOffKQ + 24576, tq, bar, 64, qh, t);
-    tma_load_3d(stage + kOffV + 0, tv, bar, 0, vh, t);
-    tma_load_3d(stage + kOffV + 8192, tv, bar, 64, vh, t);
+__device__ __forceinline__ GatePrefetch load_gates(const ChunkParams& p, int64_t tc, int32_t Lc, int32_t h, int lane) {
+    GatePrefetch g{1.f, 1.f, 0.f, 0.f};
+    const int r0 = 2 * lane, r1 = r0 + 1;
+    if (r0 < Lc) {
+        const size_t gi = static_cast<size_t>(tc + r0) * p.H + h;
+        g.a0 = p.g ? p.g[gi] : 1.f;
+        g.b0 = p.beta ? p.beta[gi] : 1.f;
+    }
+    if (r1 < Lc) {
+        const size_t gi = static_cast<size_t>(tc + r1) * p.H + h;
+        g.a1 = p.g ? p.g[gi] : 1.f;
+        g.b1 = p.beta ? p.beta[gi] : 1.f;
+    }
+    return g;
+}
+
+__device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, float scale, int lane) {
+    const int r0 = 2 * lane, r1 = r0 + 1;
+    const float la0 = __logf(g.a0), la1 = __logf(g.a1);
+    float incl = la0 + la1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const float G1 = incl, G0 = incl - la1;
+    const float G63 = __shfl_sync(0xffffffffu, incl, 31);
+    const float e0 = __expf(G0), e1 = __expf(G1);
+    gb[kGG + r0] = G0;
+    gb[kGG + r1] = G1;
+    gb[kGGam + r0] = e0;
+    gb[kGGam + r1] = e1;
+    gb[kGBeta + r0] = g.b0;
+    gb[kGBeta + r1] = g.b1;
+    gb[kGRn + r0] = 1.f;
+    gb[kGRn + r1] = 1.f;
+    gb[kGRm + r0] = 1.f;
+    gb[kGRm + r1] = 1.f;
+    gb[kGCw + r0] = g.b0 * e0;
+    gb[kGCw + r1] = g.b1 * e1;
+    gb[kGDec + r0] = __expf(G63 - G0);
+    gb[kGDec + r1] = __expf(G63 - G1);
+    gb[kGOr + r0] = scale * e0;
+    gb[kGOr + r1] = scale * e1;
+    gb[kGRa + r0] = g.b0;
+    gb[kGRa + r1] = g.b1;
+}
+
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]) {
+    tmem_ld16(taddr, r);
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15])
+                 :
+                 : "memory");
+}
+
+__device__ __forceinline__ void lds16(const float* src, float* x) {
+#pragma unroll
+    for (int q = 0; q < 16; q += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src + q);
+        x[q] = v.x;
+        x[q + 1] = v.y;
+        x[q + 2] = v.z;
+        x[q + 3] = v.w;
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -227,47 +336,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, warp = tid >> 5;
-
-    float* sG = reinterpret_cast<float*>(sm + kSmG);
-    float* sGam = reinterpret_cast<float*>(sm + kSmGam);
-    float* sBeta = reinterpret_cast<float*>(sm + kSmBeta);
-    Bars bars;
-    bars.tma[0] = reinterpret_cast<uint64_t*>(sm + kSmBar);
-    bars.tma[1] = bars.tma[0] + 1;
-    bars.mma = bars.tma[0] + 2;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kSmMisc);
-    int32_t* s_unit = reinterpret_cast<int32_t*>(sm + kSmMisc + 4);
-    int32_t* s_abort = reinterpret_cast<int32_t*>(sm + kSmMisc + 8);
-    uint8_t* stage[2] = {sm, sm + kStageBytes};
-    uint8_t* sTp = sm + kSmTp;
-    uint8_t* sTpp = sm + kSmTpp;
-    uint8_t* sP = sm + kSmP;
-    uint8_t* sWb = sm + kSmWb;
-    uint8_t* sSb = sm + kSmSb;
-    uint8_t* sDb = sm + kSmDb;
-    uint8_t* sDtb = sm + kSmDtb;
-    float* sA = reinterpret_cast<float*>(sm + kSmDb);   // aliases Delta^T (dead by then)
-    float* sT = reinterpret_cast<float*>(sm + kSmDtb);  // aliases decayed Delta^T
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    Ctx cx;
+    cx.sm = sm;
+    cx.bars = reinterpret_cast<uint64_t*>(sm + kBars);
+    cx.abort = reinterpret_cast<volatile int32_t*>(sm + kMisc + 4);
+    cx.status = p.status;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kMisc);
 
     // Bad input flagged by the prepare kernel: every thread sees one copy of the word.
-    if (tid == 0) *s_abort = *reinterpret_cast<volatile int32_t*>(p.status);
+    if (tid == 0) *cx.abort = *reinterpret_cast<volatile int32_t*>(p.status);
     __syncthreads();
-    if (*reinterpret_cast<volatile int32_t*>(s_abort) != 0) return;
+    if (*cx.abort != 0) return;
     __syncthreads();
+
     if (tid == 0) {
-        mbar_init(bars.tma[0], 1);
-        mbar_init(bars.tma[1], 1);
-        mbar_init(bars.mma, 1);
+        for (int b = 0; b < B_COUNT; ++b) mbar_init(cx.bars + b, 1);
+        mbar_init(cx.bars + B_UNIT_EMPTY + 0, 5);
+        mbar_init(cx.bars + B_UNIT_EMPTY + 1, 5);
         fence_mbar_init();
-        *s_abort = 0;
         if (p.has_tokens) {
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
         }
     }
-    if (warp == 0) {
+    for (uint32_t off = tid * 16; off < 32768; off += kThreads * 16)  // T', T'' and both P buffers
+        *reinterpret_cast<uint4*>(sm + kTp + off) = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (warp == 3) {
         tmem_alloc(s_tmem, kTmCols);
         tmem_relinquish();
     }
@@ -275,391 +372,570 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tm_row = tmem + lane_base;  // this thread's TMEM lane, column 0
-
-    uint32_t tma_phase[2] = {0u, 0u};
-    uint32_t mma_phase = 0u;
-    int pending[2] = {0, 0};  // TMA loads issued and not yet waited on (thread 0's view)
     const int32_t H = p.H;
     const int64_t units = static_cast<int64_t>(p.num_seqs) * H;
-    bool abort = false;
 
-    auto fail = [&](void) {
-        atomicOr(p.status, static_cast<int32_t>(GDN_DEVICE_ERR_TIMEOUT));
-        atomicExch(s_abort, 1);
-    };
-    auto wait_mma = [&](void) {
-        if (!mbar_wait(bars.mma, mma_phase & 1u)) fail();
-        ++mma_phase;
-        tc_fence_after();
-    };
-
-    for (;;) {
-        if (tid == 0) *s_unit = atomicAdd(p.counter, 1);
-        __syncthreads();
-        const int64_t u = *s_unit;
-        const bool stop = u >= units || *reinterpret_cast<volatile int32_t*>(s_abort) != 0;
-        __syncthreads();  // everyone has read s_unit before thread 0 may overwrite it
-        if (stop) break;
-        const int32_t seq = p.seq_order[u / H];
-        const int32_t h = static_cast<int32_t>(u % H);
-        const int64_t t0 = load_index(p.cu_seqlens, p.cu_i64, seq);
-        const int64_t L = load_index(p.cu_seqlens, p.cu_i64, seq + 1) - t0;
-        const int32_t nC = static_cast<int32_t>((L + kChunk - 1) / kChunk);
-        const int qh = h / (H / p.hq), kh = h / (H / p.hk), vh = h / (H / p.hv);
-        const int64_t srow = p.state_indices ? load_index(p.state_indices, p.idx_i64, seq) : seq;
-        const size_t state_off = (static_cast<size_t>(srow) * H + h) * kHead * kHead;
-        const int32_t flat0 = p.chunk_offsets[seq];
-
-        // ---- start loads of the first two chunks
-        if (tid == 0) {
-            for (int c = 0; c < 2 && c < nC; ++c) {
-                issue_chunk_loads(stage[c], bars.tma[c], &tm_q, &tm_k, &tm_v, qh, kh, vh,
-                                  static_cast<int32_t>(t0 + c * kChunk));
-                pending[c] = 1;
+    if (warp == 0) {
+        // ================= TMA producer and unit scheduler =================
+        if (lane == 0) {
+            uint32_t n = 0, u = 0;
+            int issued_kq[2] = {-1, -1};
+            int issued_v = -1;
+            for (;;) {
+                const int64_t uid = atomicAdd(p.counter, 1);
+                const int slot = u & 1;
+                if (u >= 2 && !wait_bar(cx, B_UNIT_EMPTY + slot, ((u - 2) >> 1) & 1)) break;
+                UnitInfo info;
+                info.valid = uid < units ? 1 : 0;
+                int32_t nC = 0;
+                if (info.valid) {
+                    const int32_t seq = p.seq_order[uid / H];
+                    const int32_t h = static_cast<int32_t>(uid % H);
+                    info.seq = seq;
+                    info.h = h;
+                    info.t0 = load_index(p.cu_seqlens, p.cu_i64, seq);
+                    info.L = load_index(p.cu_seqlens, p.cu_i64, seq + 1) - info.t0;
+                    nC = static_cast<int32_t>((info.L + kChunk - 1) / kChunk);
+                    info.nC = nC;
+                    info.qh = h / (H / p.hq);
+                    info.kh = h / (H / p.hk);
+                    info.vh = h / (H / p.hv);
+                    info.flat0 = p.chunk_offsets[seq];
+                    info.srow = p.state_indices ? load_index(p.state_indices, p.idx_i64, seq) : seq;
+                    info.ckpt_base = p.ckpt_n > 0 ? load_index(p.ckpt_cu_starts, p.ckpt_i64, seq) : 0;
+                }
+                *reinterpret_cast<UnitInfo*>(sm + kRing + slot * 64) = info;
+                mbar_arrive(cx.bars + B_UNIT_FULL + slot);
+                ++u;
+                if (!info.valid) break;
+                bool ok = true;
+                for (int32_t c = 0; c < nC && ok; ++c, ++n) {
+                    const int s = n & 1;
+                    const int32_t t = static_cast<int32_t>(info.t0 + static_cast<int64_t>(c) * kChunk);
+                    if (n >= 2 && !(ok = wait_bar(cx, B_KQ_EMPTY + s, ((n - 2) >> 1) & 1))) break;
+                    uint8_t* st = sm + kKQ + s * kKQStage;
+                    uint64_t* fb = cx.bars + B_KQ_FULL + s;
+                    mbar_arrive_expect_tx(fb, kKQStage);
+                    tma_load_3d(st + 0, &tm_k, fb, 0, info.kh, t);
+                    tma_load_3d(st + 8192, &tm_q, fb, 0, info.qh, t);
+                    tma_load_3d(st + 16384, &tm_k, fb, 64, info.kh, t);
+                    tma_load_3d(st + 24576, &tm_q, fb, 64, info.qh, t);
+                    issued_kq[s] = static_cast<int>(n);
+                    if (n >= 1 && !(ok = wait_bar(cx, B_V_EMPTY, (n - 1) & 1))) break;
+                    uint64_t* vb = cx.bars + B_V_FULL;
+                    mbar_arrive_expect_tx(vb, 16384);
+                    tma_load_3d(sm + kV, &tm_v, vb, 0, info.vh, t);
+                    tma_load_3d(sm + kV + 8192, &tm_v, vb, 64, info.vh, t);
+                    issued_v = static_cast<int>(n);
+                }
+                if (!ok) break;
+            }
+            // drain: every issued load has landed before the CTA may exit
+            for (int s = 0; s < 2; ++s)
+                if (issued_kq[s] >= 0) drain_bar(cx, B_KQ_FULL + s, (issued_kq[s] >> 1) & 1);
+            if (issued_v >= 0) drain_bar(cx, B_V_FULL, issued_v & 1);
+        }
+    } else if (warp == 1) {
+        // ================= tcgen05 issue: D1, W, U =================
+        if (lane == 0) {
+            uint32_t n = 0, u = 0;
+            bool ok = true;
+            for (; ok;) {
+                const int slot = u & 1;
+                if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
+                const UnitInfo info = read_unit(sm, slot);
+                mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
+                ++u;
+                if (!info.valid) break;
+                for (int32_t c = 0; c < info.nC; ++c, ++n) {
+                    const int s = n & 1;
+                    if (!(ok = wait_bar(cx, B_KQ_FULL + s, (n >> 1) & 1))) break;
+                    if (n >= 1 && !(ok = wait_bar(cx, B_D1_EMPTY, (n - 1) & 1))) break;
+                    tc_fence_after();
+                    const uint32_t kq = smem_u32(sm + kKQ + s * kKQStage);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16_ss(tmem + kTmD1, desc_kmajor_sw128(kq + off), desc_kmajor_sw128(kq + off), kIdescD1,
+                                    ks > 0);
+                    }
+                    mma_commit(cx.bars + B_D1_FULL);
+                    if (!(ok = wait_bar(cx, B_T_FULL, n & 1))) break;
+                    if (!(ok = wait_bar(cx, B_V_FULL, n & 1))) break;
+                    if (n >= 2 && !(ok = wait_bar(cx, B_S_FULL + s, ((n - 2) >> 1) & 1))) break;
+                    tc_fence_after();
+                    const uint32_t vv = smem_u32(sm + kV);
+                    const uint32_t tp = smem_u32(sm + kTp), tpp = smem_u32(sm + kTpp);
+                    const uint32_t dbuf = tmem + kTmDelta + s * 64;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        mma_bf16_ss(tmem + kTmW, desc_mnmajor_sw128(kq + ks * 2048, 16384),
+                                    desc_kmajor_sw128(tp + ks * 32), kIdescWU, ks > 0);
+                        mma_bf16_ss(dbuf, desc_mnmajor_sw128(vv + ks * 2048, 8192), desc_kmajor_sw128(tpp + ks * 32),
+                                    kIdescWU, ks > 0);
+                    }
+                    mma_commit(cx.bars + B_WU_FULL);
+                    mma_commit(cx.bars + B_V_EMPTY);
+                }
+            }
+            mma_commit(cx.bars + B_DRAIN_I);
+            drain_bar(cx, B_DRAIN_I, 0);
+        }
+    } else if (warp == 2) {
+        // ================= tcgen05 issue: Delta, S Q^T, Delta P^T, S =================
+        if (lane == 0) {
+            uint32_t n = 0, u = 0;
+            bool ok = true;
+            for (; ok;) {
+                const int slot = u & 1;
+                if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
+                const UnitInfo info = read_unit(sm, slot);
+                mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
+                ++u;
+                if (!info.valid) break;
+                for (int32_t c = 0; c < info.nC; ++c, ++n) {
+                    const int s = n & 1;
+                    const uint32_t ph = (n >> 1) & 1;
+                    if (!(ok = wait_bar(cx, B_WB_FULL + s, ph))) break;
+                    if (!(ok = wait_bar(cx, B_SB_FULL + s, ph))) break;
+                    if (!(ok = wait_bar(cx, B_KQ_FULL + s, ph))) break;
+                    tc_fence_after();
+                    const uint32_t kq = smem_u32(sm + kKQ + s * kKQStage);
+                    const uint32_t sb = smem_u32(sm + kSb), wb = smem_u32(sm + kWb);
+                    const uint32_t dbuf = tmem + kTmDelta + s * 64;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t aoff = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16_ss(dbuf, desc_kmajor_sw128(sb + aoff), desc_mnmajor_sw128(wb + ks * 2048, 8192),
+                                    kIdescDelta, 1);
+                    }
+                    mma_commit(cx.bars + B_DELTA_FULL + s);
+                    if (n >= 1 && !(ok = wait_bar(cx, B_O_EMPTY + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16_ss(tmem + kTmO1, desc_kmajor_sw128(sb + off), desc_kmajor_sw128(kq + 8192 + off),
+                                    kIdescO, ks > 0);
+                    }
+                    if (!(ok = wait_bar(cx, B_DD_FULL + s, ph))) break;
+                    tc_fence_after();
+                    const uint32_t pb = smem_u32(sm + kPb + s * 8192);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        mma_bf16_ts(tmem + kTmO2, dbuf + ks * 8, desc_kmajor_sw128(pb + ks * 32), kIdescO, ks > 0);
+                        mma_bf16_ts(tmem + kTmS, dbuf + 32 + ks * 8, desc_mnmajor_sw128(kq + ks * 2048, 16384),
+                                    kIdescS, 1);
+                    }
+                    mma_commit(cx.bars + B_S_FULL + s);
+                    mma_commit(cx.bars + B_KQ_EMPTY + s);
+                }
+            }
+            mma_commit(cx.bars + B_DRAIN_S);
+            drain_bar(cx, B_DRAIN_S, 0);
+        }
+    } else if (warp == 3) {
+        // ================= gates warp: G, gamma, beta and factor vectors per chunk =================
+        uint32_t n = 0, u = 0;
+        bool ok = true;
+        for (; ok;) {
+            const int slot = u & 1;
+            if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
+            const UnitInfo info = read_unit(sm, slot);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
+            ++u;
+            if (!info.valid) break;
+            GatePrefetch gpf{1.f, 1.f, 0.f, 0.f};
+            if (info.nC > 0)
+                gpf = load_gates(p, info.t0, info.L < kChunk ? static_cast<int32_t>(info.L) : kChunk, info.h, lane);
+            for (int32_t c = 0; c < info.nC; ++c, ++n) {
+                const int gs = n & 1;
+                const GatePrefetch cur = gpf;
+                if (c + 1 < info.nC) {
+                    const int64_t rem1 = info.L - static_cast<int64_t>(c + 1) * kChunk;
+                    gpf = load_gates(p, info.t0 + static_cast<int64_t>(c + 1) * kChunk,
+                                     rem1 < kChunk ? static_cast<int32_t>(rem1) : kChunk, info.h, lane);
+                }
+                if (n >= 2 && !(ok = wait_bar(cx, B_GATES_EMPTY + gs, ((n - 2) >> 1) & 1))) break;
+                compute_gates(cur, reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats, p.scale, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cx.bars + B_GATES_FULL + gs);
             }
         }
-        // ---- initial state: row v = tid into TMEM (fp32) and smem (bf16, K-major)
-        {
-            const float* src = p.initial_state ? p.initial_state + state_off + static_cast<size_t>(tid) * kHead
-                                               : nullptr;
-            float* dst_final = (nC == 0 && p.output_state)
-                                   ? p.output_state + state_off + static_cast<size_t>(tid) * kHead
-                                   : nullptr;
-#pragma unroll 1
-            for (int c0 = 0; c0 < kHead; c0 += 16) {
-                float x[16];
-                if (src) {
+    } else if (warp >= 4 && warp < 12) {
+        // ================= intra warpgroups (two; each TMEM lane row split in column halves) =================
+        const int it = tid - 128;                      // 0..255
+        const int wq = warp & 3;                       // TMEM lane quarter
+        const int hh = (warp - 4) >> 2;                // column half
+        const int r = wq * 32 + lane;                  // TMEM lane: A row r (< 64) or P row r - 64
+        const uint32_t tm_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const int imax = (wq & 1) * 32 + 31;           // last A or P row of this warp
+        float* Abuf = reinterpret_cast<float*>(sm + kAbuf);
+        float* Tbuf = reinterpret_cast<float*>(sm + kTbuf);
+        float* X1 = reinterpret_cast<float*>(sm + kXs);
+        float* X2 = X1 + 2 * 16 * 20;
+        uint32_t n = 0, u = 0;
+        bool ok = true;
+        for (; ok;) {
+            const int slot = u & 1;
+            if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
+            const UnitInfo info = read_unit(sm, slot);
+            named_bar_sync(kBarIntra, kIntraThreads);
+            if (it == 0) mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
+            ++u;
+            if (!info.valid) break;
+            for (int32_t c = 0; c < info.nC && ok; ++c, ++n) {
+                const int s = n & 1;
+                const int64_t rem = info.L - static_cast<int64_t>(c) * kChunk;
+                const int32_t Lc = rem < kChunk ? static_cast<int32_t>(rem) : kChunk;
+                float* gb = reinterpret_cast<float*>(sm + kGbuf) + s * kGFloats;
+                uint8_t* kqs = sm + kKQ + s * kKQStage;
+                if (!(ok = wait_bar(cx, B_GATES_FULL + s, (n >> 1) & 1))) break;
+                if (!(ok = wait_bar(cx, B_KQ_FULL + s, (n >> 1) & 1))) break;
+                // q norms from the Q tile (rows i = r - 64)
+                if (p.l2norm && hh == 0 && r >= 64) {
+                    const int i = r - 64;
+                    float ss = 0.f;
+#pragma unroll 4
+                    for (int cch = 0; cch < 16; ++cch) {
+                        float f[8];
+                        bf16x8_to_float(*reinterpret_cast<const uint4*>(kqs + 8192 + (cch >> 3) * 16384 +
+                                                                        sw128_offset(i, cch & 7)), f);
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        const float4 f = *reinterpret_cast<const float4*>(src + c0 + j);
-                        x[j] = f.x; x[j + 1] = f.y; x[j + 2] = f.z; x[j + 3] = f.w;
+                        for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
                     }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) x[j] = 0.f;
+                    gb[kGRm + i] = i < Lc ? rsqrtf(ss + 1e-6f) : 0.f;
                 }
-                if (dst_final) {
-#pragma unroll
-                    for (int j = 0; j < 16; j += 4)
-                        *reinterpret_cast<float4*>(dst_final + c0 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
-                }
-                if (nC > 0) {
-                    uint32_t r[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(x[j]);
-                    tmem_st16(tm_row + kTmS + c0, r);
-                    uint8_t* half = sSb + (c0 >> 6) * 16384;
-                    st_chunk_bf16(half, tid, (c0 & 63) >> 3, x);
-                    st_chunk_bf16(half, tid, ((c0 & 63) >> 3) + 1, x + 8);
-                }
-            }
-            if (nC > 0) tmem_wait_st();
-        }
-        if (nC == 0) continue;  // zero-length sequence: state passed through
-
-        for (int32_t c = 0; c < nC && !abort; ++c) {
-            const int s = c & 1;
-            uint8_t* st = stage[s];
-            const int64_t tc = t0 + static_cast<int64_t>(c) * kChunk;
-            const int32_t Lc = static_cast<int32_t>(L - static_cast<int64_t>(c) * kChunk < kChunk
-                                                        ? L - static_cast<int64_t>(c) * kChunk
-                                                        : kChunk);
-            // ---- P1: gates; masking and L2 norm of the staged tiles; MMA D1 and S Q^T
-            if (tid < kChunk) {
-                const int r = tid;
-                float la = 0.f, b = 0.f;
-                if (r < Lc) {
-                    const size_t gi = static_cast<size_t>(tc + r) * H + h;
-                    la = p.g ? logf(p.g[gi]) : 0.f;
-                    b = p.beta ? p.beta[gi] : 1.f;
-                }
-                float run = la;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, run, o);
-                    if ((tid & 31) >= o) run += y;
-                }
-                sG[r] = run;
-                sBeta[r] = b;
-            }
-            __syncthreads();
-            if (tid >= 32 && tid < kChunk) sG[tid] += sG[31];
-            __syncthreads();
-            if (tid < kChunk) sGam[tid] = expf(sG[tid]);
-
-            if (!mbar_wait(bars.tma[s], tma_phase[s] & 1u)) fail();
-            ++tma_phase[s];
-            if (tid == 0) pending[s] = 0;
-            if (tid < kChunk) {
-                const int r = tid;
-                fix_row(st + kOffKQ, 16384, r, r >= Lc, p.l2norm != 0);   // K row
-                if (r >= Lc) fix_row(st + kOffV, 8192, r, true, false);  // V row
-            } else {
-                const int r = tid - kChunk;
-                fix_row(st + kOffKQ + 8192, 16384, r, r >= Lc, p.l2norm != 0);  // Q row
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            abort = *reinterpret_cast<volatile int32_t*>(s_abort) != 0;
-            if (abort) break;
-            if (tid == 0) {
+                // P buffer s is free once O2 of chunk n-2 has completed
+                if (n >= 2 && !(ok = wait_bar(cx, B_S_FULL + s, ((n - 2) >> 1) & 1))) break;
+                if (!(ok = wait_bar(cx, B_D1_FULL, n & 1))) break;
                 tc_fence_after();
-                const uint32_t kq = smem_u32(st + kOffKQ);
-                const uint32_t sb = smem_u32(sSb);
+                if (p.l2norm) {
+                    // k norms from the diagonal of K K^T (lanes 0..63)
+                    if (hh == 0 && r < 64) {
+                        uint32_t rr[32];
+                        tmem_ld32_wait(tm_lane + kTmD1 + 32 * wq, rr);
+                        float kk = 0.f;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    // [K; Q] (128 rows) x K^T (64 rows)
-                    mma_bf16_ss(tmem + kTmD1, desc_kmajor_sw128(kq + off), desc_kmajor_sw128(kq + off), kIdescD1,
-                                ks > 0);
-                    // S (128 rows v) x Q^T (64 rows i)
-                    mma_bf16_ss(tmem + kTmO1, desc_kmajor_sw128(sb + off), desc_kmajor_sw128(kq + 8192 + off),
-                                kIdescD1, ks > 0);
-                }
-                mma_commit(bars.mma);
-            }
-            __syncwarp();
-            wait_mma();
-
-            // ---- P2: A (strictly lower, beta and decay) and P (causal, decay)
-            {
-                const int i = tid & 63;
-                const float Gi = sG[i];
-                const float bi = sBeta[i];
-                if (tid < kChunk) {
-#pragma unroll 1
-                    for (int j0 = 0; j0 < kChunk; j0 += 16) {
-                        float d[16];
-                        tmem_ld16_f(tm_row + kTmD1 + j0, d);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int jj = j0 + j;
-                            d[j] = (jj < i) ? bi * expf(Gi - sG[jj]) * d[j] : 0.f;
+                        for (int j = 0; j < 32; ++j) kk = (j == lane) ? __uint_as_float(rr[j]) : kk;
+                        gb[kGRn + r] = r < Lc ? rsqrtf(kk + 1e-6f) : 0.f;
+                    }
+                    named_bar_sync(kBarIntra, kIntraThreads);
+                    // factor vectors that depend on the norms
+                    if (hh == 0) {
+                        if (r < 64) {
+                            const float rn = gb[kGRn + r], b = gb[kGBeta + r];
+                            gb[kGCw + r] = b * gb[kGGam + r] * rn;
+                            gb[kGDec + r] *= rn;
+                            gb[kGRa + r] = b * rn;
+                        } else {
+                            const int i = r - 64;
+                            gb[kGOr + i] = p.scale * gb[kGGam + i] * gb[kGRm + i];
                         }
-#pragma unroll
-                        for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4*>(sA + i * 64 + j0 + j) = make_float4(d[j], d[j + 1], d[j + 2], d[j + 3]);
                     }
-                } else {
+                    named_bar_sync(kBarIntra, kIntraThreads);
+                }
+                // A rows (lanes 0..63) and P rows (lanes 64..127), this warp's 32 columns, 16 per step;
+                // blocks entirely above the diagonal are skipped (A's upper part is never read, P's stays zero)
+                {
+                    const bool arow = r < 64;
+                    const int i = r & 63;
+                    const float Gi = gb[kGG + i];
+                    const float rf = arow ? gb[kGRa + i] : gb[kGRm + i];
+                    uint8_t* pb = sm + kPb + s * 8192;
 #pragma unroll 1
-                    for (int j0 = 0; j0 < kChunk; j0 += 16) {
-                        float d[16];
-                        tmem_ld16_f(tm_row + kTmD1 + j0, d);
+                    for (int jb = 32 * hh; jb < 32 * hh + 32; jb += 16) {
+                        if (jb > imax) break;  // warp-uniform
+                        uint32_t rr[16];
+                        tmem_ld16_wait(tm_lane + kTmD1 + jb, rr);
+                        float gj[16], cj[16], x[16];
+                        lds16(gb + kGG + jb, gj);
+                        lds16(gb + kGRn + jb, cj);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int jj = j0 + j;
-                            d[j] = (jj <= i) ? expf(Gi - sG[jj]) * d[j] : 0.f;
+                        for (int q = 0; q < 16; ++q) {
+                            const int j = jb + q;
+                            const bool keep = arow ? (j < i) : (j <= i);
+                            x[q] = keep ? rf * __expf(Gi - gj[q]) * cj[q] * __uint_as_float(rr[q]) : 0.f;
                         }
-                        st_chunk_bf16(sP, i, j0 >> 3, d);
-                        st_chunk_bf16(sP, i, (j0 >> 3) + 1, d + 8);
-                    }
-                }
-            }
-            __syncthreads();
-
-            // ---- P3: T = (I + A)^-1; T' = T diag(beta gamma), T'' = T diag(beta); W^T, U^T
-            tri_inverse_64(sA, sT, tid);
-            {
-                const int i = tid & 63;
-                const bool wpart = tid < kChunk;
-                uint8_t* dst = wpart ? sTp : sTpp;
-#pragma unroll 1
-                for (int j0 = 0; j0 < kChunk; j0 += 8) {
-                    float x[8];
+                        if (arow) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int jj = j0 + j;
-                        const float sc = wpart ? sBeta[jj] * sGam[jj] : sBeta[jj];
-                        x[j] = (jj <= i) ? sT[i * 64 + jj] * sc : 0.f;
+                            for (int q = 0; q < 16; q += 4)
+                                *reinterpret_cast<float4*>(Abuf + i * kLd + jb + q) =
+                                    make_float4(x[q], x[q + 1], x[q + 2], x[q + 3]);
+                        } else {
+                            st_chunk_bf16(pb, i, jb >> 3, x);
+                            st_chunk_bf16(pb, i, (jb >> 3) + 1, x + 8);
+                        }
                     }
-                    st_chunk_bf16(dst, i, j0 >> 3, x);
                 }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            if (tid == 0) {
+                // zero the padded rows of the K and V tiles (they hold the next
+                // sequence or TMA zero fill; only exact zeros may meet them)
+                if (Lc < kChunk) {
+                    if (!(ok = wait_bar(cx, B_V_FULL, n & 1))) break;
+                    const int zr = it & 63;
+                    if (it < 128 && zr >= Lc) {
+                        const uint4 z = make_uint4(0, 0, 0, 0);
+                        uint8_t* base = (it < 64) ? kqs : sm + kV;
+                        const uint32_t hs = (it < 64) ? 16384 : 8192;
+#pragma unroll
+                        for (int cch = 0; cch < 16; ++cch)
+                            *reinterpret_cast<uint4*>(base + (cch >> 3) * hs + sw128_offset(zr, cch & 7)) = z;
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar_sync(kBarIntra, kIntraThreads);
+                if (it == 0) mbar_arrive(cx.bars + B_D1_EMPTY);
+                // T = (I + A)^-1, then T' = T diag(cw) (lanes 0..63), T'' = T diag(beta) (64..127)
+                tri_inverse_64(Abuf, Tbuf, X1, X2, it);
+                {
+                    const bool wpart = r < 64;
+                    const int i = r & 63;
+                    uint8_t* dst = sm + (wpart ? kTp : kTpp);
+                    const float* trow = Tbuf + i * kLd;
+                    const float* cf = gb + (wpart ? kGCw : kGBeta);
+#pragma unroll 1
+                    for (int j0 = 32 * hh; j0 < 32 * hh + 32; j0 += 8) {
+                        if (j0 > imax) break;  // warp-uniform; these chunks stay zero
+                        const float4 t0 = *reinterpret_cast<const float4*>(trow + j0);
+                        const float4 t1 = *reinterpret_cast<const float4*>(trow + j0 + 4);
+                        const float4 c0 = *reinterpret_cast<const float4*>(cf + j0);
+                        const float4 c1 = *reinterpret_cast<const float4*>(cf + j0 + 4);
+                        const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+                        const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                        float x[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) x[q] = (j0 + q <= i) ? tv[q] * cv[q] : 0.f;
+                        st_chunk_bf16(dst, i, j0 >> 3, x);
+                    }
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(kBarIntra, kIntraThreads);
+                if (it == 0) mbar_arrive(cx.bars + B_T_FULL);
+                // W^T -> shared memory (MN-major B operand of -S W^T), after Delta(n-1) read the old one
+                if (!(ok = wait_bar(cx, B_WU_FULL, n & 1))) break;
+                if (n >= 1 && !(ok = wait_bar(cx, B_DELTA_FULL + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
                 tc_fence_after();
-                const uint32_t kq = smem_u32(st + kOffKQ);
-                const uint32_t vv = smem_u32(st + kOffV);
-                const uint32_t tp = smem_u32(sTp), tpp = smem_u32(sTpp);
+                {
+                    const size_t dump = (static_cast<size_t>(info.flat0 + c) * H + info.h) * kChunk * kHead;
+                    const int i0 = 32 * hh;
+                    uint32_t rr[32];
+                    tmem_ld32_wait(tm_lane + kTmW + i0, rr);
+                    float w[32];
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    // A = K^T: K tile read MN-major (d halves 16 KB apart); B = T' rows i, K-major over j
-                    mma_bf16_ss(tmem + kTmW, desc_mnmajor_sw128(kq + ks * 2048, 16384),
-                                desc_kmajor_sw128(tp + ks * 32), kIdescWU, ks > 0);
-                    mma_bf16_ss(tmem + kTmDelta, desc_mnmajor_sw128(vv + ks * 2048, 8192),
-                                desc_kmajor_sw128(tpp + ks * 32), kIdescWU, ks > 0);
-                }
-                mma_commit(bars.mma);
-            }
-            __syncwarp();
-            wait_mma();
-
-            // ---- P4: W^T to smem (MN-major B for -S W^T); optional dumps of G, W, U
-            {
-#pragma unroll 1
-                for (int i0 = 0; i0 < kChunk; i0 += 16) {
-                    float w[16];
-                    tmem_ld16_f(tm_row + kTmW + i0, w);
-                    st_chunk_bf16(sWb, tid, i0 >> 3, w);
-                    st_chunk_bf16(sWb, tid, (i0 >> 3) + 1, w + 8);
+                    for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(rr[j]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) st_chunk_bf16(sm + kWb, r, (i0 >> 3) + q, w + 8 * q);
                     if (p.intra_w) {
-                        float* dw = p.intra_w + (static_cast<size_t>(flat0 + c) * H + h) * kChunk * kHead;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) dw[static_cast<size_t>(i0 + j) * kHead + tid] = w[j];
+                        for (int j = 0; j < 32; ++j) p.intra_w[dump + static_cast<size_t>(i0 + j) * kHead + r] = w[j];
                     }
                     if (p.intra_u) {
-                        float uu[16];
-                        tmem_ld16_f(tm_row + kTmDelta + i0, uu);
-                        float* du = p.intra_u + (static_cast<size_t>(flat0 + c) * H + h) * kChunk * kHead;
+                        tmem_ld32_wait(tm_lane + kTmDelta + s * 64 + i0, rr);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) du[static_cast<size_t>(i0 + j) * kHead + tid] = uu[j];
+                        for (int j = 0; j < 32; ++j)
+                            p.intra_u[dump + static_cast<size_t>(i0 + j) * kHead + r] = __uint_as_float(rr[j]);
                     }
+                    if (p.intra_g && it < 64)
+                        p.intra_g[(static_cast<size_t>(info.flat0 + c) * H + info.h) * kChunk + it] = gb[kGG + it];
                 }
-                if (p.intra_g && tid < kChunk)
-                    p.intra_g[(static_cast<size_t>(flat0 + c) * H + h) * kChunk + tid] = sG[tid];
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar_sync(kBarIntra, kIntraThreads);
+                if (it == 0) mbar_arrive(cx.bars + B_WB_FULL + s);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            if (tid == 0) {
-                tc_fence_after();
-                const uint32_t sb = smem_u32(sSb), wb = smem_u32(sWb);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t aoff = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_bf16_ss(tmem + kTmDelta, desc_kmajor_sw128(sb + aoff), desc_mnmajor_sw128(wb + ks * 2048, 8192),
-                                kIdescDelta, 1);
+        }
+    } else if (warp >= 12) {
+        // ================= state warpgroup =================
+        const int t = tid - 384;                       // 0..127 = TMEM lane = state row v
+        const uint32_t tm_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        uint8_t* sb = sm + kSb;
+        __nv_bfloat16* outT = reinterpret_cast<__nv_bfloat16*>(sm + kOutT);
+        uint32_t n = 0, u = 0;
+        bool ok = true;
+        for (; ok;) {
+            const int slot = u & 1;
+            if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
+            const UnitInfo info = read_unit(sm, slot);
+            named_bar_sync(kBarState, kWgThreads);
+            if (t == 0) mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
+            ++u;
+            if (!info.valid) break;
+            const size_t state_off = (static_cast<size_t>(info.srow) * H + info.h) * kHead * kHead +
+                                     static_cast<size_t>(t) * kHead;
+            const float* s0 = p.initial_state ? p.initial_state + state_off : nullptr;
+            if (info.nC == 0) {
+                if (p.output_state) {
+                    float* dst = p.output_state + state_off;
+#pragma unroll 4
+                    for (int c0 = 0; c0 < kHead; c0 += 4)
+                        *reinterpret_cast<float4*>(dst + c0) =
+                            s0 ? *reinterpret_cast<const float4*>(s0 + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                mma_commit(bars.mma);
+                continue;
             }
-            __syncwarp();
-            wait_mma();
-
-            // ---- P5: Delta^T and decayed Delta^T to smem; S *= gamma_63 in TMEM
+            // initial state: S0 -> Sb (bf16) and gamma_63(first chunk) * S0 -> TMEM
             {
-                const float Glast = sG[kChunk - 1];
+                if (!(ok = wait_bar(cx, B_GATES_FULL + (n & 1), (n >> 1) & 1))) break;
+                const float g63 = reinterpret_cast<const float*>(sm + kGbuf)[(n & 1) * kGFloats + kGGam + 63];
 #pragma unroll 1
-                for (int j0 = 0; j0 < kChunk; j0 += 16) {
-                    float d[16], e[16];
-                    tmem_ld16_f(tm_row + kTmDelta + j0, d);
+                for (int c0 = 0; c0 < kHead; c0 += 32) {
+                    float x[32];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) e[j] = d[j] * expf(Glast - sG[j0 + j]);
-                    st_chunk_bf16(sDb, tid, j0 >> 3, d);
-                    st_chunk_bf16(sDb, tid, (j0 >> 3) + 1, d + 8);
-                    st_chunk_bf16(sDtb, tid, j0 >> 3, e);
-                    st_chunk_bf16(sDtb, tid, (j0 >> 3) + 1, e + 8);
-                }
-                const float gl = sGam[kChunk - 1];
-#pragma unroll 1
-                for (int c0 = 0; c0 < kHead; c0 += 16) {
-                    float x[16];
-                    tmem_ld16_f(tm_row + kTmS + c0, x);
-                    uint32_t r[16];
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 f = s0 ? *reinterpret_cast<const float4*>(s0 + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        x[j] = f.x; x[j + 1] = f.y; x[j + 2] = f.z; x[j + 3] = f.w;
+                    }
+                    uint8_t* half = sb + (c0 >> 6) * 16384;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(x[j] * gl);
-                    tmem_st16(tm_row + kTmS + c0, r);
+                    for (int q = 0; q < 4; ++q) st_chunk_bf16(half, t, ((c0 & 63) >> 3) + q, x + 8 * q);
+                    uint32_t r[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j] * g63);
+                    tmem_st32(tm_lane + kTmS + c0, r);
                 }
                 tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar_sync(kBarState, kWgThreads);
+                if (t == 0) mbar_arrive(cx.bars + B_SB_FULL + (n & 1));
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            if (tid == 0) {
+            for (int32_t c = 0; c < info.nC && ok; ++c, ++n) {
+                const int s = n & 1;
+                const uint32_t ph = (n >> 1) & 1;
+                const int64_t tc = info.t0 + static_cast<int64_t>(c) * kChunk;
+                const int64_t rem = info.L - static_cast<int64_t>(c) * kChunk;
+                const int32_t Lc = rem < kChunk ? static_cast<int32_t>(rem) : kChunk;
+                const float* gb = reinterpret_cast<const float*>(sm + kGbuf) + s * kGFloats;
+                const uint32_t dbuf = tm_lane + kTmDelta + s * 64;
+                // ---- Delta epilogue: bf16 Delta^T and decayed Delta^T back into TMEM (A operands)
+                if (!(ok = wait_bar(cx, B_DELTA_FULL + s, ph))) break;
+                if (!(ok = wait_bar(cx, B_WB_FULL + s, ph))) break;  // factor vectors of chunk n are final
                 tc_fence_after();
-                const uint32_t db = smem_u32(sDb), dtb = smem_u32(sDtb), pp = smem_u32(sP);
-                const uint32_t kq = smem_u32(st + kOffKQ);
+                {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32_wait(dbuf, ra);
+                    tmem_ld32_wait(dbuf + 32, rb);
+                    // every fp32 column is in registers now: the packed copies may overwrite them
+                    uint32_t pk[16];
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    mma_bf16_ss(tmem + kTmO2, desc_kmajor_sw128(db + ks * 32), desc_kmajor_sw128(pp + ks * 32),
-                                kIdescO2, ks > 0);
-                    // B = K tile read MN-major: rows j (K dim), d contiguous (N), d halves 16 KB apart
-                    mma_bf16_ss(tmem + kTmS, desc_kmajor_sw128(dtb + ks * 32), desc_mnmajor_sw128(kq + ks * 2048, 16384),
-                                kIdescS, 1);
+                    for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(__uint_as_float(ra[2 * q]), __uint_as_float(ra[2 * q + 1]));
+                    tmem_st16(dbuf, pk);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(__uint_as_float(rb[2 * q]), __uint_as_float(rb[2 * q + 1]));
+                    tmem_st16(dbuf + 16, pk);
+                    float dv[16];
+#pragma unroll
+                    for (int part = 0; part < 4; ++part) {
+                        lds16(gb + kGDec + 16 * part, dv);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const uint32_t a = (part < 2) ? ra[16 * part + 2 * q] : rb[16 * (part - 2) + 2 * q];
+                            const uint32_t b = (part < 2) ? ra[16 * part + 2 * q + 1] : rb[16 * (part - 2) + 2 * q + 1];
+                            pk[8 * (part & 1) + q] = pack_bf16x2(__uint_as_float(a) * dv[2 * q], __uint_as_float(b) * dv[2 * q + 1]);
+                        }
+                        if (part & 1) tmem_st16(dbuf + 32 + 16 * (part >> 1), pk);
+                    }
+                    tmem_wait_st();
                 }
-                mma_commit(bars.mma);
-            }
-            __syncwarp();
-            wait_mma();
-
-            // ---- P6: output rows, next S operand, checkpoints, final state
-            {
-                const float sc = p.scale;
-                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.output);
+                tc_fence_before();
+                named_bar_sync(kBarState, kWgThreads);
+                if (t == 0) mbar_arrive(cx.bars + B_DD_FULL + s);
+                // ---- state epilogue: checkpoint / final state, next S operand, prescale
+                if (!(ok = wait_bar(cx, B_S_FULL + s, ph))) break;
+                tc_fence_after();
+                const bool last = (c + 1 == info.nC);
+                float gnext = 1.f;
+                if (!last) {
+                    if (!(ok = wait_bar(cx, B_GATES_FULL + ((n + 1) & 1), ((n + 1) >> 1) & 1))) break;
+                    gnext = reinterpret_cast<const float*>(sm + kGbuf)[((n + 1) & 1) * kGFloats + kGGam + 63];
+                }
+                {
+                    const int64_t pend = static_cast<int64_t>(c + 1) * kChunk;
+                    float* ck = nullptr;
+                    if (p.checkpoints && p.ckpt_n > 0 && pend % p.ckpt_n == 0 && pend <= info.L)
+                        ck = p.checkpoints + (static_cast<size_t>(info.ckpt_base + pend / p.ckpt_n - 1) * H + info.h) *
+                                                 kHead * kHead + static_cast<size_t>(t) * kHead;
+                    float* fin = (last && p.output_state) ? p.output_state + state_off : nullptr;
 #pragma unroll 1
-                for (int i0 = 0; i0 < kChunk; i0 += 16) {
-                    float o1[16], o2[16];
-                    tmem_ld16_f(tm_row + kTmO1 + i0, o1);
-                    tmem_ld16_f(tm_row + kTmO2 + i0, o2);
+                    for (int c0 = 0; c0 < kHead; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_ld32_wait(tm_lane + kTmS + c0, r);
+                        float x[32];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int i = i0 + j;
-                        if (i < Lc) {
-                            const float o = sc * (sGam[i] * o1[j] + o2[j]);
-                            out[(static_cast<size_t>(tc + i) * H + h) * kHead + tid] = __float2bfloat16_rn(o);
+                        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+                        if (ck) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4)
+                                *reinterpret_cast<float4*>(ck + c0 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                        }
+                        if (fin) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4)
+                                *reinterpret_cast<float4*>(fin + c0 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                        }
+                        if (!last) {
+                            uint8_t* half = sb + (c0 >> 6) * 16384;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) st_chunk_bf16(half, t, ((c0 & 63) >> 3) + q, x + 8 * q);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j] * gnext);
+                            tmem_st32(tm_lane + kTmS + c0, r);
+                        }
+                    }
+                    if (!last) tmem_wait_st();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar_sync(kBarState, kWgThreads);
+                if (t == 0 && !last) mbar_arrive(cx.bars + B_SB_FULL + ((n + 1) & 1));
+                // ---- output epilogue: o_i = orow_i (S Q^T)_i + scale (Delta^T P^T)_i
+                {
+                    const float sc = p.scale;
+#pragma unroll 1
+                    for (int i0 = 0; i0 < kChunk; i0 += 32) {
+                        uint32_t r1[32], r2[32];
+                        tmem_ld32_wait(tm_lane + kTmO1 + i0, r1);
+                        tmem_ld32_wait(tm_lane + kTmO2 + i0, r2);
+                        float orow[32];
+                        lds16(gb + kGOr + i0, orow);
+                        lds16(gb + kGOr + i0 + 16, orow + 16);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float o = orow[j] * __uint_as_float(r1[j]) + sc * __uint_as_float(r2[j]);
+                            outT[(i0 + j) * kHead + t] = __float2bfloat16_rn(o);
                         }
                     }
                 }
-                const int64_t pend = static_cast<int64_t>(c + 1) * kChunk;
-                float* ck = nullptr;
-                if (p.checkpoints && p.ckpt_n > 0 && pend % p.ckpt_n == 0 && pend <= L) {
-                    const int64_t slot = load_index(p.ckpt_cu_starts, p.ckpt_i64, seq) + pend / p.ckpt_n - 1;
-                    ck = p.checkpoints + (static_cast<size_t>(slot) * H + h) * kHead * kHead +
-                         static_cast<size_t>(tid) * kHead;
+                tc_fence_before();
+                named_bar_sync(kBarState, kWgThreads);
+                if (t == 0) {
+                    mbar_arrive(cx.bars + B_O_EMPTY + s);
+                    mbar_arrive(cx.bars + B_GATES_EMPTY + s);
                 }
-                float* fin = (c == nC - 1 && p.output_state)
-                                 ? p.output_state + state_off + static_cast<size_t>(tid) * kHead
-                                 : nullptr;
-                const bool need_sb = c + 1 < nC;
-#pragma unroll 1
-                for (int c0 = 0; c0 < kHead; c0 += 16) {
-                    float x[16];
-                    tmem_ld16_f(tm_row + kTmS + c0, x);
-                    if (need_sb) {
-                        uint8_t* half = sSb + (c0 >> 6) * 16384;
-                        st_chunk_bf16(half, tid, (c0 & 63) >> 3, x);
-                        st_chunk_bf16(half, tid, ((c0 & 63) >> 3) + 1, x + 8);
-                    }
-                    if (ck) {
+                {
+                    // coalesced copy of the valid rows: 16 threads per 256-byte row
+                    uint8_t* gout = static_cast<uint8_t*>(p.output);
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4*>(ck + c0 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
-                    }
-                    if (fin) {
-#pragma unroll
-                        for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4*>(fin + c0 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                    for (int k = 0; k < 8; ++k) {
+                        const int id = t + 128 * k, row = id >> 4, col = id & 15;
+                        if (row < Lc) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(sm + kOutT + row * 256 + col * 16);
+                            *reinterpret_cast<uint4*>(gout + ((static_cast<size_t>(tc + row) * H + info.h) * kHead) * 2 +
+                                                      col * 16) = v;
+                        }
                     }
                 }
+                named_bar_sync(kBarState, kWgThreads);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            if (tid == 0 && c + 2 < nC) {
-                issue_chunk_loads(stage[s], bars.tma[s], &tm_q, &tm_k, &tm_v, qh, kh, vh,
-                                  static_cast<int32_t>(t0 + static_cast<int64_t>(c + 2) * kChunk));
-                pending[s] = 1;
-            }
-            abort = *reinterpret_cast<volatile int32_t*>(s_abort) != 0;
         }
-        if (abort) break;
     }
 
-    // ---- clean up: drain TMA loads still in flight (bounded), free TMEM
-    if (tid == 0) {
-        for (int s = 0; s < 2; ++s)
-            if (pending[s]) {
-                if (!mbar_wait(bars.tma[s], tma_phase[s] & 1u)) atomicOr(p.status, GDN_DEVICE_ERR_TIMEOUT);
-                ++tma_phase[s];
-            }
-    }
+    // ---- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmCols);
+    if (warp == 3) tmem_dealloc(tmem, kTmCols);
 }
 
 }  // namespace

@@ -159,7 +159,8 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
     if (T > 0 && (!a.q || !a.k || !a.v || !a.output)) return GDN_ERR_INVALID_ARG;
     if (!aligned(a.q, 16) || !aligned(a.k, 16) || !aligned(a.v, 16) || !aligned(a.output, 16))
         return GDN_ERR_INVALID_ARG;
-    if (((f & GDN_FLAG_HAS_G) && !a.g) || ((f & GDN_FLAG_HAS_BETA) && !a.beta)) return GDN_ERR_INVALID_ARG;
+    if (T > 0 && (((f & GDN_FLAG_HAS_G) && !a.g) || ((f & GDN_FLAG_HAS_BETA) && !a.beta)))
+        return GDN_ERR_INVALID_ARG;
     if ((f & GDN_FLAG_HAS_INITIAL_STATE) && (!a.initial_state || !aligned(a.initial_state, 16)))
         return GDN_ERR_INVALID_ARG;
     if ((f & GDN_FLAG_OUTPUT_FINAL_STATE) && (!a.output_state || !aligned(a.output_state, 16)))
