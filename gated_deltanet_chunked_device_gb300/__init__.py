@@ -35,7 +35,7 @@ from . import _build
 
 __all__ = [
     "build", "lib", "chunk_gated_delta_rule", "gdn_prefill_plan", "gdn_prefill_run", "gdn_prefill_prepare",
-    "gdn_prefill_chunks", "gdn_prefill_read_status",
+    "gdn_prefill_chunks", "gdn_prefill_run_static", "gdn_prefill_read_status",
     "gdn_prefill_workspace_layout", "gdn_prefill_plan_destroy", "gdn_status_string", "Desc", "Args", "Layout",
     "GdnError", "STATUS", "DEVICE_ERR", "FLAGS",
 ]
@@ -113,6 +113,8 @@ def lib():
                     fn = getattr(L, name)
                     fn.argtypes = L.gdn_prefill_run.argtypes
                     fn.restype = ctypes.c_int
+                L.gdn_prefill_run_static.argtypes = [ctypes.c_void_p, ctypes.POINTER(Args), ctypes.c_void_p]
+                L.gdn_prefill_run_static.restype = ctypes.c_int
                 L.gdn_prefill_read_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                       ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
                 L.gdn_prefill_read_status.restype = ctypes.c_int
@@ -151,6 +153,12 @@ def gdn_prefill_prepare(plan, args: Args, workspace_ptr: int, workspace_bytes: i
 def gdn_prefill_chunks(plan, args: Args, workspace_ptr: int, workspace_bytes: int, stream_ptr: int) -> int:
     return lib().gdn_prefill_chunks(plan, ctypes.byref(args), ctypes.c_void_p(workspace_ptr), workspace_bytes,
                                     ctypes.c_void_p(stream_ptr))
+
+
+def gdn_prefill_run_static(plan, args: Args, stream_ptr: int) -> int:
+    """The run that allocates nothing: its workspace is a fixed array in the
+    library's device globals (see include/gdn_prefill.h)."""
+    return lib().gdn_prefill_run_static(plan, ctypes.byref(args), ctypes.c_void_p(stream_ptr))
 
 
 def gdn_prefill_read_status(plan, workspace_ptr, device_status_ptr, stream_ptr):

@@ -95,5 +95,6 @@ cudaError_t launch_chunk_bf16(const ChunkParams& p, const CUtensorMap& tm_q, con
                               const CUtensorMap& tm_v, int grid, cudaStream_t stream);
 cudaError_t launch_chunk_f32(const ChunkParams& p, int grid, cudaStream_t stream);
 size_t chunk_bf16_smem_bytes();
+size_t plan_workspace_bytes(gdn_prefill_plan_t plan);
 
 }  // namespace gdn

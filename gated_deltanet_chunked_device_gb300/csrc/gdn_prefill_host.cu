@@ -97,6 +97,8 @@ int sm_count() {
 
 }  // namespace
 
+size_t gdn::plan_workspace_bytes(gdn_prefill_plan_t plan) { return plan ? plan->ws.total : 0; }
+
 extern "C" {
 
 gdn_status gdn_prefill_plan(const gdn_prefill_desc* desc, gdn_prefill_plan_t* plan, size_t* workspace_bytes) {

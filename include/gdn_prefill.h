@@ -180,6 +180,31 @@ typedef struct gdn_prefill_layout {
 } gdn_prefill_layout;
 gdn_status gdn_prefill_workspace_layout(gdn_prefill_plan_t plan, gdn_prefill_layout *layout);
 
+/* A run that allocates nothing.  The pages have no counterpart to this entry
+ * point; it exists for callers that cannot allocate device memory when they
+ * run the prefill (an allocator or memory-pool callback, or a host framework
+ * that owns every allocation of the process) and so cannot supply a
+ * workspace.  It runs exactly what gdn_prefill_run runs, with the workspace
+ * taken from one fixed array of GDN_PREFILL_STATIC_WORKSPACE_BYTES in the
+ * library's device globals; every GPU that loads the library holds that array
+ * until the process exits.
+ *   - Plans whose workspace is larger than the array are rejected with
+ *     GDN_ERR_UNSUPPORTED before anything is launched (the plan's
+ *     workspace_bytes tells in advance; 1 MiB covers, for example, 4096
+ *     sequences and 6 million tokens).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the array, and the prepare kernel resets what must start
+ *     at zero on every call.  Calls whose kernels overlap on the GPU (other
+ *     streams, or host threads without ordering between them) race on it.
+ *   - With args.device_status NULL the status word lives in the array and
+ *     cannot be read back; pass a device_status pointer to read it with
+ *     gdn_prefill_read_status.
+ * Nothing here allocates: no cudaMalloc, no cudaFree, no library allocator. */
+#define GDN_PREFILL_STATIC_WORKSPACE_BYTES (1u << 20)
+gdn_status gdn_prefill_run_static(gdn_prefill_plan_t plan, const gdn_prefill_args *args, void *stream);
+
 void gdn_prefill_plan_destroy(gdn_prefill_plan_t plan);
 
 const char *gdn_status_string(gdn_status status);
