@@ -63,11 +63,11 @@ constexpr uint32_t kAbuf = 163840;    // A fp32 [64][kLd]
 constexpr uint32_t kTbuf = 181248;    // T fp32 [64][kLd]
 constexpr uint32_t kXs = 198656;      // inverse scratch: [2][16][20] then [32][36] fp32
 constexpr uint32_t kOutT = 205824;    // output tile bf16 [64 i][128 v]
-constexpr uint32_t kGbuf = 222208;    // 2 x 576 floats of per-row / per-column factors (see kG*)
-constexpr uint32_t kBars = 226816;    // 32 mbarriers
-constexpr uint32_t kRing = 227072;    // 2 unit descriptors
-constexpr uint32_t kMisc = 227200;    // tmem base, abort flag
-constexpr uint32_t kSmemBytes = 227264;
+constexpr uint32_t kGbuf = 222208;    // 2 x kGFloats floats of per-row / per-column factors (see kG*)
+constexpr uint32_t kBars = 229504;    // 32 mbarriers
+constexpr uint32_t kRing = 229760;    // 2 unit descriptors
+constexpr uint32_t kMisc = 229888;    // tmem base, abort flag
+constexpr uint32_t kSmemBytes = 229952;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 constexpr int kLd = 68;               // fp32 row stride of A and T (bank-conflict free rows)
 
@@ -76,8 +76,11 @@ constexpr int kLd = 68;               // fp32 row stride of A and T (bank-confli
 //   beta   beta (0 on padded rows)             rn, rm 1/|k_j|, 1/|q_i| (1 without the L2 norm)
 //   cw     beta_j gamma_j rn_j (T' columns)    dec    e^{G_63 - G_j} rn_j (decayed Delta columns)
 //   orow   scale gamma_i rm_i (output rows)    ra     beta_i rn_i (A rows)
+//   colf   rn_j e^{G_16b - G_j}, b = j / 16      rowf   [4][64] e^{G_i - G_16b} (i >= 16 b, else 0)
+//   safe   1 when the chunk's G range is small enough for e^{G_i - G_j} = rowf * colf
 constexpr int kGG = 0, kGGam = 64, kGBeta = 128, kGRn = 192, kGRm = 256, kGCw = 320, kGDec = 384, kGOr = 448,
-              kGRa = 512, kGFloats = 576;
+              kGRa = 512, kGColf = 576, kGRowf = 640, kGSafe = 896, kGFloats = 912;
+static_assert(2 * kGFloats * 4 <= kBars - kGbuf, "gbuf overflows");
 
 // ---- barriers
 enum {
@@ -158,16 +161,47 @@ __device__ __forceinline__ UnitInfo read_unit(const uint8_t* sm, int slot) {
 
 // ===========================================================================
 // Triangular inverse T = (I + A)^-1 of a strictly lower 64 x 64 A (fp32,
-// rows of kLd floats), by the two intra warpgroups (256 threads):
+// rows of kLd floats), by the two intra warpgroups (256 threads, 8 warps):
 //   level 0: the four 16 x 16 diagonal blocks by forward substitution, one
-//            column per thread;
+//            column per thread (fp32);
 //   level 1: T_ab = -T_aa A_ab T_bb for (a, b) = (1, 0), (3, 2);
 //   level 2: T_21 = -T_22 A_21 T_11 on 32 x 32 blocks.
+// The level 1 and 2 products are 16- and 32-row matrices, below the 64-row
+// minimum of tcgen05.mma, so they run as warp-level m16n8k8 tf32 MMAs (fp32
+// accumulate); T is later rounded to bf16 for the W and U products anyway.
 // On return T holds the lower triangle including the diagonal; the upper
 // triangle is unspecified.
 // ===========================================================================
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// D (16 x 8) += A (16 x 8, row-major, stride lda) * B (8 x 8, row-major K x N, stride ldb)
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const float* A, int lda, const float* B, int ldb,
+                                                int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t a0 = to_tf32(A[g * lda + t]), a1 = to_tf32(A[(g + 8) * lda + t]);
+    const uint32_t a2 = to_tf32(A[g * lda + t + 4]), a3 = to_tf32(A[(g + 8) * lda + t + 4]);
+    const uint32_t b0 = to_tf32(B[t * ldb + g]), b1 = to_tf32(B[(t + 4) * ldb + g]);
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Store a 16 x 8 accumulator tile (times `sign`) to row-major C.
+__device__ __forceinline__ void store_tile_16x8(float* C, int ldc, const float (&d)[4], float sign, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    *reinterpret_cast<float2*>(C + g * ldc + 2 * t) = make_float2(sign * d[0], sign * d[1]);
+    *reinterpret_cast<float2*>(C + (g + 8) * ldc + 2 * t) = make_float2(sign * d[2], sign * d[3]);
+}
+
 __device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ T, float* __restrict__ X1,
                                float* __restrict__ X2, int t) {
+    const int wi = t >> 5, lane = t & 31;  // warp index 0..7 within the intra groups
     if (t < 64) {
         const int o = (t >> 4) * 16, col = t & 15;
         float x[16];
@@ -194,60 +228,39 @@ __device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ 
         for (int q = 0; q < 8; ++q) T[(ro + r) * kLd + co + c0 + q] = 0.f;
     }
     named_bar_sync(kBarIntra, kIntraThreads);
-    {   // level 1: 2 blocks x 16 x 16 outputs, 2 per thread
-        const int pr = t >> 7, a = 2 * pr + 1, b = 2 * pr;
-        const int idx = t & 127, r = idx >> 3, c0 = (idx & 7) * 2;
-        float x0 = 0.f, x1 = 0.f;
-        const float* arow = A + (16 * a + r) * kLd + 16 * b;
+    // level 1: warps 0..3 each own one 16 x 8 output tile: block pair pr = wi >> 1, columns nt = wi & 1
+    if (wi < 4) {
+        const int pr = wi >> 1, nt = (wi & 1) * 8, a = 2 * pr + 1, b = 2 * pr;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float av = arow[m];
-            const float2 tv = *reinterpret_cast<const float2*>(T + (16 * b + m) * kLd + 16 * b + c0);
-            x0 += av * tv.x;
-            x1 += av * tv.y;
-        }
-        float* xs = X1 + pr * 16 * 20;
-        *reinterpret_cast<float2*>(xs + r * 20 + c0) = make_float2(x0, x1);
-        named_bar_sync(kBarIntra, kIntraThreads);
-        float y0 = 0.f, y1 = 0.f;
-        const float* trow = T + (16 * a + r) * kLd + 16 * a;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float tv = trow[m];  // zero above the diagonal
-            const float2 xv = *reinterpret_cast<const float2*>(xs + m * 20 + c0);
-            y0 += tv * xv.x;
-            y1 += tv * xv.y;
-        }
-        *reinterpret_cast<float2*>(T + (16 * a + r) * kLd + 16 * b + c0) = make_float2(-y0, -y1);
+        for (int k0 = 0; k0 < 16; k0 += 8)   // X_ab = A_ab T_bb
+            mma_tf32_16x8x8(d, A + (16 * a) * kLd + 16 * b + k0, kLd, T + (16 * b + k0) * kLd + 16 * b + nt, kLd, lane);
+        store_tile_16x8(X1 + pr * 16 * 20 + nt, 20, d, 1.f, lane);
     }
     named_bar_sync(kBarIntra, kIntraThreads);
-    {   // level 2: 32 x 32 outputs, 4 per thread
-        const int r = t >> 3, c0 = (t & 7) * 4;
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        const float* arow = A + (32 + r) * kLd;
-#pragma unroll 4
-        for (int m = c0; m < 32; ++m) {  // T_11[m][c] = 0 for m < c
-            const float av = arow[m];
-            const float4 tv = *reinterpret_cast<const float4*>(T + m * kLd + c0);
-            x[0] += av * tv.x;
-            x[1] += av * tv.y;
-            x[2] += av * tv.z;
-            x[3] += av * tv.w;
-        }
-        *reinterpret_cast<float4*>(X2 + r * 36 + c0) = make_float4(x[0], x[1], x[2], x[3]);
+    if (wi < 4) {
+        const int pr = wi >> 1, nt = (wi & 1) * 8, a = 2 * pr + 1, b = 2 * pr;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k0 = 0; k0 < 16; k0 += 8)   // T_ab = -T_aa X_ab
+            mma_tf32_16x8x8(d, T + (16 * a) * kLd + 16 * a + k0, kLd, X1 + pr * 16 * 20 + k0 * 20 + nt, 20, lane);
+        store_tile_16x8(T + (16 * a) * kLd + 16 * b + nt, kLd, d, -1.f, lane);
+    }
+    named_bar_sync(kBarIntra, kIntraThreads);
+    // level 2: eight warps, one 16 x 8 tile each of the 32 x 32 products
+    {
+        const int mt = (wi >> 2) * 16, nt = (wi & 3) * 8;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k0 = 0; k0 < 32; k0 += 8)   // X = A_21 T_11
+            mma_tf32_16x8x8(d, A + (32 + mt) * kLd + k0, kLd, T + k0 * kLd + nt, kLd, lane);
+        store_tile_16x8(X2 + mt * 36 + nt, 36, d, 1.f, lane);
         named_bar_sync(kBarIntra, kIntraThreads);
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
-        const float* trow = T + (32 + r) * kLd + 32;
-#pragma unroll 4
-        for (int m = 0; m <= r; ++m) {  // T_22[r][m] = 0 for m > r
-            const float tv = trow[m];
-            const float4 xv = *reinterpret_cast<const float4*>(X2 + m * 36 + c0);
-            y[0] += tv * xv.x;
-            y[1] += tv * xv.y;
-            y[2] += tv * xv.z;
-            y[3] += tv * xv.w;
-        }
-        *reinterpret_cast<float4*>(T + (32 + r) * kLd + c0) = make_float4(-y[0], -y[1], -y[2], -y[3]);
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k0 = 0; k0 < 32; k0 += 8)   // T_21 = -T_22 X
+            mma_tf32_16x8x8(e, T + (32 + mt) * kLd + 32 + k0, kLd, X2 + k0 * 36 + nt, 36, lane);
+        store_tile_16x8(T + (32 + mt) * kLd + nt, kLd, e, -1.f, lane);
     }
     named_bar_sync(kBarIntra, kIntraThreads);
 }
@@ -278,7 +291,25 @@ __device__ __forceinline__ GatePrefetch load_gates(const ChunkParams& p, int64_t
     return g;
 }
 
-__device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, float scale, int lane) {
+// Sum of squares of row r of a staged 64 x 128 bf16 tile (two 64-column
+// halves 16 KB apart, 128-byte swizzle).
+__device__ __forceinline__ float row_sumsq(const uint8_t* half0, int r) {
+    float ss = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < 16; ++c) {
+        float f[8];
+        bf16x8_to_float(*reinterpret_cast<const uint4*>(half0 + (c >> 3) * 16384 + sw128_offset(r, c & 7)), f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
+    }
+    return ss;
+}
+
+// The norm-independent vectors of one chunk (see kG*): G, gamma, beta, and
+// cw, dec, orow, ra, colf as they are with unit norms (rn = rm = 1).  When the
+// L2 norm is on, the intra warpgroups multiply the norm factors in once the
+// norms are known.  Rows at or past Lc are padding (alpha = 1, beta = 0).
+__device__ void compute_gates(const GatePrefetch& g, float* gb, float scale, int lane) {
     const int r0 = 2 * lane, r1 = r0 + 1;
     const float la0 = __logf(g.a0), la1 = __logf(g.a1);
     float incl = la0 + la1;
@@ -289,25 +320,34 @@ __device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, 
     }
     const float G1 = incl, G0 = incl - la1;
     const float G63 = __shfl_sync(0xffffffffu, incl, 31);
-    const float e0 = __expf(G0), e1 = __expf(G1);
-    gb[kGG + r0] = G0;
-    gb[kGG + r1] = G1;
-    gb[kGGam + r0] = e0;
-    gb[kGGam + r1] = e1;
-    gb[kGBeta + r0] = g.b0;
-    gb[kGBeta + r1] = g.b1;
-    gb[kGRn + r0] = 1.f;
-    gb[kGRn + r1] = 1.f;
-    gb[kGRm + r0] = 1.f;
-    gb[kGRm + r1] = 1.f;
-    gb[kGCw + r0] = g.b0 * e0;
-    gb[kGCw + r1] = g.b1 * e1;
-    gb[kGDec + r0] = __expf(G63 - G0);
-    gb[kGDec + r1] = __expf(G63 - G1);
-    gb[kGOr + r0] = scale * e0;
-    gb[kGOr + r1] = scale * e1;
-    gb[kGRa + r0] = g.b0;
-    gb[kGRa + r1] = g.b1;
+    float Gb[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) Gb[b] = __shfl_sync(0xffffffffu, G0, 8 * b);  // G at row 16 b
+    const float Gv[2] = {G0, G1}, bv[2] = {g.b0, g.b1};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int r = r0 + k;
+        const float e = __expf(Gv[k]);
+        gb[kGG + r] = Gv[k];
+        gb[kGGam + r] = e;
+        gb[kGBeta + r] = bv[k];
+        gb[kGRn + r] = 1.f;
+        gb[kGRm + r] = 1.f;
+        gb[kGCw + r] = bv[k] * e;
+        gb[kGDec + r] = __expf(G63 - Gv[k]);
+        gb[kGOr + r] = scale * e;
+        gb[kGRa + r] = bv[k];
+        gb[kGColf + r] = __expf(Gb[r >> 4] - Gv[k]);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) gb[kGRowf + b * 64 + r] = (r >= 16 * b) ? __expf(Gv[k] - Gb[b]) : 0.f;
+    }
+    float gmax = fmaxf(G0, G1), gmin = fminf(G0, G1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+        gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
+    }
+    if (lane == 0) gb[kGSafe] = (gmax - gmin < 60.f) ? 1.f : 0.f;
 }
 
 __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]) {
@@ -333,7 +373,8 @@ __device__ __forceinline__ void lds16(const float* src, float* x) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_chunk_bf16_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
-                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_o) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -359,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
+            prefetch_tensormap(&tm_o);
         }
     }
     for (uint32_t off = tid * 16; off < 32768; off += kThreads * 16)  // T', T'' and both P buffers
@@ -592,71 +634,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* gb = reinterpret_cast<float*>(sm + kGbuf) + s * kGFloats;
                 uint8_t* kqs = sm + kKQ + s * kKQStage;
                 if (!(ok = wait_bar(cx, B_GATES_FULL + s, (n >> 1) & 1))) break;
-                if (!(ok = wait_bar(cx, B_KQ_FULL + s, (n >> 1) & 1))) break;
-                // q norms from the Q tile (rows i = r - 64)
-                if (p.l2norm && hh == 0 && r >= 64) {
-                    const int i = r - 64;
-                    float ss = 0.f;
-#pragma unroll 4
-                    for (int cch = 0; cch < 16; ++cch) {
-                        float f[8];
-                        bf16x8_to_float(*reinterpret_cast<const uint4*>(kqs + 8192 + (cch >> 3) * 16384 +
-                                                                        sw128_offset(i, cch & 7)), f);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
-                    }
-                    gb[kGRm + i] = i < Lc ? rsqrtf(ss + 1e-6f) : 0.f;
-                }
                 // P buffer s is free once O2 of chunk n-2 has completed
                 if (n >= 2 && !(ok = wait_bar(cx, B_S_FULL + s, ((n - 2) >> 1) & 1))) break;
                 if (!(ok = wait_bar(cx, B_D1_FULL, n & 1))) break;
                 tc_fence_after();
                 if (p.l2norm) {
-                    // k norms from the diagonal of K K^T (lanes 0..63)
-                    if (hh == 0 && r < 64) {
-                        uint32_t rr[32];
-                        tmem_ld32_wait(tm_lane + kTmD1 + 32 * wq, rr);
-                        float kk = 0.f;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) kk = (j == lane) ? __uint_as_float(rr[j]) : kk;
-                        gb[kGRn + r] = r < Lc ? rsqrtf(kk + 1e-6f) : 0.f;
-                    }
-                    named_bar_sync(kBarIntra, kIntraThreads);
-                    // factor vectors that depend on the norms
+                    // k norms: the diagonal of K K^T (lanes 0..63); q norms: the Q tile rows (lanes 64..127)
                     if (hh == 0) {
                         if (r < 64) {
-                            const float rn = gb[kGRn + r], b = gb[kGBeta + r];
-                            gb[kGCw + r] = b * gb[kGGam + r] * rn;
-                            gb[kGDec + r] *= rn;
-                            gb[kGRa + r] = b * rn;
+                            uint32_t rr[32];
+                            tmem_ld32_wait(tm_lane + kTmD1 + 32 * wq, rr);
+                            float kk = 0.f;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) kk = (j == lane) ? __uint_as_float(rr[j]) : kk;
+                            const float rn = r < Lc ? rsqrtf(kk + 1e-6f) : 0.f;
+                            gb[kGRn + r] = rn;
+                            gb[kGRa + r] *= rn;
                         } else {
                             const int i = r - 64;
-                            gb[kGOr + i] = p.scale * gb[kGGam + i] * gb[kGRm + i];
+                            const float rm = i < Lc ? rsqrtf(row_sumsq(sm + kKQ + s * kKQStage + 8192, i) + 1e-6f) : 0.f;
+                            gb[kGRm + i] = rm;
+                            gb[kGOr + i] *= rm;
                         }
                     }
                     named_bar_sync(kBarIntra, kIntraThreads);
+                    if (hh == 1 && r < 64) {  // column factors that meet n_j (read only after T')
+                        const float rn = gb[kGRn + r];
+                        gb[kGCw + r] *= rn;
+                        gb[kGDec + r] *= rn;
+                    }
                 }
                 // A rows (lanes 0..63) and P rows (lanes 64..127), this warp's 32 columns, 16 per step;
-                // blocks entirely above the diagonal are skipped (A's upper part is never read, P's stays zero)
+                // blocks entirely above the diagonal are skipped (A's upper part is never read, P's stays zero).
+                // e^{G_i - G_j} = rowf[b][i] colf[j] inside column block b when the chunk's gate range is
+                // moderate, else computed pairwise.
                 {
                     const bool arow = r < 64;
                     const int i = r & 63;
-                    const float Gi = gb[kGG + i];
-                    const float rf = arow ? gb[kGRa + i] : gb[kGRm + i];
+                    const bool safe = gb[kGSafe] != 0.f;
+                    const float rbase = arow ? gb[kGRa + i] : gb[kGRm + i];
                     uint8_t* pb = sm + kPb + s * 8192;
 #pragma unroll 1
                     for (int jb = 32 * hh; jb < 32 * hh + 32; jb += 16) {
                         if (jb > imax) break;  // warp-uniform
                         uint32_t rr[16];
                         tmem_ld16_wait(tm_lane + kTmD1 + jb, rr);
-                        float gj[16], cj[16], x[16];
-                        lds16(gb + kGG + jb, gj);
-                        lds16(gb + kGRn + jb, cj);
+                        float x[16];
+                        if (safe) {
+                            float cj[16], nj[16];
+                            lds16(gb + kGColf + jb, cj);
+                            lds16(gb + kGRn + jb, nj);
+                            const float rf = rbase * gb[kGRowf + (jb >> 4) * 64 + i];
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) {
-                            const int j = jb + q;
-                            const bool keep = arow ? (j < i) : (j <= i);
-                            x[q] = keep ? rf * __expf(Gi - gj[q]) * cj[q] * __uint_as_float(rr[q]) : 0.f;
+                            for (int q = 0; q < 16; ++q) {
+                                const int j = jb + q;
+                                const bool keep = arow ? (j < i) : (j <= i);
+                                x[q] = keep ? rf * cj[q] * nj[q] * __uint_as_float(rr[q]) : 0.f;
+                            }
+                        } else {
+                            float gj[16], nj[16];
+                            lds16(gb + kGG + jb, gj);
+                            lds16(gb + kGRn + jb, nj);
+                            const float Gi = gb[kGG + i];
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) {
+                                const int j = jb + q;
+                                const bool keep = arow ? (j < i) : (j <= i);
+                                x[q] = keep ? rbase * __expf(Gi - gj[q]) * nj[q] * __uint_as_float(rr[q]) : 0.f;
+                            }
                         }
                         if (arow) {
 #pragma unroll
@@ -886,6 +931,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (!last) tmem_wait_st();
                 }
+                if (t == 0) bulk_wait_group_read0();  // the previous chunk's output store has read outT
                 fence_proxy_async_smem();
                 tc_fence_before();
                 named_bar_sync(kBarState, kWgThreads);
@@ -908,14 +954,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
+                fence_proxy_async_smem();
                 tc_fence_before();
                 named_bar_sync(kBarState, kWgThreads);
                 if (t == 0) {
                     mbar_arrive(cx.bars + B_O_EMPTY + s);
                     mbar_arrive(cx.bars + B_GATES_EMPTY + s);
                 }
-                {
-                    // coalesced copy of the valid rows: 16 threads per 256-byte row
+                if (Lc == kChunk) {
+                    // a full chunk: one TMA store of the 64 x 128 tile (rows all belong to this sequence)
+                    if (t == 0) {
+                        tma_store_3d(&tm_o, sm + kOutT, 0, info.h, static_cast<int32_t>(tc));
+                        bulk_commit_group();
+                    }
+                } else {
+                    // the tail: coalesced copy of the valid rows only, 16 threads per 256-byte row
                     uint8_t* gout = static_cast<uint8_t*>(p.output);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
@@ -927,12 +980,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                named_bar_sync(kBarState, kWgThreads);
             }
         }
     }
 
     // ---- teardown
+    if (warp >= 12 && tid == 384) bulk_wait_group0();  // output stores in flight have landed
     tc_fence_before();
     __syncthreads();
     if (warp == 3) tmem_dealloc(tmem, kTmCols);
@@ -943,7 +996,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t chunk_bf16_smem_bytes() { return kSmemAlloc; }
 
 cudaError_t launch_chunk_bf16(const ChunkParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                              const CUtensorMap& tm_v, int grid, cudaStream_t stream) {
+                              const CUtensorMap& tm_v, const CUtensorMap& tm_o, int grid, cudaStream_t stream) {
     static int configured = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -954,7 +1007,7 @@ cudaError_t launch_chunk_bf16(const ChunkParams& p, const CUtensorMap& tm_q, con
         if (e != cudaSuccess) return e;
         configured = dev;
     }
-    gdn_chunk_bf16_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(p, tm_q, tm_k, tm_v);
+    gdn_chunk_bf16_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(p, tm_q, tm_k, tm_v, tm_o);
     return cudaGetLastError();
 }
 

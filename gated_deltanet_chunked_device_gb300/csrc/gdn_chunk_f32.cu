@@ -1,0 +1,262 @@
+// gdn_chunk_f32.cu -- chunked Gated DeltaNet prefill for fp32 q/k/v: the same
+// 64-token chunk algebra as the tensor-core kernel, in fp32 on CUDA cores.
+//
+// fp32 inputs are held to a 1e-3 bar; tf32 tensor-core operands (10-bit
+// mantissa) would sit close to it, and 4-byte operand tiles of the fused
+// tensor-core kernel do not fit in shared memory.  This kernel keeps every
+// product in fp32.  One CTA owns (sequence, state head, 64-row slice of V):
+// rows of the state are independent (S[v,:] only meets v_t[v] and Delta[:,v]),
+// so the two slices of a head run in parallel and each recomputes the
+// slice-independent parts (A, T, W, P).
+//
+// Per chunk ("GDN 与 Chunked Prefill": cumsum, triangular solve, recompute):
+//   G = running sum of log alpha, gamma = e^G
+//   A_ij = beta_i e^{G_i - G_j} (k_i.k_j)  j < i;   T = (I + A)^-1
+//   W = T diag(beta gamma) K,  U = T diag(beta) V
+//   Delta = U - W S^T
+//   O_i = scale (gamma_i S q_i + sum_{j<=i} e^{G_i - G_j} (q_i.k_j) Delta_j)
+//   S <- gamma_63 S + sum_j e^{G_63 - G_j} Delta_j k_j^T
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kF32Threads = 256;
+constexpr int kVs = 64;          // rows of V (and of the state) per CTA
+constexpr int kLdK = 129;        // padded row stride for 128-wide rows
+constexpr int kLdV = 65;         // padded row stride for 64-wide rows
+
+// shared memory layout (floats)
+constexpr int kOffK = 0;                       // K  [64][kLdK]
+constexpr int kOffQ = kOffK + 64 * kLdK;       // Q  [64][kLdK]
+constexpr int kOffW = kOffQ + 64 * kLdK;       // W  [64][kLdK]
+constexpr int kOffS = kOffW + 64 * kLdK;       // S slice [64 v][kLdK]
+constexpr int kOffV = kOffS + kVs * kLdK;      // V slice [64 j][kLdV]
+constexpr int kOffX = kOffV + 64 * kLdV;       // U, then Delta [64 j][kLdV]
+constexpr int kOffA = kOffX + 64 * kLdV;       // A, then T, then P [64][kLdV]
+constexpr int kOffG = kOffA + 64 * kLdV;       // G[64], gamma[64], beta[64]
+constexpr int kF32SmemFloats = kOffG + 3 * 64;
+constexpr size_t kF32Smem = sizeof(float) * kF32SmemFloats;
+
+__global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkParams p) {
+    extern __shared__ float sf[];
+    __shared__ int s_bad;
+    const int tid = threadIdx.x;
+    if (tid == 0) s_bad = *reinterpret_cast<volatile int32_t*>(p.status);
+    __syncthreads();
+    if (s_bad) return;
+
+    const int32_t H = p.H;
+    const int64_t unit = blockIdx.x / 2;
+    const int v0 = (blockIdx.x & 1) * kVs;
+    const int32_t seq = static_cast<int32_t>(unit / H);
+    const int32_t h = static_cast<int32_t>(unit % H);
+    const int qh = h / (H / p.hq), kh = h / (H / p.hk), vh = h / (H / p.hv);
+    const int64_t t0 = load_index(p.cu_seqlens, p.cu_i64, seq);
+    const int64_t L = load_index(p.cu_seqlens, p.cu_i64, seq + 1) - t0;
+    const int64_t srow = p.state_indices ? load_index(p.state_indices, p.idx_i64, seq) : seq;
+    const size_t state_base = (static_cast<size_t>(srow) * H + h) * kHead * kHead;
+    const float* qg = static_cast<const float*>(p.q);
+    const float* kg = static_cast<const float*>(p.k);
+    const float* vg = static_cast<const float*>(p.v);
+    float* og = static_cast<float*>(p.output);
+
+    float* Ks = sf + kOffK;
+    float* Qs = sf + kOffQ;
+    float* Ws = sf + kOffW;
+    float* Ss = sf + kOffS;
+    float* Vs = sf + kOffV;
+    float* Xs = sf + kOffX;
+    float* Am = sf + kOffA;
+    float* sG = sf + kOffG;
+    float* sGam = sG + 64;
+    float* sBeta = sG + 128;
+
+    // state slice: rows v0..v0+63 of [V][K]
+    for (int e = tid; e < kVs * kHead; e += kF32Threads) {
+        const int vv = e / kHead, kk = e % kHead;
+        Ss[vv * kLdK + kk] = p.initial_state ? p.initial_state[state_base + static_cast<size_t>(v0 + vv) * kHead + kk] : 0.f;
+    }
+    __syncthreads();
+
+    const int64_t nC = (L + kChunk - 1) / kChunk;
+    for (int64_t c = 0; c < nC; ++c) {
+        const int64_t tc = t0 + c * kChunk;
+        const int Lc = static_cast<int>(L - c * kChunk < kChunk ? L - c * kChunk : kChunk);
+        // ---- load the chunk (padded rows: zeros), L2-normalise q and k rows when asked
+        for (int e = tid; e < kChunk * kHead; e += kF32Threads) {
+            const int r = e / kHead, d = e % kHead;
+            const bool ok = r < Lc;
+            Ks[r * kLdK + d] = ok ? kg[(static_cast<size_t>(tc + r) * p.hk + kh) * kHead + d] : 0.f;
+            Qs[r * kLdK + d] = ok ? qg[(static_cast<size_t>(tc + r) * p.hq + qh) * kHead + d] : 0.f;
+        }
+        for (int e = tid; e < kChunk * kVs; e += kF32Threads) {
+            const int r = e / kVs, d = e % kVs;
+            Vs[r * kLdV + d] = r < Lc ? vg[(static_cast<size_t>(tc + r) * p.hv + vh) * kHead + v0 + d] : 0.f;
+        }
+        __syncthreads();
+        if (p.l2norm && tid < 2 * kChunk) {
+            float* row = (tid < kChunk ? Ks : Qs) + (tid & 63) * kLdK;
+            float ss = 0.f;
+            for (int d = 0; d < kHead; ++d) ss += row[d] * row[d];
+            const float inv = 1.0f / sqrtf(ss + 1e-6f);
+            for (int d = 0; d < kHead; ++d) row[d] *= inv;
+        }
+        // ---- gates (warp 0: two rows per lane, shuffle scan of log alpha)
+        if (tid < 32) {
+            const int r0 = 2 * tid, r1 = r0 + 1;
+            float la0 = 0.f, la1 = 0.f, b0 = 0.f, b1 = 0.f;
+            if (r0 < Lc) {
+                const size_t gi = static_cast<size_t>(tc + r0) * H + h;
+                la0 = p.g ? logf(p.g[gi]) : 0.f;
+                b0 = p.beta ? p.beta[gi] : 1.f;
+            }
+            if (r1 < Lc) {
+                const size_t gi = static_cast<size_t>(tc + r1) * H + h;
+                la1 = p.g ? logf(p.g[gi]) : 0.f;
+                b1 = p.beta ? p.beta[gi] : 1.f;
+            }
+            float incl = la0 + la1;
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += y;
+            }
+            sG[r0] = incl - la1;
+            sG[r1] = incl;
+            sGam[r0] = expf(incl - la1);
+            sGam[r1] = expf(incl);
+            sBeta[r0] = b0;
+            sBeta[r1] = b1;
+        }
+        __syncthreads();
+        // ---- A (strictly lower)
+        for (int e = tid; e < kChunk * kChunk; e += kF32Threads) {
+            const int i = e / kChunk, j = e % kChunk;
+            float a = 0.f;
+            if (j < i) {
+                float dot = 0.f;
+                for (int d = 0; d < kHead; ++d) dot += Ks[i * kLdK + d] * Ks[j * kLdK + d];
+                a = sBeta[i] * expf(sG[i] - sG[j]) * dot;
+            }
+            Am[i * kLdV + j] = a;
+        }
+        __syncthreads();
+        // ---- T = (I + A)^-1, one column per thread, in registers, then written over A
+        {
+            float x[kChunk];
+            const int j = tid;
+            if (j < kChunk) {
+                for (int i = 0; i < kChunk; ++i) {
+                    float acc = (i == j) ? 1.f : 0.f;
+                    if (i > j)
+                        for (int m = j; m < i; ++m) acc -= Am[i * kLdV + m] * x[m];
+                    x[i] = (i < j) ? 0.f : acc;
+                }
+            }
+            __syncthreads();
+            if (j < kChunk)
+                for (int i = 0; i < kChunk; ++i) Am[i * kLdV + j] = x[i];
+        }
+        __syncthreads();
+        // ---- W = T diag(beta gamma) K,  U = T diag(beta) V_slice
+        for (int e = tid; e < kChunk * kHead; e += kF32Threads) {
+            const int i = e / kHead, d = e % kHead;
+            float acc = 0.f;
+            for (int j = 0; j <= i; ++j) acc += Am[i * kLdV + j] * sBeta[j] * sGam[j] * Ks[j * kLdK + d];
+            Ws[i * kLdK + d] = acc;
+        }
+        for (int e = tid; e < kChunk * kVs; e += kF32Threads) {
+            const int i = e / kVs, d = e % kVs;
+            float acc = 0.f;
+            for (int j = 0; j <= i; ++j) acc += Am[i * kLdV + j] * sBeta[j] * Vs[j * kLdV + d];
+            Xs[i * kLdV + d] = acc;
+        }
+        __syncthreads();
+        if (p.intra_w && v0 == 0) {
+            const size_t base = (static_cast<size_t>(p.chunk_offsets[seq] + c) * H + h) * kChunk * kHead;
+            for (int e = tid; e < kChunk * kHead; e += kF32Threads)
+                p.intra_w[base + e] = Ws[(e / kHead) * kLdK + e % kHead];
+        }
+        if (p.intra_u) {
+            const size_t base = (static_cast<size_t>(p.chunk_offsets[seq] + c) * H + h) * kChunk * kHead;
+            for (int e = tid; e < kChunk * kVs; e += kF32Threads)
+                p.intra_u[base + (e / kVs) * kHead + v0 + e % kVs] = Xs[(e / kVs) * kLdV + e % kVs];
+        }
+        if (p.intra_g && v0 == 0 && tid < kChunk)
+            p.intra_g[(static_cast<size_t>(p.chunk_offsets[seq] + c) * H + h) * kChunk + tid] = sG[tid];
+        // ---- Delta = U - W S^T (slice columns), in place over U
+        for (int e = tid; e < kChunk * kVs; e += kF32Threads) {
+            const int i = e / kVs, vv = e % kVs;
+            float acc = 0.f;
+            for (int d = 0; d < kHead; ++d) acc += Ws[i * kLdK + d] * Ss[vv * kLdK + d];
+            Xs[i * kLdV + vv] -= acc;
+        }
+        __syncthreads();
+        // ---- P_ij = e^{G_i - G_j} (q_i . k_j) for j <= i, over T (done with it)
+        for (int e = tid; e < kChunk * kChunk; e += kF32Threads) {
+            const int i = e / kChunk, j = e % kChunk;
+            float pv = 0.f;
+            if (j <= i) {
+                float dot = 0.f;
+                for (int d = 0; d < kHead; ++d) dot += Qs[i * kLdK + d] * Ks[j * kLdK + d];
+                pv = expf(sG[i] - sG[j]) * dot;
+            }
+            Am[i * kLdV + j] = pv;
+        }
+        __syncthreads();
+        // ---- output rows of the slice
+        for (int e = tid; e < kChunk * kVs; e += kF32Threads) {
+            const int i = e / kVs, vv = e % kVs;
+            if (i >= Lc) continue;
+            float sq = 0.f;
+            for (int d = 0; d < kHead; ++d) sq += Ss[vv * kLdK + d] * Qs[i * kLdK + d];
+            float acc = sGam[i] * sq;
+            for (int j = 0; j <= i; ++j) acc += Am[i * kLdV + j] * Xs[j * kLdV + vv];
+            og[(static_cast<size_t>(tc + i) * H + h) * kHead + v0 + vv] = p.scale * acc;
+        }
+        __syncthreads();
+        // ---- state: S <- gamma_63 S + sum_j e^{G_63 - G_j} Delta_j k_j^T
+        {
+            const float g63 = sG[kChunk - 1];
+            for (int e = tid; e < kVs * kHead; e += kF32Threads) {
+                const int vv = e / kHead, d = e % kHead;
+                float acc = expf(g63) * Ss[vv * kLdK + d];
+                for (int j = 0; j < kChunk; ++j) acc += expf(g63 - sG[j]) * Xs[j * kLdV + vv] * Ks[j * kLdK + d];
+                Ss[vv * kLdK + d] = acc;
+            }
+        }
+        __syncthreads();
+        // ---- checkpoint at the chunk end
+        const int64_t pend = (c + 1) * kChunk;
+        if (p.checkpoints && p.ckpt_n > 0 && pend % p.ckpt_n == 0 && pend <= L) {
+            const int64_t slot = load_index(p.ckpt_cu_starts, p.ckpt_i64, seq) + pend / p.ckpt_n - 1;
+            float* ck = p.checkpoints + (static_cast<size_t>(slot) * H + h) * kHead * kHead;
+            for (int e = tid; e < kVs * kHead; e += kF32Threads)
+                ck[static_cast<size_t>(v0 + e / kHead) * kHead + e % kHead] = Ss[(e / kHead) * kLdK + e % kHead];
+        }
+    }
+    if (p.output_state) {
+        for (int e = tid; e < kVs * kHead; e += kF32Threads)
+            p.output_state[state_base + static_cast<size_t>(v0 + e / kHead) * kHead + e % kHead] =
+                Ss[(e / kHead) * kLdK + e % kHead];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_f32(const ChunkParams& p, int grid, cudaStream_t stream) {
+    static int configured = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured != dev) {
+        e = cudaFuncSetAttribute(gdn_chunk_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kF32Smem));
+        if (e != cudaSuccess) return e;
+        configured = dev;
+    }
+    gdn_chunk_f32_kernel<<<grid, kF32Threads, kF32Smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -88,6 +88,22 @@ bool encode_qkv_map(CUtensorMap* map, const void* base, int64_t T, int32_t heads
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output [T, H, 128] bf16 as a 3-D TMA map with 128 x 1 x 64 boxes, no swizzle
+// (the kernel stages a 64 x 128 row-major tile).
+bool encode_out_map(CUtensorMap* map, void* base, int64_t T, int32_t heads) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(gdn::kHead), static_cast<cuuint64_t>(heads),
+                          static_cast<cuuint64_t>(T)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(gdn::kHead) * 2,
+                             static_cast<cuuint64_t>(heads) * gdn::kHead * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(gdn::kHead), 1, static_cast<cuuint32_t>(gdn::kChunk)};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -183,7 +199,6 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
         if (a.max_seqlen > T || a.max_seqlen < lo) return GDN_ERR_INVALID_ARG;
     }
     if (!workspace || workspace_bytes < plan->ws.total || !aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
-    if (d.qkv_dtype != GDN_DTYPE_BF16) return GDN_ERR_UNSUPPORTED;
 
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -247,20 +262,28 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
     cp.intra_u = a.intra_u;
     cp.has_tokens = T > 0 ? 1 : 0;
 
-    CUtensorMap tq, tk, tv;
+    if (d.qkv_dtype == GDN_DTYPE_F32) {
+        // fp32 inputs: CUDA-core kernel, one CTA per (sequence, state head, half of the V rows)
+        const int64_t blocks = static_cast<int64_t>(N) * plan->H * 2;
+        if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+        if (gdn::launch_chunk_f32(cp, static_cast<int>(blocks), stream) != cudaSuccess) return GDN_ERR_CUDA;
+        return GDN_OK;
+    }
+    CUtensorMap tq, tk, tv, to;
     std::memset(&tq, 0, sizeof(tq));
     std::memset(&tk, 0, sizeof(tk));
     std::memset(&tv, 0, sizeof(tv));
+    std::memset(&to, 0, sizeof(to));
     if (T > 0) {
         if (!encode_qkv_map(&tq, a.q, T, d.num_q_heads) || !encode_qkv_map(&tk, a.k, T, d.num_k_heads) ||
-            !encode_qkv_map(&tv, a.v, T, d.num_v_heads))
+            !encode_qkv_map(&tv, a.v, T, d.num_v_heads) || !encode_out_map(&to, a.output, T, plan->H))
             return GDN_ERR_CUDA;
     }
     const int sms = sm_count();
     if (sms <= 0) return GDN_ERR_CUDA;
     const int64_t units = static_cast<int64_t>(N) * plan->H;
     const int grid = static_cast<int>(units < sms ? units : sms);
-    if (gdn::launch_chunk_bf16(cp, tq, tk, tv, grid, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    if (gdn::launch_chunk_bf16(cp, tq, tk, tv, to, grid, stream) != cudaSuccess) return GDN_ERR_CUDA;
     return GDN_OK;
 }
 
