@@ -45,9 +45,10 @@
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWgThreads = 128;     // state warpgroup
+constexpr int kThreads = 640;
+constexpr int kStateThreads = 256;  // two state warpgroups
 constexpr int kIntraThreads = 256;  // two intra warpgroups
+constexpr uint32_t kRegsLaunch = 96, kRegsSched = 64, kRegsIntra = 96, kRegsState = 104;  // per thread
 constexpr uint32_t kBarIntra = 1, kBarState = 2;  // named barrier ids
 
 // ---- shared memory map (bytes from a 1024-aligned base)
@@ -305,11 +306,12 @@ __device__ __forceinline__ float row_sumsq(const uint8_t* half0, int r) {
     return ss;
 }
 
-// The norm-independent vectors of one chunk (see kG*): G, gamma, beta, and
-// cw, dec, orow, ra, colf as they are with unit norms (rn = rm = 1).  When the
-// L2 norm is on, the intra warpgroups multiply the norm factors in once the
-// norms are known.  Rows at or past Lc are padding (alpha = 1, beta = 0).
-__device__ void compute_gates(const GatePrefetch& g, float* gb, float scale, int lane) {
+// The vectors of one chunk (see kG*): G, gamma, beta, and cw, dec, ra, colf
+// as they are with unit key norms (rn = 1), orow and rm with the query norms
+// when `q` (the staged Q tile) is given, else with rm = 1.  The intra
+// warpgroups multiply the key norms in once the K K^T diagonal is known.
+// Rows at or past Lc are padding (alpha = 1, beta = 0, rm = 0).
+__device__ void compute_gates(const GatePrefetch& g, float* gb, float scale, const uint8_t* q, int32_t Lc, int lane) {
     const int r0 = 2 * lane, r1 = r0 + 1;
     const float la0 = __logf(g.a0), la1 = __logf(g.a1);
     float incl = la0 + la1;
@@ -323,7 +325,12 @@ __device__ void compute_gates(const GatePrefetch& g, float* gb, float scale, int
     float Gb[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) Gb[b] = __shfl_sync(0xffffffffu, G0, 8 * b);  // G at row 16 b
-    const float Gv[2] = {G0, G1}, bv[2] = {g.b0, g.b1};
+    float rm0 = 1.f, rm1 = 1.f;
+    if (q) {
+        rm0 = r0 < Lc ? rsqrtf(row_sumsq(q, r0) + 1e-6f) : 0.f;
+        rm1 = r1 < Lc ? rsqrtf(row_sumsq(q, r1) + 1e-6f) : 0.f;
+    }
+    const float Gv[2] = {G0, G1}, bv[2] = {g.b0, g.b1}, rmv[2] = {rm0, rm1};
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         const int r = r0 + k;
@@ -332,10 +339,10 @@ __device__ void compute_gates(const GatePrefetch& g, float* gb, float scale, int
         gb[kGGam + r] = e;
         gb[kGBeta + r] = bv[k];
         gb[kGRn + r] = 1.f;
-        gb[kGRm + r] = 1.f;
+        gb[kGRm + r] = rmv[k];
         gb[kGCw + r] = bv[k] * e;
         gb[kGDec + r] = __expf(G63 - Gv[k]);
-        gb[kGOr + r] = scale * e;
+        gb[kGOr + r] = scale * e * rmv[k];
         gb[kGRa + r] = bv[k];
         gb[kGColf + r] = __expf(Gb[r >> 4] - Gv[k]);
 #pragma unroll
@@ -415,197 +422,213 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const int32_t H = p.H;
+    // register split: launch 640 x 96; the scheduling warpgroup gives up 32 a thread, the state ones take 8 more
+    // (128 x 64 + 256 x 96 + 256 x 104 <= 640 x 96)
+    static_assert(128 * kRegsSched + kIntraThreads * kRegsIntra + kStateThreads * kRegsState <= kThreads * kRegsLaunch,
+                  "register split exceeds the launch budget");
     const int64_t units = static_cast<int64_t>(p.num_seqs) * H;
 
-    if (warp == 0) {
-        // ================= TMA producer and unit scheduler =================
-        if (lane == 0) {
-            uint32_t n = 0, u = 0;
-            int issued_kq[2] = {-1, -1};
-            int issued_v = -1;
-            for (;;) {
-                const int64_t uid = atomicAdd(p.counter, 1);
-                const int slot = u & 1;
-                if (u >= 2 && !wait_bar(cx, B_UNIT_EMPTY + slot, ((u - 2) >> 1) & 1)) break;
-                UnitInfo info;
-                info.valid = uid < units ? 1 : 0;
-                int32_t nC = 0;
-                if (info.valid) {
-                    const int32_t seq = p.seq_order[uid / H];
-                    const int32_t h = static_cast<int32_t>(uid % H);
-                    info.seq = seq;
-                    info.h = h;
-                    info.t0 = load_index(p.cu_seqlens, p.cu_i64, seq);
-                    info.L = load_index(p.cu_seqlens, p.cu_i64, seq + 1) - info.t0;
-                    nC = static_cast<int32_t>((info.L + kChunk - 1) / kChunk);
-                    info.nC = nC;
-                    info.qh = h / (H / p.hq);
-                    info.kh = h / (H / p.hk);
-                    info.vh = h / (H / p.hv);
-                    info.flat0 = p.chunk_offsets[seq];
-                    info.srow = p.state_indices ? load_index(p.state_indices, p.idx_i64, seq) : seq;
-                    info.ckpt_base = p.ckpt_n > 0 ? load_index(p.ckpt_cu_starts, p.ckpt_i64, seq) : 0;
+    if (warp < 4) {
+        // the scheduling warpgroup: TMA producer, two MMA issuers, gates warp
+        regs_dec<kRegsSched>();
+        if (warp == 0) {
+            // ================= TMA producer and unit scheduler =================
+            if (lane == 0) {
+                uint32_t n = 0, u = 0;
+                int issued_kq[2] = {-1, -1};
+                int issued_v = -1;
+                for (;;) {
+                    const int64_t uid = atomicAdd(p.counter, 1);
+                    const int slot = u & 1;
+                    if (u >= 2 && !wait_bar(cx, B_UNIT_EMPTY + slot, ((u - 2) >> 1) & 1)) break;
+                    UnitInfo info;
+                    info.valid = uid < units ? 1 : 0;
+                    int32_t nC = 0;
+                    if (info.valid) {
+                        const int32_t seq = p.seq_order[uid / H];
+                        const int32_t h = static_cast<int32_t>(uid % H);
+                        info.seq = seq;
+                        info.h = h;
+                        info.t0 = load_index(p.cu_seqlens, p.cu_i64, seq);
+                        info.L = load_index(p.cu_seqlens, p.cu_i64, seq + 1) - info.t0;
+                        nC = static_cast<int32_t>((info.L + kChunk - 1) / kChunk);
+                        info.nC = nC;
+                        info.qh = h / (H / p.hq);
+                        info.kh = h / (H / p.hk);
+                        info.vh = h / (H / p.hv);
+                        info.flat0 = p.chunk_offsets[seq];
+                        info.srow = p.state_indices ? load_index(p.state_indices, p.idx_i64, seq) : seq;
+                        info.ckpt_base = p.ckpt_n > 0 ? load_index(p.ckpt_cu_starts, p.ckpt_i64, seq) : 0;
+                    }
+                    *reinterpret_cast<UnitInfo*>(sm + kRing + slot * 64) = info;
+                    mbar_arrive(cx.bars + B_UNIT_FULL + slot);
+                    ++u;
+                    if (!info.valid) break;
+                    bool ok = true;
+                    for (int32_t c = 0; c < nC && ok; ++c, ++n) {
+                        const int s = n & 1;
+                        const int32_t t = static_cast<int32_t>(info.t0 + static_cast<int64_t>(c) * kChunk);
+                        if (n >= 2 && !(ok = wait_bar(cx, B_KQ_EMPTY + s, ((n - 2) >> 1) & 1))) break;
+                        uint8_t* st = sm + kKQ + s * kKQStage;
+                        uint64_t* fb = cx.bars + B_KQ_FULL + s;
+                        mbar_arrive_expect_tx(fb, kKQStage);
+                        tma_load_3d(st + 0, &tm_k, fb, 0, info.kh, t);
+                        tma_load_3d(st + 8192, &tm_q, fb, 0, info.qh, t);
+                        tma_load_3d(st + 16384, &tm_k, fb, 64, info.kh, t);
+                        tma_load_3d(st + 24576, &tm_q, fb, 64, info.qh, t);
+                        issued_kq[s] = static_cast<int>(n);
+                        if (n >= 1 && !(ok = wait_bar(cx, B_V_EMPTY, (n - 1) & 1))) break;
+                        uint64_t* vb = cx.bars + B_V_FULL;
+                        mbar_arrive_expect_tx(vb, 16384);
+                        tma_load_3d(sm + kV, &tm_v, vb, 0, info.vh, t);
+                        tma_load_3d(sm + kV + 8192, &tm_v, vb, 64, info.vh, t);
+                        issued_v = static_cast<int>(n);
+                    }
+                    if (!ok) break;
                 }
-                *reinterpret_cast<UnitInfo*>(sm + kRing + slot * 64) = info;
-                mbar_arrive(cx.bars + B_UNIT_FULL + slot);
-                ++u;
-                if (!info.valid) break;
+                // drain: every issued load has landed before the CTA may exit
+                for (int s = 0; s < 2; ++s)
+                    if (issued_kq[s] >= 0) drain_bar(cx, B_KQ_FULL + s, (issued_kq[s] >> 1) & 1);
+                if (issued_v >= 0) drain_bar(cx, B_V_FULL, issued_v & 1);
+            }
+        } else if (warp == 1) {
+            // ================= tcgen05 issue: D1, W, U =================
+            if (lane == 0) {
+                uint32_t n = 0, u = 0;
                 bool ok = true;
-                for (int32_t c = 0; c < nC && ok; ++c, ++n) {
-                    const int s = n & 1;
-                    const int32_t t = static_cast<int32_t>(info.t0 + static_cast<int64_t>(c) * kChunk);
-                    if (n >= 2 && !(ok = wait_bar(cx, B_KQ_EMPTY + s, ((n - 2) >> 1) & 1))) break;
-                    uint8_t* st = sm + kKQ + s * kKQStage;
-                    uint64_t* fb = cx.bars + B_KQ_FULL + s;
-                    mbar_arrive_expect_tx(fb, kKQStage);
-                    tma_load_3d(st + 0, &tm_k, fb, 0, info.kh, t);
-                    tma_load_3d(st + 8192, &tm_q, fb, 0, info.qh, t);
-                    tma_load_3d(st + 16384, &tm_k, fb, 64, info.kh, t);
-                    tma_load_3d(st + 24576, &tm_q, fb, 64, info.qh, t);
-                    issued_kq[s] = static_cast<int>(n);
-                    if (n >= 1 && !(ok = wait_bar(cx, B_V_EMPTY, (n - 1) & 1))) break;
-                    uint64_t* vb = cx.bars + B_V_FULL;
-                    mbar_arrive_expect_tx(vb, 16384);
-                    tma_load_3d(sm + kV, &tm_v, vb, 0, info.vh, t);
-                    tma_load_3d(sm + kV + 8192, &tm_v, vb, 64, info.vh, t);
-                    issued_v = static_cast<int>(n);
+                for (; ok;) {
+                    const int slot = u & 1;
+                    if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
+                    const UnitInfo info = read_unit(sm, slot);
+                    mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
+                    ++u;
+                    if (!info.valid) break;
+                    for (int32_t c = 0; c < info.nC; ++c, ++n) {
+                        const int s = n & 1;
+                        if (!(ok = wait_bar(cx, B_KQ_FULL + s, (n >> 1) & 1))) break;
+                        if (n >= 1 && !(ok = wait_bar(cx, B_D1_EMPTY, (n - 1) & 1))) break;
+                        tc_fence_after();
+                        const uint32_t kq = smem_u32(sm + kKQ + s * kKQStage);
+    #pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                            mma_bf16_ss(tmem + kTmD1, desc_kmajor_sw128(kq + off), desc_kmajor_sw128(kq + off), kIdescD1,
+                                        ks > 0);
+                        }
+                        mma_commit(cx.bars + B_D1_FULL);
+                        if (!(ok = wait_bar(cx, B_T_FULL, n & 1))) break;
+                        if (!(ok = wait_bar(cx, B_V_FULL, n & 1))) break;
+                        if (n >= 2 && !(ok = wait_bar(cx, B_S_FULL + s, ((n - 2) >> 1) & 1))) break;
+                        tc_fence_after();
+                        const uint32_t vv = smem_u32(sm + kV);
+                        const uint32_t tp = smem_u32(sm + kTp), tpp = smem_u32(sm + kTpp);
+                        const uint32_t dbuf = tmem + kTmDelta + s * 64;
+    #pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            mma_bf16_ss(tmem + kTmW, desc_mnmajor_sw128(kq + ks * 2048, 16384),
+                                        desc_kmajor_sw128(tp + ks * 32), kIdescWU, ks > 0);
+                            mma_bf16_ss(dbuf, desc_mnmajor_sw128(vv + ks * 2048, 8192), desc_kmajor_sw128(tpp + ks * 32),
+                                        kIdescWU, ks > 0);
+                        }
+                        mma_commit(cx.bars + B_WU_FULL);
+                        mma_commit(cx.bars + B_V_EMPTY);
+                    }
                 }
-                if (!ok) break;
+                mma_commit(cx.bars + B_DRAIN_I);
+                drain_bar(cx, B_DRAIN_I, 0);
             }
-            // drain: every issued load has landed before the CTA may exit
-            for (int s = 0; s < 2; ++s)
-                if (issued_kq[s] >= 0) drain_bar(cx, B_KQ_FULL + s, (issued_kq[s] >> 1) & 1);
-            if (issued_v >= 0) drain_bar(cx, B_V_FULL, issued_v & 1);
-        }
-    } else if (warp == 1) {
-        // ================= tcgen05 issue: D1, W, U =================
-        if (lane == 0) {
+        } else if (warp == 2) {
+            // ================= tcgen05 issue: Delta, S Q^T, Delta P^T, S =================
+            if (lane == 0) {
+                uint32_t n = 0, u = 0;
+                bool ok = true;
+                for (; ok;) {
+                    const int slot = u & 1;
+                    if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
+                    const UnitInfo info = read_unit(sm, slot);
+                    mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
+                    ++u;
+                    if (!info.valid) break;
+                    for (int32_t c = 0; c < info.nC; ++c, ++n) {
+                        const int s = n & 1;
+                        const uint32_t ph = (n >> 1) & 1;
+                        if (!(ok = wait_bar(cx, B_WB_FULL + s, ph))) break;
+                        if (!(ok = wait_bar(cx, B_SB_FULL + s, ph))) break;
+                        if (!(ok = wait_bar(cx, B_KQ_FULL + s, ph))) break;
+                        tc_fence_after();
+                        const uint32_t kq = smem_u32(sm + kKQ + s * kKQStage);
+                        const uint32_t sb = smem_u32(sm + kSb), wb = smem_u32(sm + kWb);
+                        const uint32_t dbuf = tmem + kTmDelta + s * 64;
+    #pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t aoff = (ks >> 2) * 16384 + (ks & 3) * 32;
+                            mma_bf16_ss(dbuf, desc_kmajor_sw128(sb + aoff), desc_mnmajor_sw128(wb + ks * 2048, 8192),
+                                        kIdescDelta, 1);
+                        }
+                        mma_commit(cx.bars + B_DELTA_FULL + s);
+                        if (n >= 1 && !(ok = wait_bar(cx, B_O_EMPTY + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
+                        tc_fence_after();
+    #pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                            mma_bf16_ss(tmem + kTmO1, desc_kmajor_sw128(sb + off), desc_kmajor_sw128(kq + 8192 + off),
+                                        kIdescO, ks > 0);
+                        }
+                        if (!(ok = wait_bar(cx, B_DD_FULL + s, ph))) break;
+                        tc_fence_after();
+                        const uint32_t pb = smem_u32(sm + kPb + s * 8192);
+    #pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint32_t acol = dbuf + 32 * (ks >> 1) + 8 * (ks & 1);  // packed j = 16 ks .. 16 ks + 15
+                            mma_bf16_ts(tmem + kTmO2, acol, desc_kmajor_sw128(pb + ks * 32), kIdescO, ks > 0);
+                            mma_bf16_ts(tmem + kTmS, acol + 16, desc_mnmajor_sw128(kq + ks * 2048, 16384), kIdescS, 1);
+                        }
+                        mma_commit(cx.bars + B_S_FULL + s);
+                        mma_commit(cx.bars + B_KQ_EMPTY + s);
+                    }
+                }
+                mma_commit(cx.bars + B_DRAIN_S);
+                drain_bar(cx, B_DRAIN_S, 0);
+            }
+        } else if (warp == 3) {
+            // ================= gates warp: G, gamma, beta and factor vectors per chunk =================
             uint32_t n = 0, u = 0;
             bool ok = true;
             for (; ok;) {
                 const int slot = u & 1;
                 if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
                 const UnitInfo info = read_unit(sm, slot);
-                mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
-                ++u;
-                if (!info.valid) break;
-                for (int32_t c = 0; c < info.nC; ++c, ++n) {
-                    const int s = n & 1;
-                    if (!(ok = wait_bar(cx, B_KQ_FULL + s, (n >> 1) & 1))) break;
-                    if (n >= 1 && !(ok = wait_bar(cx, B_D1_EMPTY, (n - 1) & 1))) break;
-                    tc_fence_after();
-                    const uint32_t kq = smem_u32(sm + kKQ + s * kKQStage);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_bf16_ss(tmem + kTmD1, desc_kmajor_sw128(kq + off), desc_kmajor_sw128(kq + off), kIdescD1,
-                                    ks > 0);
-                    }
-                    mma_commit(cx.bars + B_D1_FULL);
-                    if (!(ok = wait_bar(cx, B_T_FULL, n & 1))) break;
-                    if (!(ok = wait_bar(cx, B_V_FULL, n & 1))) break;
-                    if (n >= 2 && !(ok = wait_bar(cx, B_S_FULL + s, ((n - 2) >> 1) & 1))) break;
-                    tc_fence_after();
-                    const uint32_t vv = smem_u32(sm + kV);
-                    const uint32_t tp = smem_u32(sm + kTp), tpp = smem_u32(sm + kTpp);
-                    const uint32_t dbuf = tmem + kTmDelta + s * 64;
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        mma_bf16_ss(tmem + kTmW, desc_mnmajor_sw128(kq + ks * 2048, 16384),
-                                    desc_kmajor_sw128(tp + ks * 32), kIdescWU, ks > 0);
-                        mma_bf16_ss(dbuf, desc_mnmajor_sw128(vv + ks * 2048, 8192), desc_kmajor_sw128(tpp + ks * 32),
-                                    kIdescWU, ks > 0);
-                    }
-                    mma_commit(cx.bars + B_WU_FULL);
-                    mma_commit(cx.bars + B_V_EMPTY);
-                }
-            }
-            mma_commit(cx.bars + B_DRAIN_I);
-            drain_bar(cx, B_DRAIN_I, 0);
-        }
-    } else if (warp == 2) {
-        // ================= tcgen05 issue: Delta, S Q^T, Delta P^T, S =================
-        if (lane == 0) {
-            uint32_t n = 0, u = 0;
-            bool ok = true;
-            for (; ok;) {
-                const int slot = u & 1;
-                if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
-                const UnitInfo info = read_unit(sm, slot);
-                mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
-                ++u;
-                if (!info.valid) break;
-                for (int32_t c = 0; c < info.nC; ++c, ++n) {
-                    const int s = n & 1;
-                    const uint32_t ph = (n >> 1) & 1;
-                    if (!(ok = wait_bar(cx, B_WB_FULL + s, ph))) break;
-                    if (!(ok = wait_bar(cx, B_SB_FULL + s, ph))) break;
-                    if (!(ok = wait_bar(cx, B_KQ_FULL + s, ph))) break;
-                    tc_fence_after();
-                    const uint32_t kq = smem_u32(sm + kKQ + s * kKQStage);
-                    const uint32_t sb = smem_u32(sm + kSb), wb = smem_u32(sm + kWb);
-                    const uint32_t dbuf = tmem + kTmDelta + s * 64;
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t aoff = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_bf16_ss(dbuf, desc_kmajor_sw128(sb + aoff), desc_mnmajor_sw128(wb + ks * 2048, 8192),
-                                    kIdescDelta, 1);
-                    }
-                    mma_commit(cx.bars + B_DELTA_FULL + s);
-                    if (n >= 1 && !(ok = wait_bar(cx, B_O_EMPTY + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_bf16_ss(tmem + kTmO1, desc_kmajor_sw128(sb + off), desc_kmajor_sw128(kq + 8192 + off),
-                                    kIdescO, ks > 0);
-                    }
-                    if (!(ok = wait_bar(cx, B_DD_FULL + s, ph))) break;
-                    tc_fence_after();
-                    const uint32_t pb = smem_u32(sm + kPb + s * 8192);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        mma_bf16_ts(tmem + kTmO2, dbuf + ks * 8, desc_kmajor_sw128(pb + ks * 32), kIdescO, ks > 0);
-                        mma_bf16_ts(tmem + kTmS, dbuf + 32 + ks * 8, desc_mnmajor_sw128(kq + ks * 2048, 16384),
-                                    kIdescS, 1);
-                    }
-                    mma_commit(cx.bars + B_S_FULL + s);
-                    mma_commit(cx.bars + B_KQ_EMPTY + s);
-                }
-            }
-            mma_commit(cx.bars + B_DRAIN_S);
-            drain_bar(cx, B_DRAIN_S, 0);
-        }
-    } else if (warp == 3) {
-        // ================= gates warp: G, gamma, beta and factor vectors per chunk =================
-        uint32_t n = 0, u = 0;
-        bool ok = true;
-        for (; ok;) {
-            const int slot = u & 1;
-            if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
-            const UnitInfo info = read_unit(sm, slot);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
-            ++u;
-            if (!info.valid) break;
-            GatePrefetch gpf{1.f, 1.f, 0.f, 0.f};
-            if (info.nC > 0)
-                gpf = load_gates(p, info.t0, info.L < kChunk ? static_cast<int32_t>(info.L) : kChunk, info.h, lane);
-            for (int32_t c = 0; c < info.nC; ++c, ++n) {
-                const int gs = n & 1;
-                const GatePrefetch cur = gpf;
-                if (c + 1 < info.nC) {
-                    const int64_t rem1 = info.L - static_cast<int64_t>(c + 1) * kChunk;
-                    gpf = load_gates(p, info.t0 + static_cast<int64_t>(c + 1) * kChunk,
-                                     rem1 < kChunk ? static_cast<int32_t>(rem1) : kChunk, info.h, lane);
-                }
-                if (n >= 2 && !(ok = wait_bar(cx, B_GATES_EMPTY + gs, ((n - 2) >> 1) & 1))) break;
-                compute_gates(cur, reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats, p.scale, lane);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(cx.bars + B_GATES_FULL + gs);
+                if (lane == 0) mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
+                ++u;
+                if (!info.valid) break;
+                GatePrefetch gpf{1.f, 1.f, 0.f, 0.f};
+                if (info.nC > 0)
+                    gpf = load_gates(p, info.t0, info.L < kChunk ? static_cast<int32_t>(info.L) : kChunk, info.h, lane);
+                for (int32_t c = 0; c < info.nC; ++c, ++n) {
+                    const int gs = n & 1;
+                    const GatePrefetch cur = gpf;
+                    if (c + 1 < info.nC) {
+                        const int64_t rem1 = info.L - static_cast<int64_t>(c + 1) * kChunk;
+                        gpf = load_gates(p, info.t0 + static_cast<int64_t>(c + 1) * kChunk,
+                                         rem1 < kChunk ? static_cast<int32_t>(rem1) : kChunk, info.h, lane);
+                    }
+                    if (n >= 2 && !(ok = wait_bar(cx, B_GATES_EMPTY + gs, ((n - 2) >> 1) & 1))) break;
+                    const uint8_t* qt = nullptr;
+                    if (p.l2norm) {
+                        if (!(ok = wait_bar(cx, B_KQ_FULL + gs, (n >> 1) & 1))) break;
+                        qt = sm + kKQ + gs * kKQStage + 8192;
+                    }
+                    const int64_t rem = info.L - static_cast<int64_t>(c) * kChunk;
+                    compute_gates(cur, reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats, p.scale, qt,
+                                  rem < kChunk ? static_cast<int32_t>(rem) : kChunk, lane);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(cx.bars + B_GATES_FULL + gs);
+                }
             }
         }
-    } else if (warp >= 4 && warp < 12) {
+    } else if (warp < 12) {
+        if (kRegsIntra > kRegsLaunch) regs_inc<kRegsIntra>();
         // ================= intra warpgroups (two; each TMEM lane row split in column halves) =================
         const int it = tid - 128;                      // 0..255
         const int wq = warp & 3;                       // TMEM lane quarter
@@ -639,23 +662,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = wait_bar(cx, B_D1_FULL, n & 1))) break;
                 tc_fence_after();
                 if (p.l2norm) {
-                    // k norms: the diagonal of K K^T (lanes 0..63); q norms: the Q tile rows (lanes 64..127)
-                    if (hh == 0) {
-                        if (r < 64) {
-                            uint32_t rr[32];
-                            tmem_ld32_wait(tm_lane + kTmD1 + 32 * wq, rr);
-                            float kk = 0.f;
+                    // k norms: the diagonal of K K^T (lanes 0..63)
+                    if (hh == 0 && r < 64) {
+                        uint32_t rr[32];
+                        tmem_ld32_wait(tm_lane + kTmD1 + 32 * wq, rr);
+                        float kk = 0.f;
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) kk = (j == lane) ? __uint_as_float(rr[j]) : kk;
-                            const float rn = r < Lc ? rsqrtf(kk + 1e-6f) : 0.f;
-                            gb[kGRn + r] = rn;
-                            gb[kGRa + r] *= rn;
-                        } else {
-                            const int i = r - 64;
-                            const float rm = i < Lc ? rsqrtf(row_sumsq(sm + kKQ + s * kKQStage + 8192, i) + 1e-6f) : 0.f;
-                            gb[kGRm + i] = rm;
-                            gb[kGOr + i] *= rm;
-                        }
+                        for (int j = 0; j < 32; ++j) kk = (j == lane) ? __uint_as_float(rr[j]) : kk;
+                        const float rn = r < Lc ? rsqrtf(kk + 1e-6f) : 0.f;
+                        gb[kGRn + r] = rn;
+                        gb[kGRa + r] *= rn;
                     }
                     named_bar_sync(kBarIntra, kIntraThreads);
                     if (hh == 1 && r < 64) {  // column factors that meet n_j (read only after T')
@@ -728,8 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<uint4*>(base + (cch >> 3) * hs + sw128_offset(zr, cch & 7)) = z;
                     }
                 }
-                fence_proxy_async_smem();
-                tc_fence_before();
+                tc_fence_before();  // P and the zeroed tile rows reach the async proxy with the T' and Wb fences
                 named_bar_sync(kBarIntra, kIntraThreads);
                 if (it == 0) mbar_arrive(cx.bars + B_D1_EMPTY);
                 // T = (I + A)^-1, then T' = T diag(cw) (lanes 0..63), T'' = T diag(beta) (64..127)
@@ -791,10 +806,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it == 0) mbar_arrive(cx.bars + B_WB_FULL + s);
             }
         }
-    } else if (warp >= 12) {
-        // ================= state warpgroup =================
-        const int t = tid - 384;                       // 0..127 = TMEM lane = state row v
-        const uint32_t tm_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    } else {
+        // ================= state warpgroups (two; each TMEM lane row split in column halves) =================
+        if (kRegsState > kRegsLaunch) regs_inc<kRegsState>();
+        const int st = tid - 384;                      // 0..255
+        const int wq = warp & 3;
+        const int hh = (warp - 12) >> 2;               // column half
+        const int v = wq * 32 + lane;                  // TMEM lane = state row v
+        const uint32_t tm_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         uint8_t* sb = sm + kSb;
         __nv_bfloat16* outT = reinterpret_cast<__nv_bfloat16*>(sm + kOutT);
         uint32_t n = 0, u = 0;
@@ -803,18 +822,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int slot = u & 1;
             if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
             const UnitInfo info = read_unit(sm, slot);
-            named_bar_sync(kBarState, kWgThreads);
-            if (t == 0) mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
+            named_bar_sync(kBarState, kStateThreads);
+            if (st == 0) mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
             ++u;
             if (!info.valid) break;
             const size_t state_off = (static_cast<size_t>(info.srow) * H + info.h) * kHead * kHead +
-                                     static_cast<size_t>(t) * kHead;
+                                     static_cast<size_t>(v) * kHead + 64 * hh;  // this thread's 64 columns
             const float* s0 = p.initial_state ? p.initial_state + state_off : nullptr;
             if (info.nC == 0) {
                 if (p.output_state) {
                     float* dst = p.output_state + state_off;
 #pragma unroll 4
-                    for (int c0 = 0; c0 < kHead; c0 += 4)
+                    for (int c0 = 0; c0 < 64; c0 += 4)
                         *reinterpret_cast<float4*>(dst + c0) =
                             s0 ? *reinterpret_cast<const float4*>(s0 + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
@@ -825,26 +844,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = wait_bar(cx, B_GATES_FULL + (n & 1), (n >> 1) & 1))) break;
                 const float g63 = reinterpret_cast<const float*>(sm + kGbuf)[(n & 1) * kGFloats + kGGam + 63];
 #pragma unroll 1
-                for (int c0 = 0; c0 < kHead; c0 += 32) {
+                for (int c0 = 0; c0 < 64; c0 += 32) {
                     float x[32];
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
                         const float4 f = s0 ? *reinterpret_cast<const float4*>(s0 + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
                         x[j] = f.x; x[j + 1] = f.y; x[j + 2] = f.z; x[j + 3] = f.w;
                     }
-                    uint8_t* half = sb + (c0 >> 6) * 16384;
+                    uint8_t* half = sb + hh * 16384;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) st_chunk_bf16(half, t, ((c0 & 63) >> 3) + q, x + 8 * q);
+                    for (int q = 0; q < 4; ++q) st_chunk_bf16(half, v, (c0 >> 3) + q, x + 8 * q);
                     uint32_t r[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j] * g63);
-                    tmem_st32(tm_lane + kTmS + c0, r);
+                    tmem_st32(tm_lane + kTmS + 64 * hh + c0, r);
                 }
                 tmem_wait_st();
                 fence_proxy_async_smem();
                 tc_fence_before();
-                named_bar_sync(kBarState, kWgThreads);
-                if (t == 0) mbar_arrive(cx.bars + B_SB_FULL + (n & 1));
+                named_bar_sync(kBarState, kStateThreads);
+                if (st == 0) mbar_arrive(cx.bars + B_SB_FULL + (n & 1));
             }
             for (int32_t c = 0; c < info.nC && ok; ++c, ++n) {
                 const int s = n & 1;
@@ -854,40 +873,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t Lc = rem < kChunk ? static_cast<int32_t>(rem) : kChunk;
                 const float* gb = reinterpret_cast<const float*>(sm + kGbuf) + s * kGFloats;
                 const uint32_t dbuf = tm_lane + kTmDelta + s * 64;
-                // ---- Delta epilogue: bf16 Delta^T and decayed Delta^T back into TMEM (A operands)
+                // ---- Delta epilogue: this thread's 32 columns j in [32 hh, 32 hh + 32) go back into TMEM as
+                //      16 packed bf16 Delta words followed by 16 packed decayed words (A operands of O2 and S)
                 if (!(ok = wait_bar(cx, B_DELTA_FULL + s, ph))) break;
-                if (!(ok = wait_bar(cx, B_WB_FULL + s, ph))) break;  // factor vectors of chunk n are final
+                if (!(ok = wait_bar(cx, B_WB_FULL + s, ph))) break;  // key-norm factors of chunk n are final
                 tc_fence_after();
                 {
-                    uint32_t ra[32], rb[32];
-                    tmem_ld32_wait(dbuf, ra);
-                    tmem_ld32_wait(dbuf + 32, rb);
-                    // every fp32 column is in registers now: the packed copies may overwrite them
-                    uint32_t pk[16];
+                    uint32_t ra[32], pk[16];
+                    tmem_ld32_wait(dbuf + 32 * hh, ra);
 #pragma unroll
                     for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(__uint_as_float(ra[2 * q]), __uint_as_float(ra[2 * q + 1]));
-                    tmem_st16(dbuf, pk);
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(__uint_as_float(rb[2 * q]), __uint_as_float(rb[2 * q + 1]));
-                    tmem_st16(dbuf + 16, pk);
+                    tmem_st16(dbuf + 32 * hh, pk);
                     float dv[16];
 #pragma unroll
-                    for (int part = 0; part < 4; ++part) {
-                        lds16(gb + kGDec + 16 * part, dv);
+                    for (int part = 0; part < 2; ++part) {
+                        lds16(gb + kGDec + 32 * hh + 16 * part, dv);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const uint32_t a = (part < 2) ? ra[16 * part + 2 * q] : rb[16 * (part - 2) + 2 * q];
-                            const uint32_t b = (part < 2) ? ra[16 * part + 2 * q + 1] : rb[16 * (part - 2) + 2 * q + 1];
-                            pk[8 * (part & 1) + q] = pack_bf16x2(__uint_as_float(a) * dv[2 * q], __uint_as_float(b) * dv[2 * q + 1]);
-                        }
-                        if (part & 1) tmem_st16(dbuf + 32 + 16 * (part >> 1), pk);
+                        for (int q = 0; q < 8; ++q)
+                            pk[8 * part + q] = pack_bf16x2(__uint_as_float(ra[16 * part + 2 * q]) * dv[2 * q],
+                                                           __uint_as_float(ra[16 * part + 2 * q + 1]) * dv[2 * q + 1]);
                     }
+                    tmem_st16(dbuf + 32 * hh + 16, pk);
                     tmem_wait_st();
                 }
                 tc_fence_before();
-                named_bar_sync(kBarState, kWgThreads);
-                if (t == 0) mbar_arrive(cx.bars + B_DD_FULL + s);
-                // ---- state epilogue: checkpoint / final state, next S operand, prescale
+                named_bar_sync(kBarState, kStateThreads);
+                if (st == 0) mbar_arrive(cx.bars + B_DD_FULL + s);
+                // ---- state epilogue: checkpoint / final state, next S operand, prescale (this thread's 64 columns)
                 if (!(ok = wait_bar(cx, B_S_FULL + s, ph))) break;
                 tc_fence_after();
                 const bool last = (c + 1 == info.nC);
@@ -901,69 +913,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float* ck = nullptr;
                     if (p.checkpoints && p.ckpt_n > 0 && pend % p.ckpt_n == 0 && pend <= info.L)
                         ck = p.checkpoints + (static_cast<size_t>(info.ckpt_base + pend / p.ckpt_n - 1) * H + info.h) *
-                                                 kHead * kHead + static_cast<size_t>(t) * kHead;
+                                                 kHead * kHead + static_cast<size_t>(v) * kHead + 64 * hh;
                     float* fin = (last && p.output_state) ? p.output_state + state_off : nullptr;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < kHead; c0 += 32) {
-                        uint32_t r[32];
-                        tmem_ld32_wait(tm_lane + kTmS + c0, r);
-                        float x[32];
+                    for (int c0 = 0; c0 < 64; c0 += 16) {
+                        uint32_t r[16];
+                        tmem_ld16_wait(tm_lane + kTmS + 64 * hh + c0, r);
+                        float x[16];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+                        for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(r[j]);
                         if (ck) {
 #pragma unroll
-                            for (int j = 0; j < 32; j += 4)
+                            for (int j = 0; j < 16; j += 4)
                                 *reinterpret_cast<float4*>(ck + c0 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
                         }
                         if (fin) {
 #pragma unroll
-                            for (int j = 0; j < 32; j += 4)
+                            for (int j = 0; j < 16; j += 4)
                                 *reinterpret_cast<float4*>(fin + c0 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
                         }
                         if (!last) {
-                            uint8_t* half = sb + (c0 >> 6) * 16384;
+                            uint8_t* half = sb + hh * 16384;
+                            st_chunk_bf16(half, v, c0 >> 3, x);
+                            st_chunk_bf16(half, v, (c0 >> 3) + 1, x + 8);
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) st_chunk_bf16(half, t, ((c0 & 63) >> 3) + q, x + 8 * q);
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j] * gnext);
-                            tmem_st32(tm_lane + kTmS + c0, r);
+                            for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(x[j] * gnext);
+                            tmem_st16(tm_lane + kTmS + 64 * hh + c0, r);
                         }
                     }
                     if (!last) tmem_wait_st();
                 }
-                if (t == 0) bulk_wait_group_read0();  // the previous chunk's output store has read outT
+                if (st == 0) bulk_wait_group_read0();  // the previous chunk's output store has read outT
                 fence_proxy_async_smem();
                 tc_fence_before();
-                named_bar_sync(kBarState, kWgThreads);
-                if (t == 0 && !last) mbar_arrive(cx.bars + B_SB_FULL + ((n + 1) & 1));
-                // ---- output epilogue: o_i = orow_i (S Q^T)_i + scale (Delta^T P^T)_i
+                named_bar_sync(kBarState, kStateThreads);
+                if (st == 0 && !last) mbar_arrive(cx.bars + B_SB_FULL + ((n + 1) & 1));
+                // ---- output epilogue: o_i = orow_i (S Q^T)_i + scale (Delta^T P^T)_i, tokens i in [32 hh, 32 hh + 32)
                 {
                     const float sc = p.scale;
-#pragma unroll 1
-                    for (int i0 = 0; i0 < kChunk; i0 += 32) {
-                        uint32_t r1[32], r2[32];
-                        tmem_ld32_wait(tm_lane + kTmO1 + i0, r1);
-                        tmem_ld32_wait(tm_lane + kTmO2 + i0, r2);
-                        float orow[32];
-                        lds16(gb + kGOr + i0, orow);
-                        lds16(gb + kGOr + i0 + 16, orow + 16);
+                    uint32_t r1[32], r2[32];
+                    tmem_ld32_wait(tm_lane + kTmO1 + 32 * hh, r1);
+                    tmem_ld32_wait(tm_lane + kTmO2 + 32 * hh, r2);
+                    float orow[16];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float o = orow[j] * __uint_as_float(r1[j]) + sc * __uint_as_float(r2[j]);
-                            outT[(i0 + j) * kHead + t] = __float2bfloat16_rn(o);
+                    for (int part = 0; part < 2; ++part) {
+                        lds16(gb + kGOr + 32 * hh + 16 * part, orow);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int jj = 16 * part + j;
+                            const float o = orow[j] * __uint_as_float(r1[jj]) + sc * __uint_as_float(r2[jj]);
+                            outT[(32 * hh + jj) * kHead + v] = __float2bfloat16_rn(o);
                         }
                     }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                named_bar_sync(kBarState, kWgThreads);
-                if (t == 0) {
+                named_bar_sync(kBarState, kStateThreads);
+                if (st == 0) {
                     mbar_arrive(cx.bars + B_O_EMPTY + s);
                     mbar_arrive(cx.bars + B_GATES_EMPTY + s);
                 }
                 if (Lc == kChunk) {
                     // a full chunk: one TMA store of the 64 x 128 tile (rows all belong to this sequence)
-                    if (t == 0) {
+                    if (st == 0) {
                         tma_store_3d(&tm_o, sm + kOutT, 0, info.h, static_cast<int32_t>(tc));
                         bulk_commit_group();
                     }
@@ -971,12 +983,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the tail: coalesced copy of the valid rows only, 16 threads per 256-byte row
                     uint8_t* gout = static_cast<uint8_t*>(p.output);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int id = t + 128 * k, row = id >> 4, col = id & 15;
+                    for (int k = 0; k < 4; ++k) {
+                        const int id = st + 256 * k, row = id >> 4, col = id & 15;
                         if (row < Lc) {
-                            const uint4 v = *reinterpret_cast<const uint4*>(sm + kOutT + row * 256 + col * 16);
+                            const uint4 val = *reinterpret_cast<const uint4*>(sm + kOutT + row * 256 + col * 16);
                             *reinterpret_cast<uint4*>(gout + ((static_cast<size_t>(tc + row) * H + info.h) * kHead) * 2 +
-                                                      col * 16) = v;
+                                                      col * 16) = val;
                         }
                     }
                 }
@@ -985,7 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- teardown
-    if (warp >= 12 && tid == 384) bulk_wait_group0();  // output stores in flight have landed
+    if (tid == 384) bulk_wait_group0();  // output stores in flight have landed
     tc_fence_before();
     __syncthreads();
     if (warp == 3) tmem_dealloc(tmem, kTmCols);
