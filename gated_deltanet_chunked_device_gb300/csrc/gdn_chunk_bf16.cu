@@ -10,7 +10,7 @@
 //     D1 = [K; Q] K^T                               tcgen05, M=128 N=64 K=128
 //     A_ij = beta_i e^{G_i-G_j} n_i n_j (k_i.k_j), j < i
 //     P_ij = e^{G_i-G_j} m_i n_j (q_i.k_j),       j <= i
-//     T = (I + A)^-1                                blocked substitution, CUDA cores
+//     T = (I + A)^-1                                blocked substitution + tf32 mma.sync
 //     W^T = K^T (T diag(beta gamma n))^T,  U^T = V^T (T diag(beta))^T   tcgen05
 //   state pass ("块内 state 和块间 final state": only the chunk's last state
 //   crosses the boundary):
@@ -24,16 +24,19 @@
 // only as the per-row factors n and m above, applied in fp32: the same values
 // as normalising the rows first, without re-rounding them to bf16.
 //
-// Roles (384 threads, one work unit = (sequence, state head) at a time,
-// units taken longest first from an atomic counter):
-//   warp 0      TMA: K, Q tiles (2 stages) and V tile; unit scheduler
-//   warp 1      tcgen05 issue for the intra-chunk products (D1, W, U)
-//   warp 2      tcgen05 issue for the state chain (Delta, S Q^T, Delta P^T, S)
-//   warp 3      TMEM allocation
-//   warps 4-7   intra warpgroup: gates, A and P, T, W to shared memory,
-//               one chunk ahead of the state warpgroup
-//   warps 8-11  state warpgroup: Delta epilogue, state epilogue (next S
-//               operand, checkpoints, final state), output epilogue
+// Roles (640 threads in five warpgroups, one work unit = (sequence, state
+// head) at a time, units taken longest first from an atomic counter):
+//   warp 0       TMA: K, Q tiles (2 stages) and V tile; unit scheduler
+//   warp 1       tcgen05 issue for the intra-chunk products (D1, W, U)
+//   warp 2       tcgen05 issue for the state chain (Delta, S Q^T, Delta P^T, S)
+//   warp 3       TMEM allocation; gates: G, gamma, beta, the q and k row
+//                norms and the per-row / per-column factor vectors
+//   warps 4-11   two intra warpgroups (TMEM lane quarter x column half):
+//                A and P, T in place with T' and T'', W to shared memory,
+//                one chunk ahead of the state warpgroups
+//   warps 12-19  two state warpgroups (lane quarter x column half): Delta
+//                epilogue, state epilogue (next S operand, checkpoints,
+//                final state), output epilogue
 // Every wait is bounded; a timeout sets GDN_DEVICE_ERR_TIMEOUT, raises a
 // shared abort flag that every other wait polls, drains the CTA's in-flight
 // copies and tensor-core work, frees TMEM and returns.
@@ -48,7 +51,6 @@ namespace {
 constexpr int kThreads = 640;
 constexpr int kStateThreads = 256;  // two state warpgroups
 constexpr int kIntraThreads = 256;  // two intra warpgroups
-constexpr uint32_t kRegsLaunch = 96, kRegsSched = 64, kRegsIntra = 96, kRegsState = 104;  // per thread
 constexpr uint32_t kBarIntra = 1, kBarState = 2;  // named barrier ids
 
 // ---- shared memory map (bytes from a 1024-aligned base)
@@ -61,34 +63,36 @@ constexpr uint32_t kPb = 98304;       // 2 x P bf16 [64 i][64 j] K-major
 constexpr uint32_t kWb = 114688;      // W^T bf16 as MN-major B: [128 k][64 i]
 constexpr uint32_t kSb = 131072;      // S bf16 K-major: 2 halves of [128 v][64 k]
 constexpr uint32_t kAbuf = 163840;    // A fp32 [64][kLd]
-constexpr uint32_t kTbuf = 181248;    // T fp32 [64][kLd]
-constexpr uint32_t kXs = 198656;      // inverse scratch: [2][16][20] then [32][36] fp32
+constexpr uint32_t kXs = 181248;      // inverse scratch: [2][16][24] then [32][40] fp32
 constexpr uint32_t kOutT = 205824;    // output tile bf16 [64 i][128 v]
 constexpr uint32_t kGbuf = 222208;    // 2 x kGFloats floats of per-row / per-column factors (see kG*)
-constexpr uint32_t kBars = 229504;    // 32 mbarriers
-constexpr uint32_t kRing = 229760;    // 2 unit descriptors
-constexpr uint32_t kMisc = 229888;    // tmem base, abort flag
+constexpr uint32_t kBars = 189440;    // up to 64 mbarriers
+constexpr uint32_t kRing = 189952;    // 2 unit descriptors
+constexpr uint32_t kMisc = 190080;    // tmem base, abort flag
 constexpr uint32_t kSmemBytes = 229952;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 constexpr int kLd = 68;               // fp32 row stride of A and T (bank-conflict free rows)
 
 // gbuf field offsets (floats), one 64-vector each, per chunk:
 //   G      running sum of log alpha            gamma  e^G
-//   beta   beta (0 on padded rows)             rn, rm 1/|k_j|, 1/|q_i| (1 without the L2 norm)
-//   cw     beta_j gamma_j rn_j (T' columns)    dec    e^{G_63 - G_j} rn_j (decayed Delta columns)
-//   orow   scale gamma_i rm_i (output rows)    ra     beta_i rn_i (A rows)
-//   colf   rn_j e^{G_16b - G_j}, b = j / 16      rowf   [4][64] e^{G_i - G_16b} (i >= 16 b, else 0)
+//   beta   beta (0 on padded rows)             rn     1/|k_j| (1 without the L2 norm; written by the
+//                                                      intra warps that hold the K K^T diagonal)
+//   rm     1/|q_i| (1 without the L2 norm)     cw     beta_j gamma_j (T' columns, times rn_j^2)
+//   dec    e^{G_63 - G_j} (decayed Delta)      orow   scale gamma_i rm_i (output rows)
+//   ra     beta_i (A rows, times rn_i^2)       colf   e^{G_16b - G_j}, b = j / 16
+//   rowf   [4][64] e^{G_i - G_16b} (i >= 16 b, else 0)
 //   safe   1 when the chunk's G range is small enough for e^{G_i - G_j} = rowf * colf
 constexpr int kGG = 0, kGGam = 64, kGBeta = 128, kGRn = 192, kGRm = 256, kGCw = 320, kGDec = 384, kGOr = 448,
               kGRa = 512, kGColf = 576, kGRowf = 640, kGSafe = 896, kGFloats = 912;
-static_assert(2 * kGFloats * 4 <= kBars - kGbuf, "gbuf overflows");
+static_assert(2 * kGFloats * 4 <= kSmemBytes - kGbuf, "gbuf overflows");
+static_assert(kXs + 4 * (2 * 16 * 24 + 32 * 40) <= kBars && kMisc + 64 <= kOutT, "scratch / barrier block overlap");
 
 // ---- barriers
 enum {
     B_KQ_FULL = 0, B_KQ_EMPTY = 2, B_V_FULL = 4, B_V_EMPTY = 5, B_D1_FULL = 6, B_D1_EMPTY = 7, B_T_FULL = 8,
     B_WU_FULL = 9, B_WB_FULL = 10, B_SB_FULL = 12, B_DELTA_FULL = 14, B_DD_FULL = 16, B_S_FULL = 18,
     B_O_EMPTY = 20, B_GATES_FULL = 22, B_GATES_EMPTY = 24, B_UNIT_FULL = 26, B_UNIT_EMPTY = 28,
-    B_DRAIN_I = 30, B_DRAIN_S = 31, B_COUNT = 32
+    B_DRAIN_I = 30, B_DRAIN_S = 31, B_QN_FULL = 32, B_COUNT = 34
 };
 
 // ---- TMEM columns
@@ -118,9 +122,8 @@ struct Ctx {
 };
 
 // Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_bar(const Ctx& cx, int b, uint32_t parity) {
+__device__ __forceinline__ bool wait_loop(const Ctx& cx, int b, uint32_t parity) {
     uint64_t* bar = cx.bars + b;
-    if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, 2000)) return true;
@@ -131,6 +134,16 @@ __device__ __forceinline__ bool wait_bar(const Ctx& cx, int b, uint32_t parity) 
             return false;
         }
     }
+}
+
+// Every role shares one out-of-line copy of the sleeping loop: the many wait
+// sites stay small, which keeps the per-chunk code of all twenty warps
+// resident in the instruction cache.
+__device__ __noinline__ bool wait_bar_slow(const Ctx& cx, int b, uint32_t parity) { return wait_loop(cx, b, parity); }
+
+__device__ __forceinline__ bool wait_bar(const Ctx& cx, int b, uint32_t parity) {
+    if (mbar_try_wait(cx.bars + b, parity)) return true;
+    return wait_bar_slow(cx, b, parity);
 }
 
 // Bounded wait used while draining (ignores the abort flag).
@@ -161,17 +174,21 @@ __device__ __forceinline__ UnitInfo read_unit(const uint8_t* sm, int slot) {
 }
 
 // ===========================================================================
-// Triangular inverse T = (I + A)^-1 of a strictly lower 64 x 64 A (fp32,
-// rows of kLd floats), by the two intra warpgroups (256 threads, 8 warps):
-//   level 0: the four 16 x 16 diagonal blocks by forward substitution, one
-//            column per thread (fp32);
-//   level 1: T_ab = -T_aa A_ab T_bb for (a, b) = (1, 0), (3, 2);
-//   level 2: T_21 = -T_22 A_21 T_11 on 32 x 32 blocks.
-// The level 1 and 2 products are 16- and 32-row matrices, below the 64-row
-// minimum of tcgen05.mma, so they run as warp-level m16n8k8 tf32 MMAs (fp32
-// accumulate); T is later rounded to bf16 for the W and U products anyway.
-// On return T holds the lower triangle including the diagonal; the upper
-// triangle is unspecified.
+// Triangular inverse T = (I + A)^-1 of a strictly lower 64 x 64 A (fp32, rows
+// of kLd floats), computed in place by the two intra warpgroups (256 threads),
+// followed by the two bf16 operands of the W and U products,
+// T' = T diag(cw) and T'' = T diag(beta) (K-major [64 i][64 j], 128-byte
+// swizzle; their blocks above the diagonal are never written and stay zero).
+//   stage 1 (warps 0, 1; warp w owns rows and columns 32w..32w+31): the two
+//     16 x 16 diagonal blocks by forward substitution, one column per lane,
+//     then the block under them, T_10 = -T_11 (A_10 T_00), and a zeroed block
+//     above them, with no block-wide barrier;
+//   stage 2 (all eight warps): T_21 = -T_22 (A_21 T_11) on the 32 x 32 halves;
+//     its tiles go from the MMA fragments straight into T' and T'', while the
+//     two diagonal 32 x 32 blocks are converted from shared memory.
+// The 16- and 32-row products are below the 64-row minimum of tcgen05.mma, so
+// they run as warp-level m16n8k8 tf32 MMAs (fp32 accumulate); T is rounded to
+// bf16 for the W and U products anyway.
 // ===========================================================================
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
@@ -200,77 +217,125 @@ __device__ __forceinline__ void store_tile_16x8(float* C, int ldc, const float (
     *reinterpret_cast<float2*>(C + (g + 8) * ldc + 2 * t) = make_float2(sign * d[2], sign * d[3]);
 }
 
-__device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ T, float* __restrict__ X1,
-                               float* __restrict__ X2, int t) {
+// Two adjacent bf16 values (row i, columns j, j + 1; j even) of a swizzled K-major [64][64] tile.
+__device__ __forceinline__ void st_pair_bf16(uint8_t* tile, int i, int j, float x0, float x1) {
+    *reinterpret_cast<uint32_t*>(tile + i * 128 + (((j >> 3) ^ (i & 7)) << 4) + (j & 7) * 2) = pack_bf16x2(x0, x1);
+}
+
+constexpr int kLdX1 = 24, kLdX2 = 40;  // scratch strides: conflict-free B-fragment reads
+
+__device__ __forceinline__ void tri_inverse_64(float* __restrict__ A, uint8_t* __restrict__ tp,
+                                               uint8_t* __restrict__ tpp, const float* __restrict__ cw,
+                                               const float* __restrict__ beta, const float* __restrict__ rn,
+                                               float* __restrict__ X1, float* __restrict__ X2, int t) {
     const int wi = t >> 5, lane = t & 31;  // warp index 0..7 within the intra groups
-    if (t < 64) {
-        const int o = (t >> 4) * 16, col = t & 15;
+    if (wi < 2) {
+        // ---- stage 1: diagonal 16 x 16 blocks, one column per lane
+        const int o = (wi * 2 + (lane >> 4)) * 16, col = lane & 15;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             const float* arow = A + (o + r) * kLd + o;
             float acc0 = (r == col) ? 1.f : 0.f, acc1 = 0.f;
 #pragma unroll
-            for (int m = 0; m + 1 < r; m += 2) {
-                acc0 -= arow[m] * x[m];
-                acc1 -= arow[m + 1] * x[m + 1];
+            for (int m = 0; m + 3 < r; m += 4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(arow + m);
+                acc0 -= a4.x * x[m];
+                acc1 -= a4.y * x[m + 1];
+                acc0 -= a4.z * x[m + 2];
+                acc1 -= a4.w * x[m + 3];
             }
-            if (r & 1) acc0 -= arow[r - 1] * x[r - 1];
+#pragma unroll
+            for (int m = r & ~3; m < r; ++m) acc0 -= arow[m] * x[m];
             x[r] = (r < col) ? 0.f : acc0 + acc1;
         }
+        __syncwarp();
 #pragma unroll
-        for (int r = 0; r < 16; ++r) T[(o + r) * kLd + o + col] = x[r];
-    } else if (t < 128) {
-        // zero the upper blocks (0,1) and (2,3) so that T_11, T_22 read as triangular
-        const int idx = t - 64;            // 64 threads x 8 values = 2 blocks x 256
-        const int blk = idx >> 5, r = (idx & 31) >> 1, c0 = (idx & 1) * 8;
-        const int ro = blk * 32, co = blk * 32 + 16;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) T[(ro + r) * kLd + co + c0 + q] = 0.f;
+        for (int r = 0; r < 16; ++r) A[(o + r) * kLd + o + col] = x[r];
+        {   // the block above the pair is zero: rows 32w..32w+15, columns 32w+16..32w+31
+            float* z = A + (32 * wi + (lane >> 1)) * kLd + 32 * wi + 16 + (lane & 1) * 8;
+            *reinterpret_cast<float4*>(z) = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(z + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncwarp();
+        // ---- T_10 = -T_11 (A_10 T_00) inside the warp's 32 x 32 block
+        const int b0 = 32 * wi, b1 = b0 + 16;
+        float* xs = X1 + wi * 16 * kLdX1;
+#pragma unroll 1
+        for (int nt = 0; nt < 16; nt += 8) {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+            for (int k0 = 0; k0 < 16; k0 += 8)
+                mma_tf32_16x8x8(d, A + b1 * kLd + b0 + k0, kLd, A + (b0 + k0) * kLd + b0 + nt, kLd, lane);
+            store_tile_16x8(xs + nt, kLdX1, d, 1.f, lane);
+        }
+        __syncwarp();
+#pragma unroll 1
+        for (int nt = 0; nt < 16; nt += 8) {
+            float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+            for (int k0 = 0; k0 < 16; k0 += 8)
+                mma_tf32_16x8x8(e, A + b1 * kLd + b1 + k0, kLd, xs + k0 * kLdX1 + nt, kLdX1, lane);
+            store_tile_16x8(A + b1 * kLd + b0 + nt, kLd, e, -1.f, lane);
+        }
     }
     named_bar_sync(kBarIntra, kIntraThreads);
-    // level 1: warps 0..3 each own one 16 x 8 output tile: block pair pr = wi >> 1, columns nt = wi & 1
-    if (wi < 4) {
-        const int pr = wi >> 1, nt = (wi & 1) * 8, a = 2 * pr + 1, b = 2 * pr;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k0 = 0; k0 < 16; k0 += 8)   // X_ab = A_ab T_bb
-            mma_tf32_16x8x8(d, A + (16 * a) * kLd + 16 * b + k0, kLd, T + (16 * b + k0) * kLd + 16 * b + nt, kLd, lane);
-        store_tile_16x8(X1 + pr * 16 * 20 + nt, 20, d, 1.f, lane);
-    }
-    named_bar_sync(kBarIntra, kIntraThreads);
-    if (wi < 4) {
-        const int pr = wi >> 1, nt = (wi & 1) * 8, a = 2 * pr + 1, b = 2 * pr;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k0 = 0; k0 < 16; k0 += 8)   // T_ab = -T_aa X_ab
-            mma_tf32_16x8x8(d, T + (16 * a) * kLd + 16 * a + k0, kLd, X1 + pr * 16 * 20 + k0 * 20 + nt, 20, lane);
-        store_tile_16x8(T + (16 * a) * kLd + 16 * b + nt, kLd, d, -1.f, lane);
-    }
-    named_bar_sync(kBarIntra, kIntraThreads);
-    // level 2: eight warps, one 16 x 8 tile each of the 32 x 32 products
+    // ---- stage 2: X = A_21 T_11 (one 16 x 8 tile per warp) and the diagonal 32 x 32 blocks of T' and T''
+    const int mt = (wi >> 2) * 16, nt = (wi & 3) * 8;
     {
-        const int mt = (wi >> 2) * 16, nt = (wi & 3) * 8;
         float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int k0 = 0; k0 < 32; k0 += 8)
+            mma_tf32_16x8x8(d, A + (32 + mt) * kLd + k0, kLd, A + k0 * kLd + nt, kLd, lane);
+        store_tile_16x8(X2 + mt * kLdX2 + nt, kLdX2, d, 1.f, lane);
+    }
+    {
+        const int blk = t >> 7, i = blk * 32 + ((t >> 2) & 31), j0 = blk * 32 + (t & 3) * 8;
+        const float* trow = A + i * kLd + j0;
+        const float4 t0 = *reinterpret_cast<const float4*>(trow);
+        const float4 t1 = *reinterpret_cast<const float4*>(trow + 4);
+        const float4 c0 = *reinterpret_cast<const float4*>(cw + j0);
+        const float4 c1 = *reinterpret_cast<const float4*>(cw + j0 + 4);
+        const float4 e0 = *reinterpret_cast<const float4*>(beta + j0);
+        const float4 e1 = *reinterpret_cast<const float4*>(beta + j0 + 4);
+        const float4 n0 = *reinterpret_cast<const float4*>(rn + j0);
+        const float4 n1 = *reinterpret_cast<const float4*>(rn + j0 + 4);
+        const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+        const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+        const float nv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+        float x[8], y[8];
 #pragma unroll
-        for (int k0 = 0; k0 < 32; k0 += 8)   // X = A_21 T_11
-            mma_tf32_16x8x8(d, A + (32 + mt) * kLd + k0, kLd, T + k0 * kLd + nt, kLd, lane);
-        store_tile_16x8(X2 + mt * 36 + nt, 36, d, 1.f, lane);
-        named_bar_sync(kBarIntra, kIntraThreads);
-        float e[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k0 = 0; k0 < 32; k0 += 8)   // T_21 = -T_22 X
-            mma_tf32_16x8x8(e, T + (32 + mt) * kLd + 32 + k0, kLd, X2 + k0 * 36 + nt, 36, lane);
-        store_tile_16x8(T + (32 + mt) * kLd + nt, kLd, e, -1.f, lane);
+        for (int q = 0; q < 8; ++q) {
+            const float tn = tv[q] * nv[q];
+            x[q] = tn * nv[q] * cv[q];
+            y[q] = tn * ev[q];
+        }
+        st_chunk_bf16(tp, i, j0 >> 3, x);
+        st_chunk_bf16(tpp, i, j0 >> 3, y);
     }
     named_bar_sync(kBarIntra, kIntraThreads);
+    // ---- T_21 = -T_22 X, written as T' and T'' tiles from the fragments
+    {
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int k0 = 0; k0 < 32; k0 += 8)
+            mma_tf32_16x8x8(e, A + (32 + mt) * kLd + 32 + k0, kLd, X2 + k0 * kLdX2 + nt, kLdX2, lane);
+        const int g = lane >> 2, j = nt + 2 * (lane & 3);
+        const int i0 = 32 + mt + g, i1 = i0 + 8;
+        const float n0 = rn[j], n1 = rn[j + 1];
+        const float be0 = beta[j] * n0, be1 = beta[j + 1] * n1, cw0 = cw[j] * n0 * n0, cw1 = cw[j + 1] * n1 * n1;
+        st_pair_bf16(tp, i0, j, -e[0] * cw0, -e[1] * cw1);
+        st_pair_bf16(tp, i1, j, -e[2] * cw0, -e[3] * cw1);
+        st_pair_bf16(tpp, i0, j, -e[0] * be0, -e[1] * be1);
+        st_pair_bf16(tpp, i1, j, -e[2] * be0, -e[3] * be1);
+    }
 }
 
 // ===========================================================================
 // Gates of one chunk (one warp; lane l owns rows 2l, 2l+1).  load_gates issues
 // the global loads early (alpha = 1, beta = 0 on padded rows); compute_gates
-// forms G = running sum of log alpha, gamma = e^G and the factor vectors as
-// they are without the L2 norm (rn = rm = 1).
+// forms G = running sum of log alpha, gamma = e^G and the factor vectors.
 // ===========================================================================
 struct GatePrefetch {
     float a0, a1, b0, b1;
@@ -296,7 +361,7 @@ __device__ __forceinline__ GatePrefetch load_gates(const ChunkParams& p, int64_t
 // halves 16 KB apart, 128-byte swizzle).
 __device__ __forceinline__ float row_sumsq(const uint8_t* half0, int r) {
     float ss = 0.f;
-#pragma unroll 4
+#pragma unroll 2
     for (int c = 0; c < 16; ++c) {
         float f[8];
         bf16x8_to_float(*reinterpret_cast<const uint4*>(half0 + (c >> 3) * 16384 + sw128_offset(r, c & 7)), f);
@@ -306,13 +371,24 @@ __device__ __forceinline__ float row_sumsq(const uint8_t* half0, int r) {
     return ss;
 }
 
-// The vectors of one chunk (see kG*): G, gamma, beta, and cw, dec, ra, colf
-// as they are with unit key norms (rn = 1), orow and rm with the query norms
-// when `q` (the staged Q tile) is given, else with rm = 1.  The intra
-// warpgroups multiply the key norms in once the K K^T diagonal is known.
-// Rows at or past Lc are padding (alpha = 1, beta = 0, rm = 0).
-__device__ void compute_gates(const GatePrefetch& g, float* gb, float scale, const uint8_t* q, int32_t Lc, int lane) {
+// Squared norms of rows 2 lane and 2 lane + 1 of a staged tile.  Each lane
+// sums rows lane and lane + 32 (eight consecutive rows meet all eight 16-byte
+// columns of the swizzle, so the reads are conflict-free), then the sums move
+// to the lanes that own the rows.
+__device__ __forceinline__ void pair_sumsq(const uint8_t* half0, int lane, float& s0, float& s1) {
+    const float lo = row_sumsq(half0, lane), hi = row_sumsq(half0, lane + 32);
     const int r0 = 2 * lane, r1 = r0 + 1;
+    const float a0 = __shfl_sync(0xffffffffu, lo, r0 & 31), b0 = __shfl_sync(0xffffffffu, hi, r0 & 31);
+    const float a1 = __shfl_sync(0xffffffffu, lo, r1 & 31), b1 = __shfl_sync(0xffffffffu, hi, r1 & 31);
+    s0 = r0 < 32 ? a0 : b0;
+    s1 = r1 < 32 ? a1 : b1;
+}
+
+// The vectors of one chunk (see kG*) that need no norm; orow and rm are left
+// to query_norms when the L2 norm is on.  Rows at or past Lc are padding
+// (alpha = 1, beta = 0).
+__device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, float scale, bool l2norm, int lane) {
+    const int r0 = 2 * lane;
     const float la0 = __logf(g.a0), la1 = __logf(g.a1);
     float incl = la0 + la1;
 #pragma unroll
@@ -325,12 +401,7 @@ __device__ void compute_gates(const GatePrefetch& g, float* gb, float scale, con
     float Gb[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) Gb[b] = __shfl_sync(0xffffffffu, G0, 8 * b);  // G at row 16 b
-    float rm0 = 1.f, rm1 = 1.f;
-    if (q) {
-        rm0 = r0 < Lc ? rsqrtf(row_sumsq(q, r0) + 1e-6f) : 0.f;
-        rm1 = r1 < Lc ? rsqrtf(row_sumsq(q, r1) + 1e-6f) : 0.f;
-    }
-    const float Gv[2] = {G0, G1}, bv[2] = {g.b0, g.b1}, rmv[2] = {rm0, rm1};
+    const float Gv[2] = {G0, G1}, bv[2] = {g.b0, g.b1};
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         const int r = r0 + k;
@@ -339,10 +410,12 @@ __device__ void compute_gates(const GatePrefetch& g, float* gb, float scale, con
         gb[kGGam + r] = e;
         gb[kGBeta + r] = bv[k];
         gb[kGRn + r] = 1.f;
-        gb[kGRm + r] = rmv[k];
         gb[kGCw + r] = bv[k] * e;
         gb[kGDec + r] = __expf(G63 - Gv[k]);
-        gb[kGOr + r] = scale * e * rmv[k];
+        if (!l2norm) {
+            gb[kGRm + r] = 1.f;
+            gb[kGOr + r] = scale * e;
+        }
         gb[kGRa + r] = bv[k];
         gb[kGColf + r] = __expf(Gb[r >> 4] - Gv[k]);
 #pragma unroll
@@ -355,6 +428,18 @@ __device__ void compute_gates(const GatePrefetch& g, float* gb, float scale, con
         gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
     }
     if (lane == 0) gb[kGSafe] = (gmax - gmin < 60.f) ? 1.f : 0.f;
+}
+
+// rm = 1/|q_i| of the staged Q tile and orow = scale gamma_i rm_i (padded rows 0).
+__device__ __forceinline__ void query_norms(const uint8_t* q, float* gb, float scale, int32_t Lc, int lane) {
+    float s0, s1;
+    pair_sumsq(q, lane, s0, s1);
+    const int r0 = 2 * lane, r1 = r0 + 1;
+    const float rm0 = r0 < Lc ? rsqrtf(s0 + 1e-6f) : 0.f, rm1 = r1 < Lc ? rsqrtf(s1 + 1e-6f) : 0.f;
+    gb[kGRm + r0] = rm0;
+    gb[kGRm + r1] = rm1;
+    gb[kGOr + r0] = scale * gb[kGGam + r0] * rm0;
+    gb[kGOr + r1] = scale * gb[kGGam + r1] * rm1;
 }
 
 __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]) {
@@ -376,6 +461,42 @@ __device__ __forceinline__ void lds16(const float* src, float* x) {
         x[q + 2] = v.z;
         x[q + 3] = v.w;
     }
+}
+
+// Intermediates for tests (only when requested): this thread's 32 values of W
+// and U (row r = k or v, columns i0..i0+31) and G, in fp32.  Out of line, so
+// the hot loop stays compact in the instruction cache.
+__device__ __noinline__ void dump_intra(float* intra_w, float* intra_u, float* intra_g, size_t dump, size_t gdump,
+                                        uint32_t tm_w, uint32_t tm_u, int r, int i0, int it, const float* G) {
+    uint32_t rr[32];
+    tmem_ld32_wait(tm_w, rr);
+    if (intra_w)
+        for (int j = 0; j < 32; ++j) intra_w[dump + static_cast<size_t>(i0 + j) * kHead + r] = __uint_as_float(rr[j]);
+    tmem_ld32_wait(tm_u, rr);
+    if (intra_u)
+        for (int j = 0; j < 32; ++j) intra_u[dump + static_cast<size_t>(i0 + j) * kHead + r] = __uint_as_float(rr[j]);
+    if (intra_g && it < 64) intra_g[gdump + it] = G[it];
+}
+
+// Start of a unit's state: S0 (this thread's row v, 64 columns) to its half of
+// the bf16 S operand and gamma_63 S0 to the TMEM accumulator (S0 null: zeros).
+// Once per unit, so out of line.
+__device__ __noinline__ void load_initial_state(const float* s0, uint8_t* half, uint32_t tm, int v, float g63) {
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+        float x[32];
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            const float4 f = s0 ? *reinterpret_cast<const float4*>(s0 + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            x[j] = f.x; x[j + 1] = f.y; x[j + 2] = f.z; x[j + 3] = f.w;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st_chunk_bf16(half, v, (c0 >> 3) + q, x + 8 * q);
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j] * g63);
+        tmem_st32(tm + c0, r);
+    }
+    tmem_wait_st();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -422,15 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const int32_t H = p.H;
-    // register split: launch 640 x 96; the scheduling warpgroup gives up 32 a thread, the state ones take 8 more
-    // (128 x 64 + 256 x 96 + 256 x 104 <= 640 x 96)
-    static_assert(128 * kRegsSched + kIntraThreads * kRegsIntra + kStateThreads * kRegsState <= kThreads * kRegsLaunch,
-                  "register split exceeds the launch budget");
     const int64_t units = static_cast<int64_t>(p.num_seqs) * H;
 
     if (warp < 4) {
         // the scheduling warpgroup: TMA producer, two MMA issuers, gates warp
-        regs_dec<kRegsSched>();
         if (warp == 0) {
             // ================= TMA producer and unit scheduler =================
             if (lane == 0) {
@@ -509,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (n >= 1 && !(ok = wait_bar(cx, B_D1_EMPTY, (n - 1) & 1))) break;
                         tc_fence_after();
                         const uint32_t kq = smem_u32(sm + kKQ + s * kKQStage);
-    #pragma unroll
+    #pragma unroll 1
                         for (int ks = 0; ks < 8; ++ks) {
                             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
                             mma_bf16_ss(tmem + kTmD1, desc_kmajor_sw128(kq + off), desc_kmajor_sw128(kq + off), kIdescD1,
@@ -523,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t vv = smem_u32(sm + kV);
                         const uint32_t tp = smem_u32(sm + kTp), tpp = smem_u32(sm + kTpp);
                         const uint32_t dbuf = tmem + kTmDelta + s * 64;
-    #pragma unroll
+    #pragma unroll 1
                         for (int ks = 0; ks < 4; ++ks) {
                             mma_bf16_ss(tmem + kTmW, desc_mnmajor_sw128(kq + ks * 2048, 16384),
                                         desc_kmajor_sw128(tp + ks * 32), kIdescWU, ks > 0);
@@ -559,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t kq = smem_u32(sm + kKQ + s * kKQStage);
                         const uint32_t sb = smem_u32(sm + kSb), wb = smem_u32(sm + kWb);
                         const uint32_t dbuf = tmem + kTmDelta + s * 64;
-    #pragma unroll
+    #pragma unroll 1
                         for (int ks = 0; ks < 8; ++ks) {
                             const uint32_t aoff = (ks >> 2) * 16384 + (ks & 3) * 32;
                             mma_bf16_ss(dbuf, desc_kmajor_sw128(sb + aoff), desc_mnmajor_sw128(wb + ks * 2048, 8192),
@@ -568,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_commit(cx.bars + B_DELTA_FULL + s);
                         if (n >= 1 && !(ok = wait_bar(cx, B_O_EMPTY + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
                         tc_fence_after();
-    #pragma unroll
+    #pragma unroll 1
                         for (int ks = 0; ks < 8; ++ks) {
                             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
                             mma_bf16_ss(tmem + kTmO1, desc_kmajor_sw128(sb + off), desc_kmajor_sw128(kq + 8192 + off),
@@ -577,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!(ok = wait_bar(cx, B_DD_FULL + s, ph))) break;
                         tc_fence_after();
                         const uint32_t pb = smem_u32(sm + kPb + s * 8192);
-    #pragma unroll
+    #pragma unroll 1
                         for (int ks = 0; ks < 4; ++ks) {
                             const uint32_t acol = dbuf + 32 * (ks >> 1) + 8 * (ks & 1);  // packed j = 16 ks .. 16 ks + 15
                             mma_bf16_ts(tmem + kTmO2, acol, desc_kmajor_sw128(pb + ks * 32), kIdescO, ks > 0);
@@ -614,21 +730,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          rem1 < kChunk ? static_cast<int32_t>(rem1) : kChunk, info.h, lane);
                     }
                     if (n >= 2 && !(ok = wait_bar(cx, B_GATES_EMPTY + gs, ((n - 2) >> 1) & 1))) break;
-                    const uint8_t* qt = nullptr;
-                    if (p.l2norm) {
-                        if (!(ok = wait_bar(cx, B_KQ_FULL + gs, (n >> 1) & 1))) break;
-                        qt = sm + kKQ + gs * kKQStage + 8192;
-                    }
                     const int64_t rem = info.L - static_cast<int64_t>(c) * kChunk;
-                    compute_gates(cur, reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats, p.scale, qt,
-                                  rem < kChunk ? static_cast<int32_t>(rem) : kChunk, lane);
+                    const int32_t Lc = rem < kChunk ? static_cast<int32_t>(rem) : kChunk;
+                    float* gbw = reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats;
+                    compute_gates(cur, gbw, p.scale, p.l2norm != 0, lane);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(cx.bars + B_GATES_FULL + gs);
+                    // query norms (needed only by the output epilogue) after the intra side has its vectors
+                    if (p.l2norm) {
+                        if (!(ok = wait_bar(cx, B_KQ_FULL + gs, (n >> 1) & 1))) break;
+                        query_norms(sm + kKQ + gs * kKQStage + 8192, gbw, p.scale, Lc, lane);
+                        __syncwarp();
+                    }
+                    if (lane == 0) mbar_arrive(cx.bars + B_QN_FULL + gs);
                 }
             }
         }
     } else if (warp < 12) {
-        if (kRegsIntra > kRegsLaunch) regs_inc<kRegsIntra>();
         // ================= intra warpgroups (two; each TMEM lane row split in column halves) =================
         const int it = tid - 128;                      // 0..255
         const int wq = warp & 3;                       // TMEM lane quarter
@@ -637,9 +755,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tm_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const int imax = (wq & 1) * 32 + 31;           // last A or P row of this warp
         float* Abuf = reinterpret_cast<float*>(sm + kAbuf);
-        float* Tbuf = reinterpret_cast<float*>(sm + kTbuf);
         float* X1 = reinterpret_cast<float*>(sm + kXs);
-        float* X2 = X1 + 2 * 16 * 20;
+        float* X2 = X1 + 2 * 16 * kLdX1;
         uint32_t n = 0, u = 0;
         bool ok = true;
         for (; ok;) {
@@ -661,25 +778,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (n >= 2 && !(ok = wait_bar(cx, B_S_FULL + s, ((n - 2) >> 1) & 1))) break;
                 if (!(ok = wait_bar(cx, B_D1_FULL, n & 1))) break;
                 tc_fence_after();
-                if (p.l2norm) {
-                    // k norms: the diagonal of K K^T (lanes 0..63)
-                    if (hh == 0 && r < 64) {
-                        uint32_t rr[32];
-                        tmem_ld32_wait(tm_lane + kTmD1 + 32 * wq, rr);
-                        float kk = 0.f;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) kk = (j == lane) ? __uint_as_float(rr[j]) : kk;
-                        const float rn = r < Lc ? rsqrtf(kk + 1e-6f) : 0.f;
-                        gb[kGRn + r] = rn;
-                        gb[kGRa + r] *= rn;
-                    }
-                    named_bar_sync(kBarIntra, kIntraThreads);
-                    if (hh == 1 && r < 64) {  // column factors that meet n_j (read only after T')
-                        const float rn = gb[kGRn + r];
-                        gb[kGCw + r] *= rn;
-                        gb[kGDec + r] *= rn;
-                    }
-                }
                 // A rows (lanes 0..63) and P rows (lanes 64..127), this warp's 32 columns, 16 per step;
                 // blocks entirely above the diagonal are skipped (A's upper part is never read, P's stays zero).
                 // e^{G_i - G_j} = rowf[b][i] colf[j] inside column block b when the chunk's gate range is
@@ -688,7 +786,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool arow = r < 64;
                     const int i = r & 63;
                     const bool safe = gb[kGSafe] != 0.f;
-                    const float rbase = arow ? gb[kGRa + i] : gb[kGRm + i];
+                    float rbase = arow ? gb[kGRa + i] : 1.f;
+                    if (p.l2norm && arow) {
+                        // |k_i|^2 is the diagonal of K K^T: lane l of this warp finds it in column 32 wq + l
+                        uint32_t rr[32];
+                        tmem_ld32_wait(tm_lane + kTmD1 + 32 * wq, rr);
+                        float kk = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) kk = (j == lane) ? __uint_as_float(rr[j]) : kk;
+                        const float rn = i < Lc ? rsqrtf(kk + 1e-6f) : 0.f;
+                        rbase *= rn * rn;
+                        if (hh == wq) gb[kGRn + i] = rn;
+                    }
                     uint8_t* pb = sm + kPb + s * 8192;
 #pragma unroll 1
                     for (int jb = 32 * hh; jb < 32 * hh + 32; jb += 16) {
@@ -697,26 +806,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld16_wait(tm_lane + kTmD1 + jb, rr);
                         float x[16];
                         if (safe) {
-                            float cj[16], nj[16];
+                            float cj[16];
                             lds16(gb + kGColf + jb, cj);
-                            lds16(gb + kGRn + jb, nj);
                             const float rf = rbase * gb[kGRowf + (jb >> 4) * 64 + i];
 #pragma unroll
                             for (int q = 0; q < 16; ++q) {
                                 const int j = jb + q;
                                 const bool keep = arow ? (j < i) : (j <= i);
-                                x[q] = keep ? rf * cj[q] * nj[q] * __uint_as_float(rr[q]) : 0.f;
+                                x[q] = keep ? rf * cj[q] * __uint_as_float(rr[q]) : 0.f;
                             }
                         } else {
-                            float gj[16], nj[16];
+                            float gj[16];
                             lds16(gb + kGG + jb, gj);
-                            lds16(gb + kGRn + jb, nj);
                             const float Gi = gb[kGG + i];
 #pragma unroll
                             for (int q = 0; q < 16; ++q) {
                                 const int j = jb + q;
                                 const bool keep = arow ? (j < i) : (j <= i);
-                                x[q] = keep ? rbase * __expf(Gi - gj[q]) * nj[q] * __uint_as_float(rr[q]) : 0.f;
+                                x[q] = keep ? rbase * __expf(Gi - gj[q]) * __uint_as_float(rr[q]) : 0.f;
                             }
                         }
                         if (arow) {
@@ -739,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint4 z = make_uint4(0, 0, 0, 0);
                         uint8_t* base = (it < 64) ? kqs : sm + kV;
                         const uint32_t hs = (it < 64) ? 16384 : 8192;
-#pragma unroll
+#pragma unroll 1
                         for (int cch = 0; cch < 16; ++cch)
                             *reinterpret_cast<uint4*>(base + (cch >> 3) * hs + sw128_offset(zr, cch & 7)) = z;
                     }
@@ -747,29 +854,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();  // P and the zeroed tile rows reach the async proxy with the T' and Wb fences
                 named_bar_sync(kBarIntra, kIntraThreads);
                 if (it == 0) mbar_arrive(cx.bars + B_D1_EMPTY);
-                // T = (I + A)^-1, then T' = T diag(cw) (lanes 0..63), T'' = T diag(beta) (64..127)
-                tri_inverse_64(Abuf, Tbuf, X1, X2, it);
-                {
-                    const bool wpart = r < 64;
-                    const int i = r & 63;
-                    uint8_t* dst = sm + (wpart ? kTp : kTpp);
-                    const float* trow = Tbuf + i * kLd;
-                    const float* cf = gb + (wpart ? kGCw : kGBeta);
-#pragma unroll 1
-                    for (int j0 = 32 * hh; j0 < 32 * hh + 32; j0 += 8) {
-                        if (j0 > imax) break;  // warp-uniform; these chunks stay zero
-                        const float4 t0 = *reinterpret_cast<const float4*>(trow + j0);
-                        const float4 t1 = *reinterpret_cast<const float4*>(trow + j0 + 4);
-                        const float4 c0 = *reinterpret_cast<const float4*>(cf + j0);
-                        const float4 c1 = *reinterpret_cast<const float4*>(cf + j0 + 4);
-                        const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-                        const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                        float x[8];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) x[q] = (j0 + q <= i) ? tv[q] * cv[q] : 0.f;
-                        st_chunk_bf16(dst, i, j0 >> 3, x);
-                    }
-                }
+                // T = (I + A)^-1 in place, with T' = T diag(cw) and T'' = T diag(beta) in their bf16 tiles
+                tri_inverse_64(Abuf, sm + kTp, sm + kTpp, gb + kGCw, gb + kGBeta, gb + kGRn, X1, X2, it);
                 fence_proxy_async_smem();
                 named_bar_sync(kBarIntra, kIntraThreads);
                 if (it == 0) mbar_arrive(cx.bars + B_T_FULL);
@@ -778,7 +864,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (n >= 1 && !(ok = wait_bar(cx, B_DELTA_FULL + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
                 tc_fence_after();
                 {
-                    const size_t dump = (static_cast<size_t>(info.flat0 + c) * H + info.h) * kChunk * kHead;
                     const int i0 = 32 * hh;
                     uint32_t rr[32];
                     tmem_ld32_wait(tm_lane + kTmW + i0, rr);
@@ -787,18 +872,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(rr[j]);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) st_chunk_bf16(sm + kWb, r, (i0 >> 3) + q, w + 8 * q);
-                    if (p.intra_w) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) p.intra_w[dump + static_cast<size_t>(i0 + j) * kHead + r] = w[j];
-                    }
-                    if (p.intra_u) {
-                        tmem_ld32_wait(tm_lane + kTmDelta + s * 64 + i0, rr);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            p.intra_u[dump + static_cast<size_t>(i0 + j) * kHead + r] = __uint_as_float(rr[j]);
-                    }
-                    if (p.intra_g && it < 64)
-                        p.intra_g[(static_cast<size_t>(info.flat0 + c) * H + info.h) * kChunk + it] = gb[kGG + it];
+                    if (p.intra_w || p.intra_u || p.intra_g)
+                        dump_intra(p.intra_w, p.intra_u, p.intra_g,
+                                   (static_cast<size_t>(info.flat0 + c) * H + info.h) * kChunk * kHead, (static_cast<size_t>(info.flat0 + c) * H + info.h) * kChunk,
+                                   tm_lane + kTmW + i0, tm_lane + kTmDelta + s * 64 + i0, r, i0, it, gb + kGG);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -808,7 +885,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ================= state warpgroups (two; each TMEM lane row split in column halves) =================
-        if (kRegsState > kRegsLaunch) regs_inc<kRegsState>();
         const int st = tid - 384;                      // 0..255
         const int wq = warp & 3;
         const int hh = (warp - 12) >> 2;               // column half
@@ -843,23 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 if (!(ok = wait_bar(cx, B_GATES_FULL + (n & 1), (n >> 1) & 1))) break;
                 const float g63 = reinterpret_cast<const float*>(sm + kGbuf)[(n & 1) * kGFloats + kGGam + 63];
-#pragma unroll 1
-                for (int c0 = 0; c0 < 64; c0 += 32) {
-                    float x[32];
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const float4 f = s0 ? *reinterpret_cast<const float4*>(s0 + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        x[j] = f.x; x[j + 1] = f.y; x[j + 2] = f.z; x[j + 3] = f.w;
-                    }
-                    uint8_t* half = sb + hh * 16384;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) st_chunk_bf16(half, v, (c0 >> 3) + q, x + 8 * q);
-                    uint32_t r[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j] * g63);
-                    tmem_st32(tm_lane + kTmS + 64 * hh + c0, r);
-                }
-                tmem_wait_st();
+                load_initial_state(s0, sb + hh * 16384, tm_lane + kTmS + 64 * hh, v, g63);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 named_bar_sync(kBarState, kStateThreads);
@@ -876,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---- Delta epilogue: this thread's 32 columns j in [32 hh, 32 hh + 32) go back into TMEM as
                 //      16 packed bf16 Delta words followed by 16 packed decayed words (A operands of O2 and S)
                 if (!(ok = wait_bar(cx, B_DELTA_FULL + s, ph))) break;
-                if (!(ok = wait_bar(cx, B_WB_FULL + s, ph))) break;  // key-norm factors of chunk n are final
+                if (!(ok = wait_bar(cx, B_WB_FULL + s, ph))) break;  // W of chunk n is in place
                 tc_fence_after();
                 {
                     uint32_t ra[32], pk[16];
@@ -948,21 +1008,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 named_bar_sync(kBarState, kStateThreads);
                 if (st == 0 && !last) mbar_arrive(cx.bars + B_SB_FULL + ((n + 1) & 1));
-                // ---- output epilogue: o_i = orow_i (S Q^T)_i + scale (Delta^T P^T)_i, tokens i in [32 hh, 32 hh + 32)
+                // ---- output epilogue: o_i = orow_i (S Q^T)_i + scale rm_i (Delta^T P^T)_i, tokens i in [32 hh, 32 hh + 32)
+                if (!(ok = wait_bar(cx, B_QN_FULL + s, ph))) break;
                 {
                     const float sc = p.scale;
-                    uint32_t r1[32], r2[32];
-                    tmem_ld32_wait(tm_lane + kTmO1 + 32 * hh, r1);
-                    tmem_ld32_wait(tm_lane + kTmO2 + 32 * hh, r2);
-                    float orow[16];
+#pragma unroll 1
+                    for (int i0 = 32 * hh; i0 < 32 * hh + 32; i0 += 8) {
+                        uint32_t r1[8], r2[8];
+                        tmem_ld8(tm_lane + kTmO1 + i0, r1);
+                        tmem_ld8(tm_lane + kTmO2 + i0, r2);
+                        const float4 oa = *reinterpret_cast<const float4*>(gb + kGOr + i0);
+                        const float4 ob = *reinterpret_cast<const float4*>(gb + kGOr + i0 + 4);
+                        const float4 ma = *reinterpret_cast<const float4*>(gb + kGRm + i0);
+                        const float4 mb = *reinterpret_cast<const float4*>(gb + kGRm + i0 + 4);
+                        const float orow[8] = {oa.x, oa.y, oa.z, oa.w, ob.x, ob.y, ob.z, ob.w};
+                        const float rm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+                        tmem_wait_ld();
+                        tmem_regs_ready(r1);
+                        tmem_regs_ready(r2);
 #pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        lds16(gb + kGOr + 32 * hh + 16 * part, orow);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int jj = 16 * part + j;
-                            const float o = orow[j] * __uint_as_float(r1[jj]) + sc * __uint_as_float(r2[jj]);
-                            outT[(32 * hh + jj) * kHead + v] = __float2bfloat16_rn(o);
+                        for (int j = 0; j < 8; ++j) {
+                            const float o = orow[j] * __uint_as_float(r1[j]) + sc * rm[j] * __uint_as_float(r2[j]);
+                            outT[(i0 + j) * kHead + v] = __float2bfloat16_rn(o);
                         }
                     }
                 }
@@ -982,7 +1049,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     // the tail: coalesced copy of the valid rows only, 16 threads per 256-byte row
                     uint8_t* gout = static_cast<uint8_t*>(p.output);
-#pragma unroll
+#pragma unroll 1
                     for (int k = 0; k < 4; ++k) {
                         const int id = st + 256 * k, row = id >> 4, col = id & 15;
                         if (row < Lc) {

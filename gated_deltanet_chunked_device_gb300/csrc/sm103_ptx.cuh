@@ -188,6 +188,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 
 
+// 32 lanes x 32 bits, 8 consecutive columns (no wait; see tmem_regs_ready).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+// After tcgen05.wait::ld: ties the loaded registers to this point, so that no
+// use of them is scheduled between the load and the wait.
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[8]) {
+    asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]));
+}
+
 // 32 lanes x 32 bits, 32 consecutive columns, followed by the wait: when this
 // returns, r[] holds columns [col, col+32) of lane (lane_base + thread).
 __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]) {
