@@ -261,19 +261,19 @@ __device__ __forceinline__ void tri_inverse_64(float* __restrict__ A, uint8_t* _
         // ---- T_10 = -T_11 (A_10 T_00) inside the warp's 32 x 32 block
         const int b0 = 32 * wi, b1 = b0 + 16;
         float* xs = X1 + wi * 16 * kLdX1;
-#pragma unroll 1
+#pragma unroll
         for (int nt = 0; nt < 16; nt += 8) {
             float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
+#pragma unroll
             for (int k0 = 0; k0 < 16; k0 += 8)
                 mma_tf32_16x8x8(d, A + b1 * kLd + b0 + k0, kLd, A + (b0 + k0) * kLd + b0 + nt, kLd, lane);
             store_tile_16x8(xs + nt, kLdX1, d, 1.f, lane);
         }
         __syncwarp();
-#pragma unroll 1
+#pragma unroll
         for (int nt = 0; nt < 16; nt += 8) {
             float e[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
+#pragma unroll
             for (int k0 = 0; k0 < 16; k0 += 8)
                 mma_tf32_16x8x8(e, A + b1 * kLd + b1 + k0, kLd, xs + k0 * kLdX1 + nt, kLdX1, lane);
             store_tile_16x8(A + b1 * kLd + b0 + nt, kLd, e, -1.f, lane);
@@ -284,7 +284,7 @@ __device__ __forceinline__ void tri_inverse_64(float* __restrict__ A, uint8_t* _
     const int mt = (wi >> 2) * 16, nt = (wi & 3) * 8;
     {
         float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
+#pragma unroll
         for (int k0 = 0; k0 < 32; k0 += 8)
             mma_tf32_16x8x8(d, A + (32 + mt) * kLd + k0, kLd, A + k0 * kLd + nt, kLd, lane);
         store_tile_16x8(X2 + mt * kLdX2 + nt, kLdX2, d, 1.f, lane);
@@ -318,7 +318,7 @@ __device__ __forceinline__ void tri_inverse_64(float* __restrict__ A, uint8_t* _
     // ---- T_21 = -T_22 X, written as T' and T'' tiles from the fragments
     {
         float e[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
+#pragma unroll
         for (int k0 = 0; k0 < 32; k0 += 8)
             mma_tf32_16x8x8(e, A + (32 + mt) * kLd + 32 + k0, kLd, X2 + k0 * kLdX2 + nt, kLdX2, lane);
         const int g = lane >> 2, j = nt + 2 * (lane & 3);
@@ -634,6 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_commit(cx.bars + B_D1_FULL);
                         if (!(ok = wait_bar(cx, B_T_FULL, n & 1))) break;
                         if (!(ok = wait_bar(cx, B_V_FULL, n & 1))) break;
+                        // the W columns are free once the state warps have copied W of chunk n-1
+                        if (n >= 1 && !(ok = wait_bar(cx, B_WB_FULL + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
                         if (n >= 2 && !(ok = wait_bar(cx, B_S_FULL + s, ((n - 2) >> 1) & 1))) break;
                         tc_fence_after();
                         const uint32_t vv = smem_u32(sm + kV);
@@ -855,32 +857,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar_sync(kBarIntra, kIntraThreads);
                 if (it == 0) mbar_arrive(cx.bars + B_D1_EMPTY);
                 // T = (I + A)^-1 in place, with T' = T diag(cw) and T'' = T diag(beta) in their bf16 tiles
+                // (the W and U products of the previous chunk have read the old ones)
+                if (n >= 1 && !(ok = wait_bar(cx, B_WU_FULL, (n - 1) & 1))) break;
                 tri_inverse_64(Abuf, sm + kTp, sm + kTpp, gb + kGCw, gb + kGBeta, gb + kGRn, X1, X2, it);
                 fence_proxy_async_smem();
                 named_bar_sync(kBarIntra, kIntraThreads);
                 if (it == 0) mbar_arrive(cx.bars + B_T_FULL);
-                // W^T -> shared memory (MN-major B operand of -S W^T), after Delta(n-1) read the old one
-                if (!(ok = wait_bar(cx, B_WU_FULL, n & 1))) break;
-                if (n >= 1 && !(ok = wait_bar(cx, B_DELTA_FULL + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
-                tc_fence_after();
-                {
-                    const int i0 = 32 * hh;
-                    uint32_t rr[32];
-                    tmem_ld32_wait(tm_lane + kTmW + i0, rr);
-                    float w[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(rr[j]);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) st_chunk_bf16(sm + kWb, r, (i0 >> 3) + q, w + 8 * q);
-                    if (p.intra_w || p.intra_u || p.intra_g)
-                        dump_intra(p.intra_w, p.intra_u, p.intra_g,
-                                   (static_cast<size_t>(info.flat0 + c) * H + info.h) * kChunk * kHead, (static_cast<size_t>(info.flat0 + c) * H + info.h) * kChunk,
-                                   tm_lane + kTmW + i0, tm_lane + kTmDelta + s * 64 + i0, r, i0, it, gb + kGG);
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                named_bar_sync(kBarIntra, kIntraThreads);
-                if (it == 0) mbar_arrive(cx.bars + B_WB_FULL + s);
             }
         }
     } else {
@@ -933,10 +915,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t Lc = rem < kChunk ? static_cast<int32_t>(rem) : kChunk;
                 const float* gb = reinterpret_cast<const float*>(sm + kGbuf) + s * kGFloats;
                 const uint32_t dbuf = tm_lane + kTmDelta + s * 64;
+                // ---- W^T -> shared memory (MN-major B operand of -S W^T).  Delta(n-1), the reader of the old
+                //      copy, completed before this warpgroup's previous Delta epilogue.
+                if (!(ok = wait_bar(cx, B_WU_FULL, n & 1))) break;
+                tc_fence_after();
+                {
+                    const int i0 = 32 * hh;
+                    uint32_t rr[32];
+                    tmem_ld32_wait(tm_lane + kTmW + i0, rr);
+                    float w[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(rr[j]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) st_chunk_bf16(sm + kWb, v, (i0 >> 3) + q, w + 8 * q);
+                    if (p.intra_w || p.intra_u || p.intra_g)
+                        dump_intra(p.intra_w, p.intra_u, p.intra_g,
+                                   (static_cast<size_t>(info.flat0 + c) * H + info.h) * kChunk * kHead,
+                                   (static_cast<size_t>(info.flat0 + c) * H + info.h) * kChunk, tm_lane + kTmW + i0,
+                                   dbuf + i0, v, i0, st, gb + kGG);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar_sync(kBarState, kStateThreads);
+                if (st == 0) mbar_arrive(cx.bars + B_WB_FULL + s);
                 // ---- Delta epilogue: this thread's 32 columns j in [32 hh, 32 hh + 32) go back into TMEM as
                 //      16 packed bf16 Delta words followed by 16 packed decayed words (A operands of O2 and S)
                 if (!(ok = wait_bar(cx, B_DELTA_FULL + s, ph))) break;
-                if (!(ok = wait_bar(cx, B_WB_FULL + s, ph))) break;  // W of chunk n is in place
                 tc_fence_after();
                 {
                     uint32_t ra[32], pk[16];
