@@ -57,19 +57,19 @@ constexpr uint32_t kBarIntra = 1, kBarState = 2;  // named barrier ids
 constexpr uint32_t kKQ = 0;           // 2 stages x 32 KB: K_h0 | Q_h0 | K_h1 | Q_h1 (64 rows x 128 B each)
 constexpr uint32_t kKQStage = 32768;
 constexpr uint32_t kV = 65536;        // V_h0 | V_h1
-constexpr uint32_t kTp = 81920;       // T diag(beta gamma n) bf16 [64 i][64 j] K-major
-constexpr uint32_t kTpp = 90112;      // T diag(beta)
+constexpr uint32_t kTp = 81920;       // T' = T diag(beta gamma rn^2) bf16 [64 i][64 j] K-major
+constexpr uint32_t kTpp = 90112;      // T'' = T diag(beta rn)
 constexpr uint32_t kPb = 98304;       // 2 x P bf16 [64 i][64 j] K-major
 constexpr uint32_t kWb = 114688;      // W^T bf16 as MN-major B: [128 k][64 i]
 constexpr uint32_t kSb = 131072;      // S bf16 K-major: 2 halves of [128 v][64 k]
-constexpr uint32_t kAbuf = 163840;    // A fp32 [64][kLd]
+constexpr uint32_t kAbuf = 163840;    // A, then T in place: fp32 [64][kLd]
 constexpr uint32_t kXs = 181248;      // inverse scratch: [2][16][24] then [32][40] fp32
-constexpr uint32_t kOutT = 205824;    // output tile bf16 [64 i][128 v]
-constexpr uint32_t kGbuf = 222208;    // 2 x kGFloats floats of per-row / per-column factors (see kG*)
 constexpr uint32_t kBars = 189440;    // up to 64 mbarriers
 constexpr uint32_t kRing = 189952;    // 2 unit descriptors
 constexpr uint32_t kMisc = 190080;    // tmem base, abort flag
-constexpr uint32_t kSmemBytes = 229952;
+constexpr uint32_t kGbuf = 190144;    // 3 x kGFloats floats of per-row / per-column factors (see kG*)
+constexpr uint32_t kOutT = 205824;    // output tile bf16 [64 i][128 v]
+constexpr uint32_t kSmemBytes = 222208;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 constexpr int kLd = 68;               // fp32 row stride of A and T (bank-conflict free rows)
 
@@ -84,15 +84,16 @@ constexpr int kLd = 68;               // fp32 row stride of A and T (bank-confli
 //   safe   1 when the chunk's G range is small enough for e^{G_i - G_j} = rowf * colf
 constexpr int kGG = 0, kGGam = 64, kGBeta = 128, kGRn = 192, kGRm = 256, kGCw = 320, kGDec = 384, kGOr = 448,
               kGRa = 512, kGColf = 576, kGRowf = 640, kGSafe = 896, kGFloats = 912;
-static_assert(2 * kGFloats * 4 <= kSmemBytes - kGbuf, "gbuf overflows");
+static_assert(kGbuf >= kMisc + 64 && kGbuf + 3 * kGFloats * 4 <= kOutT && kOutT + 16384 == kSmemBytes,
+              "shared memory map overlaps");
 static_assert(kXs + 4 * (2 * 16 * 24 + 32 * 40) <= kBars && kMisc + 64 <= kOutT, "scratch / barrier block overlap");
 
 // ---- barriers
 enum {
     B_KQ_FULL = 0, B_KQ_EMPTY = 2, B_V_FULL = 4, B_V_EMPTY = 5, B_D1_FULL = 6, B_D1_EMPTY = 7, B_T_FULL = 8,
     B_WU_FULL = 9, B_WB_FULL = 10, B_SB_FULL = 12, B_DELTA_FULL = 14, B_DD_FULL = 16, B_S_FULL = 18,
-    B_O_EMPTY = 20, B_GATES_FULL = 22, B_GATES_EMPTY = 24, B_UNIT_FULL = 26, B_UNIT_EMPTY = 28,
-    B_DRAIN_I = 30, B_DRAIN_S = 31, B_QN_FULL = 32, B_COUNT = 34
+    B_O_EMPTY = 20, B_UNIT_FULL = 26, B_UNIT_EMPTY = 28,
+    B_DRAIN_I = 30, B_DRAIN_S = 31, B_GATES_FULL = 32, B_GATES_EMPTY = 35, B_QN_FULL = 38, B_COUNT = 41
 };
 
 // ---- TMEM columns
@@ -724,14 +725,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (info.nC > 0)
                     gpf = load_gates(p, info.t0, info.L < kChunk ? static_cast<int32_t>(info.L) : kChunk, info.h, lane);
                 for (int32_t c = 0; c < info.nC; ++c, ++n) {
-                    const int gs = n & 1;
+                    const uint32_t gs = n % 3;  // gates slot (three in flight); the K | Q stage is n & 1
                     const GatePrefetch cur = gpf;
                     if (c + 1 < info.nC) {
                         const int64_t rem1 = info.L - static_cast<int64_t>(c + 1) * kChunk;
                         gpf = load_gates(p, info.t0 + static_cast<int64_t>(c + 1) * kChunk,
                                          rem1 < kChunk ? static_cast<int32_t>(rem1) : kChunk, info.h, lane);
                     }
-                    if (n >= 2 && !(ok = wait_bar(cx, B_GATES_EMPTY + gs, ((n - 2) >> 1) & 1))) break;
+                    if (n >= 3 && !(ok = wait_bar(cx, B_GATES_EMPTY + gs, ((n - 3) / 3) & 1))) break;
                     const int64_t rem = info.L - static_cast<int64_t>(c) * kChunk;
                     const int32_t Lc = rem < kChunk ? static_cast<int32_t>(rem) : kChunk;
                     float* gbw = reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats;
@@ -740,8 +741,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(cx.bars + B_GATES_FULL + gs);
                     // query norms (needed only by the output epilogue) after the intra side has its vectors
                     if (p.l2norm) {
-                        if (!(ok = wait_bar(cx, B_KQ_FULL + gs, (n >> 1) & 1))) break;
-                        query_norms(sm + kKQ + gs * kKQStage + 8192, gbw, p.scale, Lc, lane);
+                        if (!(ok = wait_bar(cx, B_KQ_FULL + (n & 1), (n >> 1) & 1))) break;
+                        query_norms(sm + kKQ + (n & 1) * kKQStage + 8192, gbw, p.scale, Lc, lane);
                         __syncwarp();
                     }
                     if (lane == 0) mbar_arrive(cx.bars + B_QN_FULL + gs);
@@ -773,9 +774,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = n & 1;
                 const int64_t rem = info.L - static_cast<int64_t>(c) * kChunk;
                 const int32_t Lc = rem < kChunk ? static_cast<int32_t>(rem) : kChunk;
-                float* gb = reinterpret_cast<float*>(sm + kGbuf) + s * kGFloats;
+                const uint32_t gs = n % 3;
+                float* gb = reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats;
                 uint8_t* kqs = sm + kKQ + s * kKQStage;
-                if (!(ok = wait_bar(cx, B_GATES_FULL + s, (n >> 1) & 1))) break;
+                if (!(ok = wait_bar(cx, B_GATES_FULL + gs, (n / 3) & 1))) break;
                 // P buffer s is free once O2 of chunk n-2 has completed
                 if (n >= 2 && !(ok = wait_bar(cx, B_S_FULL + s, ((n - 2) >> 1) & 1))) break;
                 if (!(ok = wait_bar(cx, B_D1_FULL, n & 1))) break;
@@ -899,8 +901,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // initial state: S0 -> Sb (bf16) and gamma_63(first chunk) * S0 -> TMEM
             {
-                if (!(ok = wait_bar(cx, B_GATES_FULL + (n & 1), (n >> 1) & 1))) break;
-                const float g63 = reinterpret_cast<const float*>(sm + kGbuf)[(n & 1) * kGFloats + kGGam + 63];
+                if (!(ok = wait_bar(cx, B_GATES_FULL + n % 3, (n / 3) & 1))) break;
+                const float g63 = reinterpret_cast<const float*>(sm + kGbuf)[(n % 3) * kGFloats + kGGam + 63];
                 load_initial_state(s0, sb + hh * 16384, tm_lane + kTmS + 64 * hh, v, g63);
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -913,7 +915,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t tc = info.t0 + static_cast<int64_t>(c) * kChunk;
                 const int64_t rem = info.L - static_cast<int64_t>(c) * kChunk;
                 const int32_t Lc = rem < kChunk ? static_cast<int32_t>(rem) : kChunk;
-                const float* gb = reinterpret_cast<const float*>(sm + kGbuf) + s * kGFloats;
+                const uint32_t gs = n % 3;
+                const float* gb = reinterpret_cast<const float*>(sm + kGbuf) + gs * kGFloats;
                 const uint32_t dbuf = tm_lane + kTmDelta + s * 64;
                 // ---- W^T -> shared memory (MN-major B operand of -S W^T).  Delta(n-1), the reader of the old
                 //      copy, completed before this warpgroup's previous Delta epilogue.
@@ -967,18 +970,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = wait_bar(cx, B_S_FULL + s, ph))) break;
                 tc_fence_after();
                 const bool last = (c + 1 == info.nC);
-                float gnext = 1.f;
-                if (!last) {
-                    if (!(ok = wait_bar(cx, B_GATES_FULL + ((n + 1) & 1), ((n + 1) >> 1) & 1))) break;
-                    gnext = reinterpret_cast<const float*>(sm + kGbuf)[((n + 1) & 1) * kGFloats + kGGam + 63];
-                }
                 {
+                    // pass 1: S_n -> the bf16 operand of the next Delta and S Q^T products, checkpoint, final state
                     const int64_t pend = static_cast<int64_t>(c + 1) * kChunk;
                     float* ck = nullptr;
                     if (p.checkpoints && p.ckpt_n > 0 && pend % p.ckpt_n == 0 && pend <= info.L)
                         ck = p.checkpoints + (static_cast<size_t>(info.ckpt_base + pend / p.ckpt_n - 1) * H + info.h) *
                                                  kHead * kHead + static_cast<size_t>(v) * kHead + 64 * hh;
                     float* fin = (last && p.output_state) ? p.output_state + state_off : nullptr;
+                    uint8_t* half = sb + hh * 16384;
 #pragma unroll 1
                     for (int c0 = 0; c0 < 64; c0 += 16) {
                         uint32_t r[16];
@@ -997,23 +997,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 *reinterpret_cast<float4*>(fin + c0 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
                         }
                         if (!last) {
-                            uint8_t* half = sb + hh * 16384;
                             st_chunk_bf16(half, v, c0 >> 3, x);
                             st_chunk_bf16(half, v, (c0 >> 3) + 1, x + 8);
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(x[j] * gnext);
-                            tmem_st16(tm_lane + kTmS + 64 * hh + c0, r);
                         }
                     }
-                    if (!last) tmem_wait_st();
                 }
                 if (st == 0) bulk_wait_group_read0();  // the previous chunk's output store has read outT
                 fence_proxy_async_smem();
                 tc_fence_before();
                 named_bar_sync(kBarState, kStateThreads);
                 if (st == 0 && !last) mbar_arrive(cx.bars + B_SB_FULL + ((n + 1) & 1));
+                if (!last) {
+                    // pass 2: gamma_63 of the next chunk into the accumulator, before that chunk's S product
+                    const uint32_t gn = (n + 1) % 3;
+                    if (!(ok = wait_bar(cx, B_GATES_FULL + gn, ((n + 1) / 3) & 1))) break;
+                    const float gnext = reinterpret_cast<const float*>(sm + kGbuf)[gn * kGFloats + kGGam + 63];
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 64; c0 += 16) {
+                        uint32_t r[16];
+                        tmem_ld16_wait(tm_lane + kTmS + 64 * hh + c0, r);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gnext);
+                        tmem_st16(tm_lane + kTmS + 64 * hh + c0, r);
+                    }
+                    tmem_wait_st();
+                }
                 // ---- output epilogue: o_i = orow_i (S Q^T)_i + scale rm_i (Delta^T P^T)_i, tokens i in [32 hh, 32 hh + 32)
-                if (!(ok = wait_bar(cx, B_QN_FULL + s, ph))) break;
+                if (!(ok = wait_bar(cx, B_QN_FULL + gs, (n / 3) & 1))) break;
                 {
                     const float sc = p.scale;
 #pragma unroll 1
@@ -1042,7 +1052,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar_sync(kBarState, kStateThreads);
                 if (st == 0) {
                     mbar_arrive(cx.bars + B_O_EMPTY + s);
-                    mbar_arrive(cx.bars + B_GATES_EMPTY + s);
+                    mbar_arrive(cx.bars + B_GATES_EMPTY + gs);
                 }
                 if (Lc == kChunk) {
                     // a full chunk: one TMA store of the 64 x 128 tile (rows all belong to this sequence)
