@@ -62,6 +62,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x, dist=None, device=None):
+    """The largest value of x over all ranks (x itself without a process group):
+    the job's time is its slowest rank's."""
+    if dist is None:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_rank, ms):
+    """Whole-job throughput: every rank prefills its own copy of the workload
+    (units are independent), so the job processes world x tokens per step."""
+    return world * tokens_per_rank / (ms / 1e3)
+
+
 def algorithmic_bytes(w, inp):
     """Bytes the method must move once: q, k, v read, g and beta read, o written,
     initial / final states, checkpoints."""
@@ -384,10 +400,7 @@ def main():
     chunk_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     ms_per_step = sum(step_ms) / K
     chunk_avg_ms = sum(chunk_ms) / K
-    if pg:
-        t = torch.tensor([ms_per_step], device=device)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = max_over_ranks(ms_per_step, pg, device)
     bits = gdn.read_status(plan, ws)
     if bits:
         raise RuntimeError(f"device status bits {bits:#x} after the timed steps")
@@ -435,11 +448,8 @@ def main():
             ee.record(stream)
         torch.cuda.synchronize(device)
         e2e_ms = es.elapsed_time(ee) / Ke
-        if pg:
-            t = torch.tensor([e2e_ms], device=device)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * inp["T"] / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        e2e_ms = max_over_ranks(e2e_ms, pg, device)
+        e2e = {"value": job_tokens_per_s(world, inp["T"], e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     clocks = sampler.stop() if sampler else None
@@ -456,7 +466,7 @@ def main():
     tflops_tri = T * H * FLOP_TRI / (ms_per_step / 1e3) / 1e12
     roof_time = max(abytes / (hbm * 1e9), T * H * FLOP_DENSE / (bf16 * 1e12))
     line = {
-        "metric": METRIC, "value": world * T / (ms_per_step / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": job_tokens_per_s(world, T, ms_per_step), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(w, inp, args),
         "tflops": {"dense_tile_count": tflops_dense, "triangular_aware": tflops_tri,

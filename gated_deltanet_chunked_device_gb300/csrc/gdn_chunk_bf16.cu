@@ -3,26 +3,32 @@
 // warp-specialised and pipelined across chunks.
 //
 // Per chunk of C = 64 tokens (G_r = sum_{m<=r} log alpha_m inside the chunk,
-// gamma_r = e^{G_r}; n_j, m_i = 1/|k_j|, 1/|q_i| when the L2 norm is on, else 1):
+// gamma_r = e^{G_r}; n_j, m_i = 1/|k_j|, 1/|q_i| when the L2 norm is on, else
+// 1; K and Q are the tiles as stored, not normalised):
 //
 //   intra-chunk step ("GDN 与 Chunked Prefill": cumsum, triangular solve,
 //   recompute; the 4-token expansion table generalised to a 64 x 64 table):
 //     D1 = [K; Q] K^T                               tcgen05, M=128 N=64 K=128
-//     A_ij = beta_i e^{G_i-G_j} n_i n_j (k_i.k_j), j < i
-//     P_ij = e^{G_i-G_j} m_i n_j (q_i.k_j),       j <= i
-//     T = (I + A)^-1                                blocked substitution + tf32 mma.sync
-//     W^T = K^T (T diag(beta gamma n))^T,  U^T = V^T (T diag(beta))^T   tcgen05
+//     A~_ij = beta_i n_i^2 e^{G_i-G_j} (k_i.k_j), j < i      (n_i from diag D1)
+//     P_ij = e^{G_i-G_j} (q_i.k_j),                j <= i
+//     T~ = (I + A~)^-1                              blocked substitution + tf32 mma.sync
+//     W~^T = K^T (T~ diag(beta gamma n^2))^T,  U~^T = V^T (T~ diag(beta n))^T   tcgen05
 //   state pass ("块内 state 和块间 final state": only the chunk's last state
 //   crosses the boundary):
-//     Delta^T = U^T - S W^T                         tcgen05, A negated
-//     S <- gamma_63 S + (Delta^T diag(e^{G_63-G_j} n_j)) K     tcgen05, in TMEM
+//     Delta~^T = U~^T - S W~^T                      tcgen05, A negated
+//     S <- gamma_63 S + (Delta~^T diag(e^{G_63-G_j})) K          tcgen05, in TMEM
 //   output ("GDN与线性注意力GPU并行实现" section 3.3: O_init = Q S plus a
 //   triangular-masked product):
-//     O^T = scale (S Q^T diag(gamma m) + Delta^T P^T)           tcgen05
+//     O^T = scale (S Q^T diag(gamma m) + Delta~^T P^T diag(m))   tcgen05
 //
 // The L2 norm of q and k ("FlashInfer GDN Prefill 完全指南", API table) enters
-// only as the per-row factors n and m above, applied in fp32: the same values
-// as normalising the rows first, without re-rounding them to bf16.
+// only through the factors n and m, in fp32: the same values as normalising
+// the rows first, without re-rounding them to bf16.  With the normalised
+// matrix A = diag(beta n) M diag(n) (M_ij = e^{G_i-G_j} k_i.k_j), the
+// similarity diag(n) (I + A) diag(n)^-1 = I + A~ gives T = diag(1/n) T~ diag(n);
+// so W~ = diag(n) W, U~ = diag(n) U, Delta~ = diag(n) Delta, and n cancels
+// from the state update and from P: every norm factor is a row factor of the
+// matrix that uses it, known to the thread that holds that row.
 //
 // Roles (640 threads in five warpgroups, one work unit = (sequence, state
 // head) at a time, units taken longest first from an atomic counter):

@@ -134,7 +134,9 @@ typedef struct gdn_prefill_args {
      * (the order of the chunk map: sequence by sequence, chunk by chunk):
      * intra_g [F, H, 64] fp32 (G = running sum of log alpha in the chunk),
      * intra_w and intra_u [F, H, 64, 128] fp32 (W = T diag(beta*gamma) K,
-     * U = T diag(beta) V with T = (I + A)^-1), F = ceil(T/64) + N rows. */
+     * U = T diag(beta) V with T = (I + A)^-1, for the keys as normalised; with
+     * GDN_FLAG_QK_L2NORM row i of both comes multiplied by 1/|k_i|),
+     * F = ceil(T/64) + N rows. */
     float *intra_g, *intra_w, *intra_u;
 } gdn_prefill_args;
 
