@@ -915,6 +915,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar_sync(kBarState, kStateThreads);
                 if (st == 0) mbar_arrive(cx.bars + B_SB_FULL + (n & 1));
             }
+            // W^T of chunk m (unit-local index cm) -> shared memory, the MN-major B operand of -S W^T.  The
+            // reader of the previous copy, Delta of chunk m-1, completed before this warpgroup's Delta epilogue
+            // of that chunk.
+            auto copy_w = [&](uint32_t m, int32_t cm) -> bool {
+                if (!wait_bar(cx, B_WU_FULL, m & 1)) return false;
+                tc_fence_after();
+                const int i0 = 32 * hh;
+                uint32_t rr[32];
+                tmem_ld32_wait(tm_lane + kTmW + i0, rr);
+                float w[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(rr[j]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st_chunk_bf16(sm + kWb, v, (i0 >> 3) + q, w + 8 * q);
+                if (p.intra_w || p.intra_u || p.intra_g)
+                    dump_intra(p.intra_w, p.intra_u, p.intra_g,
+                               (static_cast<size_t>(info.flat0 + cm) * H + info.h) * kChunk * kHead,
+                               (static_cast<size_t>(info.flat0 + cm) * H + info.h) * kChunk, tm_lane + kTmW + i0,
+                               tm_lane + kTmDelta + (m & 1) * 64 + i0, v, i0, st,
+                               reinterpret_cast<const float*>(sm + kGbuf) + (m % 3) * kGFloats + kGG);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar_sync(kBarState, kStateThreads);
+                if (st == 0) mbar_arrive(cx.bars + B_WB_FULL + (m & 1));
+                return true;
+            };
             for (int32_t c = 0; c < info.nC && ok; ++c, ++n) {
                 const int s = n & 1;
                 const uint32_t ph = (n >> 1) & 1;
@@ -924,29 +950,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t gs = n % 3;
                 const float* gb = reinterpret_cast<const float*>(sm + kGbuf) + gs * kGFloats;
                 const uint32_t dbuf = tm_lane + kTmDelta + s * 64;
-                // ---- W^T -> shared memory (MN-major B operand of -S W^T).  Delta(n-1), the reader of the old
-                //      copy, completed before this warpgroup's previous Delta epilogue.
-                if (!(ok = wait_bar(cx, B_WU_FULL, n & 1))) break;
-                tc_fence_after();
-                {
-                    const int i0 = 32 * hh;
-                    uint32_t rr[32];
-                    tmem_ld32_wait(tm_lane + kTmW + i0, rr);
-                    float w[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(rr[j]);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) st_chunk_bf16(sm + kWb, v, (i0 >> 3) + q, w + 8 * q);
-                    if (p.intra_w || p.intra_u || p.intra_g)
-                        dump_intra(p.intra_w, p.intra_u, p.intra_g,
-                                   (static_cast<size_t>(info.flat0 + c) * H + info.h) * kChunk * kHead,
-                                   (static_cast<size_t>(info.flat0 + c) * H + info.h) * kChunk, tm_lane + kTmW + i0,
-                                   dbuf + i0, v, i0, st, gb + kGG);
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                named_bar_sync(kBarState, kStateThreads);
-                if (st == 0) mbar_arrive(cx.bars + B_WB_FULL + s);
+                // W of the unit's first chunk (the later ones are copied right after the previous chunk's state)
+                if (c == 0 && !(ok = copy_w(n, c))) break;
                 // ---- Delta epilogue: this thread's 32 columns j in [32 hh, 32 hh + 32) go back into TMEM as
                 //      16 packed bf16 Delta words followed by 16 packed decayed words (A operands of O2 and S)
                 if (!(ok = wait_bar(cx, B_DELTA_FULL + s, ph))) break;
@@ -1013,6 +1018,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 named_bar_sync(kBarState, kStateThreads);
                 if (st == 0 && !last) mbar_arrive(cx.bars + B_SB_FULL + ((n + 1) & 1));
+                // W of the next chunk now: with the bf16 state just published, it is all the next Delta product
+                // waits for, while this chunk's prescale and output epilogue run behind it.
+                if (!last && !(ok = copy_w(n + 1, c + 1))) break;
                 if (!last) {
                     // pass 2: gamma_63 of the next chunk into the accumulator, before that chunk's S product
                     const uint32_t gn = (n + 1) % 3;
