@@ -15,11 +15,11 @@
 //     W~^T = K^T (T~ diag(beta gamma n^2))^T,  U~^T = V^T (T~ diag(beta n))^T   tcgen05
 //   state pass ("块内 state 和块间 final state": only the chunk's last state
 //   crosses the boundary):
-//     Delta~^T = U~^T - S W~^T                      tcgen05, A negated
+//     Delta~^T = U~^T - S W~^T                      tcgen05, A (bf16 S) from TMEM, negated
 //     S <- gamma_63 S + (Delta~^T diag(e^{G_63-G_j})) K          tcgen05, in TMEM
 //   output ("GDN与线性注意力GPU并行实现" section 3.3: O_init = Q S plus a
 //   triangular-masked product):
-//     O^T = scale (S Q^T diag(gamma m) + Delta~^T P^T diag(m))   tcgen05
+//     O^T = scale (S Q'^T + Delta~^T P^T) diag(m),  Q' = diag(gamma) Q     tcgen05, one accumulator
 //
 // The L2 norm of q and k ("FlashInfer GDN Prefill 完全指南", API table) enters
 // only through the factors n and m, in fp32: the same values as normalising
@@ -32,17 +32,18 @@
 //
 // Roles (640 threads in five warpgroups, one work unit = (sequence, state
 // head) at a time, units taken longest first from an atomic counter):
-//   warp 0       TMA: K, Q tiles (2 stages) and V tile; unit scheduler
+//   warp 0       TMA: K, Q tiles (3 stages) and V tile; unit scheduler
 //   warp 1       tcgen05 issue for the intra-chunk products (D1, W, U)
 //   warp 2       tcgen05 issue for the state chain (Delta, S Q^T, Delta P^T, S)
-//   warp 3       TMEM allocation; gates: G, gamma, beta, the q and k row
-//                norms and the per-row / per-column factor vectors
+//   warp 3       TMEM allocation; gates: G, gamma, beta and the per-row /
+//                per-column factor vectors
 //   warps 4-11   two intra warpgroups (TMEM lane quarter x column half):
-//                A and P, T in place with T' and T'', W to shared memory,
-//                one chunk ahead of the state warpgroups
-//   warps 12-19  two state warpgroups (lane quarter x column half): Delta
-//                epilogue, state epilogue (next S operand, checkpoints,
-//                final state), output epilogue
+//                A and P, Q' = diag(gamma) Q with the q norms, T in place
+//                with T' and T'', one chunk ahead of the state warpgroups
+//   warps 12-19  two state warpgroups (lane quarter x column half): W to
+//                shared memory, Delta epilogue, state epilogue (next bf16 S
+//                operand in TMEM, checkpoints, final state, prescale),
+//                output epilogue
 // Every wait is bounded; a timeout sets GDN_DEVICE_ERR_TIMEOUT, raises a
 // shared abort flag that every other wait polls, drains the CTA's in-flight
 // copies and tensor-core work, frees TMEM and returns.
@@ -60,14 +61,14 @@ constexpr int kIntraThreads = 256;  // two intra warpgroups
 constexpr uint32_t kBarIntra = 1, kBarState = 2;  // named barrier ids
 
 // ---- shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t kKQ = 0;           // 2 stages x 32 KB: K_h0 | Q_h0 | K_h1 | Q_h1 (64 rows x 128 B each)
+constexpr uint32_t kKQ = 0;           // 3 stages x 32 KB: K_h0 | Q_h0 | K_h1 | Q_h1 (64 rows x 128 B each)
 constexpr uint32_t kKQStage = 32768;
-constexpr uint32_t kV = 65536;        // V_h0 | V_h1
-constexpr uint32_t kTp = 81920;       // T' = T diag(beta gamma rn^2) bf16 [64 i][64 j] K-major
-constexpr uint32_t kTpp = 90112;      // T'' = T diag(beta rn)
-constexpr uint32_t kPb = 98304;       // 2 x P bf16 [64 i][64 j] K-major
-constexpr uint32_t kWb = 114688;      // W^T bf16 as MN-major B: [128 k][64 i]
-constexpr uint32_t kSb = 131072;      // S bf16 K-major: 2 halves of [128 v][64 k]
+constexpr uint32_t kKQStages = 3;
+constexpr uint32_t kV = 98304;        // V_h0 | V_h1
+constexpr uint32_t kTp = 114688;      // T' = T diag(beta gamma rn^2) bf16 [64 i][64 j] K-major
+constexpr uint32_t kTpp = 122880;     // T'' = T diag(beta rn)
+constexpr uint32_t kPb = 131072;      // 2 x P bf16 [64 i][64 j] K-major
+constexpr uint32_t kWb = 147456;      // W^T bf16 as MN-major B: [128 k][64 i]
 constexpr uint32_t kAbuf = 163840;    // A, then T in place: fp32 [64][kLd]
 constexpr uint32_t kXs = 181248;      // inverse scratch: [2][16][24] then [32][40] fp32
 constexpr uint32_t kBars = 189440;    // up to 64 mbarriers
@@ -83,27 +84,31 @@ constexpr int kLd = 68;               // fp32 row stride of A and T (bank-confli
 //   G      running sum of log alpha            gamma  e^G
 //   beta   beta (0 on padded rows)             rn     1/|k_j| (1 without the L2 norm; written by the
 //                                                      intra warps that hold the K K^T diagonal)
-//   rm     1/|q_i| (1 without the L2 norm)     cw     beta_j gamma_j (T' columns, times rn_j^2)
-//   dec    e^{G_63 - G_j} (decayed Delta)      orow   scale gamma_i rm_i (output rows)
+//   rm     1/|q_i| (1 without the L2 norm; written by the intra warps from the Q pass)
+//   cw     beta_j gamma_j (T' columns, times rn_j^2)
+//   dec    e^{G_63 - G_j} (decayed Delta)      (448..511 unused)
 //   ra     beta_i (A rows, times rn_i^2)       colf   e^{G_16b - G_j}, b = j / 16
 //   rowf   [4][64] e^{G_i - G_16b} (i >= 16 b, else 0)
 //   safe   1 when the chunk's G range is small enough for e^{G_i - G_j} = rowf * colf
-constexpr int kGG = 0, kGGam = 64, kGBeta = 128, kGRn = 192, kGRm = 256, kGCw = 320, kGDec = 384, kGOr = 448,
+constexpr int kGG = 0, kGGam = 64, kGBeta = 128, kGRn = 192, kGRm = 256, kGCw = 320, kGDec = 384,
               kGRa = 512, kGColf = 576, kGRowf = 640, kGSafe = 896, kGFloats = 912;
 static_assert(kGbuf >= kMisc + 64 && kGbuf + 3 * kGFloats * 4 <= kOutT && kOutT + 16384 == kSmemBytes,
               "shared memory map overlaps");
 static_assert(kXs + 4 * (2 * 16 * 24 + 32 * 40) <= kBars && kMisc + 64 <= kOutT, "scratch / barrier block overlap");
+static_assert(kKQ + kKQStages * kKQStage == kV && kV + 16384 == kTp && kWb + 16384 == kAbuf, "tile block overlap");
 
 // ---- barriers
 enum {
-    B_KQ_FULL = 0, B_KQ_EMPTY = 2, B_V_FULL = 4, B_V_EMPTY = 5, B_D1_FULL = 6, B_D1_EMPTY = 7, B_T_FULL = 8,
-    B_WU_FULL = 9, B_WB_FULL = 10, B_SB_FULL = 12, B_DELTA_FULL = 14, B_DD_FULL = 16, B_S_FULL = 18,
-    B_O_EMPTY = 20, B_UNIT_FULL = 26, B_UNIT_EMPTY = 28,
-    B_DRAIN_I = 30, B_DRAIN_S = 31, B_GATES_FULL = 32, B_GATES_EMPTY = 35, B_QN_FULL = 38, B_COUNT = 41
+    B_KQ_FULL = 0 /* 3 */, B_KQ_EMPTY = 3 /* 3 */, B_V_FULL = 6, B_V_EMPTY = 7, B_D1_FULL = 8, B_D1_EMPTY = 9,
+    B_T_FULL = 10, B_WU_FULL = 11, B_WB_FULL = 12 /* 2 */, B_SB_FULL = 14 /* 2 */, B_DELTA_FULL = 16 /* 2 */,
+    B_DD_FULL = 18 /* 2 */, B_S_FULL = 20 /* 2 */, B_O_EMPTY = 22 /* 2 */, B_GATES_FULL = 24 /* 3 */,
+    B_GATES_EMPTY = 27 /* 3 */, B_UNIT_FULL = 30 /* 2 */, B_UNIT_EMPTY = 32 /* 2 */, B_DRAIN_I = 34, B_DRAIN_S = 35,
+    B_COUNT = 36
 };
 
 // ---- TMEM columns
-constexpr uint32_t kTmS = 0, kTmDelta = 128 /* 2 x 64 */, kTmW = 256, kTmD1 = 320, kTmO1 = 384, kTmO2 = 448;
+// S fp32 | Delta 2 x 64 | W | D1 | O (S Q'^T + Delta^T P^T) | S as packed bf16 pairs (A operand)
+constexpr uint32_t kTmS = 0, kTmDelta = 128, kTmW = 256, kTmD1 = 320, kTmO = 384, kTmSbf = 448;
 constexpr uint32_t kTmCols = 512;
 
 constexpr uint32_t kIdescD1 = idesc_bf16_f32(128, 64);
@@ -364,37 +369,10 @@ __device__ __forceinline__ GatePrefetch load_gates(const ChunkParams& p, int64_t
     return g;
 }
 
-// Sum of squares of row r of a staged 64 x 128 bf16 tile (two 64-column
-// halves 16 KB apart, 128-byte swizzle).
-__device__ __forceinline__ float row_sumsq(const uint8_t* half0, int r) {
-    float ss = 0.f;
-#pragma unroll 2
-    for (int c = 0; c < 16; ++c) {
-        float f[8];
-        bf16x8_to_float(*reinterpret_cast<const uint4*>(half0 + (c >> 3) * 16384 + sw128_offset(r, c & 7)), f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
-    }
-    return ss;
-}
-
-// Squared norms of rows 2 lane and 2 lane + 1 of a staged tile.  Each lane
-// sums rows lane and lane + 32 (eight consecutive rows meet all eight 16-byte
-// columns of the swizzle, so the reads are conflict-free), then the sums move
-// to the lanes that own the rows.
-__device__ __forceinline__ void pair_sumsq(const uint8_t* half0, int lane, float& s0, float& s1) {
-    const float lo = row_sumsq(half0, lane), hi = row_sumsq(half0, lane + 32);
-    const int r0 = 2 * lane, r1 = r0 + 1;
-    const float a0 = __shfl_sync(0xffffffffu, lo, r0 & 31), b0 = __shfl_sync(0xffffffffu, hi, r0 & 31);
-    const float a1 = __shfl_sync(0xffffffffu, lo, r1 & 31), b1 = __shfl_sync(0xffffffffu, hi, r1 & 31);
-    s0 = r0 < 32 ? a0 : b0;
-    s1 = r1 < 32 ? a1 : b1;
-}
-
-// The vectors of one chunk (see kG*) that need no norm; orow and rm are left
-// to query_norms when the L2 norm is on.  Rows at or past Lc are padding
-// (alpha = 1, beta = 0).
-__device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, float scale, bool l2norm, int lane) {
+// The vectors of one chunk (see kG*) that need no norm; under the L2 norm the
+// intra warps add rn and rm.  Rows at or past Lc are padding (alpha = 1,
+// beta = 0).
+__device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, bool l2norm, int lane) {
     const int r0 = 2 * lane;
     const float la0 = __logf(g.a0), la1 = __logf(g.a1);
     float incl = la0 + la1;
@@ -419,10 +397,7 @@ __device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, 
         gb[kGRn + r] = 1.f;
         gb[kGCw + r] = bv[k] * e;
         gb[kGDec + r] = __expf(G63 - Gv[k]);
-        if (!l2norm) {
-            gb[kGRm + r] = 1.f;
-            gb[kGOr + r] = scale * e;
-        }
+        if (!l2norm) gb[kGRm + r] = 1.f;
         gb[kGRa + r] = bv[k];
         gb[kGColf + r] = __expf(Gb[r >> 4] - Gv[k]);
 #pragma unroll
@@ -435,18 +410,6 @@ __device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, 
         gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
     }
     if (lane == 0) gb[kGSafe] = (gmax - gmin < 60.f) ? 1.f : 0.f;
-}
-
-// rm = 1/|q_i| of the staged Q tile and orow = scale gamma_i rm_i (padded rows 0).
-__device__ __forceinline__ void query_norms(const uint8_t* q, float* gb, float scale, int32_t Lc, int lane) {
-    float s0, s1;
-    pair_sumsq(q, lane, s0, s1);
-    const int r0 = 2 * lane, r1 = r0 + 1;
-    const float rm0 = r0 < Lc ? rsqrtf(s0 + 1e-6f) : 0.f, rm1 = r1 < Lc ? rsqrtf(s1 + 1e-6f) : 0.f;
-    gb[kGRm + r0] = rm0;
-    gb[kGRm + r1] = rm1;
-    gb[kGOr + r0] = scale * gb[kGGam + r0] * rm0;
-    gb[kGOr + r1] = scale * gb[kGGam + r1] * rm1;
 }
 
 __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]) {
@@ -485,10 +448,10 @@ __device__ __noinline__ void dump_intra(float* intra_w, float* intra_u, float* i
     if (intra_g && it < 64) intra_g[gdump + it] = G[it];
 }
 
-// Start of a unit's state: S0 (this thread's row v, 64 columns) to its half of
-// the bf16 S operand and gamma_63 S0 to the TMEM accumulator (S0 null: zeros).
-// Once per unit, so out of line.
-__device__ __noinline__ void load_initial_state(const float* s0, uint8_t* half, uint32_t tm, int v, float g63) {
+// Start of a unit's state: S0 (this thread's row v, 64 columns) as packed bf16
+// pairs into the A operand columns, and gamma_63 S0 into the fp32 accumulator
+// (S0 null: zeros).  Once per unit, so out of line.
+__device__ __noinline__ void load_initial_state(const float* s0, uint32_t tm_sbf, uint32_t tm_s, float g63) {
     for (int c0 = 0; c0 < 64; c0 += 32) {
         float x[32];
 #pragma unroll
@@ -496,12 +459,14 @@ __device__ __noinline__ void load_initial_state(const float* s0, uint8_t* half, 
             const float4 f = s0 ? *reinterpret_cast<const float4*>(s0 + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
             x[j] = f.x; x[j + 1] = f.y; x[j + 2] = f.z; x[j + 3] = f.w;
         }
+        uint32_t pk[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) st_chunk_bf16(half, v, (c0 >> 3) + q, x + 8 * q);
+        for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(x[2 * q], x[2 * q + 1]);
+        tmem_st16(tm_sbf + c0 / 2, pk);
         uint32_t r[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j] * g63);
-        tmem_st32(tm + c0, r);
+        tmem_st32(tm_s + c0, r);
     }
     tmem_wait_st();
 }
@@ -558,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ================= TMA producer and unit scheduler =================
             if (lane == 0) {
                 uint32_t n = 0, u = 0;
-                int issued_kq[2] = {-1, -1};
+                int64_t issued_kq[kKQStages] = {-1, -1, -1};
                 int issued_v = -1;
                 for (;;) {
                     const int64_t uid = atomicAdd(p.counter, 1);
@@ -589,9 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!info.valid) break;
                     bool ok = true;
                     for (int32_t c = 0; c < nC && ok; ++c, ++n) {
-                        const int s = n & 1;
+                        const uint32_t s = n % kKQStages;
                         const int32_t t = static_cast<int32_t>(info.t0 + static_cast<int64_t>(c) * kChunk);
-                        if (n >= 2 && !(ok = wait_bar(cx, B_KQ_EMPTY + s, ((n - 2) >> 1) & 1))) break;
+                        if (n >= kKQStages && !(ok = wait_bar(cx, B_KQ_EMPTY + s, ((n - kKQStages) / kKQStages) & 1))) break;
                         uint8_t* st = sm + kKQ + s * kKQStage;
                         uint64_t* fb = cx.bars + B_KQ_FULL + s;
                         mbar_arrive_expect_tx(fb, kKQStage);
@@ -599,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(st + 8192, &tm_q, fb, 0, info.qh, t);
                         tma_load_3d(st + 16384, &tm_k, fb, 64, info.kh, t);
                         tma_load_3d(st + 24576, &tm_q, fb, 64, info.qh, t);
-                        issued_kq[s] = static_cast<int>(n);
+                        issued_kq[s] = n;
                         if (n >= 1 && !(ok = wait_bar(cx, B_V_EMPTY, (n - 1) & 1))) break;
                         uint64_t* vb = cx.bars + B_V_FULL;
                         mbar_arrive_expect_tx(vb, 16384);
@@ -610,54 +575,81 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                 }
                 // drain: every issued load has landed before the CTA may exit
-                for (int s = 0; s < 2; ++s)
-                    if (issued_kq[s] >= 0) drain_bar(cx, B_KQ_FULL + s, (issued_kq[s] >> 1) & 1);
+                for (uint32_t s = 0; s < kKQStages; ++s)
+                    if (issued_kq[s] >= 0) drain_bar(cx, B_KQ_FULL + s, (issued_kq[s] / kKQStages) & 1);
                 if (issued_v >= 0) drain_bar(cx, B_V_FULL, issued_v & 1);
             }
         } else if (warp == 1) {
             // ================= tcgen05 issue: D1, W, U =================
+            // D1 of the next chunk needs only the intra side to be done with D1 of this one (mid-chunk) and
+            // its K | Q tiles (three stages), while W and U of this chunk need the full inverse: D1 goes
+            // first, so the intra side finds it computed when it starts the next chunk.
             if (lane == 0) {
                 uint32_t n = 0, u = 0;
                 bool ok = true;
-                for (; ok;) {
-                    const int slot = u & 1;
-                    if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
-                    const UnitInfo info = read_unit(sm, slot);
-                    mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
-                    ++u;
-                    if (!info.valid) break;
-                    for (int32_t c = 0; c < info.nC; ++c, ++n) {
-                        const int s = n & 1;
-                        if (!(ok = wait_bar(cx, B_KQ_FULL + s, (n >> 1) & 1))) break;
-                        if (n >= 1 && !(ok = wait_bar(cx, B_D1_EMPTY, (n - 1) & 1))) break;
-                        tc_fence_after();
-                        const uint32_t kq = smem_u32(sm + kKQ + s * kKQStage);
-    #pragma unroll 1
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                            mma_bf16_ss(tmem + kTmD1, desc_kmajor_sw128(kq + off), desc_kmajor_sw128(kq + off), kIdescD1,
-                                        ks > 0);
-                        }
-                        mma_commit(cx.bars + B_D1_FULL);
-                        if (!(ok = wait_bar(cx, B_T_FULL, n & 1))) break;
-                        if (!(ok = wait_bar(cx, B_V_FULL, n & 1))) break;
-                        // the W columns are free once the state warps have copied W of chunk n-1
-                        if (n >= 1 && !(ok = wait_bar(cx, B_WB_FULL + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
-                        if (n >= 2 && !(ok = wait_bar(cx, B_S_FULL + s, ((n - 2) >> 1) & 1))) break;
-                        tc_fence_after();
-                        const uint32_t vv = smem_u32(sm + kV);
-                        const uint32_t tp = smem_u32(sm + kTp), tpp = smem_u32(sm + kTpp);
-                        const uint32_t dbuf = tmem + kTmDelta + s * 64;
-    #pragma unroll 1
-                        for (int ks = 0; ks < 4; ++ks) {
-                            mma_bf16_ss(tmem + kTmW, desc_mnmajor_sw128(kq + ks * 2048, 16384),
-                                        desc_kmajor_sw128(tp + ks * 32), kIdescWU, ks > 0);
-                            mma_bf16_ss(dbuf, desc_mnmajor_sw128(vv + ks * 2048, 8192), desc_kmajor_sw128(tpp + ks * 32),
-                                        kIdescWU, ks > 0);
-                        }
-                        mma_commit(cx.bars + B_WU_FULL);
-                        mma_commit(cx.bars + B_V_EMPTY);
+                auto next_unit = [&](UnitInfo& info) -> bool {  // next unit with chunks (or the end marker)
+                    for (;;) {
+                        const int slot = u & 1;
+                        if (!wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1)) return false;
+                        info = read_unit(sm, slot);
+                        mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
+                        ++u;
+                        if (!info.valid || info.nC > 0) return true;
                     }
+                };
+                auto issue_d1 = [&](uint32_t m) -> bool {  // D1 of global chunk m
+                    const uint32_t st = m % kKQStages;
+                    if (!wait_bar(cx, B_KQ_FULL + st, (m / kKQStages) & 1)) return false;
+                    if (m >= 1 && !wait_bar(cx, B_D1_EMPTY, (m - 1) & 1)) return false;
+                    tc_fence_after();
+                    const uint32_t kq = smem_u32(sm + kKQ + st * kKQStage);
+    #pragma unroll 1
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16_ss(tmem + kTmD1, desc_kmajor_sw128(kq + off), desc_kmajor_sw128(kq + off), kIdescD1,
+                                    ks > 0);
+                    }
+                    mma_commit(cx.bars + B_D1_FULL);
+                    return true;
+                };
+                auto issue_wu = [&](uint32_t m) -> bool {  // W and U of global chunk m
+                    if (!wait_bar(cx, B_T_FULL, m & 1) || !wait_bar(cx, B_V_FULL, m & 1)) return false;
+                    // the W columns are free once the state warps have copied W of chunk m-1
+                    if (m >= 1 && !wait_bar(cx, B_WB_FULL + ((m - 1) & 1), ((m - 1) >> 1) & 1)) return false;
+                    // the Delta slot is free once S of chunk m-2 has read it
+                    if (m >= 2 && !wait_bar(cx, B_S_FULL + (m & 1), ((m - 2) >> 1) & 1)) return false;
+                    tc_fence_after();
+                    const uint32_t kq = smem_u32(sm + kKQ + (m % kKQStages) * kKQStage);
+                    const uint32_t vv = smem_u32(sm + kV);
+                    const uint32_t tp = smem_u32(sm + kTp), tpp = smem_u32(sm + kTpp);
+                    const uint32_t dbuf = tmem + kTmDelta + (m & 1) * 64;
+    #pragma unroll 1
+                    for (int ks = 0; ks < 4; ++ks) {
+                        mma_bf16_ss(tmem + kTmW, desc_mnmajor_sw128(kq + ks * 2048, 16384),
+                                    desc_kmajor_sw128(tp + ks * 32), kIdescWU, ks > 0);
+                        mma_bf16_ss(dbuf, desc_mnmajor_sw128(vv + ks * 2048, 8192), desc_kmajor_sw128(tpp + ks * 32),
+                                    kIdescWU, ks > 0);
+                    }
+                    mma_commit(cx.bars + B_WU_FULL);
+                    mma_commit(cx.bars + B_V_EMPTY);
+                    return true;
+                };
+                UnitInfo cur;
+                ok = next_unit(cur);
+                if (ok && cur.valid) ok = issue_d1(0);
+                while (ok && cur.valid) {
+                    UnitInfo nxt;
+                    nxt.valid = 0;
+                    for (int32_t c = 0; c < cur.nC && ok; ++c, ++n) {
+                        if (c + 1 < cur.nC) {
+                            ok = issue_d1(n + 1);
+                        } else {
+                            ok = next_unit(nxt);
+                            if (ok && nxt.valid) ok = issue_d1(n + 1);
+                        }
+                        if (ok) ok = issue_wu(n);
+                    }
+                    cur = nxt;
                 }
                 mma_commit(cx.bars + B_DRAIN_I);
                 drain_bar(cx, B_DRAIN_I, 0);
@@ -679,24 +671,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t ph = (n >> 1) & 1;
                         if (!(ok = wait_bar(cx, B_WB_FULL + s, ph))) break;
                         if (!(ok = wait_bar(cx, B_SB_FULL + s, ph))) break;
-                        if (!(ok = wait_bar(cx, B_KQ_FULL + s, ph))) break;
+                        const uint32_t st = n % kKQStages;
+                        if (!(ok = wait_bar(cx, B_KQ_FULL + st, (n / kKQStages) & 1))) break;
                         tc_fence_after();
-                        const uint32_t kq = smem_u32(sm + kKQ + s * kKQStage);
-                        const uint32_t sb = smem_u32(sm + kSb), wb = smem_u32(sm + kWb);
+                        const uint32_t kq = smem_u32(sm + kKQ + st * kKQStage);
+                        const uint32_t wb = smem_u32(sm + kWb);
                         const uint32_t dbuf = tmem + kTmDelta + s * 64;
     #pragma unroll 1
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const uint32_t aoff = (ks >> 2) * 16384 + (ks & 3) * 32;
-                            mma_bf16_ss(dbuf, desc_kmajor_sw128(sb + aoff), desc_mnmajor_sw128(wb + ks * 2048, 8192),
+                        for (int ks = 0; ks < 8; ++ks)  // A = S (bf16 pairs in TMEM), k = 16 ks .. 16 ks + 15
+                            mma_bf16_ts(dbuf, tmem + kTmSbf + ks * 8, desc_mnmajor_sw128(wb + ks * 2048, 8192),
                                         kIdescDelta, 1);
-                        }
                         mma_commit(cx.bars + B_DELTA_FULL + s);
                         if (n >= 1 && !(ok = wait_bar(cx, B_O_EMPTY + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
                         tc_fence_after();
     #pragma unroll 1
-                        for (int ks = 0; ks < 8; ++ks) {
+                        for (int ks = 0; ks < 8; ++ks) {  // O = S Q'^T, Q' = diag(gamma) Q
                             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                            mma_bf16_ss(tmem + kTmO1, desc_kmajor_sw128(sb + off), desc_kmajor_sw128(kq + 8192 + off),
+                            mma_bf16_ts(tmem + kTmO, tmem + kTmSbf + ks * 8, desc_kmajor_sw128(kq + 8192 + off),
                                         kIdescO, ks > 0);
                         }
                         if (!(ok = wait_bar(cx, B_DD_FULL + s, ph))) break;
@@ -705,11 +696,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     #pragma unroll 1
                         for (int ks = 0; ks < 4; ++ks) {
                             const uint32_t acol = dbuf + 32 * (ks >> 1) + 8 * (ks & 1);  // packed j = 16 ks .. 16 ks + 15
-                            mma_bf16_ts(tmem + kTmO2, acol, desc_kmajor_sw128(pb + ks * 32), kIdescO, ks > 0);
+                            mma_bf16_ts(tmem + kTmO, acol, desc_kmajor_sw128(pb + ks * 32), kIdescO, 1);  // O += Delta^T P^T
                             mma_bf16_ts(tmem + kTmS, acol + 16, desc_mnmajor_sw128(kq + ks * 2048, 16384), kIdescS, 1);
                         }
                         mma_commit(cx.bars + B_S_FULL + s);
-                        mma_commit(cx.bars + B_KQ_EMPTY + s);
+                        mma_commit(cx.bars + B_KQ_EMPTY + st);
                     }
                 }
                 mma_commit(cx.bars + B_DRAIN_S);
@@ -731,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (info.nC > 0)
                     gpf = load_gates(p, info.t0, info.L < kChunk ? static_cast<int32_t>(info.L) : kChunk, info.h, lane);
                 for (int32_t c = 0; c < info.nC; ++c, ++n) {
-                    const uint32_t gs = n % 3;  // gates slot (three in flight); the K | Q stage is n & 1
+                    const uint32_t gs = n % 3;  // gates slot (three in flight)
                     const GatePrefetch cur = gpf;
                     if (c + 1 < info.nC) {
                         const int64_t rem1 = info.L - static_cast<int64_t>(c + 1) * kChunk;
@@ -739,19 +730,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          rem1 < kChunk ? static_cast<int32_t>(rem1) : kChunk, info.h, lane);
                     }
                     if (n >= 3 && !(ok = wait_bar(cx, B_GATES_EMPTY + gs, ((n - 3) / 3) & 1))) break;
-                    const int64_t rem = info.L - static_cast<int64_t>(c) * kChunk;
-                    const int32_t Lc = rem < kChunk ? static_cast<int32_t>(rem) : kChunk;
                     float* gbw = reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats;
-                    compute_gates(cur, gbw, p.scale, p.l2norm != 0, lane);
+                    compute_gates(cur, gbw, p.l2norm != 0, lane);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(cx.bars + B_GATES_FULL + gs);
-                    // query norms (needed only by the output epilogue) after the intra side has its vectors
-                    if (p.l2norm) {
-                        if (!(ok = wait_bar(cx, B_KQ_FULL + (n & 1), (n >> 1) & 1))) break;
-                        query_norms(sm + kKQ + (n & 1) * kKQStage + 8192, gbw, p.scale, Lc, lane);
-                        __syncwarp();
-                    }
-                    if (lane == 0) mbar_arrive(cx.bars + B_QN_FULL + gs);
                 }
             }
         }
@@ -782,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t Lc = rem < kChunk ? static_cast<int32_t>(rem) : kChunk;
                 const uint32_t gs = n % 3;
                 float* gb = reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats;
-                uint8_t* kqs = sm + kKQ + s * kKQStage;
+                uint8_t* kqs = sm + kKQ + (n % kKQStages) * kKQStage;
                 if (!(ok = wait_bar(cx, B_GATES_FULL + gs, (n / 3) & 1))) break;
                 // P buffer s is free once O2 of chunk n-2 has completed
                 if (n >= 2 && !(ok = wait_bar(cx, B_S_FULL + s, ((n - 2) >> 1) & 1))) break;
@@ -847,6 +829,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
+                // Q' = diag(gamma) Q in place, for the S Q'^T product (D1 has read Q already); under the L2 norm
+                // the same pass sums |q_i|^2.  Four threads per row, 32 values each.
+                {
+                    const int qr = it >> 2, qq = it & 3;
+                    const float gam = gb[kGGam + qr];
+                    float ss = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int cch = 4 * qq + k;  // 16-byte column of the 256-byte row
+                        uint8_t* half = kqs + 8192 + (cch >> 3) * 16384;
+                        float f[8];
+                        bf16x8_to_float(*reinterpret_cast<const uint4*>(half + sw128_offset(qr, cch & 7)), f);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            ss += f[j] * f[j];
+                            f[j] *= gam;
+                        }
+                        st_chunk_bf16(half, qr, cch & 7, f);
+                    }
+                    if (p.l2norm) {
+                        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                        if (qq == 0) gb[kGRm + qr] = qr < Lc ? rsqrtf(ss + 1e-6f) : 0.f;
+                    }
+                }
                 // zero the padded rows of the K and V tiles (they hold the next
                 // sequence or TMA zero fill; only exact zeros may meet them)
                 if (Lc < kChunk) {
@@ -880,7 +887,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hh = (warp - 12) >> 2;               // column half
         const int v = wq * 32 + lane;                  // TMEM lane = state row v
         const uint32_t tm_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-        uint8_t* sb = sm + kSb;
         __nv_bfloat16* outT = reinterpret_cast<__nv_bfloat16*>(sm + kOutT);
         uint32_t n = 0, u = 0;
         bool ok = true;
@@ -905,12 +911,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 continue;
             }
-            // initial state: S0 -> Sb (bf16) and gamma_63(first chunk) * S0 -> TMEM
+            // initial state: S0 -> the bf16 operand columns and gamma_63(first chunk) * S0 -> the accumulator
+            // (the previous unit's last products, their readers, completed before its last state epilogue)
             {
                 if (!(ok = wait_bar(cx, B_GATES_FULL + n % 3, (n / 3) & 1))) break;
                 const float g63 = reinterpret_cast<const float*>(sm + kGbuf)[(n % 3) * kGFloats + kGGam + 63];
-                load_initial_state(s0, sb + hh * 16384, tm_lane + kTmS + 64 * hh, v, g63);
-                fence_proxy_async_smem();
+                load_initial_state(s0, tm_lane + kTmSbf + 32 * hh, tm_lane + kTmS + 64 * hh, g63);
                 tc_fence_before();
                 named_bar_sync(kBarState, kStateThreads);
                 if (st == 0) mbar_arrive(cx.bars + B_SB_FULL + (n & 1));
@@ -989,7 +995,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ck = p.checkpoints + (static_cast<size_t>(info.ckpt_base + pend / p.ckpt_n - 1) * H + info.h) *
                                                  kHead * kHead + static_cast<size_t>(v) * kHead + 64 * hh;
                     float* fin = (last && p.output_state) ? p.output_state + state_off : nullptr;
-                    uint8_t* half = sb + hh * 16384;
 #pragma unroll 1
                     for (int c0 = 0; c0 < 64; c0 += 16) {
                         uint32_t r[16];
@@ -1007,14 +1012,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int j = 0; j < 16; j += 4)
                                 *reinterpret_cast<float4*>(fin + c0 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
                         }
-                        if (!last) {
-                            st_chunk_bf16(half, v, c0 >> 3, x);
-                            st_chunk_bf16(half, v, (c0 >> 3) + 1, x + 8);
+                        if (!last) {  // bf16 pairs (c, c + 1) in column c / 2 of the operand
+                            uint32_t pk[8];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) pk[q] = pack_bf16x2(x[2 * q], x[2 * q + 1]);
+                            tmem_st8(tm_lane + kTmSbf + 32 * hh + c0 / 2, pk);
                         }
                     }
+                    if (!last) tmem_wait_st();
                 }
                 if (st == 0) bulk_wait_group_read0();  // the previous chunk's output store has read outT
-                fence_proxy_async_smem();
                 tc_fence_before();
                 named_bar_sync(kBarState, kStateThreads);
                 if (st == 0 && !last) mbar_arrive(cx.bars + B_SB_FULL + ((n + 1) & 1));
@@ -1036,29 +1043,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_st();
                 }
-                // ---- output epilogue: o_i = orow_i (S Q^T)_i + scale rm_i (Delta^T P^T)_i, tokens i in [32 hh, 32 hh + 32)
-                if (!(ok = wait_bar(cx, B_QN_FULL + gs, (n / 3) & 1))) break;
+                // ---- output epilogue: o_i = scale rm_i (S Q'^T + Delta^T P^T)_i, tokens i in [32 hh, 32 hh + 32)
                 {
                     const float sc = p.scale;
 #pragma unroll 1
                     for (int i0 = 32 * hh; i0 < 32 * hh + 32; i0 += 8) {
-                        uint32_t r1[8], r2[8];
-                        tmem_ld8(tm_lane + kTmO1 + i0, r1);
-                        tmem_ld8(tm_lane + kTmO2 + i0, r2);
-                        const float4 oa = *reinterpret_cast<const float4*>(gb + kGOr + i0);
-                        const float4 ob = *reinterpret_cast<const float4*>(gb + kGOr + i0 + 4);
+                        uint32_t r1[8];
+                        tmem_ld8(tm_lane + kTmO + i0, r1);
                         const float4 ma = *reinterpret_cast<const float4*>(gb + kGRm + i0);
                         const float4 mb = *reinterpret_cast<const float4*>(gb + kGRm + i0 + 4);
-                        const float orow[8] = {oa.x, oa.y, oa.z, oa.w, ob.x, ob.y, ob.z, ob.w};
                         const float rm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
                         tmem_wait_ld();
                         tmem_regs_ready(r1);
-                        tmem_regs_ready(r2);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float o = orow[j] * __uint_as_float(r1[j]) + sc * rm[j] * __uint_as_float(r2[j]);
-                            outT[(i0 + j) * kHead + v] = __float2bfloat16_rn(o);
-                        }
+                        for (int j = 0; j < 8; ++j)
+                            outT[(i0 + j) * kHead + v] = __float2bfloat16_rn(sc * rm[j] * __uint_as_float(r1[j]));
                     }
                 }
                 fence_proxy_async_smem();
