@@ -581,9 +581,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else if (warp == 1) {
             // ================= tcgen05 issue: D1, W, U =================
-            // D1 of the next chunk needs only the intra side to be done with D1 of this one (mid-chunk) and
-            // its K | Q tiles (three stages), while W and U of this chunk need the full inverse: D1 goes
-            // first, so the intra side finds it computed when it starts the next chunk.
+            // D1 of the next chunk of the unit needs only the intra side to be done with D1 of this one
+            // (mid-chunk) and its K | Q tiles (three stages), while W and U of this chunk need the full
+            // inverse: D1 goes first, so the intra side finds it computed when it starts the next chunk.
             if (lane == 0) {
                 uint32_t n = 0, u = 0;
                 bool ok = true;
@@ -634,22 +634,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(cx.bars + B_V_EMPTY);
                     return true;
                 };
-                UnitInfo cur;
-                ok = next_unit(cur);
-                if (ok && cur.valid) ok = issue_d1(0);
-                while (ok && cur.valid) {
-                    UnitInfo nxt;
-                    nxt.valid = 0;
+                // Look-ahead stays inside a unit: reading the next unit early could wait on a ring slot that the
+                // other roles free only after this unit's last W and U (two empty units in a row do that).
+                while (ok) {
+                    UnitInfo cur;
+                    if (!(ok = next_unit(cur)) || !cur.valid) break;
+                    ok = issue_d1(n);
                     for (int32_t c = 0; c < cur.nC && ok; ++c, ++n) {
-                        if (c + 1 < cur.nC) {
-                            ok = issue_d1(n + 1);
-                        } else {
-                            ok = next_unit(nxt);
-                            if (ok && nxt.valid) ok = issue_d1(n + 1);
-                        }
+                        if (c + 1 < cur.nC) ok = issue_d1(n + 1);
                         if (ok) ok = issue_wu(n);
                     }
-                    cur = nxt;
                 }
                 mma_commit(cx.bars + B_DRAIN_I);
                 drain_bar(cx, B_DRAIN_I, 0);

@@ -19,8 +19,10 @@ def to_device(inp, device="cuda"):
     return out
 
 
-def run_gpu(inp, intermediates=None, return_plan=False, **override):
-    """Run the CUDA path on device inputs `inp` (from to_device)."""
+def run_gpu(inp, intermediates=None, return_plan=False, check_status=True, **override):
+    """Run the CUDA path on device inputs `inp` (from to_device).  With
+    check_status the device status word must come back clear: no input flag
+    and no timed-out wait inside a kernel."""
     d = inp["q"].device
     H = inp["H"]
     T = inp["T"]
@@ -42,10 +44,11 @@ def run_gpu(inp, intermediates=None, return_plan=False, **override):
         kw["state_checkpoints"] = torch.full((max(nck, 1), H, 128, 128), float("nan"), device=d)
     kw.update(override)
     res = gdn.chunk_gated_delta_rule(inp["q"], inp["k"], inp["v"], intermediates=intermediates,
-                                     return_plan=return_plan, **kw)
-    plan = ws = None
-    if return_plan:
-        res, plan, ws = res
+                                     return_plan=True, **kw)
+    res, plan, ws = res
+    if check_status:
+        bits = gdn.read_status(plan, ws)
+        assert bits == 0, f"device status bits {bits:#x}"
     if kw.get("output_final_state"):
         out, fin = res
     else:

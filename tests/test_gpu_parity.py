@@ -86,6 +86,15 @@ def test_all_sequences_empty():
     assert torch.equal(res["final_state"].cpu(), inp["initial_state"])
 
 
+def test_runs_of_empty_sequences_between_chunks():
+    # several zero-length sequences in a row between non-empty ones: every role must step over them
+    # without waiting for the next non-empty unit early (the status word must stay clear: no timed-out wait)
+    w = wl.custom(seq_lens=[100, 0, 0, 0, 70, 0, 0, 130, 0, 0, 0, 0, 5, 0, 0], hq=2, hk=2, hv=2,
+                  initial_state="dense", checkpoint_every=64)
+    inp = wl.generate(w, seed=17)
+    check_against_oracle(inp, run_gpu(to_device(inp)))
+
+
 def test_zero_initial_state_and_no_final_state():
     w = wl.custom(seq_lens=[100, 0, 37], hq=4, hk=4, hv=4, output_final_state=False)
     inp = wl.generate(w, seed=6)
@@ -177,7 +186,7 @@ def test_intra_stage_matches_oracle_intermediates(dtype):
 
 
 def _status_after(inp_dev, **override):
-    res = run_gpu(inp_dev, return_plan=True, **override)
+    res = run_gpu(inp_dev, return_plan=True, check_status=False, **override)
     return gdn.read_status(res["plan"], res["ws"])
 
 
@@ -208,3 +217,30 @@ def test_fp32_inputs_tails_heads_pool_checkpoints(l2):
                   l2norm_in_kernel=l2, initial_state="pool", n_pool=6, checkpoint_every=64)
     inp = wl.generate(w, seed=14)
     check_against_oracle(inp, run_gpu(to_device(inp)))
+
+
+def test_steep_gates_take_the_pairwise_decay_path():
+    # alpha ~ U(0.05, 0.3): log alpha ~ -1.2 .. -3 per token, so a chunk's gate range is far above the
+    # limit of the row x column factorisation and every A / P entry takes e^{G_i - G_j} pairwise
+    w = wl.custom(seq_lens=[200, 64, 5, 130], hq=2, hk=2, hv=4, alpha="u(0.05,0.3)", l2norm_in_kernel=True,
+                  qk_prenorm=False, initial_state="dense", checkpoint_every=64)
+    inp = wl.generate(w, seed=15)
+    check_against_oracle(inp, run_gpu(to_device(inp)))
+
+
+def test_more_sequences_than_the_on_chip_sort():
+    # 9000 sequences (above the 8192 the prepare kernel sorts on chip; the rest keep their order), most of
+    # them a few tokens long, a few of them several chunks long
+    rng = np.random.default_rng(16)
+    lens = rng.integers(0, 4, size=9000)
+    lens[::997] = rng.integers(60, 300, size=len(lens[::997]))
+    w = wl.custom(seq_lens=[int(x) for x in lens], hq=1, hk=1, hv=1, initial_state="dense")
+    inp = wl.generate(w, seed=16)
+    res = run_gpu(to_device(inp), return_plan=True)
+    check_against_oracle(inp, res)
+    offsets, cmap, n_chunks, order = gdn.read_chunk_map(res["plan"], res["ws"], len(lens))
+    ref_off, ref_map, ref_n = oracle.chunk_map(inp["cu_seqlens"].numpy(), 64)
+    assert n_chunks == ref_n
+    assert np.array_equal(offsets.numpy(), ref_off)
+    assert np.array_equal(cmap.numpy(), ref_map[:ref_n])
+    assert sorted(order.numpy().tolist()) == list(range(len(lens)))
