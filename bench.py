@@ -6,7 +6,7 @@ pass, output, checkpoints) over the benchmark workload, inputs resident in HBM.
 Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--seed S] [--no-cpu-baseline]
+                  [--workload NAME] [--seed S] [--no-cpu-baseline] [--op prefill|decode]
 
 * value: tokens/s of the whole job (all ranks), device-timed with CUDA events,
   L2 flushed (256 MiB write) between steps, outside the timed events.
@@ -19,6 +19,11 @@ Prints one JSON line (rank 0).
   bounded sample of the same workload (a subset of state heads), scaled to
   tokens/s of the whole workload.
 * --impl reference: the oracle as the reference arm (host cores only).
+
+--op decode times the decode step (gdn_decode_run) on a decode workload
+(default decode_gva_512seq_bf16: 512 sequences, one token each, a pool of
+1024 states) instead; its JSON line carries the same roofline and
+cpu_baseline objects.
 
 Multi-GPU: launched by torch.distributed.run, every rank runs its own replica
 of the workload (units are independent: no data-path collective); only a
@@ -246,8 +251,13 @@ def cpu_baseline(inp, budget_s=15.0):
         k = f64(inp["k"])[:, [h // (H // hk) for h in hs]]
         v = f64(inp["v"])[:, [h // (H // hv) for h in hs]]
         g, b = f64(inp["g"])[:, hs], f64(inp["beta"])[:, hs]
-        s0 = None if inp.get("initial_state") is None else f64(inp["initial_state"])[:, hs]
-        idx = None if inp.get("state_indices") is None else inp["state_indices"].numpy().astype(np.int64)
+        s0, idx = None, None
+        if inp.get("initial_state") is not None:
+            st = inp["initial_state"]
+            if inp.get("state_indices") is not None:  # only the named pool rows, renumbered in order
+                st = st[inp["state_indices"].long()]
+                idx = np.arange(st.shape[0], dtype=np.int64)
+            s0 = f64(st[:, hs])
         n = inp.get("checkpoint_every_n_tokens") or 0
         ccs = None if not n else inp["checkpoint_cu_starts"].numpy().astype(np.int64)
         t0 = time.perf_counter()
@@ -314,6 +324,88 @@ def run_reference(args, w, inp):
     print(json.dumps(line), flush=True)
 
 
+def decode_bytes(w, inp):
+    """Bytes a decode step must move: every named state read and written,
+    q, k, v and g, beta read, o written, the pool indices read."""
+    T, H, D = inp["T"], inp["H"], 128
+    N = len(inp["seq_lens"])
+    esz = inp["q"].element_size()
+    return (2 * N * H * D * D * 4 + T * (w.hq + w.hk + w.hv) * D * esz + T * H * 8 + T * H * D * esz
+            + (N * 4 if inp.get("state_indices") is not None else 0))
+
+
+def run_decode_bench(args, w, inp, device):
+    m = inp["seq_lens"][0]
+    if any(x != m for x in inp["seq_lens"]):
+        raise SystemExit("--op decode needs a workload whose sequences all have the same length")
+    d = {k: (v.to(device).contiguous() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    pool = d["initial_state"]
+    out, _ = gdn.gated_delta_rule_decode(d["q"], d["k"], d["v"], g=d["g"], beta=d["beta"], scale=inp["scale"],
+                                         initial_state=pool, state_indices=d.get("state_indices"),
+                                         use_qk_l2norm_in_kernel=inp["use_qk_l2norm_in_kernel"],
+                                         tokens_per_seq=m, device_status=status)
+    torch.cuda.synchronize(device)
+    if int(status.item()):
+        raise RuntimeError(f"device status bits {int(status.item()):#x} on the decode workload")
+    N, T, H = len(inp["seq_lens"]), inp["T"], inp["H"]
+    plan = gdn.get_plan(w.hq, w.hk, w.hv, gdn.DTYPE_BF16 if inp["q"].dtype == torch.bfloat16 else gdn.DTYPE_F32,
+                        gdn.FLAGS["HAS_G"] | gdn.FLAGS["HAS_BETA"] | gdn.FLAGS["HAS_SCALE"] |
+                        (gdn.FLAGS["QK_L2NORM"] if inp["use_qk_l2norm_in_kernel"] else 0) |
+                        gdn.FLAGS["HAS_INITIAL_STATE"] | gdn.FLAGS["OUTPUT_FINAL_STATE"] |
+                        gdn.FLAGS["HAS_STATE_INDICES"], 0, T, N, pool.shape[0])
+    cargs = gdn.Args(q=d["q"].data_ptr(), k=d["k"].data_ptr(), v=d["v"].data_ptr(), g=d["g"].data_ptr(),
+                     beta=d["beta"].data_ptr(), scale=float(inp["scale"]), num_seqs=N, total_tokens=T,
+                     initial_state=pool.data_ptr(), output_state=pool.data_ptr(), n_pool=pool.shape[0],
+                     state_indices=d["state_indices"].data_ptr(), output=out.data_ptr(),
+                     device_status=status.data_ptr())
+    stream = torch.cuda.Stream(device)
+    sp = stream.cuda_stream
+
+    def step():
+        st = gdn.gdn_decode_run(plan.handle, cargs, m, sp)
+        if st:
+            raise RuntimeError(f"gdn_decode_run returned {st}")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(device.index or 0)
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark_start()
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    sampler.mark_end()
+    ms = e0.elapsed_time(e1) / K
+    clocks = sampler.stop()
+    if int(status.item()):
+        raise RuntimeError(f"device status bits {int(status.item()):#x} after the timed steps")
+    hbm, _, src = measured_peaks()
+    abytes = decode_bytes(w, inp)
+    achieved = abytes / (ms / 1e3) / 1e9
+    line = {"metric": "GDN decode step tokens/s, 1 GPU", "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
+            "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if inp["q"].dtype == torch.bfloat16 else "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "op": "decode", "num_seqs": N, "tokens_per_seq": m,
+                       "num_q_heads": w.hq, "num_k_heads": w.hk, "num_v_heads": w.hv, "state_heads": H,
+                       "pool_rows": pool.shape[0], "qk_l2norm_in_kernel": w.l2norm_in_kernel,
+                       "l2": f"inputs larger than L2 ({abytes / 2**20:.0f} MiB moved per step), no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": None, "kernel": "gdn_decode_kernel", "kernel_ms": ms,
+                         "algorithmic_bytes": abytes, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"},
+            "gpu_launches": K}
+    if clocks:
+        line["clocks"] = clocks
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp)
+    print(json.dumps(line), flush=True)
+
+
 def workload_config(w, inp, args):
     return {"workload": w.name, "total_tokens": inp["T"], "num_seqs": len(inp["seq_lens"]),
             "seq_lens": inp["seq_lens"] if len(inp["seq_lens"]) <= 16 else f"{len(inp['seq_lens'])} sequences",
@@ -333,8 +425,11 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", choices=["prefill", "decode"], default="prefill")
     args = ap.parse_args()
     world, rank, local = dist_env()
+    if args.op == "decode" and args.workload == wl.BENCH_WORKLOAD:
+        args.workload = "decode_gva_512seq_bf16"
     w = wl.WORKLOADS[args.workload]
     inp = wl.generate(w, seed=args.seed)
 
@@ -353,6 +448,10 @@ def main():
         dist.init_process_group("nccl", device_id=device)
         pg = dist
     gdn.build()
+    if args.op == "decode":
+        if rank == 0:
+            run_decode_bench(args, w, inp, device)
+        return
     call = make_call(inp, device)
     plan, ws, cargs = call["plan"], call["ws"], call["args"]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)

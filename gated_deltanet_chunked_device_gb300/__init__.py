@@ -34,7 +34,8 @@ import torch
 from . import _build
 
 __all__ = [
-    "build", "lib", "chunk_gated_delta_rule", "gdn_prefill_plan", "gdn_prefill_run", "gdn_prefill_prepare",
+    "build", "lib", "chunk_gated_delta_rule", "gated_delta_rule_decode", "gdn_prefill_plan", "gdn_prefill_run",
+    "gdn_prefill_prepare", "gdn_decode_run",
     "gdn_prefill_chunks", "gdn_prefill_run_static", "gdn_prefill_read_status",
     "gdn_prefill_workspace_layout", "gdn_prefill_plan_destroy", "gdn_status_string", "Desc", "Args", "Layout",
     "GdnError", "STATUS", "DEVICE_ERR", "FLAGS",
@@ -113,6 +114,8 @@ def lib():
                     fn = getattr(L, name)
                     fn.argtypes = L.gdn_prefill_run.argtypes
                     fn.restype = ctypes.c_int
+                L.gdn_decode_run.argtypes = [ctypes.c_void_p, ctypes.POINTER(Args), ctypes.c_int32, ctypes.c_void_p]
+                L.gdn_decode_run.restype = ctypes.c_int
                 L.gdn_prefill_run_static.argtypes = [ctypes.c_void_p, ctypes.POINTER(Args), ctypes.c_void_p]
                 L.gdn_prefill_run_static.restype = ctypes.c_int
                 L.gdn_prefill_read_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -153,6 +156,10 @@ def gdn_prefill_prepare(plan, args: Args, workspace_ptr: int, workspace_bytes: i
 def gdn_prefill_chunks(plan, args: Args, workspace_ptr: int, workspace_bytes: int, stream_ptr: int) -> int:
     return lib().gdn_prefill_chunks(plan, ctypes.byref(args), ctypes.c_void_p(workspace_ptr), workspace_bytes,
                                     ctypes.c_void_p(stream_ptr))
+
+
+def gdn_decode_run(plan, args: Args, tokens_per_seq: int, stream_ptr: int) -> int:
+    return lib().gdn_decode_run(plan, ctypes.byref(args), int(tokens_per_seq), ctypes.c_void_p(stream_ptr))
 
 
 def gdn_prefill_run_static(plan, args: Args, stream_ptr: int) -> int:
@@ -363,6 +370,77 @@ def chunk_gated_delta_rule(q, k, v, g=None, beta=None, scale=None, initial_state
     if return_plan:
         return res, plan, ws
     return res
+
+
+def gated_delta_rule_decode(q, k, v, g=None, beta=None, scale=None, initial_state=None, state_indices=None,
+                            output_final_state=True, output_state=None, use_qk_l2norm_in_kernel=False,
+                            tokens_per_seq=1, output=None, device_status=None):
+    """Decode step (or a short run of tokens) for N sequences of ``tokens_per_seq``
+    tokens each, rows i * tokens_per_seq + j of q, k, v [N * m, heads, 128],
+    g and beta [N * m, H].  Reads each sequence's state (its pool row with
+    ``state_indices``), carries it through the tokens and writes it back to
+    ``output_state`` (the pool itself, in place, with ``state_indices``).
+    Returns ``output`` or ``(output, final_state)``."""
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k, v must be [N * tokens_per_seq, heads, head_size]")
+    device = q.device
+    if device.type != "cuda":
+        raise ValueError("q, k, v must be CUDA tensors: this library has no CPU path")
+    T, hq, D = q.shape
+    hk, hv = k.shape[1], v.shape[1]
+    m = int(tokens_per_seq)
+    if D != HEAD_SIZE or k.shape[2] != D or v.shape[2] != D or k.shape[0] != T or v.shape[0] != T or m < 1 or T % m:
+        raise ValueError("q, k, v must share N * tokens_per_seq rows and have head_size 128")
+    N = T // m
+    qkv_dtype = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32}.get(q.dtype)
+    if qkv_dtype is None:
+        raise ValueError(f"unsupported q/k/v dtype {q.dtype}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_dev(name, t, device, q.dtype)
+    H = max(hq, hv)
+    flags = 0
+    if g is not None:
+        _check_dev("g", g, device, torch.float32)
+        flags |= FLAGS["HAS_G"]
+    if beta is not None:
+        _check_dev("beta", beta, device, torch.float32)
+        flags |= FLAGS["HAS_BETA"]
+    if scale is not None:
+        flags |= FLAGS["HAS_SCALE"]
+    if use_qk_l2norm_in_kernel:
+        flags |= FLAGS["QK_L2NORM"]
+    n_pool = 0
+    if state_indices is not None:
+        _check_dev("state_indices", state_indices, device)
+        flags |= FLAGS["HAS_STATE_INDICES"]
+        if state_indices.dtype == torch.int64:
+            flags |= FLAGS["STATE_INDICES_I64"]
+        if initial_state is None:
+            raise ValueError("state_indices needs the state pool as initial_state")
+        n_pool = initial_state.shape[0]
+        if output_final_state and output_state is None:
+            output_state = initial_state
+    if initial_state is not None:
+        _check_dev("initial_state", initial_state, device, torch.float32)
+        flags |= FLAGS["HAS_INITIAL_STATE"]
+    if output_final_state:
+        if output_state is None:
+            output_state = torch.empty(N, H, D, D, dtype=torch.float32, device=device)
+        _check_dev("output_state", output_state, device, torch.float32)
+        flags |= FLAGS["OUTPUT_FINAL_STATE"]
+    if output is None:
+        output = torch.empty(T, H, D, dtype=q.dtype, device=device)
+    _check_dev("output", output, device, q.dtype)
+    plan = get_plan(hq, hk, hv, qkv_dtype, flags, 0, T, N, n_pool)
+    args = Args(q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
+                scale=float(scale) if scale is not None else 0.0, num_seqs=N, total_tokens=T,
+                initial_state=_ptr(initial_state), output_state=_ptr(output_state) if output_final_state else None,
+                n_pool=n_pool, state_indices=_ptr(state_indices), output=_ptr(output),
+                device_status=_ptr(device_status))
+    st = gdn_decode_run(plan.handle, args, m, torch.cuda.current_stream(device).cuda_stream)
+    if st != 0:
+        raise GdnError(st, "gdn_decode_run")
+    return (output, output_state) if output_final_state else output
 
 
 def read_status(plan: _Plan, ws: torch.Tensor, device_status=None):

@@ -85,6 +85,26 @@ struct ChunkParams {
     int has_tokens;                // 0: the TMA maps are blank (T == 0) and never used
 };
 
+// Arguments of the decode-step kernel (a few tokens per sequence, no chunking).
+struct DecodeParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;                // nullptr: alpha = 1
+    const float* beta;             // nullptr: beta = 1
+    float scale;
+    const float* initial_state;    // nullptr: zero state
+    float* output_state;           // nullptr: state not written back
+    const void* state_indices;     // nullptr: row = sequence
+    int idx_i64;
+    int32_t n_pool;
+    void* output;
+    int32_t* status;               // nullptr: out-of-range pool rows are skipped silently
+    int32_t N, H, hq, hk, hv;
+    int32_t m;                     // tokens per sequence
+    int l2norm;
+};
+
 __host__ __device__ inline int64_t load_index(const void* p, int i64, int64_t i) {
     return i64 ? static_cast<const int64_t*>(p)[i] : static_cast<int64_t>(static_cast<const int32_t*>(p)[i]);
 }
@@ -94,6 +114,7 @@ cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t stream);
 cudaError_t launch_chunk_bf16(const ChunkParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, const CUtensorMap& tm_o, int grid, cudaStream_t stream);
 cudaError_t launch_chunk_f32(const ChunkParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t stream);
 size_t chunk_bf16_smem_bytes();
 size_t plan_workspace_bytes(gdn_prefill_plan_t plan);
 

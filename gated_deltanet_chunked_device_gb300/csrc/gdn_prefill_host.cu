@@ -291,6 +291,59 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
 
 extern "C" {
 
+gdn_status gdn_decode_run(gdn_prefill_plan_t plan, const gdn_prefill_args* args, int32_t tokens_per_seq,
+                          void* stream_ptr) {
+    if (!plan || !args) return GDN_ERR_INVALID_ARG;
+    const gdn_prefill_desc& d = plan->desc;
+    const gdn_prefill_args& a = *args;
+    const uint32_t f = d.flags;
+    if (d.checkpoint_every_n_tokens != 0) return GDN_ERR_UNSUPPORTED;
+    if (tokens_per_seq < 1 || tokens_per_seq > GDN_DECODE_MAX_TOKENS_PER_SEQ) return GDN_ERR_INVALID_ARG;
+    const int32_t N = a.num_seqs;
+    const int64_t T = a.total_tokens;
+    if (N < 0 || N > d.max_num_seqs || T != static_cast<int64_t>(N) * tokens_per_seq || T > d.max_total_tokens)
+        return GDN_ERR_INVALID_ARG;
+    if (a.state_checkpoints || a.checkpoint_cu_starts) return GDN_ERR_INVALID_ARG;
+    if (N == 0) return GDN_OK;
+    const size_t in_align = d.qkv_dtype == GDN_DTYPE_F32 ? 16 : 8;
+    if (!a.q || !a.k || !a.v || !a.output || !aligned(a.q, in_align) || !aligned(a.k, in_align) ||
+        !aligned(a.v, in_align) || !aligned(a.output, in_align))
+        return GDN_ERR_INVALID_ARG;
+    if (((f & GDN_FLAG_HAS_G) && !a.g) || ((f & GDN_FLAG_HAS_BETA) && !a.beta)) return GDN_ERR_INVALID_ARG;
+    if ((f & GDN_FLAG_HAS_INITIAL_STATE) && (!a.initial_state || !aligned(a.initial_state, 16)))
+        return GDN_ERR_INVALID_ARG;
+    if ((f & GDN_FLAG_OUTPUT_FINAL_STATE) && (!a.output_state || !aligned(a.output_state, 16)))
+        return GDN_ERR_INVALID_ARG;
+    if ((f & GDN_FLAG_HAS_STATE_INDICES) && (!a.state_indices || a.n_pool <= 0 || a.n_pool > d.max_pool_rows))
+        return GDN_ERR_INVALID_ARG;
+    const int64_t blocks = static_cast<int64_t>(N) * plan->H;
+    if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    gdn::DecodeParams p{};
+    p.q = a.q;
+    p.k = a.k;
+    p.v = a.v;
+    p.g = (f & GDN_FLAG_HAS_G) ? a.g : nullptr;
+    p.beta = (f & GDN_FLAG_HAS_BETA) ? a.beta : nullptr;
+    p.scale = (f & GDN_FLAG_HAS_SCALE) ? a.scale : 1.0f / std::sqrt(static_cast<float>(gdn::kHead));
+    p.initial_state = (f & GDN_FLAG_HAS_INITIAL_STATE) ? a.initial_state : nullptr;
+    p.output_state = (f & GDN_FLAG_OUTPUT_FINAL_STATE) ? a.output_state : nullptr;
+    p.state_indices = (f & GDN_FLAG_HAS_STATE_INDICES) ? a.state_indices : nullptr;
+    p.idx_i64 = (f & GDN_FLAG_STATE_INDICES_I64) ? 1 : 0;
+    p.n_pool = a.n_pool;
+    p.output = a.output;
+    p.status = a.device_status;
+    p.N = N;
+    p.H = plan->H;
+    p.hq = d.num_q_heads;
+    p.hk = d.num_k_heads;
+    p.hv = d.num_v_heads;
+    p.m = tokens_per_seq;
+    p.l2norm = (f & GDN_FLAG_QK_L2NORM) ? 1 : 0;
+    return gdn::launch_decode(p, d.qkv_dtype == GDN_DTYPE_BF16, static_cast<cudaStream_t>(stream_ptr)) == cudaSuccess
+               ? GDN_OK
+               : GDN_ERR_CUDA;
+}
+
 gdn_status gdn_prefill_run(gdn_prefill_plan_t plan, const gdn_prefill_args* args, void* workspace,
                            size_t workspace_bytes, void* stream) {
     return run_stages(plan, args, workspace, workspace_bytes, stream, kStagePrepare | kStageChunks);

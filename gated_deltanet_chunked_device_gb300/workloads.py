@@ -81,6 +81,11 @@ WORKLOADS = {
     "gqa_long_plus_batch_bf16": Workload("gqa_long_plus_batch_bf16", (32768,) + (1024,) * 64, 65, 32, 16, 16,
                                          torch.bfloat16, True, False, "exp_softplus16", "none",
                                          output_final_state=True),
+    # decode steps on a state pool (one token per sequence, and four speculative tokens), GVA heads
+    "decode_gva_512seq_bf16": Workload("decode_gva_512seq_bf16", (1,) * 512, 512, 16, 16, 32, torch.bfloat16, False,
+                                       True, "u(0.9,1.0)", "pool", n_pool=1024, output_final_state=True),
+    "decode4_gva_512seq_bf16": Workload("decode4_gva_512seq_bf16", (4,) * 512, 512, 16, 16, 32, torch.bfloat16,
+                                        False, True, "u(0.9,1.0)", "pool", n_pool=1024, output_final_state=True),
 }
 
 # The benchmark workload (the configuration the headline metric is quoted on).

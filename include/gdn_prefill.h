@@ -207,6 +207,30 @@ gdn_status gdn_prefill_workspace_layout(gdn_prefill_plan_t plan, gdn_prefill_lay
 #define GDN_PREFILL_STATIC_WORKSPACE_BYTES (1u << 20)
 gdn_status gdn_prefill_run_static(gdn_prefill_plan_t plan, const gdn_prefill_args *args, void *stream);
 
+/* One decode step, or a short run of tokens, per sequence: N sequences of
+ * exactly `tokens_per_seq` tokens each (1..GDN_DECODE_MAX_TOKENS_PER_SEQ),
+ * token j of sequence i at row i * tokens_per_seq + j of q, k, v, g, beta
+ * and output.  Each sequence's state is read from initial_state (its pool row
+ * with state_indices, else row i; zero without GDN_FLAG_HAS_INITIAL_STATE),
+ * carried through its tokens with the same recurrence and read-after-update
+ * output as the prefill ("GDN 与 Chunked Prefill", section "块内 state 和块间
+ * final state": after the prefill, decode carries the final state forward one
+ * token at a time), and written to output_state with
+ * GDN_FLAG_OUTPUT_FINAL_STATE (in place when it is the same pool).
+ *   - Uses a plan made for the prefill (head mapping, dtypes, flags); the
+ *     plan must have checkpoint_every_n_tokens = 0 (else
+ *     GDN_ERR_UNSUPPORTED), and total_tokens must equal N * tokens_per_seq.
+ *   - cu_seqlens, max_seqlen, the checkpoint arguments and the workspace are
+ *     not used (checkpoint pointers must be NULL).
+ *   - Needs no workspace and no prepare step.  A pool index outside
+ *     [0, n_pool) skips that sequence and sets GDN_DEVICE_ERR_STATE_INDEX_RANGE
+ *     in args.device_status when that pointer is given; duplicate indices are
+ *     a caller error (their rows race).
+ *   - q, k, v and output 8-byte aligned for bf16, 16-byte for fp32. */
+#define GDN_DECODE_MAX_TOKENS_PER_SEQ 64
+gdn_status gdn_decode_run(gdn_prefill_plan_t plan, const gdn_prefill_args *args, int32_t tokens_per_seq,
+                          void *stream);
+
 void gdn_prefill_plan_destroy(gdn_prefill_plan_t plan);
 
 const char *gdn_status_string(gdn_status status);

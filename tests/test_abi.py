@@ -135,3 +135,34 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(gdn, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         gdn.lib()
+
+
+@pytest.mark.parametrize("desc_kw,args_kw,m,expect", [
+    ({}, dict(num_seqs=4, total_tokens=4), 0, INVALID),                 # no tokens per sequence
+    ({}, dict(num_seqs=1, total_tokens=65), 65, INVALID),               # above the decode limit
+    ({}, dict(num_seqs=4, total_tokens=5), 1, INVALID),                 # total != N * m
+    ({}, dict(num_seqs=0, total_tokens=0), 1, OK),                      # nothing to do, nothing launched
+    ({}, dict(num_seqs=4, total_tokens=8, q=None), 2, INVALID),
+    ({}, dict(num_seqs=4, total_tokens=4, q=0x7f0000000004), 1, INVALID),  # bf16 q not 8-byte aligned
+    (dict(checkpoint_every_n_tokens=64), dict(num_seqs=4, total_tokens=4), 1, UNSUPPORTED),
+    ({}, dict(num_seqs=4, total_tokens=4, state_checkpoints=0x7f0000600000), 1, INVALID),
+    (dict(flags=gdn.FLAGS["HAS_BETA"]), dict(num_seqs=4, total_tokens=4), 1, INVALID),  # beta flag without beta
+    (dict(flags=gdn.FLAGS["HAS_STATE_INDICES"] | gdn.FLAGS["HAS_INITIAL_STATE"], max_pool_rows=8),
+     dict(num_seqs=4, total_tokens=4, initial_state=0x7f0000500000, state_indices=0x7f0000500000, n_pool=0), 1,
+     INVALID),                                                           # pool without rows
+])
+def test_decode_rejects_before_launch(L, desc_kw, args_kw, m, expect):
+    st, plan, nbytes = gdn.gdn_prefill_plan(_desc(**desc_kw))
+    assert st == OK
+    try:
+        st = gdn.gdn_decode_run(plan, _valid_args(cu_seqlens=None, **args_kw), m, 0)
+        assert st == expect, gdn.STATUS.get(st)
+    finally:
+        gdn.gdn_prefill_plan_destroy(plan)
+
+
+def test_decode_wrapper_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(4, 1, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        gdn.gated_delta_rule_decode(q, q, q)
