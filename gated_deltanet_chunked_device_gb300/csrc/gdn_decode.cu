@@ -12,10 +12,12 @@
 //
 // The step is bound by the state's bytes (64 KiB read and 64 KiB written per
 // (sequence, head), a few hundred bytes of q/k/v/o per token), so it runs on
-// CUDA cores with the state in registers: one CTA of 1024 threads per
-// (sequence, state head); warp w owns state rows 4w..4w+3 and lane l columns
-// 4l..4l+3, so every state row moves as one 512-byte coalesced access, and the
-// row products S k and S q are four warp-wide sums.
+// CUDA cores with the state in registers: persistent CTAs of 1024 threads,
+// one (sequence, state head) unit at a time, with the next unit's state loads
+// in flight behind the current unit's arithmetic; warp w owns state rows
+// 4w..4w+3 and lane l columns 4l..4l+3, so every state row moves as one
+// 512-byte coalesced access, and the row products S k and S q are four
+// warp-wide sums.
 #include <cuda_bf16.h>
 
 #include "gdn_internal.cuh"
@@ -69,22 +71,33 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
+// Loads of one token: this lane's 4 columns of k and q, the warp's 4 rows of v, and alpha, beta.
+struct TokenIn {
+    float k[4], q[4], v[4], a, b;
+};
+
 template <typename T>
-__global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const DecodeParams p) {
-    const int64_t unit = blockIdx.x;
-    const int32_t seq = static_cast<int32_t>(unit / p.H), h = static_cast<int32_t>(unit % p.H);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int v0 = 4 * warp, c0 = 4 * lane;
+__device__ __forceinline__ void load_token(const DecodeParams& p, int64_t tok, int32_t h, int32_t qh, int32_t kh,
+                                           int32_t vh, int v0, int c0, TokenIn& x) {
+    load4(static_cast<const T*>(p.k) + (static_cast<size_t>(tok) * p.hk + kh) * kHead + c0, x.k);
+    load4(static_cast<const T*>(p.q) + (static_cast<size_t>(tok) * p.hq + qh) * kHead + c0, x.q);
+    load4(static_cast<const T*>(p.v) + (static_cast<size_t>(tok) * p.hv + vh) * kHead + v0, x.v);
+    const size_t gi = static_cast<size_t>(tok) * p.H + h;
+    x.a = p.g ? p.g[gi] : 1.f;
+    x.b = p.beta ? p.beta[gi] : 1.f;
+}
+
+// This thread's 16 state values of unit u (sequence u / H, head u % H); false when its pool row is out of
+// range (then the unit is skipped and flagged).
+__device__ __forceinline__ bool load_state(const DecodeParams& p, int64_t u, int v0, int c0, float (&S)[4][4],
+                                           size_t& sbase) {
+    const int32_t seq = static_cast<int32_t>(u / p.H), h = static_cast<int32_t>(u % p.H);
     int64_t srow = seq;
     if (p.state_indices) {
         srow = load_index(p.state_indices, p.idx_i64, seq);
-        if (srow < 0 || srow >= p.n_pool) {  // uniform over the CTA: nothing is read or written
-            if (threadIdx.x == 0 && p.status) atomicOr(p.status, static_cast<int32_t>(GDN_DEVICE_ERR_STATE_INDEX_RANGE));
-            return;
-        }
+        if (srow < 0 || srow >= p.n_pool) return false;
     }
-    const size_t sbase = (static_cast<size_t>(srow) * p.H + h) * kHead * kHead;
-    float S[4][4];
+    sbase = (static_cast<size_t>(srow) * p.H + h) * kHead * kHead;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         if (p.initial_state) {
@@ -94,55 +107,104 @@ __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const DecodePar
             for (int j = 0; j < 4; ++j) S[r][j] = 0.f;
         }
     }
-    const T* q = static_cast<const T*>(p.q);
-    const T* k = static_cast<const T*>(p.k);
-    const T* v = static_cast<const T*>(p.v);
-    T* out = static_cast<T*>(p.output);
-    const int32_t qh = h / (p.H / p.hq), kh = h / (p.H / p.hk), vh = h / (p.H / p.hv);
-    for (int32_t t = 0; t < p.m; ++t) {
-        const int64_t tok = static_cast<int64_t>(seq) * p.m + t;
-        float kx[4], qx[4], vx[4];
-        load4(k + (static_cast<size_t>(tok) * p.hk + kh) * kHead + c0, kx);
-        load4(q + (static_cast<size_t>(tok) * p.hq + qh) * kHead + c0, qx);
-        load4(v + (static_cast<size_t>(tok) * p.hv + vh) * kHead + v0, vx);
-        const size_t gi = static_cast<size_t>(tok) * p.H + h;
-        const float a = p.g ? p.g[gi] : 1.f;
-        const float b = p.beta ? p.beta[gi] : 1.f;
-        if (p.l2norm) {
-            const float rk = rsqrtf(warp_sum(kx[0] * kx[0] + kx[1] * kx[1] + kx[2] * kx[2] + kx[3] * kx[3]) + 1e-6f);
-            const float rq = rsqrtf(warp_sum(qx[0] * qx[0] + qx[1] * qx[1] + qx[2] * qx[2] + qx[3] * qx[3]) + 1e-6f);
+    return true;
+}
+
+// Persistent CTAs walk the (sequence, head) units.  With one token per
+// sequence (kNextUnit) the next unit's state loads are issued before the
+// current unit's arithmetic; with several, the next token's inputs are loaded
+// before the current token's arithmetic instead (the registers hold one of the
+// two prefetches, not both).  Either way memory latency overlaps work.
+template <typename T, bool kNextUnit>
+__global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const DecodeParams p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int v0 = 4 * warp, c0 = 4 * lane;
+    const int64_t units = static_cast<int64_t>(p.N) * p.H;
+    int64_t u = blockIdx.x;
+    float Sn[4][4];
+    size_t sbase_n = 0;
+    bool ok_n = kNextUnit && u < units && load_state(p, u, v0, c0, Sn, sbase_n);
+    for (; u < units; u += gridDim.x) {
+        float S[4][4];
+        size_t sbase;
+        bool ok;
+        if (kNextUnit) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                kx[j] *= rk;
-                qx[j] *= rq;
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) S[r][j] = Sn[r][j];
+            sbase = sbase_n;
+            ok = ok_n;
+            const int64_t un = u + gridDim.x;
+            if (un < units) ok_n = load_state(p, un, v0, c0, Sn, sbase_n);
+        } else {
+            ok = load_state(p, u, v0, c0, S, sbase);
+        }
+        if (!ok) {  // uniform over the CTA: nothing is read or written for this unit
+            if (threadIdx.x == 0 && p.status) atomicOr(p.status, static_cast<int32_t>(GDN_DEVICE_ERR_STATE_INDEX_RANGE));
+            continue;
+        }
+        const int32_t seq = static_cast<int32_t>(u / p.H), h = static_cast<int32_t>(u % p.H);
+        const int32_t qh = h / (p.H / p.hq), kh = h / (p.H / p.hk), vh = h / (p.H / p.hv);
+        T* out = static_cast<T*>(p.output);
+        TokenIn x, xn;
+        if (!kNextUnit) load_token<T>(p, static_cast<int64_t>(seq) * p.m, h, qh, kh, vh, v0, c0, xn);
+        for (int32_t t = 0; t < p.m; ++t) {
+            const int64_t tok = static_cast<int64_t>(seq) * p.m + t;
+            if (kNextUnit) {
+                load_token<T>(p, tok, h, qh, kh, vh, v0, c0, x);
+            } else {
+                x = xn;
+                if (t + 1 < p.m) load_token<T>(p, tok + 1, h, qh, kh, vh, v0, c0, xn);
             }
+            if (p.l2norm) {
+                const float rk = rsqrtf(
+                    warp_sum(x.k[0] * x.k[0] + x.k[1] * x.k[1] + x.k[2] * x.k[2] + x.k[3] * x.k[3]) + 1e-6f);
+                const float rq = rsqrtf(
+                    warp_sum(x.q[0] * x.q[0] + x.q[1] * x.q[1] + x.q[2] * x.q[2] + x.q[3] * x.q[3]) + 1e-6f);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    x.k[j] *= rk;
+                    x.q[j] *= rq;
+                }
+            }
+            float o[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float su = warp_sum(S[r][0] * x.k[0] + S[r][1] * x.k[1] + S[r][2] * x.k[2] + S[r][3] * x.k[3]);
+                const float w = x.b * (x.v[r] - x.a * su);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) S[r][j] = x.a * S[r][j] + w * x.k[j];
+                o[r] = p.scale * warp_sum(S[r][0] * x.q[0] + S[r][1] * x.q[1] + S[r][2] * x.q[2] + S[r][3] * x.q[3]);
+            }
+            if (lane == 0) store4(out + (static_cast<size_t>(tok) * p.H + h) * kHead + v0, o);
         }
-        float o[4];
+        if (p.output_state) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const float u = warp_sum(S[r][0] * kx[0] + S[r][1] * kx[1] + S[r][2] * kx[2] + S[r][3] * kx[3]);
-            const float w = b * (vx[r] - a * u);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) S[r][j] = a * S[r][j] + w * kx[j];
-            o[r] = p.scale * warp_sum(S[r][0] * qx[0] + S[r][1] * qx[1] + S[r][2] * qx[2] + S[r][3] * qx[3]);
+            for (int r = 0; r < 4; ++r)
+                store4(p.output_state + sbase + static_cast<size_t>(v0 + r) * kHead + c0, S[r]);
         }
-        if (lane == 0) store4(out + (static_cast<size_t>(tok) * p.H + h) * kHead + v0, o);
-    }
-    if (p.output_state) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) store4(p.output_state + sbase + static_cast<size_t>(v0 + r) * kHead + c0, S[r]);
     }
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t stream) {
-    const int64_t blocks = static_cast<int64_t>(p.N) * p.H;
-    if (blocks == 0) return cudaSuccess;
-    if (bf16)
-        gdn_decode_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), kDecThreads, 0, stream>>>(p);
-    else
-        gdn_decode_kernel<float><<<static_cast<unsigned>(blocks), kDecThreads, 0, stream>>>(p);
+    const int64_t units = static_cast<int64_t>(p.N) * p.H;
+    if (units == 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                   cudaSuccess)
+        return cudaErrorUnknown;
+    const int64_t blocks = units < sms ? units : sms;  // persistent: one CTA of 1024 threads per SM
+    const unsigned grid = static_cast<unsigned>(blocks);
+    if (bf16) {
+        if (p.m == 1) gdn_decode_kernel<__nv_bfloat16, true><<<grid, kDecThreads, 0, stream>>>(p);
+        else gdn_decode_kernel<__nv_bfloat16, false><<<grid, kDecThreads, 0, stream>>>(p);
+    } else {
+        if (p.m == 1) gdn_decode_kernel<float, true><<<grid, kDecThreads, 0, stream>>>(p);
+        else gdn_decode_kernel<float, false><<<grid, kDecThreads, 0, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 

@@ -305,9 +305,8 @@ gdn_status gdn_decode_run(gdn_prefill_plan_t plan, const gdn_prefill_args* args,
         return GDN_ERR_INVALID_ARG;
     if (a.state_checkpoints || a.checkpoint_cu_starts) return GDN_ERR_INVALID_ARG;
     if (N == 0) return GDN_OK;
-    const size_t in_align = d.qkv_dtype == GDN_DTYPE_F32 ? 16 : 8;
-    if (!a.q || !a.k || !a.v || !a.output || !aligned(a.q, in_align) || !aligned(a.k, in_align) ||
-        !aligned(a.v, in_align) || !aligned(a.output, in_align))
+    if (!a.q || !a.k || !a.v || !a.output || !aligned(a.q, 16) || !aligned(a.k, 16) || !aligned(a.v, 16) ||
+        !aligned(a.output, 16))
         return GDN_ERR_INVALID_ARG;
     if (((f & GDN_FLAG_HAS_G) && !a.g) || ((f & GDN_FLAG_HAS_BETA) && !a.beta)) return GDN_ERR_INVALID_ARG;
     if ((f & GDN_FLAG_HAS_INITIAL_STATE) && (!a.initial_state || !aligned(a.initial_state, 16)))

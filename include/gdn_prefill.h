@@ -226,7 +226,7 @@ gdn_status gdn_prefill_run_static(gdn_prefill_plan_t plan, const gdn_prefill_arg
  *     [0, n_pool) skips that sequence and sets GDN_DEVICE_ERR_STATE_INDEX_RANGE
  *     in args.device_status when that pointer is given; duplicate indices are
  *     a caller error (their rows race).
- *   - q, k, v and output 8-byte aligned for bf16, 16-byte for fp32. */
+ *   - q, k, v and output 16-byte aligned. */
 #define GDN_DECODE_MAX_TOKENS_PER_SEQ 64
 gdn_status gdn_decode_run(gdn_prefill_plan_t plan, const gdn_prefill_args *args, int32_t tokens_per_seq,
                           void *stream);

@@ -143,7 +143,7 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     ({}, dict(num_seqs=4, total_tokens=5), 1, INVALID),                 # total != N * m
     ({}, dict(num_seqs=0, total_tokens=0), 1, OK),                      # nothing to do, nothing launched
     ({}, dict(num_seqs=4, total_tokens=8, q=None), 2, INVALID),
-    ({}, dict(num_seqs=4, total_tokens=4, q=0x7f0000000004), 1, INVALID),  # bf16 q not 8-byte aligned
+    ({}, dict(num_seqs=4, total_tokens=4, q=0x7f0000000008), 1, INVALID),  # q not 16-byte aligned
     (dict(checkpoint_every_n_tokens=64), dict(num_seqs=4, total_tokens=4), 1, UNSUPPORTED),
     ({}, dict(num_seqs=4, total_tokens=4, state_checkpoints=0x7f0000600000), 1, INVALID),
     (dict(flags=gdn.FLAGS["HAS_BETA"]), dict(num_seqs=4, total_tokens=4), 1, INVALID),  # beta flag without beta
