@@ -57,6 +57,8 @@ L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ["gated_deltanet_chunked_device_gb300/csrc/gdn_chunk_bf16.cu",
                   "gated_deltanet_chunked_device_gb300/csrc/sm103_ptx.cuh",
                   "gated_deltanet_chunked_device_gb300/csrc/gdn_internal.cuh"]
+DECODE_SOURCES = ["gated_deltanet_chunked_device_gb300/csrc/gdn_decode.cu",
+                  "gated_deltanet_chunked_device_gb300/csrc/gdn_internal.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -113,22 +115,22 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(sources=KERNEL_SOURCES):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
-    """dram read+write bytes per launch of the chunk kernel from the committed
-    ncu summary, if it was taken on the current kernel source."""
+def recorded_traffic(workload, sources=KERNEL_SOURCES):
+    """dram read+write bytes per launch of the workload's kernel from the
+    committed ncu summary, if it was taken on the current kernel source."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
         e = rec.get(workload)
-        if e and e.get("kernel_source_hash") == kernel_source_hash():
+        if e and e.get("kernel_source_hash") == kernel_source_hash(sources):
             return float(e["dram_bytes_per_launch"]), e.get("note")
     except Exception:  # noqa: BLE001
         pass
@@ -396,7 +398,8 @@ def run_decode_bench(args, w, inp, device):
                        "pool_rows": pool.shape[0], "qk_l2norm_in_kernel": w.l2norm_in_kernel,
                        "l2": f"inputs larger than L2 ({abytes / 2**20:.0f} MiB moved per step), no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": None, "kernel": "gdn_decode_kernel", "kernel_ms": ms,
+                         "traffic": recorded_traffic(w.name, DECODE_SOURCES)[0], "kernel": "gdn_decode_kernel",
+                         "kernel_ms": ms,
                          "algorithmic_bytes": abytes, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"},
             "gpu_launches": K}
     if clocks:
