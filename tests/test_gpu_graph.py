@@ -1,0 +1,91 @@
+"""CUDA-Graph capture and replay of the prefill and decode calls.
+
+gdn_prefill_run and gdn_decode_run only enqueue kernels: no allocation, no
+synchronisation and no host read of device memory, so a serving loop can
+capture them once and replay them with new data in the same buffers.  These
+tests capture each call into a graph, refill the inputs in place, replay, and
+require the replay to equal an eager call on the new inputs bit for bit (each
+(sequence, head) unit is computed the same way whichever CTA takes it)."""
+import pytest
+import torch
+
+import gated_deltanet_chunked_device_gb300 as gdn
+from gated_deltanet_chunked_device_gb300 import workloads as wl
+from gdn_testlib import to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gdn.build()
+
+
+def _refill(dst, src):
+    for key in ("q", "k", "v", "g", "beta", "state_indices"):
+        if dst.get(key) is not None:
+            dst[key].copy_(src[key])
+
+
+def test_prefill_graph_replay_matches_eager():
+    w = wl.custom(seq_lens=[300, 0, 77, 130], hq=4, hk=4, hv=8, initial_state="dense", l2norm_in_kernel=True,
+                  qk_prenorm=False, checkpoint_every=64)
+    a, b = (to_device(wl.generate(w, seed=s)) for s in (40, 41))
+    ck = torch.zeros(wl.num_checkpoints(a["seq_lens"], 64), a["H"], 128, 128, device="cuda")
+    out = torch.empty(a["T"], a["H"], 128, dtype=a["q"].dtype, device="cuda")
+    fin = torch.empty_like(a["initial_state"])
+
+    def call(d, stream_out, stream_fin, stream_ck):
+        return gdn.chunk_gated_delta_rule(
+            d["q"], d["k"], d["v"], g=d["g"], beta=d["beta"], scale=d["scale"], initial_state=d["initial_state"],
+            output_final_state=True, cu_seqlens=d["cu_seqlens"], use_qk_l2norm_in_kernel=True, output=stream_out,
+            output_state=stream_fin, state_checkpoints=stream_ck, checkpoint_cu_starts=d["checkpoint_cu_starts"],
+            checkpoint_every_n_tokens=64)
+
+    live = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in a.items()}
+    call(live, out, fin, ck)  # eager warm-up: plan, workspace, one-time kernel attributes
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(live, out, fin, ck)
+    _refill(live, b)
+    live["initial_state"].copy_(b["initial_state"])
+    g.replay()
+    torch.cuda.synchronize()
+    out_e, fin_e, ck_e = torch.empty_like(out), torch.empty_like(fin), torch.zeros_like(ck)
+    call(b, out_e, fin_e, ck_e)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_e)
+    assert torch.equal(fin, fin_e)
+    assert torch.equal(ck, ck_e)
+
+
+def test_decode_graph_replay_matches_eager():
+    w = wl.custom(seq_lens=[1] * 40, hq=8, hk=8, hv=16, initial_state="pool", n_pool=64, l2norm_in_kernel=True,
+                  qk_prenorm=False)
+    a, b = (to_device(wl.generate(w, seed=s)) for s in (42, 43))
+    pool = a["initial_state"].clone()
+    out = torch.empty(a["T"], a["H"], 128, dtype=a["q"].dtype, device="cuda")
+    live = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in a.items()}
+
+    def call(d, pool_, out_):
+        return gdn.gated_delta_rule_decode(d["q"], d["k"], d["v"], g=d["g"], beta=d["beta"], scale=d["scale"],
+                                           initial_state=pool_, state_indices=d["state_indices"],
+                                           use_qk_l2norm_in_kernel=True, output=out_)
+
+    call(live, pool, out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(live, pool, out)
+    _refill(live, b)
+    pool.copy_(b["initial_state"])
+    g.replay()
+    torch.cuda.synchronize()
+    pool_e, out_e = b["initial_state"].clone(), torch.empty_like(out)
+    call(b, pool_e, out_e)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_e)
+    assert torch.equal(pool, pool_e)
