@@ -917,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // W^T of chunk m (unit-local index cm) -> shared memory, the MN-major B operand of -S W^T.  The
             // reader of the previous copy, Delta of chunk m-1, completed before this warpgroup's Delta epilogue
-            // of that chunk.
+            // of that chunk.  The caller publishes it (proxy fence, barrier, WB_FULL).
             auto copy_w = [&](uint32_t m, int32_t cm) -> bool {
                 if (!wait_bar(cx, B_WU_FULL, m & 1)) return false;
                 tc_fence_after();
@@ -935,10 +935,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                (static_cast<size_t>(info.flat0 + cm) * H + info.h) * kChunk, tm_lane + kTmW + i0,
                                tm_lane + kTmDelta + (m & 1) * 64 + i0, v, i0, st,
                                reinterpret_cast<const float*>(sm + kGbuf) + (m % 3) * kGFloats + kGG);
-                fence_proxy_async_smem();
-                tc_fence_before();
-                named_bar_sync(kBarState, kStateThreads);
-                if (st == 0) mbar_arrive(cx.bars + B_WB_FULL + (m & 1));
                 return true;
             };
             for (int32_t c = 0; c < info.nC && ok; ++c, ++n) {
@@ -951,7 +947,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float* gb = reinterpret_cast<const float*>(sm + kGbuf) + gs * kGFloats;
                 const uint32_t dbuf = tm_lane + kTmDelta + s * 64;
                 // W of the unit's first chunk (the later ones are copied right after the previous chunk's state)
-                if (c == 0 && !(ok = copy_w(n, c))) break;
+                if (c == 0) {
+                    if (!(ok = copy_w(n, c))) break;
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    named_bar_sync(kBarState, kStateThreads);
+                    if (st == 0) mbar_arrive(cx.bars + B_WB_FULL + s);
+                }
                 // ---- Delta epilogue: this thread's 32 columns j in [32 hh, 32 hh + 32) go back into TMEM as
                 //      16 packed bf16 Delta words followed by 16 packed decayed words (A operands of O2 and S)
                 if (!(ok = wait_bar(cx, B_DELTA_FULL + s, ph))) break;
@@ -1015,13 +1017,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (!last) tmem_wait_st();
                 }
+                // W of the next chunk, published with the bf16 state under one barrier: the two are all the next
+                // Delta product waits for, while this chunk's prescale and output epilogue run behind it.
+                if (!last) {
+                    if (!(ok = copy_w(n + 1, c + 1))) break;
+                    fence_proxy_async_smem();
+                }
                 if (st == 0) bulk_wait_group_read0();  // the previous chunk's output store has read outT
                 tc_fence_before();
                 named_bar_sync(kBarState, kStateThreads);
-                if (st == 0 && !last) mbar_arrive(cx.bars + B_SB_FULL + ((n + 1) & 1));
-                // W of the next chunk now: with the bf16 state just published, it is all the next Delta product
-                // waits for, while this chunk's prescale and output epilogue run behind it.
-                if (!last && !(ok = copy_w(n + 1, c + 1))) break;
+                if (st == 0 && !last) {
+                    mbar_arrive(cx.bars + B_SB_FULL + ((n + 1) & 1));
+                    mbar_arrive(cx.bars + B_WB_FULL + ((n + 1) & 1));
+                }
                 if (!last) {
                     // pass 2: gamma_63 of the next chunk into the accumulator, before that chunk's S product
                     const uint32_t gn = (n + 1) % 3;
