@@ -20,6 +20,11 @@
 //   output ("GDN与线性注意力GPU并行实现" section 3.3: O_init = Q S plus a
 //   triangular-masked product):
 //     O^T = scale (S Q'^T + Delta~^T P^T) diag(m),  Q' = diag(gamma) Q     tcgen05, one accumulator
+//   A chunk whose G stays within [-8, 8] keeps Q as stored and folds gamma
+//   into the other factors instead: P' = diag(1/gamma) P and m' = gamma m,
+//   O^T = scale (S Q^T + Delta~^T P'^T) diag(m') -- the same product without
+//   the pass that rescales Q in shared memory; the bound keeps the
+//   accumulator's terms within e^8 of one another.
 //
 // The L2 norm of q and k ("FlashInfer GDN Prefill 完全指南", API table) enters
 // only through the factors n and m, in fp32: the same values as normalising
@@ -35,10 +40,10 @@
 //   warp 0       TMA: K, Q tiles (3 stages) and V tile; unit scheduler
 //   warp 1       tcgen05 issue for the intra-chunk products (D1, W, U)
 //   warp 2       tcgen05 issue for the state chain (Delta, S Q^T, Delta P^T, S)
-//   warp 3       TMEM allocation; gates: G, gamma, beta and the per-row /
-//                per-column factor vectors
+//   warp 3       TMEM allocation; gates: G, gamma, beta, the per-row /
+//                per-column factor vectors and the q norms
 //   warps 4-11   two intra warpgroups (TMEM lane quarter x column half):
-//                A and P, Q' = diag(gamma) Q with the q norms, T in place
+//                A and P, Q' = diag(gamma) Q where needed, T in place
 //                with T' and T'', one chunk ahead of the state warpgroups
 //   warps 12-19  two state warpgroups (lane quarter x column half): W to
 //                shared memory, Delta epilogue, state epilogue (next bf16 S
@@ -84,14 +89,16 @@ constexpr int kLd = 68;               // fp32 row stride of A and T (bank-confli
 //   G      running sum of log alpha            gamma  e^G
 //   beta   beta (0 on padded rows)             rn     1/|k_j| (1 without the L2 norm; written by the
 //                                                      intra warps that hold the K K^T diagonal)
-//   rm     1/|q_i| (1 without the L2 norm; written by the intra warps from the Q pass)
+//   rm     output row factor: 1/|q_i| (1 without the L2 norm), times gamma_i when Q is kept as stored
 //   cw     beta_j gamma_j (T' columns, times rn_j^2)
-//   dec    e^{G_63 - G_j} (decayed Delta)      (448..511 unused)
+//   dec    e^{G_63 - G_j} (decayed Delta)      rp     P row factor: 1/gamma_i when Q is kept, else 1
 //   ra     beta_i (A rows, times rn_i^2)       colf   e^{G_16b - G_j}, b = j / 16
 //   rowf   [4][64] e^{G_i - G_16b} (i >= 16 b, else 0)
 //   safe   1 when the chunk's G range is small enough for e^{G_i - G_j} = rowf * colf
-constexpr int kGG = 0, kGGam = 64, kGBeta = 128, kGRn = 192, kGRm = 256, kGCw = 320, kGDec = 384,
-              kGRa = 512, kGColf = 576, kGRowf = 640, kGSafe = 896, kGFloats = 912;
+//   keepq  1 when every G_i of the chunk lies in [-8, 8]: Q stays as stored (no Q' pass)
+constexpr int kGG = 0, kGGam = 64, kGBeta = 128, kGRn = 192, kGRm = 256, kGCw = 320, kGDec = 384, kGRp = 448,
+              kGRa = 512, kGColf = 576, kGRowf = 640, kGSafe = 896, kGKeepQ = 897, kGFloats = 912;
+constexpr float kKeepQRange = 8.f;
 static_assert(kGbuf >= kMisc + 64 && kGbuf + 3 * kGFloats * 4 <= kOutT && kOutT + 16384 == kSmemBytes,
               "shared memory map overlaps");
 static_assert(kXs + 4 * (2 * 16 * 24 + 32 * 40) <= kBars && kMisc + 64 <= kOutT, "scratch / barrier block overlap");
@@ -370,8 +377,8 @@ __device__ __forceinline__ GatePrefetch load_gates(const ChunkParams& p, int64_t
 }
 
 // The vectors of one chunk (see kG*) that need no norm; under the L2 norm the
-// intra warps add rn and rm.  Rows at or past Lc are padding (alpha = 1,
-// beta = 0).
+// intra warps add rn and q_norms adds rm.  Rows at or past Lc are padding
+// (alpha = 1, beta = 0).
 __device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, bool l2norm, int lane) {
     const int r0 = 2 * lane;
     const float la0 = __logf(g.a0), la1 = __logf(g.a1);
@@ -386,6 +393,13 @@ __device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, 
     float Gb[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) Gb[b] = __shfl_sync(0xffffffffu, G0, 8 * b);  // G at row 16 b
+    float gmax = fmaxf(G0, G1), gmin = fminf(G0, G1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+        gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
+    }
+    const bool keepq = gmax <= kKeepQRange && gmin >= -kKeepQRange;
     const float Gv[2] = {G0, G1}, bv[2] = {g.b0, g.b1};
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -397,19 +411,39 @@ __device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, 
         gb[kGRn + r] = 1.f;
         gb[kGCw + r] = bv[k] * e;
         gb[kGDec + r] = __expf(G63 - Gv[k]);
-        if (!l2norm) gb[kGRm + r] = 1.f;
+        if (!l2norm) gb[kGRm + r] = keepq ? e : 1.f;
+        gb[kGRp + r] = keepq ? __expf(-Gv[k]) : 1.f;
         gb[kGRa + r] = bv[k];
         gb[kGColf + r] = __expf(Gb[r >> 4] - Gv[k]);
 #pragma unroll
         for (int b = 0; b < 4; ++b) gb[kGRowf + b * 64 + r] = (r >= 16 * b) ? __expf(Gv[k] - Gb[b]) : 0.f;
     }
-    float gmax = fmaxf(G0, G1), gmin = fminf(G0, G1);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
-        gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
+    if (lane == 0) {
+        gb[kGSafe] = (gmax - gmin < 60.f) ? 1.f : 0.f;
+        gb[kGKeepQ] = keepq ? 1.f : 0.f;
     }
-    if (lane == 0) gb[kGSafe] = (gmax - gmin < 60.f) ? 1.f : 0.f;
+}
+
+// rm of the chunk's rows lane and lane + 32 under the L2 norm: 1/|q_i| from
+// the Q tile as stored (K-major, 128B-swizzled halves), times gamma_i when the
+// chunk keeps Q; 0 on padded rows.  Runs after compute_gates (reads gamma and
+// keepq back from the same warp's stores).
+__device__ __forceinline__ void q_norms(const uint8_t* q0, float* gb, int32_t Lc, int lane) {
+    const bool keepq = gb[kGKeepQ] != 0.f;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+        const int qr = lane + 32 * h;
+        float ss = 0.f;
+#pragma unroll 4
+        for (int cch = 0; cch < 16; ++cch) {
+            float f[8];
+            bf16x8_to_float(*reinterpret_cast<const uint4*>(q0 + (cch >> 3) * 16384 + sw128_offset(qr, cch & 7)), f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
+        }
+        const float rm = qr < Lc ? rsqrtf(ss + 1e-6f) : 0.f;
+        gb[kGRm + qr] = keepq ? rm * gb[kGGam + qr] : rm;
+    }
 }
 
 __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]) {
@@ -727,6 +761,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float* gbw = reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats;
                     compute_gates(cur, gbw, p.l2norm != 0, lane);
                     __syncwarp();
+                    if (p.l2norm) {
+                        // the q norms from the chunk's Q tile (its stage is released only after this chunk's
+                        // products, which wait for these gates)
+                        if (!(ok = wait_bar(cx, B_KQ_FULL + n % kKQStages, (n / kKQStages) & 1))) break;
+                        const int64_t rem = info.L - static_cast<int64_t>(c) * kChunk;
+                        q_norms(sm + kKQ + (n % kKQStages) * kKQStage + 8192, gbw,
+                                rem < kChunk ? static_cast<int32_t>(rem) : kChunk, lane);
+                        __syncwarp();
+                    }
                     if (lane == 0) mbar_arrive(cx.bars + B_GATES_FULL + gs);
                 }
             }
@@ -772,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool arow = r < 64;
                     const int i = r & 63;
                     const bool safe = gb[kGSafe] != 0.f;
-                    float rbase = arow ? gb[kGRa + i] : 1.f;
+                    float rbase = gb[(arow ? kGRa : kGRp) + i];
                     if (p.l2norm && arow) {
                         // |k_i|^2 is the diagonal of K K^T: lane l of this warp finds it in column 32 wq + l
                         uint32_t rr[32];
@@ -823,12 +866,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                // Q' = diag(gamma) Q in place, for the S Q'^T product (D1 has read Q already); under the L2 norm
-                // the same pass sums |q_i|^2.  Four threads per row, 32 values each.
-                {
+                // Q' = diag(gamma) Q in place, for the S Q'^T product (D1 has read Q already), unless the chunk
+                // keeps Q as stored.  Four threads per row, 32 values each.
+                if (gb[kGKeepQ] == 0.f) {
                     const int qr = it >> 2, qq = it & 3;
                     const float gam = gb[kGGam + qr];
-                    float ss = 0.f;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int cch = 4 * qq + k;  // 16-byte column of the 256-byte row
@@ -836,16 +878,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float f[8];
                         bf16x8_to_float(*reinterpret_cast<const uint4*>(half + sw128_offset(qr, cch & 7)), f);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            ss += f[j] * f[j];
-                            f[j] *= gam;
-                        }
+                        for (int j = 0; j < 8; ++j) f[j] *= gam;
                         st_chunk_bf16(half, qr, cch & 7, f);
-                    }
-                    if (p.l2norm) {
-                        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-                        if (qq == 0) gb[kGRm + qr] = qr < Lc ? rsqrtf(ss + 1e-6f) : 0.f;
                     }
                 }
                 // zero the padded rows of the K and V tiles (they hold the next

@@ -228,6 +228,17 @@ def test_steep_gates_take_the_pairwise_decay_path():
     check_against_oracle(inp, run_gpu(to_device(inp)))
 
 
+@pytest.mark.parametrize("l2norm", [True, False])
+def test_moderate_gates_scale_q_in_place(l2norm):
+    # alpha ~ U(0.75, 0.95): log alpha ~ -0.05 .. -0.29 per token, so G leaves [-8, 8] inside most full chunks
+    # (those rescale Q in shared memory) while short tails stay inside it (those keep Q and fold gamma into P
+    # and the output factor); the gate range stays small enough for the row x column factorisation
+    w = wl.custom(seq_lens=[300, 64, 5, 130, 20], hq=2, hk=2, hv=4, alpha="u(0.75,0.95)", l2norm_in_kernel=l2norm,
+                  qk_prenorm=not l2norm, initial_state="dense", checkpoint_every=64)
+    inp = wl.generate(w, seed=17)
+    check_against_oracle(inp, run_gpu(to_device(inp)))
+
+
 def test_more_sequences_than_the_on_chip_sort():
     # 9000 sequences (above the 8192 the prepare kernel sorts on chip; the rest keep their order), most of
     # them a few tokens long, a few of them several chunks long
