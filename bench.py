@@ -506,6 +506,14 @@ def main():
     bits = gdn.read_status(plan, ws)
     if bits:
         raise RuntimeError(f"device status bits {bits:#x} after the timed steps")
+    # the same steps back to back without the L2 flush (inputs partly L2-resident), outside the timed region
+    Ku = min(K, 50)
+    evu = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(Ku)]
+    with torch.cuda.stream(stream):
+        for i in range(Ku):
+            step(*evu[i])
+    torch.cuda.synchronize(device)
+    unflushed_ms = sum(evu[i][0].elapsed_time(evu[i][2]) for i in range(Ku)) / Ku
 
     # ---- end to end through the public API, host buffers
     e2e = None
@@ -574,12 +582,14 @@ def main():
         "tflops": {"dense_tile_count": tflops_dense, "triangular_aware": tflops_tri,
                    "pct_of_bf16_peak": 100 * tflops_dense / bf16, "peak_tflops": bf16, "peak_source": src},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": traffic, "kernel": "gdn_chunk_bf16_kernel", "kernel_ms": chunk_avg_ms,
+                     "traffic": traffic, "kernel": "gdn_chunk_kernel<__nv_bfloat16>", "kernel_ms": chunk_avg_ms,
                      "algorithmic_bytes": abytes, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
                      if src == "measured" else "fallback 6800 GB/s",
                      "step_frac_of_roofline_time": roof_time / (ms_per_step / 1e3)},
         "gpu_launches": 2 * K,
         "wall_s_timed_region": wall,
+        "step_ms_stats": {"mean": sum(step_ms) / K, "median": statistics.median(step_ms), "min": min(step_ms),
+                          "max": max(step_ms), "unflushed_mean": unflushed_ms, "unflushed_steps": Ku},
     }
     if tnote:
         line["roofline"]["traffic_note"] = tnote

@@ -43,7 +43,8 @@ __all__ = [
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_CUDA",
           4: "GDN_ERR_DEVICE_INPUT", 5: "GDN_ERR_DEVICE_TIMEOUT"}
-DTYPE_F32, DTYPE_BF16 = 0, 1
+DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2
+_QKV_DTYPES = {torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16, torch.float32: DTYPE_F32}
 FLAGS = {
     "HAS_G": 1 << 0, "HAS_BETA": 1 << 1, "HAS_SCALE": 1 << 2, "QK_L2NORM": 1 << 3, "HAS_INITIAL_STATE": 1 << 4,
     "OUTPUT_FINAL_STATE": 1 << 5, "HAS_STATE_INDICES": 1 << 6, "CU_SEQLENS_I64": 1 << 7,
@@ -283,11 +284,8 @@ def chunk_gated_delta_rule(q, k, v, g=None, beta=None, scale=None, initial_state
     hk, hv = k.shape[1], v.shape[1]
     if D != HEAD_SIZE or k.shape[2] != D or v.shape[2] != D or k.shape[0] != T or v.shape[0] != T:
         raise ValueError("q, k, v must share total_tokens and have head_size 128")
-    if q.dtype == torch.bfloat16:
-        qkv_dtype = DTYPE_BF16
-    elif q.dtype == torch.float32:
-        qkv_dtype = DTYPE_F32
-    else:
+    qkv_dtype = _QKV_DTYPES.get(q.dtype)
+    if qkv_dtype is None:
         raise ValueError(f"unsupported q/k/v dtype {q.dtype}")
     for name, t in (("q", q), ("k", k), ("v", v)):
         _check_dev(name, t, device, q.dtype)
@@ -392,7 +390,7 @@ def gated_delta_rule_decode(q, k, v, g=None, beta=None, scale=None, initial_stat
     if D != HEAD_SIZE or k.shape[2] != D or v.shape[2] != D or k.shape[0] != T or v.shape[0] != T or m < 1 or T % m:
         raise ValueError("q, k, v must share N * tokens_per_seq rows and have head_size 128")
     N = T // m
-    qkv_dtype = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32}.get(q.dtype)
+    qkv_dtype = _QKV_DTYPES.get(q.dtype)
     if qkv_dtype is None:
         raise ValueError(f"unsupported q/k/v dtype {q.dtype}")
     for name, t in (("q", q), ("k", k), ("v", v)):

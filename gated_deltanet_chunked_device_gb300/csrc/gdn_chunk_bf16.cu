@@ -1,6 +1,10 @@
-// gdn_chunk_bf16.cu -- chunked Gated DeltaNet prefill, bf16 q/k/v, fp32 state,
-// on sm_103a: tcgen05 tensor cores with TMEM accumulators, TMA-fed operands,
-// warp-specialised and pipelined across chunks.
+// gdn_chunk_bf16.cu -- chunked Gated DeltaNet prefill, bf16 (or fp16) q/k/v,
+// fp32 state, on sm_103a: tcgen05 tensor cores with TMEM accumulators,
+// TMA-fed operands, warp-specialised and pipelined across chunks.  The two
+// input types share one kernel template (gdn_chunk_kernel<__nv_bfloat16> and
+// gdn_chunk_kernel<__half>): every 16-bit operand the kernel writes itself (P, T',
+// T'', W^T, S, Delta) takes the input type, because A and B of one tcgen05
+// kind::f16 product have the same type.
 //
 // Per chunk of C = 64 tokens (G_r = sum_{m<=r} log alpha_m inside the chunk,
 // gamma_r = e^{G_r}; n_j, m_i = 1/|k_j|, 1/|q_i| when the L2 norm is on, else
@@ -53,6 +57,9 @@
 // shared abort flag that every other wait polls, drains the CTA's in-flight
 // copies and tensor-core work, frees TMEM and returns.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "gdn_internal.cuh"
 #include "sm103_ptx.cuh"
@@ -98,7 +105,7 @@ constexpr int kLd = 68;               // fp32 row stride of A and T (bank-confli
 //   keepq  1 when every G_i of the chunk lies in [-8, 8]: Q stays as stored (no Q' pass)
 constexpr int kGG = 0, kGGam = 64, kGBeta = 128, kGRn = 192, kGRm = 256, kGCw = 320, kGDec = 384, kGRp = 448,
               kGRa = 512, kGColf = 576, kGRowf = 640, kGSafe = 896, kGKeepQ = 897, kGFloats = 912;
-constexpr float kKeepQRange = 8.f;
+constexpr float kKeepQRange = 8.f;  // bf16 only: fp16 would overflow on e^8 (q.k) with raw q and k
 static_assert(kGbuf >= kMisc + 64 && kGbuf + 3 * kGFloats * 4 <= kOutT && kOutT + 16384 == kSmemBytes,
               "shared memory map overlaps");
 static_assert(kXs + 4 * (2 * 16 * 24 + 32 * 40) <= kBars && kMisc + 64 <= kOutT, "scratch / barrier block overlap");
@@ -118,11 +125,35 @@ enum {
 constexpr uint32_t kTmS = 0, kTmDelta = 128, kTmW = 256, kTmD1 = 320, kTmO = 384, kTmSbf = 448;
 constexpr uint32_t kTmCols = 512;
 
-constexpr uint32_t kIdescD1 = idesc_bf16_f32(128, 64);
-constexpr uint32_t kIdescWU = idesc_bf16_f32(128, 64, true, false);
-constexpr uint32_t kIdescDelta = idesc_bf16_f32(128, 64, false, true, true);
-constexpr uint32_t kIdescO = idesc_bf16_f32(128, 64);
-constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, true);
+template <bool kF16> constexpr uint32_t kIdescD1 = idesc_16bit_f32(128, 64, false, false, false, kF16);
+template <bool kF16> constexpr uint32_t kIdescWU = idesc_16bit_f32(128, 64, true, false, false, kF16);
+template <bool kF16> constexpr uint32_t kIdescDelta = idesc_16bit_f32(128, 64, false, true, true, kF16);
+template <bool kF16> constexpr uint32_t kIdescO = idesc_16bit_f32(128, 64, false, false, false, kF16);
+template <bool kF16> constexpr uint32_t kIdescS = idesc_16bit_f32(128, 128, false, true, false, kF16);
+
+// The 16-bit element: bf16, or fp16 for fp16 inputs.
+template <bool kF16>
+struct Elem16;
+template <>
+struct Elem16<false> {
+    using T = __nv_bfloat16;
+    static __device__ __forceinline__ T from(float x) { return __float2bfloat16_rn(x); }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16x2(lo, hi); }
+    static __device__ __forceinline__ float2 unpack(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+};
+template <>
+struct Elem16<true> {
+    using T = __half;
+    static __device__ __forceinline__ T from(float x) { return __float2half_rn(x); }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_f16x2(lo, hi); }
+    static __device__ __forceinline__ float2 unpack(uint32_t w) {
+        __half2 h;
+        memcpy(&h, &w, 4);
+        return __half22float2(h);
+    }
+};
 
 constexpr long long kWaitCycles = 2000000000LL;  // about one second
 
@@ -170,21 +201,24 @@ __device__ __forceinline__ void drain_bar(const Ctx& cx, int b, uint32_t parity)
     if (!mbar_wait(cx.bars + b, parity, kWaitCycles)) atomicOr(cx.status, static_cast<int32_t>(GDN_DEVICE_ERR_TIMEOUT));
 }
 
-__device__ __forceinline__ void st_chunk_bf16(uint8_t* tile, uint32_t row, uint32_t chunk, const float* x) {
+template <bool kF16>
+__device__ __forceinline__ void st_chunk16(uint8_t* tile, uint32_t row, uint32_t chunk, const float* x) {
     uint4 v;
-    v.x = pack_bf16x2(x[0], x[1]);
-    v.y = pack_bf16x2(x[2], x[3]);
-    v.z = pack_bf16x2(x[4], x[5]);
-    v.w = pack_bf16x2(x[6], x[7]);
+    v.x = Elem16<kF16>::pack(x[0], x[1]);
+    v.y = Elem16<kF16>::pack(x[2], x[3]);
+    v.z = Elem16<kF16>::pack(x[4], x[5]);
+    v.w = Elem16<kF16>::pack(x[6], x[7]);
     *reinterpret_cast<uint4*>(tile + sw128_offset(row, chunk)) = v;
 }
 
-__device__ __forceinline__ void bf16x8_to_float(const uint4& v, float* f) {
+template <bool kF16>
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        f[2 * j] = __uint_as_float(w[j] << 16);
-        f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+        const float2 t = Elem16<kF16>::unpack(w[j]);
+        f[2 * j] = t.x;
+        f[2 * j + 1] = t.y;
     }
 }
 
@@ -236,13 +270,16 @@ __device__ __forceinline__ void store_tile_16x8(float* C, int ldc, const float (
     *reinterpret_cast<float2*>(C + (g + 8) * ldc + 2 * t) = make_float2(sign * d[2], sign * d[3]);
 }
 
-// Two adjacent bf16 values (row i, columns j, j + 1; j even) of a swizzled K-major [64][64] tile.
-__device__ __forceinline__ void st_pair_bf16(uint8_t* tile, int i, int j, float x0, float x1) {
-    *reinterpret_cast<uint32_t*>(tile + i * 128 + (((j >> 3) ^ (i & 7)) << 4) + (j & 7) * 2) = pack_bf16x2(x0, x1);
+// Two adjacent 16-bit values (row i, columns j, j + 1; j even) of a swizzled K-major [64][64] tile.
+template <bool kF16>
+__device__ __forceinline__ void st_pair16(uint8_t* tile, int i, int j, float x0, float x1) {
+    *reinterpret_cast<uint32_t*>(tile + i * 128 + (((j >> 3) ^ (i & 7)) << 4) + (j & 7) * 2) =
+        Elem16<kF16>::pack(x0, x1);
 }
 
 constexpr int kLdX1 = 24, kLdX2 = 40;  // scratch strides: conflict-free B-fragment reads
 
+template <bool kF16>
 __device__ __forceinline__ void tri_inverse_64(float* __restrict__ A, uint8_t* __restrict__ tp,
                                                uint8_t* __restrict__ tpp, const float* __restrict__ cw,
                                                const float* __restrict__ beta, const float* __restrict__ rn,
@@ -330,8 +367,8 @@ __device__ __forceinline__ void tri_inverse_64(float* __restrict__ A, uint8_t* _
             x[q] = tn * nv[q] * cv[q];
             y[q] = tn * ev[q];
         }
-        st_chunk_bf16(tp, i, j0 >> 3, x);
-        st_chunk_bf16(tpp, i, j0 >> 3, y);
+        st_chunk16<kF16>(tp, i, j0 >> 3, x);
+        st_chunk16<kF16>(tpp, i, j0 >> 3, y);
     }
     named_bar_sync(kBarIntra, kIntraThreads);
     // ---- T_21 = -T_22 X, written as T' and T'' tiles from the fragments
@@ -344,10 +381,10 @@ __device__ __forceinline__ void tri_inverse_64(float* __restrict__ A, uint8_t* _
         const int i0 = 32 + mt + g, i1 = i0 + 8;
         const float n0 = rn[j], n1 = rn[j + 1];
         const float be0 = beta[j] * n0, be1 = beta[j + 1] * n1, cw0 = cw[j] * n0 * n0, cw1 = cw[j + 1] * n1 * n1;
-        st_pair_bf16(tp, i0, j, -e[0] * cw0, -e[1] * cw1);
-        st_pair_bf16(tp, i1, j, -e[2] * cw0, -e[3] * cw1);
-        st_pair_bf16(tpp, i0, j, -e[0] * be0, -e[1] * be1);
-        st_pair_bf16(tpp, i1, j, -e[2] * be0, -e[3] * be1);
+        st_pair16<kF16>(tp, i0, j, -e[0] * cw0, -e[1] * cw1);
+        st_pair16<kF16>(tp, i1, j, -e[2] * cw0, -e[3] * cw1);
+        st_pair16<kF16>(tpp, i0, j, -e[0] * be0, -e[1] * be1);
+        st_pair16<kF16>(tpp, i1, j, -e[2] * be0, -e[3] * be1);
     }
 }
 
@@ -379,7 +416,8 @@ __device__ __forceinline__ GatePrefetch load_gates(const ChunkParams& p, int64_t
 // The vectors of one chunk (see kG*) that need no norm; under the L2 norm the
 // intra warps add rn and q_norms adds rm.  Rows at or past Lc are padding
 // (alpha = 1, beta = 0).
-__device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, bool l2norm, int lane) {
+__device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, bool l2norm, float keep_range,
+                                              int lane) {
     const int r0 = 2 * lane;
     const float la0 = __logf(g.a0), la1 = __logf(g.a1);
     float incl = la0 + la1;
@@ -399,7 +437,7 @@ __device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, 
         gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
         gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
     }
-    const bool keepq = gmax <= kKeepQRange && gmin >= -kKeepQRange;
+    const bool keepq = gmax <= keep_range && gmin >= -keep_range;
     const float Gv[2] = {G0, G1}, bv[2] = {g.b0, g.b1};
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -428,6 +466,7 @@ __device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, 
 // the Q tile as stored (K-major, 128B-swizzled halves), times gamma_i when the
 // chunk keeps Q; 0 on padded rows.  Runs after compute_gates (reads gamma and
 // keepq back from the same warp's stores).
+template <bool kF16>
 __device__ __forceinline__ void q_norms(const uint8_t* q0, float* gb, int32_t Lc, int lane) {
     const bool keepq = gb[kGKeepQ] != 0.f;
 #pragma unroll 1
@@ -437,7 +476,7 @@ __device__ __forceinline__ void q_norms(const uint8_t* q0, float* gb, int32_t Lc
 #pragma unroll 4
         for (int cch = 0; cch < 16; ++cch) {
             float f[8];
-            bf16x8_to_float(*reinterpret_cast<const uint4*>(q0 + (cch >> 3) * 16384 + sw128_offset(qr, cch & 7)), f);
+            unpack8<kF16>(*reinterpret_cast<const uint4*>(q0 + (cch >> 3) * 16384 + sw128_offset(qr, cch & 7)), f);
 #pragma unroll
             for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
         }
@@ -485,6 +524,7 @@ __device__ __noinline__ void dump_intra(float* intra_w, float* intra_u, float* i
 // Start of a unit's state: S0 (this thread's row v, 64 columns) as packed bf16
 // pairs into the A operand columns, and gamma_63 S0 into the fp32 accumulator
 // (S0 null: zeros).  Once per unit, so out of line.
+template <bool kF16>
 __device__ __noinline__ void load_initial_state(const float* s0, uint32_t tm_sbf, uint32_t tm_s, float g63) {
     for (int c0 = 0; c0 < 64; c0 += 32) {
         float x[32];
@@ -495,7 +535,7 @@ __device__ __noinline__ void load_initial_state(const float* s0, uint32_t tm_sbf
         }
         uint32_t pk[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(x[2 * q], x[2 * q + 1]);
+        for (int q = 0; q < 16; ++q) pk[q] = Elem16<kF16>::pack(x[2 * q], x[2 * q + 1]);
         tmem_st16(tm_sbf + c0 / 2, pk);
         uint32_t r[32];
 #pragma unroll
@@ -505,10 +545,13 @@ __device__ __noinline__ void load_initial_state(const float* s0, uint32_t tm_sbf
     tmem_wait_st();
 }
 
+// E: the input element type, __nv_bfloat16 or __half.
+template <typename E16>
 __global__ void __launch_bounds__(kThreads, 1)
-    gdn_chunk_bf16_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
-                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                          const __grid_constant__ CUtensorMap tm_o) {
+    gdn_chunk_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_o) {
+    constexpr bool kF16 = std::is_same<E16, __half>::value;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -640,8 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     #pragma unroll 1
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_bf16_ss(tmem + kTmD1, desc_kmajor_sw128(kq + off), desc_kmajor_sw128(kq + off), kIdescD1,
-                                    ks > 0);
+                        mma_bf16_ss(tmem + kTmD1, desc_kmajor_sw128(kq + off), desc_kmajor_sw128(kq + off),
+                                    kIdescD1<kF16>, ks > 0);
                     }
                     mma_commit(cx.bars + B_D1_FULL);
                     return true;
@@ -660,9 +703,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     #pragma unroll 1
                     for (int ks = 0; ks < 4; ++ks) {
                         mma_bf16_ss(tmem + kTmW, desc_mnmajor_sw128(kq + ks * 2048, 16384),
-                                    desc_kmajor_sw128(tp + ks * 32), kIdescWU, ks > 0);
+                                    desc_kmajor_sw128(tp + ks * 32), kIdescWU<kF16>, ks > 0);
                         mma_bf16_ss(dbuf, desc_mnmajor_sw128(vv + ks * 2048, 8192), desc_kmajor_sw128(tpp + ks * 32),
-                                    kIdescWU, ks > 0);
+                                    kIdescWU<kF16>, ks > 0);
                     }
                     mma_commit(cx.bars + B_WU_FULL);
                     mma_commit(cx.bars + B_V_EMPTY);
@@ -708,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     #pragma unroll 1
                         for (int ks = 0; ks < 8; ++ks)  // A = S (bf16 pairs in TMEM), k = 16 ks .. 16 ks + 15
                             mma_bf16_ts(dbuf, tmem + kTmSbf + ks * 8, desc_mnmajor_sw128(wb + ks * 2048, 8192),
-                                        kIdescDelta, 1);
+                                        kIdescDelta<kF16>, 1);
                         mma_commit(cx.bars + B_DELTA_FULL + s);
                         if (n >= 1 && !(ok = wait_bar(cx, B_O_EMPTY + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
                         tc_fence_after();
@@ -716,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int ks = 0; ks < 8; ++ks) {  // O = S Q'^T, Q' = diag(gamma) Q
                             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
                             mma_bf16_ts(tmem + kTmO, tmem + kTmSbf + ks * 8, desc_kmajor_sw128(kq + 8192 + off),
-                                        kIdescO, ks > 0);
+                                        kIdescO<kF16>, ks > 0);
                         }
                         if (!(ok = wait_bar(cx, B_DD_FULL + s, ph))) break;
                         tc_fence_after();
@@ -724,8 +767,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     #pragma unroll 1
                         for (int ks = 0; ks < 4; ++ks) {
                             const uint32_t acol = dbuf + 32 * (ks >> 1) + 8 * (ks & 1);  // packed j = 16 ks .. 16 ks + 15
-                            mma_bf16_ts(tmem + kTmO, acol, desc_kmajor_sw128(pb + ks * 32), kIdescO, 1);  // O += Delta^T P^T
-                            mma_bf16_ts(tmem + kTmS, acol + 16, desc_mnmajor_sw128(kq + ks * 2048, 16384), kIdescS, 1);
+                            // O += Delta^T P^T, then S += (decayed Delta)^T K
+                            mma_bf16_ts(tmem + kTmO, acol, desc_kmajor_sw128(pb + ks * 32), kIdescO<kF16>, 1);
+                            mma_bf16_ts(tmem + kTmS, acol + 16, desc_mnmajor_sw128(kq + ks * 2048, 16384),
+                                        kIdescS<kF16>, 1);
                         }
                         mma_commit(cx.bars + B_S_FULL + s);
                         mma_commit(cx.bars + B_KQ_EMPTY + st);
@@ -759,14 +804,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (n >= 3 && !(ok = wait_bar(cx, B_GATES_EMPTY + gs, ((n - 3) / 3) & 1))) break;
                     float* gbw = reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats;
-                    compute_gates(cur, gbw, p.l2norm != 0, lane);
+                    compute_gates(cur, gbw, p.l2norm != 0, kF16 ? 0.f : kKeepQRange, lane);
                     __syncwarp();
                     if (p.l2norm) {
                         // the q norms from the chunk's Q tile (its stage is released only after this chunk's
                         // products, which wait for these gates)
                         if (!(ok = wait_bar(cx, B_KQ_FULL + n % kKQStages, (n / kKQStages) & 1))) break;
                         const int64_t rem = info.L - static_cast<int64_t>(c) * kChunk;
-                        q_norms(sm + kKQ + (n % kKQStages) * kKQStage + 8192, gbw,
+                        q_norms<kF16>(sm + kKQ + (n % kKQStages) * kKQStage + 8192, gbw,
                                 rem < kChunk ? static_cast<int32_t>(rem) : kChunk, lane);
                         __syncwarp();
                     }
@@ -861,8 +906,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 *reinterpret_cast<float4*>(Abuf + i * kLd + jb + q) =
                                     make_float4(x[q], x[q + 1], x[q + 2], x[q + 3]);
                         } else {
-                            st_chunk_bf16(pb, i, jb >> 3, x);
-                            st_chunk_bf16(pb, i, (jb >> 3) + 1, x + 8);
+                            st_chunk16<kF16>(pb, i, jb >> 3, x);
+                            st_chunk16<kF16>(pb, i, (jb >> 3) + 1, x + 8);
                         }
                     }
                 }
@@ -876,10 +921,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int cch = 4 * qq + k;  // 16-byte column of the 256-byte row
                         uint8_t* half = kqs + 8192 + (cch >> 3) * 16384;
                         float f[8];
-                        bf16x8_to_float(*reinterpret_cast<const uint4*>(half + sw128_offset(qr, cch & 7)), f);
+                        unpack8<kF16>(*reinterpret_cast<const uint4*>(half + sw128_offset(qr, cch & 7)), f);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) f[j] *= gam;
-                        st_chunk_bf16(half, qr, cch & 7, f);
+                        st_chunk16<kF16>(half, qr, cch & 7, f);
                     }
                 }
                 // zero the padded rows of the K and V tiles (they hold the next
@@ -902,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // T = (I + A)^-1 in place, with T' = T diag(cw) and T'' = T diag(beta) in their bf16 tiles
                 // (the W and U products of the previous chunk have read the old ones)
                 if (n >= 1 && !(ok = wait_bar(cx, B_WU_FULL, (n - 1) & 1))) break;
-                tri_inverse_64(Abuf, sm + kTp, sm + kTpp, gb + kGCw, gb + kGBeta, gb + kGRn, X1, X2, it);
+                tri_inverse_64<kF16>(Abuf, sm + kTp, sm + kTpp, gb + kGCw, gb + kGBeta, gb + kGRn, X1, X2, it);
                 fence_proxy_async_smem();
                 named_bar_sync(kBarIntra, kIntraThreads);
                 if (it == 0) mbar_arrive(cx.bars + B_T_FULL);
@@ -915,7 +960,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hh = (warp - 12) >> 2;               // column half
         const int v = wq * 32 + lane;                  // TMEM lane = state row v
         const uint32_t tm_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-        __nv_bfloat16* outT = reinterpret_cast<__nv_bfloat16*>(sm + kOutT);
+        using E = Elem16<kF16>;
+        typename E::T* outT = reinterpret_cast<typename E::T*>(sm + kOutT);
         uint32_t n = 0, u = 0;
         bool ok = true;
         for (; ok;) {
@@ -944,7 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 if (!(ok = wait_bar(cx, B_GATES_FULL + n % 3, (n / 3) & 1))) break;
                 const float g63 = reinterpret_cast<const float*>(sm + kGbuf)[(n % 3) * kGFloats + kGGam + 63];
-                load_initial_state(s0, tm_lane + kTmSbf + 32 * hh, tm_lane + kTmS + 64 * hh, g63);
+                load_initial_state<kF16>(s0, tm_lane + kTmSbf + 32 * hh, tm_lane + kTmS + 64 * hh, g63);
                 tc_fence_before();
                 named_bar_sync(kBarState, kStateThreads);
                 if (st == 0) mbar_arrive(cx.bars + B_SB_FULL + (n & 1));
@@ -962,7 +1008,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(rr[j]);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) st_chunk_bf16(sm + kWb, v, (i0 >> 3) + q, w + 8 * q);
+                for (int q = 0; q < 4; ++q) st_chunk16<kF16>(sm + kWb, v, (i0 >> 3) + q, w + 8 * q);
                 if (p.intra_w || p.intra_u || p.intra_g)
                     dump_intra(p.intra_w, p.intra_u, p.intra_g,
                                (static_cast<size_t>(info.flat0 + cm) * H + info.h) * kChunk * kHead,
@@ -996,7 +1042,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t ra[32], pk[16];
                     tmem_ld32_wait(dbuf + 32 * hh, ra);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(__uint_as_float(ra[2 * q]), __uint_as_float(ra[2 * q + 1]));
+                    for (int q = 0; q < 16; ++q) pk[q] = E::pack(__uint_as_float(ra[2 * q]), __uint_as_float(ra[2 * q + 1]));
                     tmem_st16(dbuf + 32 * hh, pk);
                     float dv[16];
 #pragma unroll
@@ -1004,8 +1050,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         lds16(gb + kGDec + 32 * hh + 16 * part, dv);
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
-                            pk[8 * part + q] = pack_bf16x2(__uint_as_float(ra[16 * part + 2 * q]) * dv[2 * q],
-                                                           __uint_as_float(ra[16 * part + 2 * q + 1]) * dv[2 * q + 1]);
+                            pk[8 * part + q] = E::pack(__uint_as_float(ra[16 * part + 2 * q]) * dv[2 * q],
+                                                       __uint_as_float(ra[16 * part + 2 * q + 1]) * dv[2 * q + 1]);
                     }
                     tmem_st16(dbuf + 32 * hh + 16, pk);
                     tmem_wait_st();
@@ -1045,7 +1091,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!last) {  // bf16 pairs (c, c + 1) in column c / 2 of the operand
                             uint32_t pk[8];
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) pk[q] = pack_bf16x2(x[2 * q], x[2 * q + 1]);
+                            for (int q = 0; q < 8; ++q) pk[q] = E::pack(x[2 * q], x[2 * q + 1]);
                             tmem_st8(tm_lane + kTmSbf + 32 * hh + c0 / 2, pk);
                         }
                     }
@@ -1093,7 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_regs_ready(r1);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            outT[(i0 + j) * kHead + v] = __float2bfloat16_rn(sc * rm[j] * __uint_as_float(r1[j]));
+                            outT[(i0 + j) * kHead + v] = E::from(sc * rm[j] * __uint_as_float(r1[j]));
                     }
                 }
                 fence_proxy_async_smem();
@@ -1137,19 +1183,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t chunk_bf16_smem_bytes() { return kSmemAlloc; }
 
-cudaError_t launch_chunk_bf16(const ChunkParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                              const CUtensorMap& tm_v, const CUtensorMap& tm_o, int grid, cudaStream_t stream) {
-    static int configured = -1;
+cudaError_t launch_chunk_16bit(const ChunkParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                               const CUtensorMap& tm_v, const CUtensorMap& tm_o, bool f16, int grid,
+                               cudaStream_t stream) {
+    static int configured[2] = {-1, -1};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured != dev) {
-        e = cudaFuncSetAttribute(gdn_chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemAlloc));
+    auto* kernel = f16 ? gdn_chunk_kernel<__half> : gdn_chunk_kernel<__nv_bfloat16>;
+    if (configured[f16] != dev) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemAlloc));
         if (e != cudaSuccess) return e;
-        configured = dev;
+        configured[f16] = dev;
     }
-    gdn_chunk_bf16_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(p, tm_q, tm_k, tm_v, tm_o);
+    kernel<<<grid, kThreads, kSmemAlloc, stream>>>(p, tm_q, tm_k, tm_v, tm_o);
     return cudaGetLastError();
 }
 

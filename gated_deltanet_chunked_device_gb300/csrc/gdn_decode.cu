@@ -19,6 +19,7 @@
 // 512-byte coalesced access, and the row products S k and S q are four
 // warp-wide sums.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "gdn_internal.cuh"
 
@@ -48,6 +49,19 @@ __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, flo
     x[3] = __uint_as_float(u.y & 0xffff0000u);
 }
 
+template <>
+__device__ __forceinline__ void load4<__half>(const __half* p, float (&x)[4]) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    __half2 a, b;
+    memcpy(&a, &u.x, 4);
+    memcpy(&b, &u.y, 4);
+    const float2 fa = __half22float2(a), fb = __half22float2(b);
+    x[0] = fa.x;
+    x[1] = fa.y;
+    x[2] = fb.x;
+    x[3] = fb.y;
+}
+
 template <typename T>
 __device__ __forceinline__ void store4(T* p, const float (&x)[4]);
 
@@ -62,6 +76,15 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const fl
     uint2 u;
     u.x = *reinterpret_cast<uint32_t*>(&a);
     u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+
+template <>
+__device__ __forceinline__ void store4<__half>(__half* p, const float (&x)[4]) {
+    const __half2 a = __floats2half2_rn(x[0], x[1]), b = __floats2half2_rn(x[2], x[3]);
+    uint2 u;
+    memcpy(&u.x, &a, 4);
+    memcpy(&u.y, &b, 4);
     *reinterpret_cast<uint2*>(p) = u;
 }
 
@@ -187,9 +210,15 @@ __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const DecodePar
     }
 }
 
+template <typename T>
+void launch_decode_t(const DecodeParams& p, unsigned grid, cudaStream_t stream) {
+    if (p.m == 1) gdn_decode_kernel<T, true><<<grid, kDecThreads, 0, stream>>>(p);
+    else gdn_decode_kernel<T, false><<<grid, kDecThreads, 0, stream>>>(p);
+}
+
 }  // namespace
 
-cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeParams& p, gdn_dtype dtype, cudaStream_t stream) {
     const int64_t units = static_cast<int64_t>(p.N) * p.H;
     if (units == 0) return cudaSuccess;
     int dev = 0, sms = 0;
@@ -198,13 +227,9 @@ cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t stream)
         return cudaErrorUnknown;
     const int64_t blocks = units < sms ? units : sms;  // persistent: one CTA of 1024 threads per SM
     const unsigned grid = static_cast<unsigned>(blocks);
-    if (bf16) {
-        if (p.m == 1) gdn_decode_kernel<__nv_bfloat16, true><<<grid, kDecThreads, 0, stream>>>(p);
-        else gdn_decode_kernel<__nv_bfloat16, false><<<grid, kDecThreads, 0, stream>>>(p);
-    } else {
-        if (p.m == 1) gdn_decode_kernel<float, true><<<grid, kDecThreads, 0, stream>>>(p);
-        else gdn_decode_kernel<float, false><<<grid, kDecThreads, 0, stream>>>(p);
-    }
+    if (dtype == GDN_DTYPE_BF16) launch_decode_t<__nv_bfloat16>(p, grid, stream);
+    else if (dtype == GDN_DTYPE_F16) launch_decode_t<__half>(p, grid, stream);
+    else launch_decode_t<float>(p, grid, stream);
     return cudaGetLastError();
 }
 

@@ -111,10 +111,11 @@ __host__ __device__ inline int64_t load_index(const void* p, int i64, int64_t i)
 
 // Launchers (each file defines its own).
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t stream);
-cudaError_t launch_chunk_bf16(const ChunkParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                              const CUtensorMap& tm_v, const CUtensorMap& tm_o, int grid, cudaStream_t stream);
+cudaError_t launch_chunk_16bit(const ChunkParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                               const CUtensorMap& tm_v, const CUtensorMap& tm_o, bool f16, int grid,
+                               cudaStream_t stream);
 cudaError_t launch_chunk_f32(const ChunkParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, gdn_dtype dtype, cudaStream_t stream);
 size_t chunk_bf16_smem_bytes();
 size_t plan_workspace_bytes(gdn_prefill_plan_t plan);
 

@@ -72,9 +72,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// [T, heads, 128] bf16 tensor as a 3-D TMA map with 64 x 1 x 64 boxes and the
-// 128-byte swizzle; rows past T read as zeros.
-bool encode_qkv_map(CUtensorMap* map, const void* base, int64_t T, int32_t heads) {
+CUtensorMapDataType tma_type(gdn_dtype t) {
+    return t == GDN_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
+
+// [T, heads, 128] bf16 or fp16 tensor as a 3-D TMA map with 64 x 1 x 64 boxes
+// and the 128-byte swizzle; rows past T read as zeros.
+bool encode_qkv_map(CUtensorMap* map, const void* base, int64_t T, int32_t heads, gdn_dtype t) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(gdn::kHead), static_cast<cuuint64_t>(heads),
@@ -83,14 +87,14 @@ bool encode_qkv_map(CUtensorMap* map, const void* base, int64_t T, int32_t heads
                              static_cast<cuuint64_t>(heads) * gdn::kHead * 2};
     cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(gdn::kChunk)};
     cuuint32_t es[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+    return enc(map, tma_type(t), 3, const_cast<void*>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Output [T, H, 128] bf16 as a 3-D TMA map with 128 x 1 x 64 boxes, no swizzle
-// (the kernel stages a 64 x 128 row-major tile).
-bool encode_out_map(CUtensorMap* map, void* base, int64_t T, int32_t heads) {
+// Output [T, H, 128] (dtype of q) as a 3-D TMA map with 128 x 1 x 64 boxes, no
+// swizzle (the kernel stages a 64 x 128 row-major tile).
+bool encode_out_map(CUtensorMap* map, void* base, int64_t T, int32_t heads, gdn_dtype t) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(gdn::kHead), static_cast<cuuint64_t>(heads),
@@ -99,7 +103,7 @@ bool encode_out_map(CUtensorMap* map, void* base, int64_t T, int32_t heads) {
                              static_cast<cuuint64_t>(heads) * gdn::kHead * 2};
     cuuint32_t box[3] = {static_cast<cuuint32_t>(gdn::kHead), 1, static_cast<cuuint32_t>(gdn::kChunk)};
     cuuint32_t es[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    return enc(map, tma_type(t), 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -127,7 +131,8 @@ gdn_status gdn_prefill_plan(const gdn_prefill_desc* desc, gdn_prefill_plan_t* pl
     const bool gva = d.num_q_heads == d.num_k_heads && d.num_v_heads % d.num_q_heads == 0;
     const bool gqa = d.num_k_heads == d.num_v_heads && d.num_q_heads % d.num_k_heads == 0;
     if (!gva && !gqa) return GDN_ERR_INVALID_ARG;
-    if (d.qkv_dtype != GDN_DTYPE_BF16 && d.qkv_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
+    if (d.qkv_dtype != GDN_DTYPE_BF16 && d.qkv_dtype != GDN_DTYPE_F16 && d.qkv_dtype != GDN_DTYPE_F32)
+        return GDN_ERR_UNSUPPORTED;
     if (d.state_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
     if (d.checkpoint_every_n_tokens < 0 || d.checkpoint_every_n_tokens % gdn::kChunk != 0)
         return GDN_ERR_INVALID_ARG;
@@ -275,15 +280,17 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
     std::memset(&tv, 0, sizeof(tv));
     std::memset(&to, 0, sizeof(to));
     if (T > 0) {
-        if (!encode_qkv_map(&tq, a.q, T, d.num_q_heads) || !encode_qkv_map(&tk, a.k, T, d.num_k_heads) ||
-            !encode_qkv_map(&tv, a.v, T, d.num_v_heads) || !encode_out_map(&to, a.output, T, plan->H))
+        const gdn_dtype t = d.qkv_dtype;
+        if (!encode_qkv_map(&tq, a.q, T, d.num_q_heads, t) || !encode_qkv_map(&tk, a.k, T, d.num_k_heads, t) ||
+            !encode_qkv_map(&tv, a.v, T, d.num_v_heads, t) || !encode_out_map(&to, a.output, T, plan->H, t))
             return GDN_ERR_CUDA;
     }
     const int sms = sm_count();
     if (sms <= 0) return GDN_ERR_CUDA;
     const int64_t units = static_cast<int64_t>(N) * plan->H;
     const int grid = static_cast<int>(units < sms ? units : sms);
-    if (gdn::launch_chunk_bf16(cp, tq, tk, tv, to, grid, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    if (gdn::launch_chunk_16bit(cp, tq, tk, tv, to, d.qkv_dtype == GDN_DTYPE_F16, grid, stream) != cudaSuccess)
+        return GDN_ERR_CUDA;
     return GDN_OK;
 }
 
@@ -338,7 +345,7 @@ gdn_status gdn_decode_run(gdn_prefill_plan_t plan, const gdn_prefill_args* args,
     p.hv = d.num_v_heads;
     p.m = tokens_per_seq;
     p.l2norm = (f & GDN_FLAG_QK_L2NORM) ? 1 : 0;
-    return gdn::launch_decode(p, d.qkv_dtype == GDN_DTYPE_BF16, static_cast<cudaStream_t>(stream_ptr)) == cudaSuccess
+    return gdn::launch_decode(p, d.qkv_dtype, static_cast<cudaStream_t>(stream_ptr)) == cudaSuccess
                ? GDN_OK
                : GDN_ERR_CUDA;
 }

@@ -289,13 +289,14 @@ __device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t 
     return smem_desc(saddr, mn_atom_stride, 1024);
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulate.
-// a_mn / b_mn select MN-major operands; neg_a negates A.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn = false, bool b_mn = false,
-                                                      bool neg_a = false) {
+// Instruction descriptor for kind::f16 with fp32 accumulate; A and B are
+// both bf16, or both fp16 when f16 is set.  a_mn / b_mn select MN-major
+// operands; neg_a negates A.
+__host__ __device__ constexpr uint32_t idesc_16bit_f32(uint32_t M, uint32_t N, bool a_mn, bool b_mn, bool neg_a,
+                                                       bool f16) {
     return (1u << 4)                        // D format: f32
-           | (1u << 7)                      // A format: bf16
-           | (1u << 10)                     // B format: bf16
+           | ((f16 ? 0u : 1u) << 7)         // A format: 0 = fp16, 1 = bf16
+           | ((f16 ? 0u : 1u) << 10)        // B format
            | ((neg_a ? 1u : 0u) << 13)      // negate A
            | ((a_mn ? 1u : 0u) << 15)       // A major: 0 = K, 1 = MN
            | ((b_mn ? 1u : 0u) << 16)       // B major
@@ -303,7 +304,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bo
            | ((M >> 4) << 24);              // M / 16
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T   (one instruction: K = 16 for bf16)
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn = false, bool b_mn = false,
+                                                      bool neg_a = false) {
+    return idesc_16bit_f32(M, N, a_mn, b_mn, neg_a, false);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T   (one instruction: K = 16; bf16 or fp16 operands, per the descriptor)
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
     asm volatile(
@@ -314,7 +320,7 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T   (A: bf16 pairs packed in 32-bit TMEM cells)
+// D[tmem] (+)= A[tmem] * B[smem]^T   (A: 16-bit pairs packed in 32-bit TMEM cells)
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
     asm volatile(
@@ -335,6 +341,12 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
 

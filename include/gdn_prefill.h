@@ -16,7 +16,7 @@
  * 64-token chunk").
  *
  * Shapes (all tensors dense, row-major, device memory unless stated):
- *   q [T, HQ, 128], k [T, HK, 128], v [T, HV, 128]  bf16 or fp32
+ *   q [T, HQ, 128], k [T, HK, 128], v [T, HV, 128]  bf16, fp16 or fp32 (one type)
  *   g, beta          [T, H] fp32, H = max(HQ, HV)   (g is alpha, linear space)
  *   cu_seqlens       [N+1] int32 or int64, cu_seqlens[0] = 0, cu_seqlens[N] = T;
  *                    equal neighbours are legal zero-length sequences
@@ -68,7 +68,10 @@ typedef enum gdn_status {
     GDN_ERR_DEVICE_TIMEOUT = 5 /* gdn_prefill_read_status: a bounded device wait ran out */
 } gdn_status;
 
-typedef enum gdn_dtype { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 } gdn_dtype;
+/* fp16 q/k/v run on fp16 tensor-core operands throughout (the kernel's own
+ * 16-bit intermediates take the input type); values must stay inside fp16's
+ * range (|x| < 65504), including raw q.k products and the state entries. */
+typedef enum gdn_dtype { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1, GDN_DTYPE_F16 = 2 } gdn_dtype;
 
 /* gdn_prefill_desc.flags */
 enum {
@@ -99,7 +102,7 @@ enum {
 typedef struct gdn_prefill_desc {
     int32_t num_q_heads, num_k_heads, num_v_heads; /* HQ, HK, HV */
     int32_t head_size;                             /* must be 128 */
-    gdn_dtype qkv_dtype;                           /* q, k, v and output: BF16 or F32 */
+    gdn_dtype qkv_dtype;                           /* q, k, v and output: BF16, F16 or F32 */
     gdn_dtype state_dtype;                         /* states and checkpoints: F32 */
     int64_t max_total_tokens;                      /* upper bound of T over the plan's runs */
     int32_t max_num_seqs;                          /* upper bound of N */

@@ -8,7 +8,8 @@ import gated_deltanet_chunked_device_gb300 as gdn
 from gated_deltanet_chunked_device_gb300 import workloads as wl
 
 # Tolerances of the parity bar: elementwise |gpu - ref| <= tol + tol * |ref|
-TOL = {torch.bfloat16: 2e-2, torch.float32: 1e-3}
+# fp16 inputs take the 16-bit bound the pages give for bf16 (their only 16-bit figure)
+TOL = {torch.bfloat16: 2e-2, torch.float16: 2e-2, torch.float32: 1e-3}
 
 
 def to_device(inp, device="cuda"):

@@ -56,6 +56,8 @@ def _desc(**kw):
     (dict(checkpoint_every_n_tokens=-64), INVALID),
     (dict(state_dtype=gdn.DTYPE_BF16), UNSUPPORTED),
     (dict(qkv_dtype=7), UNSUPPORTED),
+    (dict(qkv_dtype=gdn.DTYPE_F16), OK),
+    (dict(qkv_dtype=gdn.DTYPE_F32), OK),
     (dict(flags=1 << 20), INVALID),
     (dict(max_total_tokens=-1), INVALID),
     (dict(max_total_tokens=1 << 31), UNSUPPORTED),

@@ -70,6 +70,16 @@ def test_decode_fp32_inputs():
     check_against_oracle(inp, run_decode(inp, 4))
 
 
+@pytest.mark.parametrize("m", [1, 3])
+def test_decode_fp16_inputs(m):
+    w = wl.custom(seq_lens=[m] * 24, hq=4, hk=4, hv=8, dtype=torch.float16, initial_state="pool", n_pool=32,
+                  l2norm_in_kernel=True, qk_prenorm=False)
+    inp = wl.generate(w, seed=34 + m)
+    res = run_decode(inp, m)
+    assert res["output"].dtype == torch.float16
+    check_against_oracle(inp, res)
+
+
 def test_decode_after_prefill_matches_the_whole_sequence():
     # prefill 300 tokens of 6 sequences, then decode one more token each from the prefill's final states
     L, n = 300, 6

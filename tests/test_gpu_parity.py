@@ -239,6 +239,21 @@ def test_moderate_gates_scale_q_in_place(l2norm):
     check_against_oracle(inp, run_gpu(to_device(inp)))
 
 
+@pytest.mark.parametrize("case", ["gva_l2norm_pool_ckpt", "gqa_prenorm_dense"])
+def test_fp16_inputs(case):
+    # fp16 q/k/v: the fp16 instance of the tensor-core kernel (every 16-bit operand in fp16), output in fp16
+    if case == "gva_l2norm_pool_ckpt":
+        w = wl.custom(seq_lens=[300, 0, 77, 130, 64], hq=2, hk=2, hv=4, dtype=torch.float16, initial_state="pool",
+                      n_pool=8, l2norm_in_kernel=True, qk_prenorm=False, checkpoint_every=64)
+    else:
+        w = wl.custom(seq_lens=[200, 5, 129], hq=4, hk=2, hv=2, dtype=torch.float16, initial_state="dense",
+                      alpha="exp_softplus16")
+    inp = wl.generate(w, seed=18)
+    res = run_gpu(to_device(inp))
+    assert res["output"].dtype == torch.float16
+    check_against_oracle(inp, res)
+
+
 def test_more_sequences_than_the_on_chip_sort():
     # 9000 sequences (above the 8192 the prepare kernel sorts on chip; the rest keep their order), most of
     # them a few tokens long, a few of them several chunks long
