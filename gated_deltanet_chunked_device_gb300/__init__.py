@@ -45,6 +45,7 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
           4: "GDN_ERR_DEVICE_INPUT", 5: "GDN_ERR_DEVICE_TIMEOUT"}
 DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2
 _QKV_DTYPES = {torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16, torch.float32: DTYPE_F32}
+_STATE_DTYPES = _QKV_DTYPES
 FLAGS = {
     "HAS_G": 1 << 0, "HAS_BETA": 1 << 1, "HAS_SCALE": 1 << 2, "QK_L2NORM": 1 << 3, "HAS_INITIAL_STATE": 1 << 4,
     "OUTPUT_FINAL_STATE": 1 << 5, "HAS_STATE_INDICES": 1 << 6, "CU_SEQLENS_I64": 1 << 7,
@@ -74,7 +75,8 @@ class Args(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("g", ctypes.c_void_p),
                 ("beta", ctypes.c_void_p), ("scale", ctypes.c_float), ("cu_seqlens", ctypes.c_void_p),
                 ("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int64), ("max_seqlen", ctypes.c_int64),
-                ("initial_state", ctypes.c_void_p), ("output_state", ctypes.c_void_p), ("n_pool", ctypes.c_int32),
+                ("initial_state", ctypes.c_void_p), ("output_state", ctypes.c_void_p),
+                ("state_strides", ctypes.c_int64 * 3), ("n_pool", ctypes.c_int32),
                 ("state_indices", ctypes.c_void_p), ("state_checkpoints", ctypes.c_void_p),
                 ("num_checkpoints", ctypes.c_int64), ("checkpoint_cu_starts", ctypes.c_void_p),
                 ("output", ctypes.c_void_p), ("device_status", ctypes.c_void_p), ("intra_g", ctypes.c_void_p),
@@ -232,14 +234,14 @@ def _pow2_at_least(x: int, lo: int = 1) -> int:
     return 1 << (x - 1).bit_length()
 
 
-def get_plan(hq, hk, hv, qkv_dtype, flags, ckpt_n, total_tokens, num_seqs, pool_rows) -> _Plan:
-    key = (hq, hk, hv, qkv_dtype, flags, ckpt_n)
+def get_plan(hq, hk, hv, qkv_dtype, flags, ckpt_n, total_tokens, num_seqs, pool_rows, state_dtype=DTYPE_F32) -> _Plan:
+    key = (hq, hk, hv, qkv_dtype, flags, ckpt_n, state_dtype)
     with _plans_lock:
         p = _plans.get(key)
         d = p.desc if p else None
         if p is None or d.max_total_tokens < total_tokens or d.max_num_seqs < num_seqs or d.max_pool_rows < pool_rows:
             desc = Desc(num_q_heads=hq, num_k_heads=hk, num_v_heads=hv, head_size=HEAD_SIZE, qkv_dtype=qkv_dtype,
-                        state_dtype=DTYPE_F32, max_total_tokens=_pow2_at_least(total_tokens, 64),
+                        state_dtype=state_dtype, max_total_tokens=_pow2_at_least(total_tokens, 64),
                         max_num_seqs=_pow2_at_least(num_seqs), max_pool_rows=_pow2_at_least(pool_rows) if pool_rows else 0,
                         checkpoint_every_n_tokens=ckpt_n, flags=flags)
             p = _Plan(desc)
@@ -260,6 +262,30 @@ def _check_dev(name, t, device, dtype=None):
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}")
+
+
+def _state_layout(initial_state, output_state, device):
+    """State dtype code and element strides of [row][head][v] shared by the
+    initial and output states (k contiguous); (DTYPE_F32, (0, 0, 0)) without
+    either.  The C side checks the strides for overlap."""
+    states = [t for t in (initial_state, output_state) if t is not None]
+    if not states:
+        return DTYPE_F32, (0, 0, 0)
+    t0 = states[0]
+    for name, t in zip(("initial_state", "output_state"), (initial_state, output_state)):
+        if t is None:
+            continue
+        if t.device != device:
+            raise ValueError(f"{name} must be on {device}")
+        if t.dim() != 4 or t.shape[2:] != (HEAD_SIZE, HEAD_SIZE) or t.stride(3) != 1:
+            raise ValueError(f"{name} must be [rows, heads, 128, 128] with contiguous rows of 128")
+        if t.dtype != t0.dtype or t.stride() != t0.stride():
+            raise ValueError("initial_state and output_state must share dtype and strides")
+    dt = _STATE_DTYPES.get(t0.dtype)
+    if dt is None:
+        raise ValueError(f"unsupported state dtype {t0.dtype}")
+    strides = (0, 0, 0) if t0.is_contiguous() else tuple(int(x) for x in t0.stride()[:3])
+    return dt, strides
 
 
 def chunk_gated_delta_rule(q, k, v, g=None, beta=None, scale=None, initial_state=None, output_final_state=False,
@@ -319,15 +345,18 @@ def chunk_gated_delta_rule(q, k, v, g=None, beta=None, scale=None, initial_state
             raise ValueError("state_indices needs a state pool (initial_state and/or output_state)")
         n_pool = (initial_state if initial_state is not None else output_state).shape[0]
     if initial_state is not None:
-        _check_dev("initial_state", initial_state, device, torch.float32)
         flags |= FLAGS["HAS_INITIAL_STATE"]
     if output_final_state:
         if output_state is None:
             if state_indices is not None:
                 raise ValueError("output_final_state with state_indices requires the output_state pool")
-            output_state = torch.empty(N, H, D, D, dtype=torch.float32, device=device)
-        _check_dev("output_state", output_state, device, torch.float32)
+            st_dtype = initial_state.dtype if initial_state is not None else torch.float32
+            output_state = torch.empty(N, H, D, D, dtype=st_dtype, device=device)
+            if initial_state is not None and not initial_state.is_contiguous():
+                output_state = torch.empty_strided(initial_state.shape, initial_state.stride(), dtype=st_dtype,
+                                                   device=device)
         flags |= FLAGS["OUTPUT_FINAL_STATE"]
+    state_dtype, state_strides = _state_layout(initial_state, output_state if output_final_state else None, device)
     n = int(checkpoint_every_n_tokens or 0)
     if (state_checkpoints is None) != (checkpoint_cu_starts is None):
         raise ValueError("state_checkpoints and checkpoint_cu_starts must be given together")
@@ -343,12 +372,13 @@ def chunk_gated_delta_rule(q, k, v, g=None, beta=None, scale=None, initial_state
     if output is None:
         output = torch.empty(T, H, D, dtype=q.dtype, device=device)
     _check_dev("output", output, device, q.dtype)
-    plan = get_plan(hq, hk, hv, qkv_dtype, flags, n, T, N, n_pool)
+    plan = get_plan(hq, hk, hv, qkv_dtype, flags, n, T, N, n_pool, state_dtype)
     ws = plan.workspace(device)
     args = Args(q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
                 scale=float(scale) if scale is not None else 0.0, cu_seqlens=_ptr(cu_seqlens), num_seqs=N,
                 total_tokens=T, max_seqlen=int(max_seqlen or 0), initial_state=_ptr(initial_state),
-                output_state=_ptr(output_state) if output_final_state else None, n_pool=n_pool,
+                output_state=_ptr(output_state) if output_final_state else None,
+                state_strides=(ctypes.c_int64 * 3)(*state_strides), n_pool=n_pool,
                 state_indices=_ptr(state_indices), state_checkpoints=_ptr(state_checkpoints), num_checkpoints=num_ck,
                 checkpoint_cu_starts=_ptr(checkpoint_cu_starts), output=_ptr(output),
                 device_status=_ptr(device_status))
@@ -419,20 +449,24 @@ def gated_delta_rule_decode(q, k, v, g=None, beta=None, scale=None, initial_stat
         if output_final_state and output_state is None:
             output_state = initial_state
     if initial_state is not None:
-        _check_dev("initial_state", initial_state, device, torch.float32)
         flags |= FLAGS["HAS_INITIAL_STATE"]
     if output_final_state:
         if output_state is None:
-            output_state = torch.empty(N, H, D, D, dtype=torch.float32, device=device)
-        _check_dev("output_state", output_state, device, torch.float32)
+            st_dtype = initial_state.dtype if initial_state is not None else torch.float32
+            output_state = torch.empty(N, H, D, D, dtype=st_dtype, device=device)
+            if initial_state is not None and not initial_state.is_contiguous():
+                output_state = torch.empty_strided(initial_state.shape, initial_state.stride(), dtype=st_dtype,
+                                                   device=device)
         flags |= FLAGS["OUTPUT_FINAL_STATE"]
+    state_dtype, state_strides = _state_layout(initial_state, output_state if output_final_state else None, device)
     if output is None:
         output = torch.empty(T, H, D, dtype=q.dtype, device=device)
     _check_dev("output", output, device, q.dtype)
-    plan = get_plan(hq, hk, hv, qkv_dtype, flags, 0, T, N, n_pool)
+    plan = get_plan(hq, hk, hv, qkv_dtype, flags, 0, T, N, n_pool, state_dtype)
     args = Args(q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
                 scale=float(scale) if scale is not None else 0.0, num_seqs=N, total_tokens=T,
                 initial_state=_ptr(initial_state), output_state=_ptr(output_state) if output_final_state else None,
+                state_strides=(ctypes.c_int64 * 3)(*state_strides),
                 n_pool=n_pool, state_indices=_ptr(state_indices), output=_ptr(output),
                 device_status=_ptr(device_status))
     st = gdn_decode_run(plan.handle, args, m, torch.cuda.current_stream(device).cuda_stream)

@@ -525,13 +525,15 @@ __device__ __noinline__ void dump_intra(float* intra_w, float* intra_u, float* i
 // pairs into the A operand columns, and gamma_63 S0 into the fp32 accumulator
 // (S0 null: zeros).  Once per unit, so out of line.
 template <bool kF16>
-__device__ __noinline__ void load_initial_state(const float* s0, uint32_t tm_sbf, uint32_t tm_s, float g63) {
+__device__ __noinline__ void load_initial_state(const void* s0, int64_t off, int32_t dt, uint32_t tm_sbf,
+                                                uint32_t tm_s, float g63) {
     for (int c0 = 0; c0 < 64; c0 += 32) {
         float x[32];
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
-            const float4 f = s0 ? *reinterpret_cast<const float4*>(s0 + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-            x[j] = f.x; x[j + 1] = f.y; x[j + 2] = f.z; x[j + 3] = f.w;
+            float f[4] = {0.f, 0.f, 0.f, 0.f};
+            if (s0) state_load4(s0, off + c0 + j, dt, f);
+            x[j] = f[0]; x[j + 1] = f[1]; x[j + 2] = f[2]; x[j + 3] = f[3];
         }
         uint32_t pk[16];
 #pragma unroll
@@ -543,6 +545,32 @@ __device__ __noinline__ void load_initial_state(const float* s0, uint32_t tm_sbf
         tmem_st32(tm_s + c0, r);
     }
     tmem_wait_st();
+}
+
+// A zero-length sequence: this thread's 64 elements of the initial state (or zeros) to the output state.
+__device__ __noinline__ void pass_state_through(const void* s0, void* dst, int64_t off, int32_t dt) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < 64; c0 += 4) {
+        float f[4] = {0.f, 0.f, 0.f, 0.f};
+        if (s0) state_load4(s0, off + c0, dt, f);
+        state_store4(dst, off + c0, dt, f);
+    }
+}
+
+// The final state after a unit's last chunk: this thread's 64 columns of the fp32 accumulator in TMEM
+// (tm_s) to the output state, in the state's type.  Warp-uniform (tcgen05.ld is warp-collective).
+__device__ __noinline__ void store_final_state(uint32_t tm_s, void* base, int64_t off, int32_t dt) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < 64; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16_wait(tm_s + c0, r);
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) {
+            const float f[4] = {__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                __uint_as_float(r[j + 3])};
+            state_store4(base, off + c0 + j, dt, f);
+        }
+    }
 }
 
 // E: the input element type, __nv_bfloat16 or __half.
@@ -972,17 +1000,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (st == 0) mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
             ++u;
             if (!info.valid) break;
-            const size_t state_off = (static_cast<size_t>(info.srow) * H + info.h) * kHead * kHead +
-                                     static_cast<size_t>(v) * kHead + 64 * hh;  // this thread's 64 columns
-            const float* s0 = p.initial_state ? p.initial_state + state_off : nullptr;
+            // element offset of this thread's 64 columns in the initial / output state
+            const int64_t state_off = state_offset(p.state, info.srow, info.h, v) + 64 * hh;
+            const void* s0 = p.initial_state;
             if (info.nC == 0) {
-                if (p.output_state) {
-                    float* dst = p.output_state + state_off;
-#pragma unroll 4
-                    for (int c0 = 0; c0 < 64; c0 += 4)
-                        *reinterpret_cast<float4*>(dst + c0) =
-                            s0 ? *reinterpret_cast<const float4*>(s0 + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+                if (p.output_state) pass_state_through(s0, p.output_state, state_off, p.state.dtype);
                 continue;
             }
             // initial state: S0 -> the bf16 operand columns and gamma_63(first chunk) * S0 -> the accumulator
@@ -990,7 +1012,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 if (!(ok = wait_bar(cx, B_GATES_FULL + n % 3, (n / 3) & 1))) break;
                 const float g63 = reinterpret_cast<const float*>(sm + kGbuf)[(n % 3) * kGFloats + kGGam + 63];
-                load_initial_state<kF16>(s0, tm_lane + kTmSbf + 32 * hh, tm_lane + kTmS + 64 * hh, g63);
+                load_initial_state<kF16>(s0, state_off, p.state.dtype, tm_lane + kTmSbf + 32 * hh,
+                                         tm_lane + kTmS + 64 * hh, g63);
                 tc_fence_before();
                 named_bar_sync(kBarState, kStateThreads);
                 if (st == 0) mbar_arrive(cx.bars + B_SB_FULL + (n & 1));
@@ -1070,7 +1093,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p.checkpoints && p.ckpt_n > 0 && pend % p.ckpt_n == 0 && pend <= info.L)
                         ck = p.checkpoints + (static_cast<size_t>(info.ckpt_base + pend / p.ckpt_n - 1) * H + info.h) *
                                                  kHead * kHead + static_cast<size_t>(v) * kHead + 64 * hh;
-                    float* fin = (last && p.output_state) ? p.output_state + state_off : nullptr;
 #pragma unroll 1
                     for (int c0 = 0; c0 < 64; c0 += 16) {
                         uint32_t r[16];
@@ -1083,11 +1105,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int j = 0; j < 16; j += 4)
                                 *reinterpret_cast<float4*>(ck + c0 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
                         }
-                        if (fin) {
-#pragma unroll
-                            for (int j = 0; j < 16; j += 4)
-                                *reinterpret_cast<float4*>(fin + c0 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
-                        }
                         if (!last) {  // bf16 pairs (c, c + 1) in column c / 2 of the operand
                             uint32_t pk[8];
 #pragma unroll
@@ -1096,6 +1113,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     if (!last) tmem_wait_st();
+                    if (last && p.output_state) store_final_state(tm_lane + kTmS + 64 * hh, p.output_state, state_off,
+                                                                  p.state.dtype);
                 }
                 // W of the next chunk, published with the bf16 state under one barrier: the two are all the next
                 // Delta product waits for, while this chunk's prescale and output epilogue run behind it.

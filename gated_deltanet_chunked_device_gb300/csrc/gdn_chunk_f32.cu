@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
     const int64_t t0 = load_index(p.cu_seqlens, p.cu_i64, seq);
     const int64_t L = load_index(p.cu_seqlens, p.cu_i64, seq + 1) - t0;
     const int64_t srow = p.state_indices ? load_index(p.state_indices, p.idx_i64, seq) : seq;
-    const size_t state_base = (static_cast<size_t>(srow) * H + h) * kHead * kHead;
+    const int64_t state_base = state_offset(p.state, srow, h, 0);  // element offset of v row 0
     const float* qg = static_cast<const float*>(p.q);
     const float* kg = static_cast<const float*>(p.k);
     const float* vg = static_cast<const float*>(p.v);
@@ -73,9 +73,12 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
     float* sBeta = sG + 128;
 
     // state slice: rows v0..v0+63 of [V][K]
-    for (int e = tid; e < kVs * kHead; e += kF32Threads) {
+    for (int e = 4 * tid; e < kVs * kHead; e += 4 * kF32Threads) {
         const int vv = e / kHead, kk = e % kHead;
-        Ss[vv * kLdK + kk] = p.initial_state ? p.initial_state[state_base + static_cast<size_t>(v0 + vv) * kHead + kk] : 0.f;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (p.initial_state) state_load4(p.initial_state, state_base + (v0 + vv) * p.state.s_v + kk, p.state.dtype, x);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) Ss[vv * kLdK + kk + j] = x[j];
     }
     __syncthreads();
 
@@ -236,9 +239,12 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
         }
     }
     if (p.output_state) {
-        for (int e = tid; e < kVs * kHead; e += kF32Threads)
-            p.output_state[state_base + static_cast<size_t>(v0 + e / kHead) * kHead + e % kHead] =
-                Ss[(e / kHead) * kLdK + e % kHead];
+        for (int e = 4 * tid; e < kVs * kHead; e += 4 * kF32Threads) {
+            const int vv = e / kHead, kk = e % kHead;
+            const float x[4] = {Ss[vv * kLdK + kk], Ss[vv * kLdK + kk + 1], Ss[vv * kLdK + kk + 2],
+                                Ss[vv * kLdK + kk + 3]};
+            state_store4(p.output_state, state_base + (v0 + vv) * p.state.s_v + kk, p.state.dtype, x);
+        }
     }
 }
 

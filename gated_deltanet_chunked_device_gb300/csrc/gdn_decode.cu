@@ -113,18 +113,18 @@ __device__ __forceinline__ void load_token(const DecodeParams& p, int64_t tok, i
 // This thread's 16 state values of unit u (sequence u / H, head u % H); false when its pool row is out of
 // range (then the unit is skipped and flagged).
 __device__ __forceinline__ bool load_state(const DecodeParams& p, int64_t u, int v0, int c0, float (&S)[4][4],
-                                           size_t& sbase) {
+                                           int64_t& sbase) {
     const int32_t seq = static_cast<int32_t>(u / p.H), h = static_cast<int32_t>(u % p.H);
     int64_t srow = seq;
     if (p.state_indices) {
         srow = load_index(p.state_indices, p.idx_i64, seq);
         if (srow < 0 || srow >= p.n_pool) return false;
     }
-    sbase = (static_cast<size_t>(srow) * p.H + h) * kHead * kHead;
+    sbase = state_offset(p.state, srow, h, v0) + c0;  // element offset of this thread's first value
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         if (p.initial_state) {
-            load4(p.initial_state + sbase + static_cast<size_t>(v0 + r) * kHead + c0, S[r]);
+            state_load4(p.initial_state, sbase + r * p.state.s_v, p.state.dtype, S[r]);
         } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j) S[r][j] = 0.f;
@@ -145,11 +145,11 @@ __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const DecodePar
     const int64_t units = static_cast<int64_t>(p.N) * p.H;
     int64_t u = blockIdx.x;
     float Sn[4][4];
-    size_t sbase_n = 0;
+    int64_t sbase_n = 0;
     bool ok_n = kNextUnit && u < units && load_state(p, u, v0, c0, Sn, sbase_n);
     for (; u < units; u += gridDim.x) {
         float S[4][4];
-        size_t sbase;
+        int64_t sbase;
         bool ok;
         if (kNextUnit) {
 #pragma unroll
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const DecodePar
         if (p.output_state) {
 #pragma unroll
             for (int r = 0; r < 4; ++r)
-                store4(p.output_state + sbase + static_cast<size_t>(v0 + r) * kHead + c0, S[r]);
+                state_store4(p.output_state, sbase + r * p.state.s_v, p.state.dtype, S[r]);
         }
     }
 }

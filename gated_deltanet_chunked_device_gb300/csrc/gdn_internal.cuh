@@ -5,6 +5,8 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/gdn_prefill.h"
@@ -13,6 +15,64 @@ namespace gdn {
 
 constexpr int kChunk = 64;     // tokens per chunk
 constexpr int kHead = 128;     // head size (K = V = 128)
+
+// Initial / output state layout: element type and element strides of
+// [row][state head][v]; the 128 k elements of a v row are contiguous.
+struct StateLayout {
+    int32_t dtype;                 // GDN_DTYPE_F32, GDN_DTYPE_BF16 or GDN_DTYPE_F16
+    int64_t s_row, s_head, s_v;
+};
+
+__host__ __device__ inline int64_t state_offset(StateLayout L, int64_t row, int64_t h, int64_t v) {
+    return row * L.s_row + h * L.s_head + v * L.s_v;
+}
+
+// Four consecutive k elements of a state at element offset `off` (a multiple
+// of 4), converted to or from fp32.
+__device__ __forceinline__ void state_load4(const void* base, int64_t off, int32_t dt, float (&x)[4]) {
+    if (dt == GDN_DTYPE_F32) {
+        const float4 f = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+        x[0] = f.x;
+        x[1] = f.y;
+        x[2] = f.z;
+        x[3] = f.w;
+    } else {
+        const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + off);
+        if (dt == GDN_DTYPE_BF16) {
+            x[0] = __uint_as_float(u.x << 16);
+            x[1] = __uint_as_float(u.x & 0xffff0000u);
+            x[2] = __uint_as_float(u.y << 16);
+            x[3] = __uint_as_float(u.y & 0xffff0000u);
+        } else {
+            __half2 a, b;
+            memcpy(&a, &u.x, 4);
+            memcpy(&b, &u.y, 4);
+            const float2 fa = __half22float2(a), fb = __half22float2(b);
+            x[0] = fa.x;
+            x[1] = fa.y;
+            x[2] = fb.x;
+            x[3] = fb.y;
+        }
+    }
+}
+
+__device__ __forceinline__ void state_store4(void* base, int64_t off, int32_t dt, const float (&x)[4]) {
+    if (dt == GDN_DTYPE_F32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(base) + off) = make_float4(x[0], x[1], x[2], x[3]);
+    } else {
+        uint2 u;
+        if (dt == GDN_DTYPE_BF16) {
+            const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+            memcpy(&u.x, &a, 4);
+            memcpy(&u.y, &b, 4);
+        } else {
+            const __half2 a = __floats2half2_rn(x[0], x[1]), b = __floats2half2_rn(x[2], x[3]);
+            memcpy(&u.x, &a, 4);
+            memcpy(&u.y, &b, 4);
+        }
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(base) + off) = u;
+    }
+}
 
 // Workspace layout (computed on the host from the plan).
 struct WorkspaceLayout {
@@ -66,8 +126,9 @@ struct ChunkParams {
     const void* cu_seqlens;
     int cu_i64;
     int32_t num_seqs;
-    const float* initial_state;    // nullptr = zeros
-    float* output_state;           // nullptr = no final state
+    const void* initial_state;     // nullptr = zeros
+    void* output_state;            // nullptr = no final state
+    StateLayout state;             // type and strides of both
     const void* state_indices;     // nullptr = dense [N, H, V, K]
     int idx_i64;
     float* checkpoints;            // nullptr = none
@@ -93,8 +154,9 @@ struct DecodeParams {
     const float* g;                // nullptr: alpha = 1
     const float* beta;             // nullptr: beta = 1
     float scale;
-    const float* initial_state;    // nullptr: zero state
-    float* output_state;           // nullptr: state not written back
+    const void* initial_state;     // nullptr: zero state
+    void* output_state;            // nullptr: state not written back
+    StateLayout state;
     const void* state_indices;     // nullptr: row = sequence
     int idx_i64;
     int32_t n_pool;

@@ -14,6 +14,7 @@
 #include <cudaTypedefs.h>
 #include <mutex>
 #include <new>
+#include <utility>
 
 #include "gdn_internal.cuh"
 
@@ -108,6 +109,39 @@ bool encode_out_map(CUtensorMap* map, void* base, int64_t T, int32_t heads, gdn_
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The state layout of a run: the plan's state type and the args' strides
+// ({0, 0, 0}: contiguous [rows][H][128][128]).  False when the strides are not
+// positive multiples of 16 bytes or may overlap (checked as nested: sorted by
+// stride, each dimension starts past the span of the smaller ones).
+bool make_state_layout(gdn_dtype dt, const int64_t (&st)[3], int64_t rows, int32_t H, gdn::StateLayout* L) {
+    L->dtype = dt;
+    const int64_t es = dt == GDN_DTYPE_F32 ? 4 : 2;
+    if (st[0] == 0 && st[1] == 0 && st[2] == 0) {
+        L->s_v = gdn::kHead;
+        L->s_head = static_cast<int64_t>(gdn::kHead) * gdn::kHead;
+        L->s_row = L->s_head * H;
+        return true;
+    }
+    int64_t ext[3] = {rows, H, gdn::kHead}, str[3] = {st[0], st[1], st[2]};
+    for (int i = 0; i < 3; ++i)
+        if (str[i] <= 0 || (str[i] * es) % 16 != 0) return false;
+    int order[3] = {0, 1, 2};
+    for (int i = 0; i < 3; ++i)
+        for (int j = i + 1; j < 3; ++j)
+            if (str[order[j]] < str[order[i]]) std::swap(order[i], order[j]);
+    int64_t span = gdn::kHead;  // the contiguous k elements of one v row
+    for (int i = 0; i < 3; ++i) {
+        const int d = order[i];
+        if (ext[d] <= 1) continue;
+        if (str[d] < span) return false;
+        span += str[d] * (ext[d] - 1);
+    }
+    L->s_row = st[0];
+    L->s_head = st[1];
+    L->s_v = st[2];
+    return true;
+}
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -133,7 +167,8 @@ gdn_status gdn_prefill_plan(const gdn_prefill_desc* desc, gdn_prefill_plan_t* pl
     if (!gva && !gqa) return GDN_ERR_INVALID_ARG;
     if (d.qkv_dtype != GDN_DTYPE_BF16 && d.qkv_dtype != GDN_DTYPE_F16 && d.qkv_dtype != GDN_DTYPE_F32)
         return GDN_ERR_UNSUPPORTED;
-    if (d.state_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
+    if (d.state_dtype != GDN_DTYPE_F32 && d.state_dtype != GDN_DTYPE_BF16 && d.state_dtype != GDN_DTYPE_F16)
+        return GDN_ERR_UNSUPPORTED;
     if (d.checkpoint_every_n_tokens < 0 || d.checkpoint_every_n_tokens % gdn::kChunk != 0)
         return GDN_ERR_INVALID_ARG;
     if (d.max_total_tokens < 0 || d.max_num_seqs < 0 || d.max_pool_rows < 0) return GDN_ERR_INVALID_ARG;
@@ -203,6 +238,10 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
         const int64_t lo = (T + N - 1) / N;
         if (a.max_seqlen > T || a.max_seqlen < lo) return GDN_ERR_INVALID_ARG;
     }
+    gdn::StateLayout sl{};
+    if (!make_state_layout(d.state_dtype, a.state_strides, (f & GDN_FLAG_HAS_STATE_INDICES) ? a.n_pool : N, plan->H,
+                           &sl))
+        return GDN_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < plan->ws.total || !aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
 
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
@@ -250,6 +289,7 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
     cp.cu_i64 = pp.cu_i64;
     cp.num_seqs = N;
     cp.initial_state = (f & GDN_FLAG_HAS_INITIAL_STATE) ? a.initial_state : nullptr;
+    cp.state = sl;
     cp.output_state = (f & GDN_FLAG_OUTPUT_FINAL_STATE) ? a.output_state : nullptr;
     cp.state_indices = pp.state_indices;
     cp.idx_i64 = pp.idx_i64;
@@ -322,6 +362,10 @@ gdn_status gdn_decode_run(gdn_prefill_plan_t plan, const gdn_prefill_args* args,
         return GDN_ERR_INVALID_ARG;
     if ((f & GDN_FLAG_HAS_STATE_INDICES) && (!a.state_indices || a.n_pool <= 0 || a.n_pool > d.max_pool_rows))
         return GDN_ERR_INVALID_ARG;
+    gdn::StateLayout sl{};
+    if (!make_state_layout(d.state_dtype, a.state_strides, (f & GDN_FLAG_HAS_STATE_INDICES) ? a.n_pool : N, plan->H,
+                           &sl))
+        return GDN_ERR_INVALID_ARG;
     const int64_t blocks = static_cast<int64_t>(N) * plan->H;
     if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     gdn::DecodeParams p{};
@@ -332,6 +376,7 @@ gdn_status gdn_decode_run(gdn_prefill_plan_t plan, const gdn_prefill_args* args,
     p.beta = (f & GDN_FLAG_HAS_BETA) ? a.beta : nullptr;
     p.scale = (f & GDN_FLAG_HAS_SCALE) ? a.scale : 1.0f / std::sqrt(static_cast<float>(gdn::kHead));
     p.initial_state = (f & GDN_FLAG_HAS_INITIAL_STATE) ? a.initial_state : nullptr;
+    p.state = sl;
     p.output_state = (f & GDN_FLAG_OUTPUT_FINAL_STATE) ? a.output_state : nullptr;
     p.state_indices = (f & GDN_FLAG_HAS_STATE_INDICES) ? a.state_indices : nullptr;
     p.idx_i64 = (f & GDN_FLAG_STATE_INDICES_I64) ? 1 : 0;

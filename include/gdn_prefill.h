@@ -20,8 +20,11 @@
  *   g, beta          [T, H] fp32, H = max(HQ, HV)   (g is alpha, linear space)
  *   cu_seqlens       [N+1] int32 or int64, cu_seqlens[0] = 0, cu_seqlens[N] = T;
  *                    equal neighbours are legal zero-length sequences
- *   initial_state    [N, H, 128, 128] fp32, or the pool [n_pool, H, 128, 128]
- *   output_state     same shape; may be the same buffer as initial_state
+ *   initial_state    [N, H, 128, 128], or the pool [n_pool, H, 128, 128], in
+ *                    the plan's state_dtype (fp32, bf16 or fp16); element
+ *                    strides of the row, head and v dims in state_strides
+ *                    (all 0: contiguous), the 128 k elements contiguous
+ *   output_state     same shape, type and strides; may be the same buffer
  *   state_indices    [N] int32 or int64: sequence i reads and writes pool row
  *                    state_indices[i] (unique, in [0, n_pool))
  *   state_checkpoints[sum_i floor(L_i / n), H, 128, 128] fp32: the state after
@@ -103,7 +106,7 @@ typedef struct gdn_prefill_desc {
     int32_t num_q_heads, num_k_heads, num_v_heads; /* HQ, HK, HV */
     int32_t head_size;                             /* must be 128 */
     gdn_dtype qkv_dtype;                           /* q, k, v and output: BF16, F16 or F32 */
-    gdn_dtype state_dtype;                         /* states and checkpoints: F32 */
+    gdn_dtype state_dtype;                         /* initial / output states: F32, BF16 or F16 (checkpoints: F32) */
     int64_t max_total_tokens;                      /* upper bound of T over the plan's runs */
     int32_t max_num_seqs;                          /* upper bound of N */
     int32_t max_pool_rows;                         /* upper bound of n_pool (0 without state_indices) */
@@ -124,8 +127,14 @@ typedef struct gdn_prefill_args {
     int32_t num_seqs;             /* N >= 0 */
     int64_t total_tokens;         /* T >= 0 */
     int64_t max_seqlen;           /* 0 = unknown; else ceil(T/N) <= max_seqlen <= T (upper bound of L_i) */
-    const float *initial_state;   /* required with GDN_FLAG_HAS_INITIAL_STATE */
-    float *output_state;          /* required with GDN_FLAG_OUTPUT_FINAL_STATE */
+    const void *initial_state;    /* required with GDN_FLAG_HAS_INITIAL_STATE; desc.state_dtype */
+    void *output_state;           /* required with GDN_FLAG_OUTPUT_FINAL_STATE; desc.state_dtype */
+    /* Element strides of [row][head][v] of both states; {0, 0, 0} = contiguous
+     * (H*128*128, 128*128, 128).  Otherwise each is positive, a multiple of 16
+     * bytes, and the layout does not overlap: sorted by stride, each stride is
+     * at least the extent covered by the smaller ones (128 for the v rows'
+     * own k elements).  Anything else is GDN_ERR_INVALID_ARG. */
+    int64_t state_strides[3];
     int32_t n_pool;               /* pool rows, with GDN_FLAG_HAS_STATE_INDICES */
     const void *state_indices;    /* [N], with GDN_FLAG_HAS_STATE_INDICES */
     float *state_checkpoints;     /* required when checkpoint_every_n_tokens > 0 */

@@ -54,7 +54,9 @@ def _desc(**kw):
     (dict(checkpoint_every_n_tokens=100), INVALID),
     (dict(checkpoint_every_n_tokens=512), OK),
     (dict(checkpoint_every_n_tokens=-64), INVALID),
-    (dict(state_dtype=gdn.DTYPE_BF16), UNSUPPORTED),
+    (dict(state_dtype=gdn.DTYPE_BF16), OK),
+    (dict(state_dtype=gdn.DTYPE_F16), OK),
+    (dict(state_dtype=9), UNSUPPORTED),
     (dict(qkv_dtype=7), UNSUPPORTED),
     (dict(qkv_dtype=gdn.DTYPE_F16), OK),
     (dict(qkv_dtype=gdn.DTYPE_F32), OK),
@@ -84,8 +86,9 @@ def _valid_args(**kw):
              num_seqs=2, total_tokens=100, max_seqlen=0, initial_state=None, output_state=None, n_pool=0,
              state_indices=None, state_checkpoints=None, num_checkpoints=0, checkpoint_cu_starts=None,
              output=fake + 0x400000, device_status=None)
+    strides = kw.pop("state_strides", (0, 0, 0))
     a.update(kw)
-    return gdn.Args(**a)
+    return gdn.Args(state_strides=(ctypes.c_int64 * 3)(*strides), **a)
 
 
 @pytest.mark.parametrize("desc_kw,args_kw,ws,expect", [
@@ -108,6 +111,12 @@ def _valid_args(**kw):
     (dict(checkpoint_every_n_tokens=64), dict(state_checkpoints=0x7f0000600000), 1 << 20, INVALID),  # starts missing
     ({}, dict(checkpoint_cu_starts=0x7f0000600000), 1 << 20, INVALID),  # checkpoints without an interval
     (dict(qkv_dtype=gdn.DTYPE_F32, num_q_heads=2, num_k_heads=2, num_v_heads=2), dict(q=None), 1 << 20, INVALID),
+    # state strides [row, head, v] (elements; the plan has H = 32 heads, N = 2 rows): one of them zero
+    ({}, dict(state_strides=(0, 128 * 128, 128)), 1 << 20, INVALID),
+    ({}, dict(state_strides=(32 * 128 * 128, 128 * 128, 130)), 1 << 20, INVALID),   # 520 bytes: not 16-aligned
+    ({}, dict(state_strides=(32 * 128 * 128, 128 * 128, 64)), 1 << 20, INVALID),    # v rows overlap
+    ({}, dict(state_strides=(32 * 128 * 128, 127 * 128, 128)), 1 << 20, INVALID),   # heads overlap
+    ({}, dict(state_strides=(31 * 128 * 128, 128 * 128, 128)), 1 << 20, INVALID),   # rows overlap
 ])
 def test_run_rejects_before_launch(L, desc_kw, args_kw, ws, expect):
     st, plan, nbytes = gdn.gdn_prefill_plan(_desc(**desc_kw))

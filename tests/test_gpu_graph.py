@@ -89,3 +89,22 @@ def test_decode_graph_replay_matches_eager():
     torch.cuda.synchronize()
     assert torch.equal(out, out_e)
     assert torch.equal(pool, pool_e)
+
+
+def test_one_plan_serves_rotating_buffers_and_smaller_batches():
+    # The plan holds shapes and flags only: the same plan runs over two rotating sets of buffers (different
+    # addresses) and over a smaller batch that fits its bounds, each result equal to the oracle's.
+    from gdn_testlib import check_against_oracle, run_gpu
+    gdn._plans.clear()
+    big = wl.custom(seq_lens=[200, 64, 7], hq=2, hk=2, hv=4, initial_state="dense", l2norm_in_kernel=True,
+                    qk_prenorm=False)
+    small = wl.custom(seq_lens=[90, 3], hq=2, hk=2, hv=4, initial_state="dense", l2norm_in_kernel=True,
+                      qk_prenorm=False)
+    cases = [wl.generate(big, seed=44), wl.generate(big, seed=45), wl.generate(small, seed=46)]
+    plans, live = set(), []
+    for inp in cases:
+        live.append(to_device(inp))  # kept alive: every run sees buffers at new addresses
+        check_against_oracle(inp, run_gpu(live[-1]))
+        plans.update(id(p) for p in gdn._plans.values())
+    assert len(gdn._plans) == 1 and len(plans) == 1
+    assert len({d["q"].data_ptr() for d in live}) == 3
