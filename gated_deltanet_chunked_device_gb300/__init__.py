@@ -49,7 +49,7 @@ _STATE_DTYPES = _QKV_DTYPES
 FLAGS = {
     "HAS_G": 1 << 0, "HAS_BETA": 1 << 1, "HAS_SCALE": 1 << 2, "QK_L2NORM": 1 << 3, "HAS_INITIAL_STATE": 1 << 4,
     "OUTPUT_FINAL_STATE": 1 << 5, "HAS_STATE_INDICES": 1 << 6, "CU_SEQLENS_I64": 1 << 7,
-    "STATE_INDICES_I64": 1 << 8, "CHECKPOINT_STARTS_I64": 1 << 9,
+    "STATE_INDICES_I64": 1 << 8, "CHECKPOINT_STARTS_I64": 1 << 9, "CONTEXT_PARALLEL": 1 << 10,
 }
 DEVICE_ERR = {"CU_SEQLENS": 1 << 0, "CHECKPOINT_STARTS": 1 << 1, "STATE_INDEX_RANGE": 1 << 2,
               "STATE_INDEX_DUP": 1 << 3, "MAX_SEQLEN": 1 << 4, "TIMEOUT": 1 << 5}
@@ -127,6 +127,8 @@ def lib():
                 L.gdn_prefill_workspace_layout.argtypes = [ctypes.c_void_p, ctypes.POINTER(Layout)]
                 L.gdn_prefill_workspace_layout.restype = ctypes.c_int
                 L.gdn_prefill_plan_destroy.argtypes = [ctypes.c_void_p]
+                L.gdn_prefill_cp_segments.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64]
+                L.gdn_prefill_cp_segments.restype = ctypes.c_int32
                 L.gdn_prefill_plan_destroy.restype = None
                 L.gdn_status_string.argtypes = [ctypes.c_int]
                 L.gdn_status_string.restype = ctypes.c_char_p
@@ -292,14 +294,16 @@ def chunk_gated_delta_rule(q, k, v, g=None, beta=None, scale=None, initial_state
                            cu_seqlens=None, use_qk_l2norm_in_kernel=False, output=None, output_state=None,
                            state_checkpoints=None, checkpoint_cu_starts=None, checkpoint_every_n_tokens=0,
                            state_indices=None, max_seqlen=None, num_seqs=None, intermediates=None,
-                           device_status=None, return_plan=False):
+                           device_status=None, return_plan=False, use_cp=False):
     """Chunked GDN prefill through the C ABI (see the module docstring).
 
     ``num_seqs`` may be given to avoid reading the length of ``cu_seqlens``
     (it is its length minus one).  ``intermediates``, when a dict, receives
     the intra-chunk outputs G, W and U per flat chunk (fp32).  With
     ``return_plan`` the plan and workspace are returned as well (for status
-    and chunk-map reads).
+    and chunk-map reads).  ``use_cp`` allows context parallelism: batches
+    with few (sequence, head) units run each sequence as segments on more
+    SMs (a larger workspace; the same results within rounding).
     """
     if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
         raise ValueError("q, k, v must be [total_tokens, heads, head_size]")
@@ -331,6 +335,8 @@ def chunk_gated_delta_rule(q, k, v, g=None, beta=None, scale=None, initial_state
         flags |= FLAGS["HAS_SCALE"]
     if use_qk_l2norm_in_kernel:
         flags |= FLAGS["QK_L2NORM"]
+    if use_cp:  # the library uses it when the batch has few (sequence, head) units
+        flags |= FLAGS["CONTEXT_PARALLEL"]
     if cu_seqlens.dtype == torch.int64:
         flags |= FLAGS["CU_SEQLENS_I64"]
     elif cu_seqlens.dtype != torch.int32:

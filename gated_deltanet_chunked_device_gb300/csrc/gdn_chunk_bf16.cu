@@ -158,7 +158,7 @@ struct Elem16<true> {
 constexpr long long kWaitCycles = 2000000000LL;  // about one second
 
 struct UnitInfo {
-    int32_t valid, seq, h, nC;
+    int32_t valid, seq, h, nC;  // valid: 0 = no more units, 1 = a unit, 2 = a transfer-matrix unit (identity, U = 0)
     int32_t qh, kh, vh, flat0;
     int64_t t0, L, srow, ckpt_base;
 };
@@ -557,6 +557,32 @@ __device__ __noinline__ void pass_state_through(const void* s0, void* dst, int64
     }
 }
 
+// The transfer pass's identity start: this thread's 64 columns of row v of I (a 1 in column ic, when
+// 0 <= ic < 64), into the bf16 operand and the accumulator (times g63), or straight to the output state
+// for an empty segment (dst non-null).  Called by the transfer instance only.
+template <bool kF16>
+__device__ __noinline__ void identity_state(int ic, uint32_t tm_sbf, uint32_t tm_s, float g63, float* dst) {
+    for (int c0 = 0; c0 < 64; c0 += 16) {
+        float x[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = (c0 + j == ic) ? 1.f : 0.f;
+        if (dst) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+                *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+            continue;
+        }
+        uint32_t pk[8], r[16];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) pk[q] = Elem16<kF16>::pack(x[2 * q], x[2 * q + 1]);
+        tmem_st8(tm_sbf + c0 / 2, pk);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(x[j] * g63);
+        tmem_st16(tm_s + c0, r);
+    }
+    if (!dst) tmem_wait_st();
+}
+
 // The final state after a unit's last chunk: this thread's 64 columns of the fp32 accumulator in TMEM
 // (tm_s) to the output state, in the state's type.  Warp-uniform (tcgen05.ld is warp-collective).
 __device__ __noinline__ void store_final_state(uint32_t tm_s, void* base, int64_t off, int32_t dt) {
@@ -573,8 +599,11 @@ __device__ __noinline__ void store_final_state(uint32_t tm_s, void* base, int64_
     }
 }
 
-// E: the input element type, __nv_bfloat16 or __half.
-template <typename E16>
+// E16: the input element type, __nv_bfloat16 or __half.  kTransfer: the context-parallel transfer pass --
+// units [0, N*H) run each sequence (a segment) from a zero state, units [N*H, 2*N*H) run it from the
+// identity with U = 0 (the segment's transfer matrix), into output_state rows seq and N + seq; no output
+// products, epilogue or stores.
+template <typename E16, bool kTransfer>
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_chunk_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -620,7 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const int32_t H = p.H;
-    const int64_t units = static_cast<int64_t>(p.num_seqs) * H;
+    const int64_t units1 = static_cast<int64_t>(p.num_seqs) * H;
+    const int64_t units = kTransfer ? 2 * units1 : units1;
 
     if (warp < 4) {
         // the scheduling warpgroup: TMA producer, two MMA issuers, gates warp
@@ -635,22 +665,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int slot = u & 1;
                     if (u >= 2 && !wait_bar(cx, B_UNIT_EMPTY + slot, ((u - 2) >> 1) & 1)) break;
                     UnitInfo info;
-                    info.valid = uid < units ? 1 : 0;
+                    const bool second = kTransfer && uid >= units1;  // a transfer-matrix unit
+                    info.valid = uid < units ? (second ? 2 : 1) : 0;
                     int32_t nC = 0;
                     if (info.valid) {
-                        const int32_t seq = p.seq_order[uid / H];
-                        const int32_t h = static_cast<int32_t>(uid % H);
+                        const int64_t ub = second ? uid - units1 : uid;
+                        const int32_t seq = p.seq_order[ub / H];
+                        const int32_t h = static_cast<int32_t>(ub % H);
                         info.seq = seq;
                         info.h = h;
-                        info.t0 = load_index(p.cu_seqlens, p.cu_i64, seq);
-                        info.L = load_index(p.cu_seqlens, p.cu_i64, seq + 1) - info.t0;
+                        if (kTransfer) {
+                            info.t0 = p.seg[2 * seq];
+                            info.L = p.seg[2 * seq + 1];
+                        } else {
+                            info.t0 = load_index(p.cu_seqlens, p.cu_i64, seq);
+                            info.L = load_index(p.cu_seqlens, p.cu_i64, seq + 1) - info.t0;
+                        }
                         nC = static_cast<int32_t>((info.L + kChunk - 1) / kChunk);
                         info.nC = nC;
                         info.qh = h / (H / p.hq);
                         info.kh = h / (H / p.hk);
                         info.vh = h / (H / p.hv);
-                        info.flat0 = p.chunk_offsets[seq];
-                        info.srow = p.state_indices ? load_index(p.state_indices, p.idx_i64, seq) : seq;
+                        info.flat0 = kTransfer ? 0 : p.chunk_offsets[seq];
+                        info.srow = (p.state_indices ? load_index(p.state_indices, p.idx_i64, seq) : seq) +
+                                    (second ? p.num_seqs : 0);
                         info.ckpt_base = p.ckpt_n > 0 ? load_index(p.ckpt_cu_starts, p.ckpt_i64, seq) : 0;
                     }
                     *reinterpret_cast<UnitInfo*>(sm + kRing + slot * 64) = info;
@@ -717,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(cx.bars + B_D1_FULL);
                     return true;
                 };
-                auto issue_wu = [&](uint32_t m) -> bool {  // W and U of global chunk m
+                auto issue_wu = [&](uint32_t m, bool no_u) -> bool {  // W and U of global chunk m (U = 0: no U)
                     if (!wait_bar(cx, B_T_FULL, m & 1) || !wait_bar(cx, B_V_FULL, m & 1)) return false;
                     // the W columns are free once the state warps have copied W of chunk m-1
                     if (m >= 1 && !wait_bar(cx, B_WB_FULL + ((m - 1) & 1), ((m - 1) >> 1) & 1)) return false;
@@ -732,8 +770,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ks = 0; ks < 4; ++ks) {
                         mma_bf16_ss(tmem + kTmW, desc_mnmajor_sw128(kq + ks * 2048, 16384),
                                     desc_kmajor_sw128(tp + ks * 32), kIdescWU<kF16>, ks > 0);
-                        mma_bf16_ss(dbuf, desc_mnmajor_sw128(vv + ks * 2048, 8192), desc_kmajor_sw128(tpp + ks * 32),
-                                    kIdescWU<kF16>, ks > 0);
+                        if (!(kTransfer && no_u))
+                            mma_bf16_ss(dbuf, desc_mnmajor_sw128(vv + ks * 2048, 8192),
+                                        desc_kmajor_sw128(tpp + ks * 32), kIdescWU<kF16>, ks > 0);
                     }
                     mma_commit(cx.bars + B_WU_FULL);
                     mma_commit(cx.bars + B_V_EMPTY);
@@ -747,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = issue_d1(n);
                     for (int32_t c = 0; c < cur.nC && ok; ++c, ++n) {
                         if (c + 1 < cur.nC) ok = issue_d1(n + 1);
-                        if (ok) ok = issue_wu(n);
+                        if (ok) ok = issue_wu(n, kTransfer && cur.valid == 2);
                     }
                 }
                 mma_commit(cx.bars + B_DRAIN_I);
@@ -779,12 +818,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     #pragma unroll 1
                         for (int ks = 0; ks < 8; ++ks)  // A = S (bf16 pairs in TMEM), k = 16 ks .. 16 ks + 15
                             mma_bf16_ts(dbuf, tmem + kTmSbf + ks * 8, desc_mnmajor_sw128(wb + ks * 2048, 8192),
-                                        kIdescDelta<kF16>, 1);
+                                        kIdescDelta<kF16>, ks > 0 || !(kTransfer && info.valid == 2));  // U = 0
                         mma_commit(cx.bars + B_DELTA_FULL + s);
                         if (n >= 1 && !(ok = wait_bar(cx, B_O_EMPTY + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
                         tc_fence_after();
     #pragma unroll 1
-                        for (int ks = 0; ks < 8; ++ks) {  // O = S Q'^T, Q' = diag(gamma) Q
+                        for (int ks = 0; ks < 8 && !kTransfer; ++ks) {  // O = S Q'^T, Q' = diag(gamma) Q
                             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
                             mma_bf16_ts(tmem + kTmO, tmem + kTmSbf + ks * 8, desc_kmajor_sw128(kq + 8192 + off),
                                         kIdescO<kF16>, ks > 0);
@@ -796,7 +835,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int ks = 0; ks < 4; ++ks) {
                             const uint32_t acol = dbuf + 32 * (ks >> 1) + 8 * (ks & 1);  // packed j = 16 ks .. 16 ks + 15
                             // O += Delta^T P^T, then S += (decayed Delta)^T K
-                            mma_bf16_ts(tmem + kTmO, acol, desc_kmajor_sw128(pb + ks * 32), kIdescO<kF16>, 1);
+                            if (!kTransfer)
+                                mma_bf16_ts(tmem + kTmO, acol, desc_kmajor_sw128(pb + ks * 32), kIdescO<kF16>, 1);
                             mma_bf16_ts(tmem + kTmS, acol + 16, desc_mnmajor_sw128(kq + ks * 2048, 16384),
                                         kIdescS<kF16>, 1);
                         }
@@ -834,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float* gbw = reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats;
                     compute_gates(cur, gbw, p.l2norm != 0, kF16 ? 0.f : kKeepQRange, lane);
                     __syncwarp();
-                    if (p.l2norm) {
+                    if (p.l2norm && !kTransfer) {
                         // the q norms from the chunk's Q tile (its stage is released only after this chunk's
                         // products, which wait for these gates)
                         if (!(ok = wait_bar(cx, B_KQ_FULL + n % kKQStages, (n / kKQStages) & 1))) break;
@@ -903,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* pb = sm + kPb + s * 8192;
 #pragma unroll 1
                     for (int jb = 32 * hh; jb < 32 * hh + 32; jb += 16) {
-                        if (jb > imax) break;  // warp-uniform
+                        if (jb > imax || (!arow && kTransfer)) break;  // warp-uniform
                         uint32_t rr[16];
                         tmem_ld16_wait(tm_lane + kTmD1 + jb, rr);
                         float x[16];
@@ -941,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // Q' = diag(gamma) Q in place, for the S Q'^T product (D1 has read Q already), unless the chunk
                 // keeps Q as stored.  Four threads per row, 32 values each.
-                if (gb[kGKeepQ] == 0.f) {
+                if (gb[kGKeepQ] == 0.f && !kTransfer) {
                     const int qr = it >> 2, qq = it & 3;
                     const float gam = gb[kGGam + qr];
 #pragma unroll
@@ -1003,8 +1043,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // element offset of this thread's 64 columns in the initial / output state
             const int64_t state_off = state_offset(p.state, info.srow, info.h, v) + 64 * hh;
             const void* s0 = p.initial_state;
+            // a transfer-matrix unit starts from the identity: a 1 in column v - 64 hh of this thread's row v
+            const bool ident = kTransfer && info.valid == 2;
             if (info.nC == 0) {
-                if (p.output_state) pass_state_through(s0, p.output_state, state_off, p.state.dtype);
+                if (ident)  // the transfer output is dense fp32
+                    identity_state<kF16>(v - 64 * hh, 0, 0, 1.f, static_cast<float*>(p.output_state) + state_off);
+                else if (p.output_state)
+                    pass_state_through(s0, p.output_state, state_off, p.state.dtype);
                 continue;
             }
             // initial state: S0 -> the bf16 operand columns and gamma_63(first chunk) * S0 -> the accumulator
@@ -1012,8 +1057,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 if (!(ok = wait_bar(cx, B_GATES_FULL + n % 3, (n / 3) & 1))) break;
                 const float g63 = reinterpret_cast<const float*>(sm + kGbuf)[(n % 3) * kGFloats + kGGam + 63];
-                load_initial_state<kF16>(s0, state_off, p.state.dtype, tm_lane + kTmSbf + 32 * hh,
-                                         tm_lane + kTmS + 64 * hh, g63);
+                if (ident)
+                    identity_state<kF16>(v - 64 * hh, tm_lane + kTmSbf + 32 * hh, tm_lane + kTmS + 64 * hh, g63,
+                                         nullptr);
+                else
+                    load_initial_state<kF16>(s0, state_off, p.state.dtype, tm_lane + kTmSbf + 32 * hh,
+                                             tm_lane + kTmS + 64 * hh, g63);
                 tc_fence_before();
                 named_bar_sync(kBarState, kStateThreads);
                 if (st == 0) mbar_arrive(cx.bars + B_SB_FULL + (n & 1));
@@ -1145,7 +1194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_wait_st();
                 }
                 // ---- output epilogue: o_i = scale rm_i (S Q'^T + Delta^T P^T)_i, tokens i in [32 hh, 32 hh + 32)
-                {
+                if (!kTransfer) {
                     const float sc = p.scale;
 #pragma unroll 1
                     for (int i0 = 32 * hh; i0 < 32 * hh + 32; i0 += 8) {
@@ -1168,7 +1217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(cx.bars + B_O_EMPTY + s);
                     mbar_arrive(cx.bars + B_GATES_EMPTY + gs);
                 }
-                if (Lc == kChunk) {
+                if (kTransfer) {
+                    // a transfer pass writes no output
+                } else if (Lc == kChunk) {
                     // a full chunk: one TMA store of the 64 x 128 tile (rows all belong to this sequence)
                     if (st == 0) {
                         tma_store_3d(&tm_o, sm + kOutT, 0, info.h, static_cast<int32_t>(tc));
@@ -1203,17 +1254,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t chunk_bf16_smem_bytes() { return kSmemAlloc; }
 
 cudaError_t launch_chunk_16bit(const ChunkParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                               const CUtensorMap& tm_v, const CUtensorMap& tm_o, bool f16, int grid,
+                               const CUtensorMap& tm_v, const CUtensorMap& tm_o, bool f16, bool transfer, int grid,
                                cudaStream_t stream) {
-    static int configured[2] = {-1, -1};
+    static int configured[4] = {-1, -1, -1, -1};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    auto* kernel = f16 ? gdn_chunk_kernel<__half> : gdn_chunk_kernel<__nv_bfloat16>;
-    if (configured[f16] != dev) {
+    auto* kernel = f16 ? (transfer ? gdn_chunk_kernel<__half, true> : gdn_chunk_kernel<__half, false>)
+                       : (transfer ? gdn_chunk_kernel<__nv_bfloat16, true> : gdn_chunk_kernel<__nv_bfloat16, false>);
+    const int ki = (f16 ? 2 : 0) + (transfer ? 1 : 0);
+    if (configured[ki] != dev) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemAlloc));
         if (e != cudaSuccess) return e;
-        configured[f16] = dev;
+        configured[ki] = dev;
     }
     kernel<<<grid, kThreads, kSmemAlloc, stream>>>(p, tm_q, tm_k, tm_v, tm_o);
     return cudaGetLastError();

@@ -111,6 +111,7 @@ struct PrepareParams {
     int32_t* seq_order;
     uint32_t* pool_bitmap;
     int32_t bitmap_words;
+    int keep_status;               // 1: add to the status word of an earlier prepare instead of clearing it
 };
 
 // Arguments of the chunk kernels (intra-chunk solve, state pass and output).
@@ -144,6 +145,34 @@ struct ChunkParams {
     float* intra_w;
     float* intra_u;
     int has_tokens;                // 0: the TMA maps are blank (T == 0) and never used
+    const int64_t* seg;            // transfer pass: [num_seqs][2] segment start token and length (else null)
+};
+
+// Context-parallel arguments: the real batch, its P segments per sequence and
+// the scratch buffers of the transfer pass (A) and the segment pass (C).
+struct CpParams {
+    const void* cu_seqlens;        // real [N+1]
+    int cu_i64;
+    int32_t num_seqs;              // N
+    int32_t H;
+    int32_t P;                     // segments per sequence
+    int32_t align;                 // segment length granularity (64, or the checkpoint interval)
+    int32_t ckpt_n;                // 0 = no checkpoints
+    const void* ckpt_cu_starts;    // real [N+1]
+    int ckpt_i64;
+    int64_t* seg_a;                // [N*(P-1)][2] segments 0..P-2 (start, length)
+    int32_t* order_a;              // [N*(P-1)] identity work order of the transfer pass
+    int32_t* counter_a;            // work counter of the transfer pass
+    int32_t* cu_c;                 // [N*P+1] segment cu_seqlens of the segment pass
+    int64_t* ckpt_c;               // [N*P+1] segment checkpoint starts
+    const float* trans;            // transfer pass output [2*N*(P-1)][H][128][128]: N_s rows, then M_s rows
+    float* start;                  // segment start states [N*P][H][128][128] (the segment pass runs in place)
+    const void* initial_state;     // real initial state (null: zeros)
+    void* output_state;            // real output state (null: none)
+    StateLayout state;             // its layout
+    const void* state_indices;     // real pool rows (null: row = sequence)
+    int idx_i64;
+    int32_t* status;
 };
 
 // Arguments of the decode-step kernel (a few tokens per sequence, no chunking).
@@ -174,10 +203,13 @@ __host__ __device__ inline int64_t load_index(const void* p, int i64, int64_t i)
 // Launchers (each file defines its own).
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t stream);
 cudaError_t launch_chunk_16bit(const ChunkParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                               const CUtensorMap& tm_v, const CUtensorMap& tm_o, bool f16, int grid,
+                               const CUtensorMap& tm_v, const CUtensorMap& tm_o, bool f16, bool transfer, int grid,
                                cudaStream_t stream);
 cudaError_t launch_chunk_f32(const ChunkParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, gdn_dtype dtype, cudaStream_t stream);
+cudaError_t launch_cp_prepare(const CpParams& p, cudaStream_t stream);
+cudaError_t launch_cp_fixup(const CpParams& p, cudaStream_t stream);
+cudaError_t launch_cp_final(const CpParams& p, cudaStream_t stream);
 size_t chunk_bf16_smem_bytes();
 size_t plan_workspace_bytes(gdn_prefill_plan_t plan);
 

@@ -18,10 +18,20 @@
 
 #include "gdn_internal.cuh"
 
+// Context-parallel scratch (plans with GDN_FLAG_CONTEXT_PARALLEL): byte offsets
+// in the workspace, after the main layout.
+struct CpLayout {
+    size_t trans, start, seg_a, order_a, counter_a, cu_c, ckpt_c, prep;  // prep: the segment pass's prepare
+    gdn::WorkspaceLayout wc;                                             // its layout, relative to prep
+};
+
 struct gdn_prefill_plan_s {
     gdn_prefill_desc desc;
     gdn::WorkspaceLayout ws;
     int32_t H;
+    bool cp;
+    CpLayout cpl;
+    size_t ws_total;  // the whole workspace (main layout plus the context-parallel scratch)
 };
 
 namespace {
@@ -29,7 +39,13 @@ namespace {
 constexpr uint32_t kKnownFlags = GDN_FLAG_HAS_G | GDN_FLAG_HAS_BETA | GDN_FLAG_HAS_SCALE | GDN_FLAG_QK_L2NORM |
                                  GDN_FLAG_HAS_INITIAL_STATE | GDN_FLAG_OUTPUT_FINAL_STATE |
                                  GDN_FLAG_HAS_STATE_INDICES | GDN_FLAG_CU_SEQLENS_I64 | GDN_FLAG_STATE_INDICES_I64 |
-                                 GDN_FLAG_CHECKPOINT_STARTS_I64;
+                                 GDN_FLAG_CHECKPOINT_STARTS_I64 | GDN_FLAG_CONTEXT_PARALLEL;
+
+// Context-parallel bounds: (sequence, head) rows of the transfer pass and of
+// the segment pass, and virtual sequences (segments) of either.
+constexpr int64_t kCpMaxRows = 256;
+constexpr int32_t kCpMaxSeqs = 256;
+constexpr int32_t kCpMaxSegments = 8;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -142,6 +158,20 @@ bool make_state_layout(gdn_dtype dt, const int64_t (&st)[3], int64_t rows, int32
     return true;
 }
 
+// Segments per sequence for context parallelism, or 0: only for plans that
+// allow it, 16-bit inputs, no intra-chunk dumps, and at most half as many
+// (sequence, head) units as SMs.  P fills the SMs with the transfer pass
+// (2 (P-1) N H units) within the plan's scratch bounds.
+int cp_segments(gdn_prefill_plan_t plan, const gdn_prefill_args& a, int32_t N, int64_t T, int sms) {
+    if (!plan->cp || plan->desc.qkv_dtype == GDN_DTYPE_F32 || a.intra_g || a.intra_w || a.intra_u) return 0;
+    const int64_t nh = static_cast<int64_t>(N) * plan->H;
+    if (N <= 0 || T <= 0 || 2 * nh > sms) return 0;
+    int64_t P = sms / (2 * nh) + 1;
+    if (P > kCpMaxSegments) P = kCpMaxSegments;
+    while (P >= 2 && (2 * (P - 1) * nh > kCpMaxRows || P * nh > kCpMaxRows || N * P > kCpMaxSeqs)) --P;
+    return P >= 2 ? static_cast<int>(P) : 0;
+}
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -151,7 +181,7 @@ int sm_count() {
 
 }  // namespace
 
-size_t gdn::plan_workspace_bytes(gdn_prefill_plan_t plan) { return plan ? plan->ws.total : 0; }
+size_t gdn::plan_workspace_bytes(gdn_prefill_plan_t plan) { return plan ? plan->ws_total : 0; }
 
 extern "C" {
 
@@ -179,12 +209,47 @@ gdn_status gdn_prefill_plan(const gdn_prefill_desc* desc, gdn_prefill_plan_t* pl
     p->desc = d;
     p->ws = make_layout(d);
     p->H = d.num_q_heads > d.num_v_heads ? d.num_q_heads : d.num_v_heads;
+    p->cp = (d.flags & GDN_FLAG_CONTEXT_PARALLEL) != 0;
+    size_t total = p->ws.total;
+    if (p->cp) {
+        const size_t plane = sizeof(float) * gdn::kHead * gdn::kHead;
+        CpLayout& c = p->cpl;
+        c.trans = total;
+        total = align_up(total + plane * kCpMaxRows, 256);
+        c.start = total;
+        total = align_up(total + plane * kCpMaxRows, 256);
+        c.seg_a = total;
+        total = align_up(total + sizeof(int64_t) * 2 * kCpMaxSeqs, 256);
+        c.order_a = total;
+        total = align_up(total + sizeof(int32_t) * kCpMaxSeqs, 256);
+        c.counter_a = total;
+        total = align_up(total + 16, 256);
+        c.cu_c = total;
+        total = align_up(total + sizeof(int32_t) * (kCpMaxSeqs + 1), 256);
+        c.ckpt_c = total;
+        total = align_up(total + sizeof(int64_t) * (kCpMaxSeqs + 1), 256);
+        gdn_prefill_desc dc = d;
+        dc.max_num_seqs = kCpMaxSeqs;
+        dc.max_pool_rows = 0;
+        c.wc = make_layout(dc);
+        c.prep = total;
+        total = align_up(total + c.wc.total, 256);
+    }
+    p->ws_total = total;
     *plan = p;
-    *workspace_bytes = p->ws.total;
+    *workspace_bytes = total;
     return GDN_OK;
 }
 
 void gdn_prefill_plan_destroy(gdn_prefill_plan_t plan) { delete plan; }
+
+int32_t gdn_prefill_cp_segments(gdn_prefill_plan_t plan, int32_t num_seqs, int64_t total_tokens) {
+    if (!plan) return 0;
+    const int sms = sm_count();
+    if (sms <= 0) return 0;
+    gdn_prefill_args a{};
+    return cp_segments(plan, a, num_seqs, total_tokens, sms);
+}
 
 gdn_status gdn_prefill_workspace_layout(gdn_prefill_plan_t plan, gdn_prefill_layout* layout) {
     if (!plan || !layout) return GDN_ERR_INVALID_ARG;
@@ -242,7 +307,7 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
     if (!make_state_layout(d.state_dtype, a.state_strides, (f & GDN_FLAG_HAS_STATE_INDICES) ? a.n_pool : N, plan->H,
                            &sl))
         return GDN_ERR_INVALID_ARG;
-    if (!workspace || workspace_bytes < plan->ws.total || !aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < plan->ws_total || !aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
 
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -327,10 +392,109 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
     }
     const int sms = sm_count();
     if (sms <= 0) return GDN_ERR_CUDA;
-    const int64_t units = static_cast<int64_t>(N) * plan->H;
-    const int grid = static_cast<int>(units < sms ? units : sms);
-    if (gdn::launch_chunk_16bit(cp, tq, tk, tv, to, d.qkv_dtype == GDN_DTYPE_F16, grid, stream) != cudaSuccess)
+    const bool f16 = d.qkv_dtype == GDN_DTYPE_F16;
+    const int32_t H = plan->H;
+    const int64_t units = static_cast<int64_t>(N) * H;
+    const int P = cp_segments(plan, a, N, T, sms);
+    if (P < 2) {
+        const int grid = static_cast<int>(units < sms ? units : sms);
+        if (gdn::launch_chunk_16bit(cp, tq, tk, tv, to, f16, false, grid, stream) != cudaSuccess) return GDN_ERR_CUDA;
+        return GDN_OK;
+    }
+
+    // ---- context parallelism: segments, transfer pass, fp32 scan, segment pass, final states
+    const CpLayout& c = plan->cpl;
+    gdn::CpParams q{};
+    q.cu_seqlens = a.cu_seqlens;
+    q.cu_i64 = pp.cu_i64;
+    q.num_seqs = N;
+    q.H = H;
+    q.P = P;
+    q.align = n > 0 ? n : gdn::kChunk;
+    q.ckpt_n = n;
+    q.ckpt_cu_starts = a.checkpoint_cu_starts;
+    q.ckpt_i64 = pp.ckpt_i64;
+    q.seg_a = reinterpret_cast<int64_t*>(ws + c.seg_a);
+    q.order_a = reinterpret_cast<int32_t*>(ws + c.order_a);
+    q.counter_a = reinterpret_cast<int32_t*>(ws + c.counter_a);
+    q.cu_c = reinterpret_cast<int32_t*>(ws + c.cu_c);
+    q.ckpt_c = reinterpret_cast<int64_t*>(ws + c.ckpt_c);
+    q.trans = reinterpret_cast<const float*>(ws + c.trans);
+    q.start = reinterpret_cast<float*>(ws + c.start);
+    q.initial_state = cp.initial_state;
+    q.output_state = cp.output_state;
+    q.state = sl;
+    q.state_indices = pp.state_indices;
+    q.idx_i64 = pp.idx_i64;
+    q.status = status;
+    if (gdn::launch_cp_prepare(q, stream) != cudaSuccess) return GDN_ERR_CUDA;
+
+    gdn::StateLayout dense{};
+    dense.dtype = GDN_DTYPE_F32;
+    dense.s_v = gdn::kHead;
+    dense.s_head = static_cast<int64_t>(gdn::kHead) * gdn::kHead;
+    dense.s_row = dense.s_head * H;
+
+    gdn::ChunkParams ta = cp;  // transfer pass over segments 0 .. P-2
+    ta.num_seqs = N * (P - 1);
+    ta.seg = q.seg_a;
+    ta.seq_order = q.order_a;
+    ta.counter = q.counter_a;
+    ta.chunk_offsets = nullptr;
+    ta.initial_state = nullptr;
+    ta.output_state = ws + c.trans;
+    ta.state = dense;
+    ta.state_indices = nullptr;
+    ta.checkpoints = nullptr;
+    ta.ckpt_n = 0;
+    ta.intra_g = ta.intra_w = ta.intra_u = nullptr;
+    const int64_t units_a = 2 * static_cast<int64_t>(ta.num_seqs) * H;
+    if (gdn::launch_chunk_16bit(ta, tq, tk, tv, to, f16, true, static_cast<int>(units_a < sms ? units_a : sms),
+                                stream) != cudaSuccess)
         return GDN_ERR_CUDA;
+    if (gdn::launch_cp_fixup(q, stream) != cudaSuccess) return GDN_ERR_CUDA;
+
+    uint8_t* wsc = ws + c.prep;  // the segment pass: P segments per sequence as sequences of their own
+    const int32_t nc = N * P;
+    gdn::PrepareParams pc{};
+    pc.cu_seqlens = q.cu_c;
+    pc.cu_i64 = 0;
+    pc.num_seqs = nc;
+    pc.total_tokens = T;
+    pc.max_seqlen = 0;
+    pc.ckpt_n = n;
+    pc.ckpt_cu_starts = q.ckpt_c;
+    pc.ckpt_i64 = 1;
+    pc.num_checkpoints = a.num_checkpoints;
+    pc.status = status;
+    pc.counter = reinterpret_cast<int32_t*>(wsc + c.wc.counter);
+    pc.n_chunks = reinterpret_cast<int32_t*>(wsc + c.wc.n_chunks);
+    pc.chunk_offsets = reinterpret_cast<int32_t*>(wsc + c.wc.chunk_offsets);
+    pc.chunk_map = reinterpret_cast<int32_t*>(wsc + c.wc.chunk_map);
+    pc.max_chunks = (T + gdn::kChunk - 1) / gdn::kChunk + nc;
+    pc.seq_order = reinterpret_cast<int32_t*>(wsc + c.wc.seq_order);
+    pc.pool_bitmap = reinterpret_cast<uint32_t*>(wsc + c.wc.pool_bitmap);
+    pc.bitmap_words = 0;
+    pc.keep_status = 1;
+    if (gdn::launch_prepare(pc, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    gdn::ChunkParams sc = cp;
+    sc.cu_seqlens = q.cu_c;
+    sc.cu_i64 = 0;
+    sc.num_seqs = nc;
+    sc.initial_state = q.start;
+    sc.output_state = q.start;
+    sc.state = dense;
+    sc.state_indices = nullptr;
+    sc.ckpt_cu_starts = q.ckpt_c;
+    sc.ckpt_i64 = 1;
+    sc.counter = pc.counter;
+    sc.chunk_offsets = pc.chunk_offsets;
+    sc.seq_order = pc.seq_order;
+    const int64_t units_c = static_cast<int64_t>(nc) * H;
+    if (gdn::launch_chunk_16bit(sc, tq, tk, tv, to, f16, false, static_cast<int>(units_c < sms ? units_c : sms),
+                                stream) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (gdn::launch_cp_final(q, stream) != cudaSuccess) return GDN_ERR_CUDA;
     return GDN_OK;
 }
 

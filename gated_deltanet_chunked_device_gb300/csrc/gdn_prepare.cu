@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prepare_kernel(PrepareParams
 
     if (tid == 0) {
         s_err = 0;
-        *p.status = 0;  // the word describes this run only
+        if (!p.keep_status) *p.status = 0;  // the word describes this run only
         *p.counter = 0;
     }
     for (int w = tid; w < p.bitmap_words; w += kPrepThreads) p.pool_bitmap[w] = 0u;

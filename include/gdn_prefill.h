@@ -87,7 +87,14 @@ enum {
     GDN_FLAG_HAS_STATE_INDICES = 1u << 6,  /* initial/output state are pools addressed by state_indices */
     GDN_FLAG_CU_SEQLENS_I64 = 1u << 7,     /* cu_seqlens is int64 (else int32) */
     GDN_FLAG_STATE_INDICES_I64 = 1u << 8,  /* state_indices is int64 (else int32) */
-    GDN_FLAG_CHECKPOINT_STARTS_I64 = 1u << 9 /* checkpoint_cu_starts is int64 (else int32) */
+    GDN_FLAG_CHECKPOINT_STARTS_I64 = 1u << 9, /* checkpoint_cu_starts is int64 (else int32) */
+    /* Context parallelism inside the GPU: when a run has few (sequence, head)
+     * units (N*H at most half the SM count) the sequences are cut into
+     * segments whose start states come from a transfer pass and an fp32
+     * scan, so that more SMs share each sequence.  Same results within
+     * rounding; the plan's workspace grows by about 32 MiB.  Not used with
+     * fp32 q/k/v or when intra-chunk outputs are requested. */
+    GDN_FLAG_CONTEXT_PARALLEL = 1u << 10
 };
 
 /* Device status bits (gdn_prefill_read_status). */
@@ -151,6 +158,11 @@ typedef struct gdn_prefill_args {
      * F = ceil(T/64) + N rows. */
     float *intra_g, *intra_w, *intra_u;
 } gdn_prefill_args;
+
+/* Segments per sequence that a gdn_prefill_run of this plan uses for N
+ * sequences and T tokens (context parallelism; 0 = none, one pass over whole
+ * sequences).  Queries the current device's SM count; no launch. */
+int32_t gdn_prefill_cp_segments(gdn_prefill_plan_t plan, int32_t num_seqs, int64_t total_tokens);
 
 /* Validate `desc` and create a plan.  *workspace_bytes receives the device
  * workspace size gdn_prefill_run needs (16-byte aligned, caller allocated).

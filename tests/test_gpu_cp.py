@@ -1,0 +1,59 @@
+"""GPU parity of context parallelism inside the GPU (use_cp): a batch with few
+(sequence, head) units is cut into segments whose start states come from a
+transfer pass (each segment run from zero and, with U = 0, from the
+identity) and an fp32 scan, then the segments run as sequences of their own
+("FlashInfer GDN Prefill 完全指南", the CP routing of the API table).  Every
+case is checked against the fp64 sequential oracle: outputs, final states
+(pool rows in place, 16-bit states) and checkpoints, which must land where
+the unsegmented sequence puts them."""
+import pytest
+import torch
+
+import gated_deltanet_chunked_device_gb300 as gdn
+from gated_deltanet_chunked_device_gb300 import workloads as wl
+from gdn_testlib import check_against_oracle, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gdn.build()
+
+
+def _cp_segments(res, inp):
+    return gdn.lib().gdn_prefill_cp_segments(res["plan"].handle, len(inp["seq_lens"]), inp["T"])
+
+
+def test_cp_one_long_sequence_with_checkpoints():
+    w = wl.custom(seq_lens=[1500], hq=2, hk=2, hv=4, initial_state="dense", l2norm_in_kernel=True,
+                  qk_prenorm=False, checkpoint_every=128)
+    inp = wl.generate(w, seed=60)
+    res = run_gpu(to_device(inp), use_cp=True, return_plan=True)
+    assert _cp_segments(res, inp) >= 2
+    check_against_oracle(inp, res)
+
+
+def test_cp_pool_zero_length_and_short_sequences():
+    w = wl.custom(seq_lens=[700, 0, 5, 64, 333], hq=2, hk=2, hv=2, initial_state="pool", n_pool=9,
+                  l2norm_in_kernel=True, qk_prenorm=False, checkpoint_every=64)
+    inp = wl.generate(w, seed=61)
+    check_against_oracle(inp, run_gpu(to_device(inp), use_cp=True))
+
+
+@pytest.mark.parametrize("dtype,state_dtype", [(torch.float16, torch.float32), (torch.bfloat16, torch.bfloat16)])
+def test_cp_input_and_state_types(dtype, state_dtype):
+    w = wl.custom(seq_lens=[900, 260], hq=4, hk=2, hv=2, dtype=dtype, initial_state="dense", alpha="exp_softplus16")
+    inp = wl.generate(w, seed=62)
+    inp["initial_state"] = inp["initial_state"].to(state_dtype)
+    check_against_oracle(inp, run_gpu(to_device(inp), use_cp=True))
+
+
+def test_cp_steep_gates_and_zero_initial_state():
+    # strong decay: the segment transfers are close to zero and the pairwise decay path runs
+    w = wl.custom(seq_lens=[640, 130], hq=1, hk=1, hv=2, alpha="u(0.05,0.3)", l2norm_in_kernel=True,
+                  qk_prenorm=False)
+    inp = wl.generate(w, seed=63)
+    check_against_oracle(inp, run_gpu(to_device(inp), use_cp=True))
