@@ -200,7 +200,7 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside)}
 
 
-def make_call(inp, device):
+def make_call(inp, device, use_cp=False):
     """Device buffers and C-ABI arguments for one prefill of `inp`."""
     d = {k: (v.to(device).contiguous() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     T, H = inp["T"], inp["H"]
@@ -214,7 +214,7 @@ def make_call(inp, device):
               use_qk_l2norm_in_kernel=inp["use_qk_l2norm_in_kernel"], output=out,
               initial_state=d.get("initial_state"), output_final_state=inp["output_final_state"], output_state=fin,
               state_indices=d.get("state_indices"), checkpoint_every_n_tokens=n,
-              checkpoint_cu_starts=d.get("checkpoint_cu_starts"), state_checkpoints=ck)
+              checkpoint_cu_starts=d.get("checkpoint_cu_starts"), state_checkpoints=ck, use_cp=use_cp)
     if d.get("state_indices") is not None:
         kw["output_state"] = d["initial_state"]
     # One eager call builds the plan and the workspace, and checks the device status.
@@ -429,6 +429,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--op", choices=["prefill", "decode"], default="prefill")
+    ap.add_argument("--cp", action="store_true", help="allow context parallelism (few (sequence, head) units)")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.op == "decode" and args.workload == wl.BENCH_WORKLOAD:
@@ -455,8 +456,9 @@ def main():
         if rank == 0:
             run_decode_bench(args, w, inp, device)
         return
-    call = make_call(inp, device)
+    call = make_call(inp, device, use_cp=args.cp)
     plan, ws, cargs = call["plan"], call["ws"], call["args"]
+    cp_segments = int(gdn.lib().gdn_prefill_cp_segments(plan.handle, len(inp["seq_lens"]), inp["T"])) if args.cp else 0
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.Stream(device)
     sp = stream.cuda_stream
@@ -578,15 +580,21 @@ def main():
     line = {
         "metric": METRIC, "value": job_tokens_per_s(world, T, ms_per_step), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(w, inp, args),
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(workload_config(w, inp, args), context_parallel_segments=cp_segments),
         "tflops": {"dense_tile_count": tflops_dense, "triangular_aware": tflops_tri,
                    "pct_of_bf16_peak": 100 * tflops_dense / bf16, "peak_tflops": bf16, "peak_source": src},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": traffic, "kernel": "gdn_chunk_kernel<__nv_bfloat16>", "kernel_ms": chunk_avg_ms,
+                     "traffic": traffic if not cp_segments else None,
+                     "kernel": ("gdn_chunk_kernel<__nv_bfloat16>" if not cp_segments
+                                else "chunk stage with context parallelism (transfer pass, scan, segment pass)"),
+                     "kernel_ms": chunk_avg_ms,
                      "algorithmic_bytes": abytes, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
                      if src == "measured" else "fallback 6800 GB/s",
                      "step_frac_of_roofline_time": roof_time / (ms_per_step / 1e3)},
-        "gpu_launches": 2 * K,
+        # prepare + chunk kernel; with context parallelism the chunk stage is cp_prepare, the transfer
+        # pass, the scan, the segment prepare, the segment pass and (with a final state) the state copy
+        "gpu_launches": K * ((6 + (1 if inp["output_final_state"] else 0)) if cp_segments else 2),
         "wall_s_timed_region": wall,
         "step_ms_stats": {"mean": sum(step_ms) / K, "median": statistics.median(step_ms), "min": min(step_ms),
                           "max": max(step_ms), "unflushed_mean": unflushed_ms, "unflushed_steps": Ku},
