@@ -110,8 +110,9 @@ __device__ __forceinline__ void load_token(const DecodeParams& p, int64_t tok, i
     x.b = p.beta ? p.beta[gi] : 1.f;
 }
 
-// This thread's 16 state values of unit u (sequence u / H, head u % H); false when its pool row is out of
-// range (then the unit is skipped and flagged).
+// This thread's 16 state values of unit u (sequence u / H, head u % H), states of element type SD; false
+// when its pool row is out of range (then the unit is skipped and flagged).
+template <typename SD>
 __device__ __forceinline__ bool load_state(const DecodeParams& p, int64_t u, int v0, int c0, float (&S)[4][4],
                                            int64_t& sbase) {
     const int32_t seq = static_cast<int32_t>(u / p.H), h = static_cast<int32_t>(u % p.H);
@@ -124,7 +125,7 @@ __device__ __forceinline__ bool load_state(const DecodeParams& p, int64_t u, int
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         if (p.initial_state) {
-            state_load4(p.initial_state, sbase + r * p.state.s_v, p.state.dtype, S[r]);
+            load4(static_cast<const SD*>(p.initial_state) + sbase + r * static_cast<int32_t>(p.state.s_v), S[r]);
         } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j) S[r][j] = 0.f;
@@ -138,7 +139,7 @@ __device__ __forceinline__ bool load_state(const DecodeParams& p, int64_t u, int
 // current unit's arithmetic; with several, the next token's inputs are loaded
 // before the current token's arithmetic instead (the registers hold one of the
 // two prefetches, not both).  Either way memory latency overlaps work.
-template <typename T, bool kNextUnit>
+template <typename T, typename SD, bool kNextUnit>
 __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const DecodeParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int v0 = 4 * warp, c0 = 4 * lane;
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const DecodePar
     int64_t u = blockIdx.x;
     float Sn[4][4];
     int64_t sbase_n = 0;
-    bool ok_n = kNextUnit && u < units && load_state(p, u, v0, c0, Sn, sbase_n);
+    bool ok_n = kNextUnit && u < units && load_state<SD>(p, u, v0, c0, Sn, sbase_n);
     for (; u < units; u += gridDim.x) {
         float S[4][4];
         int64_t sbase;
@@ -159,9 +160,9 @@ __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const DecodePar
             sbase = sbase_n;
             ok = ok_n;
             const int64_t un = u + gridDim.x;
-            if (un < units) ok_n = load_state(p, un, v0, c0, Sn, sbase_n);
+            if (un < units) ok_n = load_state<SD>(p, un, v0, c0, Sn, sbase_n);
         } else {
-            ok = load_state(p, u, v0, c0, S, sbase);
+            ok = load_state<SD>(p, u, v0, c0, S, sbase);
         }
         if (!ok) {  // uniform over the CTA: nothing is read or written for this unit
             if (threadIdx.x == 0 && p.status) atomicOr(p.status, static_cast<int32_t>(GDN_DEVICE_ERR_STATE_INDEX_RANGE));
@@ -205,15 +206,22 @@ __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const DecodePar
         if (p.output_state) {
 #pragma unroll
             for (int r = 0; r < 4; ++r)
-                state_store4(p.output_state, sbase + r * p.state.s_v, p.state.dtype, S[r]);
+                store4(static_cast<SD*>(p.output_state) + sbase + r * static_cast<int32_t>(p.state.s_v), S[r]);
         }
     }
 }
 
+template <typename T, typename SD>
+void launch_decode_ts(const DecodeParams& p, unsigned grid, cudaStream_t stream) {
+    if (p.m == 1) gdn_decode_kernel<T, SD, true><<<grid, kDecThreads, 0, stream>>>(p);
+    else gdn_decode_kernel<T, SD, false><<<grid, kDecThreads, 0, stream>>>(p);
+}
+
 template <typename T>
 void launch_decode_t(const DecodeParams& p, unsigned grid, cudaStream_t stream) {
-    if (p.m == 1) gdn_decode_kernel<T, true><<<grid, kDecThreads, 0, stream>>>(p);
-    else gdn_decode_kernel<T, false><<<grid, kDecThreads, 0, stream>>>(p);
+    if (p.state.dtype == GDN_DTYPE_BF16) launch_decode_ts<T, __nv_bfloat16>(p, grid, stream);
+    else if (p.state.dtype == GDN_DTYPE_F16) launch_decode_ts<T, __half>(p, grid, stream);
+    else launch_decode_ts<T, float>(p, grid, stream);
 }
 
 }  // namespace
