@@ -16,7 +16,9 @@ textbook computation:
 * chunked form == per-token form, checkpoints == truncated runs, resume,
   pool routing, head mapping by explicit head expansion, L2 norm, defaults;
 * the chunk intermediates W and U against the delta-rule residual
-  beta_i (v_i - alpha_i S_{i-1} k_i) obtained from truncated per-token runs.
+  beta_i (v_i - alpha_i S_{i-1} k_i) obtained from truncated per-token runs;
+* the segment transfer (S_end = S0 M + N, N from zero, M from the identity
+  with v = 0) that context parallelism relies on.
 """
 import os
 
@@ -257,6 +259,32 @@ def test_state_is_affine_in_initial_state():
     for key in ("final_state", "output"):
         lin = 2 * (fx[key] - z[key]) - 3 * (fy[key] - z[key])
         np.testing.assert_allclose(fxy[key] - z[key], lin, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("split", [64, 128, 200])
+def test_segment_transfer_from_zero_and_identity(split):
+    # The segment decomposition behind context parallelism ("GDN与线性注意力GPU并行实现", section 5): over
+    # the segment [0, split) the state map is S_end = S0 M + N, where N is the segment run from zero and M
+    # the run from the identity with v = 0; the rest of the sequence then continues from S0 M + N.
+    rng = np.random.default_rng(12)
+    L = 300
+    q, k, v, g, b, cu = _rand_inputs(rng, [L], D=8)
+    S0 = rng.standard_normal((1, 1, 8, 8))
+    seg = slice(0, split)
+    one = np.array([0, split], dtype=np.int64)
+    run = lambda vv, s0: oracle.gdn_sequential(q[seg], k[seg], vv, g[seg], b[seg], one, initial_state=s0,
+                                               output_final_state=True)["final_state"]
+    N = run(v[seg], np.zeros_like(S0))[0, 0]
+    M = run(np.zeros_like(v[seg]), np.eye(8)[None, None])[0, 0]
+    whole = oracle.gdn_sequential(q, k, v, g, b, cu, initial_state=S0, output_final_state=True)
+    head = oracle.gdn_sequential(q[seg], k[seg], v[seg], g[seg], b[seg], one, initial_state=S0,
+                                 output_final_state=True)
+    np.testing.assert_allclose(head["final_state"][0, 0], S0[0, 0] @ M + N, rtol=1e-11, atol=1e-12)
+    rest = slice(split, L)
+    tail = oracle.gdn_sequential(q[rest], k[rest], v[rest], g[rest], b[rest], np.array([0, L - split]),
+                                 initial_state=(S0[0, 0] @ M + N)[None, None], output_final_state=True)
+    np.testing.assert_allclose(tail["output"], whole["output"][rest], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(tail["final_state"], whole["final_state"], rtol=1e-10, atol=1e-12)
 
 
 # ---------------------------------------------------------------------------
