@@ -71,6 +71,7 @@ constexpr int kThreads = 640;
 constexpr int kStateThreads = 256;  // two state warpgroups
 constexpr int kIntraThreads = 256;  // two intra warpgroups
 constexpr uint32_t kBarIntra = 1, kBarState = 2;  // named barrier ids
+constexpr uint32_t kBarInverse = 3;               // the first four intra warps, inside the inverse
 
 // ---- shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t kKQ = 0;           // 3 stages x 32 KB: K_h0 | Q_h0 | K_h1 | Q_h1 (64 rows x 128 B each)
@@ -313,27 +314,24 @@ __device__ __forceinline__ void tri_inverse_64(float* __restrict__ A, uint8_t* _
             *reinterpret_cast<float4*>(z) = make_float4(0.f, 0.f, 0.f, 0.f);
             *reinterpret_cast<float4*>(z + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        __syncwarp();
-        // ---- T_10 = -T_11 (A_10 T_00) inside the warp's 32 x 32 block
-        const int b0 = 32 * wi, b1 = b0 + 16;
-        float* xs = X1 + wi * 16 * kLdX1;
+    }
+    if (wi < 4) {
+        // ---- T_10 = -T_11 (A_10 T_00) of the two 32 x 32 blocks: warp wi takes block wi / 2, output columns
+        //      8 (wi % 2) .. + 7, so the four warps run the products side by side
+        named_bar_sync(kBarInverse, 128);  // the diagonal blocks are in place
+        const int b0 = 32 * (wi >> 1), b1 = b0 + 16, nt = (wi & 1) * 8;
+        float* xs = X1 + (wi >> 1) * 16 * kLdX1;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int nt = 0; nt < 16; nt += 8) {
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k0 = 0; k0 < 16; k0 += 8)
+            mma_tf32_16x8x8(d, A + b1 * kLd + b0 + k0, kLd, A + (b0 + k0) * kLd + b0 + nt, kLd, lane);
+        store_tile_16x8(xs + nt, kLdX1, d, 1.f, lane);
+        named_bar_sync(kBarInverse, 128);  // every read of A_10 is done before T_10 replaces it
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int k0 = 0; k0 < 16; k0 += 8)
-                mma_tf32_16x8x8(d, A + b1 * kLd + b0 + k0, kLd, A + (b0 + k0) * kLd + b0 + nt, kLd, lane);
-            store_tile_16x8(xs + nt, kLdX1, d, 1.f, lane);
-        }
-        __syncwarp();
-#pragma unroll
-        for (int nt = 0; nt < 16; nt += 8) {
-            float e[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int k0 = 0; k0 < 16; k0 += 8)
-                mma_tf32_16x8x8(e, A + b1 * kLd + b1 + k0, kLd, xs + k0 * kLdX1 + nt, kLdX1, lane);
-            store_tile_16x8(A + b1 * kLd + b0 + nt, kLd, e, -1.f, lane);
-        }
+        for (int k0 = 0; k0 < 16; k0 += 8)
+            mma_tf32_16x8x8(e, A + b1 * kLd + b1 + k0, kLd, xs + k0 * kLdX1 + nt, kLdX1, lane);
+        store_tile_16x8(A + b1 * kLd + b0 + nt, kLd, e, -1.f, lane);
     }
     named_bar_sync(kBarIntra, kIntraThreads);
     // ---- stage 2: X = A_21 T_11 (one 16 x 8 tile per warp) and the diagonal 32 x 32 blocks of T' and T''
