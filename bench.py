@@ -586,7 +586,7 @@ def main():
                    "pct_of_bf16_peak": 100 * tflops_dense / bf16, "peak_tflops": bf16, "peak_source": src},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": traffic if not cp_segments else None,
-                     "kernel": ("gdn_chunk_kernel<__nv_bfloat16>" if not cp_segments
+                     "kernel": ("gdn_chunk_kernel<__nv_bfloat16, false>" if not cp_segments
                                 else "chunk stage with context parallelism (transfer pass, scan, segment pass)"),
                      "kernel_ms": chunk_avg_ms,
                      "algorithmic_bytes": abytes, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
