@@ -458,7 +458,7 @@ def main():
         return
     call = make_call(inp, device, use_cp=args.cp)
     plan, ws, cargs = call["plan"], call["ws"], call["args"]
-    cp_segments = int(gdn.lib().gdn_prefill_cp_segments(plan.handle, len(inp["seq_lens"]), inp["T"])) if args.cp else 0
+    cp_segments = int(gdn.lib().gdn_prefill_cp_segments(plan.handle, len(inp["seq_lens"]), inp["T"], 0)) if args.cp else 0
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.Stream(device)
     sp = stream.cuda_stream

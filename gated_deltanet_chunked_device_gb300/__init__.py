@@ -127,7 +127,7 @@ def lib():
                 L.gdn_prefill_workspace_layout.argtypes = [ctypes.c_void_p, ctypes.POINTER(Layout)]
                 L.gdn_prefill_workspace_layout.restype = ctypes.c_int
                 L.gdn_prefill_plan_destroy.argtypes = [ctypes.c_void_p]
-                L.gdn_prefill_cp_segments.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64]
+                L.gdn_prefill_cp_segments.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32]
                 L.gdn_prefill_cp_segments.restype = ctypes.c_int32
                 L.gdn_prefill_plan_destroy.restype = None
                 L.gdn_status_string.argtypes = [ctypes.c_int]

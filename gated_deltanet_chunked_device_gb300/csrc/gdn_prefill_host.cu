@@ -243,9 +243,10 @@ gdn_status gdn_prefill_plan(const gdn_prefill_desc* desc, gdn_prefill_plan_t* pl
 
 void gdn_prefill_plan_destroy(gdn_prefill_plan_t plan) { delete plan; }
 
-int32_t gdn_prefill_cp_segments(gdn_prefill_plan_t plan, int32_t num_seqs, int64_t total_tokens) {
+int32_t gdn_prefill_cp_segments(gdn_prefill_plan_t plan, int32_t num_seqs, int64_t total_tokens,
+                                int32_t sm_count_hint) {
     if (!plan) return 0;
-    const int sms = sm_count();
+    const int sms = sm_count_hint > 0 ? sm_count_hint : sm_count();
     if (sms <= 0) return 0;
     gdn_prefill_args a{};
     return cp_segments(plan, a, num_seqs, total_tokens, sms);

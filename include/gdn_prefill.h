@@ -161,8 +161,10 @@ typedef struct gdn_prefill_args {
 
 /* Segments per sequence that a gdn_prefill_run of this plan uses for N
  * sequences and T tokens (context parallelism; 0 = none, one pass over whole
- * sequences).  Queries the current device's SM count; no launch. */
-int32_t gdn_prefill_cp_segments(gdn_prefill_plan_t plan, int32_t num_seqs, int64_t total_tokens);
+ * sequences) on a GPU with sm_count_hint SMs, or on the current device when
+ * sm_count_hint <= 0 (then it queries the device).  No launch. */
+int32_t gdn_prefill_cp_segments(gdn_prefill_plan_t plan, int32_t num_seqs, int64_t total_tokens,
+                                int32_t sm_count_hint);
 
 /* Validate `desc` and create a plan.  *workspace_bytes receives the device
  * workspace size gdn_prefill_run needs (16-byte aligned, caller allocated).

@@ -78,6 +78,38 @@ def test_plan_validation(L, kw, expect):
         assert not plan.value
 
 
+_CP = gdn.FLAGS["CONTEXT_PARALLEL"]
+
+
+@pytest.mark.parametrize("desc_kw,N,T,sms,expect", [
+    (dict(flags=_CP), 1, 32768, 152, 3),                                  # 32 state heads: 3 segments fill 152 SMs
+    (dict(flags=_CP), 8, 33408, 152, 0),                                  # 256 units: one pass
+    (dict(flags=_CP, num_q_heads=1, num_k_heads=1, num_v_heads=1), 1, 5000, 152, 8),  # capped at 8 segments
+    (dict(flags=_CP, num_q_heads=4, num_k_heads=4, num_v_heads=4), 2, 1000, 152, 8),
+    (dict(flags=_CP, num_q_heads=64, num_k_heads=16, num_v_heads=16), 1, 1000, 152, 2),
+    (dict(flags=_CP, num_q_heads=128, num_k_heads=16, num_v_heads=16), 1, 1000, 1024, 2),  # scratch bound
+    ({}, 1, 32768, 152, 0),                                               # the plan does not allow it
+    (dict(flags=_CP, qkv_dtype=gdn.DTYPE_F32), 1, 1000, 152, 0),          # fp32 inputs: one pass
+    (dict(flags=_CP), 1, 0, 152, 0),                                      # no tokens
+])
+def test_context_parallel_segment_choice(L, desc_kw, N, T, sms, expect):
+    st, plan, nbytes = gdn.gdn_prefill_plan(_desc(**desc_kw))
+    assert st == OK
+    try:
+        assert L.gdn_prefill_cp_segments(plan, N, T, sms) == expect
+    finally:
+        gdn.gdn_prefill_plan_destroy(plan)
+
+
+def test_context_parallel_plan_reserves_its_scratch(L):
+    st, p0, base = gdn.gdn_prefill_plan(_desc())
+    st1, p1, with_cp = gdn.gdn_prefill_plan(_desc(flags=_CP))
+    assert st == OK and st1 == OK
+    gdn.gdn_prefill_plan_destroy(p0)
+    gdn.gdn_prefill_plan_destroy(p1)
+    assert with_cp >= base + 2 * 256 * 128 * 128 * 4  # transfer and start planes, fp32
+
+
 def _valid_args(**kw):
     # fake, 256-byte aligned device addresses: never dereferenced, because every
     # case below is rejected (or needs no launch) before the first CUDA call

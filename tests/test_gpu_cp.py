@@ -24,7 +24,7 @@ def _built():
 
 
 def _cp_segments(res, inp):
-    return gdn.lib().gdn_prefill_cp_segments(res["plan"].handle, len(inp["seq_lens"]), inp["T"])
+    return gdn.lib().gdn_prefill_cp_segments(res["plan"].handle, len(inp["seq_lens"]), inp["T"], 0)
 
 
 def test_cp_one_long_sequence_with_checkpoints():
