@@ -88,12 +88,15 @@ enum {
     GDN_FLAG_CU_SEQLENS_I64 = 1u << 7,     /* cu_seqlens is int64 (else int32) */
     GDN_FLAG_STATE_INDICES_I64 = 1u << 8,  /* state_indices is int64 (else int32) */
     GDN_FLAG_CHECKPOINT_STARTS_I64 = 1u << 9, /* checkpoint_cu_starts is int64 (else int32) */
-    /* Context parallelism inside the GPU: when a run has few (sequence, head)
-     * units (N*H at most half the SM count) the sequences are cut into
-     * segments whose start states come from a transfer pass and an fp32
-     * scan, so that more SMs share each sequence.  Same results within
-     * rounding; the plan's workspace grows by about 32 MiB.  Not used with
-     * fp32 q/k/v or when intra-chunk outputs are requested. */
+    /* Context parallelism inside the GPU ("FlashInfer GDN Prefill 完全指南",
+     * the use_cp row of the API table; the per-segment transfer and boundary
+     * scan of "GDN与线性注意力GPU并行实现", section 5): when a run has few
+     * (sequence, head) units (N*H at most half the SM count) the sequences
+     * are cut into segments whose start states come from a transfer pass and
+     * an fp32 scan, so that more SMs share each sequence.  Same results
+     * within rounding; the plan's workspace grows by about 32 MiB.  Not used
+     * with fp32 q/k/v or when intra-chunk outputs are requested
+     * (gdn_prefill_cp_segments reports the choice). */
     GDN_FLAG_CONTEXT_PARALLEL = 1u << 10
 };
 
@@ -113,7 +116,8 @@ typedef struct gdn_prefill_desc {
     int32_t num_q_heads, num_k_heads, num_v_heads; /* HQ, HK, HV */
     int32_t head_size;                             /* must be 128 */
     gdn_dtype qkv_dtype;                           /* q, k, v and output: BF16, F16 or F32 */
-    gdn_dtype state_dtype;                         /* initial / output states: F32, BF16 or F16 (checkpoints: F32) */
+    gdn_dtype state_dtype;                         /* initial / output states: F32, BF16 or F16, widened to fp32
+                                                      on load and rounded to nearest on store (checkpoints: F32) */
     int64_t max_total_tokens;                      /* upper bound of T over the plan's runs */
     int32_t max_num_seqs;                          /* upper bound of N */
     int32_t max_pool_rows;                         /* upper bound of n_pool (0 without state_indices) */
