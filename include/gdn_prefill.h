@@ -1,7 +1,7 @@
 /*
  * gdn_prefill.h -- C ABI of the chunked Gated DeltaNet prefill on one GB300 GPU.
  *
- * The operation (north-star form; "FlashInfer GDN Prefill 完全指南", section
+ * The operation ("FlashInfer GDN Prefill 完全指南", section
  * "chunk_gated_delta_rule API 全参数解析" gives the arguments, and
  * "GDN 与 Chunked Prefill", sections "GDN 是什么" and "块内 state 和块间 final
  * state", the recurrence and the read after the update): for every sequence i

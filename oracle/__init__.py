@@ -10,7 +10,7 @@ arrays through ctypes.  What each entry point computes, and which passage of
 the pages it follows, is stated in the C file's header:
 
 * :func:`gdn_sequential` -- the per-token gated delta rule recurrence
-  ("GDN 与 Chunked Prefill", section "GDN 是什么"; the spec form
+  ("GDN 与 Chunked Prefill", section "GDN 是什么": the decaying form
   S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T, o_t = scale S_t q_t).
 * :func:`gdn_chunked` -- the same result through the 64-token chunk algebra
   (log-space gate sums, triangular solve, W/U, Delta, chunk output, state
