@@ -1,7 +1,7 @@
 // gdn_cp.cu -- context parallelism inside one GPU for batches with few
 // (sequence, head) units ("FlashInfer GDN Prefill 完全指南", the CP routing and
 // max_seqlen rows of the API table; "GDN与线性注意力GPU并行实现", the
-// segment-transfer discussion of section 5).
+// per-block transfer (M, N) and the scan over the blocks of section 3.3).
 //
 // Each sequence is cut into P segments of Ls tokens (Ls a multiple of 64, or
 // of the checkpoint interval).  Over one segment the chunk recurrence is

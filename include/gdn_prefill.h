@@ -90,7 +90,7 @@ enum {
     GDN_FLAG_CHECKPOINT_STARTS_I64 = 1u << 9, /* checkpoint_cu_starts is int64 (else int32) */
     /* Context parallelism inside the GPU ("FlashInfer GDN Prefill 完全指南",
      * the use_cp row of the API table; the per-segment transfer and boundary
-     * scan of "GDN与线性注意力GPU并行实现", section 5): when a run has few
+     * scan of "GDN与线性注意力GPU并行实现", section 3.3): when a run has few
      * (sequence, head) units (N*H at most half the SM count) the sequences
      * are cut into segments whose start states come from a transfer pass and
      * an fp32 scan, so that more SMs share each sequence.  Same results

@@ -263,7 +263,7 @@ def test_state_is_affine_in_initial_state():
 
 @pytest.mark.parametrize("split", [64, 128, 200])
 def test_segment_transfer_from_zero_and_identity(split):
-    # The segment decomposition behind context parallelism ("GDN与线性注意力GPU并行实现", section 5): over
+    # The segment decomposition behind context parallelism ("GDN与线性注意力GPU并行实现", section 3.3): over
     # the segment [0, split) the state map is S_end = S0 M + N, where N is the segment run from zero and M
     # the run from the identity with v = 0; the rest of the sequence then continues from S0 M + N.
     rng = np.random.default_rng(12)
