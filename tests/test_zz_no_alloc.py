@@ -85,3 +85,19 @@ def test_static_workspace_refuses_plans_larger_than_the_array():
         assert gdn.gdn_prefill_run_static(plan, args, 0) == 2  # GDN_ERR_UNSUPPORTED, before any launch
     finally:
         gdn.gdn_prefill_plan_destroy(plan)
+
+
+def test_static_workspace_refuses_context_parallel_plans():
+    # a plan that allows context parallelism needs its segment scratch (tens of MiB): the static entry
+    # refuses it before any launch, as any plan above the array
+    gdn.build()
+    desc = gdn.Desc(num_q_heads=4, num_k_heads=4, num_v_heads=4, head_size=128, qkv_dtype=gdn.DTYPE_BF16,
+                    state_dtype=gdn.DTYPE_F32, max_total_tokens=1 << 12, max_num_seqs=4, max_pool_rows=0,
+                    checkpoint_every_n_tokens=0, flags=gdn.FLAGS["CONTEXT_PARALLEL"])
+    st, plan, nbytes = gdn.gdn_prefill_plan(desc)
+    assert st == 0 and nbytes > (1 << 20)
+    try:
+        args = gdn.Args(num_seqs=1, total_tokens=64)
+        assert gdn.gdn_prefill_run_static(plan, args, 0) == 2  # GDN_ERR_UNSUPPORTED, before any launch
+    finally:
+        gdn.gdn_prefill_plan_destroy(plan)
