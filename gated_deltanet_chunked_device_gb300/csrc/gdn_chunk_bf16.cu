@@ -59,6 +59,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "gdn_internal.cuh"
@@ -78,10 +79,11 @@ constexpr uint32_t kKQ = 0;           // 3 stages x 32 KB: K_h0 | Q_h0 | K_h1 | 
 constexpr uint32_t kKQStage = 32768;
 constexpr uint32_t kKQStages = 3;
 constexpr uint32_t kV = 98304;        // V_h0 | V_h1
-constexpr uint32_t kTp = 114688;      // T' = T diag(beta gamma rn^2) bf16 [64 i][64 j] K-major
+constexpr uint32_t kTp = 114688;      // T' = T diag(beta gamma rn^2) bf16 [64 i][64 j] K-major, chunks n % 2 == 0
 constexpr uint32_t kTpp = 122880;     // T'' = T diag(beta rn)
 constexpr uint32_t kPb = 131072;      // 2 x P bf16 [64 i][64 j] K-major
-constexpr uint32_t kWb = 147456;      // W^T bf16 as MN-major B: [128 k][64 i]
+constexpr uint32_t kTp1 = 147456;     // T' of chunks n % 2 == 1
+constexpr uint32_t kSpare = 155648;   // 8 KB, unused
 constexpr uint32_t kAbuf = 163840;    // A, then T in place: fp32 [64][kLd]
 constexpr uint32_t kXs = 181248;      // inverse scratch: [2][16][24] then [32][40] fp32
 constexpr uint32_t kBars = 189440;    // up to 64 mbarriers
@@ -93,42 +95,52 @@ constexpr uint32_t kSmemBytes = 222208;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 constexpr int kLd = 68;               // fp32 row stride of A and T (bank-conflict free rows)
 
-// gbuf field offsets (floats), one 64-vector each, per chunk:
+// gbuf field offsets (floats), one 64-vector each, per chunk (n, m = 1/|k|, 1/|q| under the L2 norm, else 1).
+// The gates warp writes them with n = m = 1; under the L2 norm the intra warps that hold the K K^T diagonal
+// put n into rn, cw and bn (before the inverse reads them), and the gates warp later puts m into rm (RM_FULL):
 //   G      running sum of log alpha            gamma  e^G
-//   beta   beta (0 on padded rows)             rn     1/|k_j| (1 without the L2 norm; written by the
-//                                                      intra warps that hold the K K^T diagonal)
-//   rm     output row factor: 1/|q_i| (1 without the L2 norm), times gamma_i when Q is kept as stored
-//   cw     beta_j gamma_j (T' columns, times rn_j^2)
-//   dec    e^{G_63 - G_j} (decayed Delta)      rp     P row factor: 1/gamma_i when Q is kept, else 1
-//   ra     beta_i (A rows, times rn_i^2)       colf   e^{G_16b - G_j}, b = j / 16
-//   rowf   [4][64] e^{G_i - G_16b} (i >= 16 b, else 0)
-//   safe   1 when the chunk's G range is small enough for e^{G_i - G_j} = rowf * colf
+//   beta   beta (0 on padded rows)             rn     n_j (0 on padded rows under the norm)
+//   rm     output row factor m_i, times gamma_i when Q is kept as stored (0 on padded rows under the norm)
+//   cw     beta_j gamma_j n_j^2 (T' columns)   bn     beta_j n_j (T'' columns)
+//   dec    e^{G_63 - G_j} (decayed Delta)      ra     A row factor beta_i n_i^2 e^{G_i - Gref}
+//   rp     P row factor e^{G_i - Gref}, over gamma_i when Q is kept as stored
+//   colf   e^{Gref - G_j}, Gref = (G_0 + G_63) / 2, so that e^{G_i - G_j} = (row factor) (colf) while the
+//          chunk's G range is below kSafeRange
+//   safe   1 when it is; else A and P take e^{G_i - G_j} pairwise
 //   keepq  1 when every G_i of the chunk lies in [-8, 8]: Q stays as stored (no Q' pass)
 constexpr int kGG = 0, kGGam = 64, kGBeta = 128, kGRn = 192, kGRm = 256, kGCw = 320, kGDec = 384, kGRp = 448,
-              kGRa = 512, kGColf = 576, kGRowf = 640, kGSafe = 896, kGKeepQ = 897, kGFloats = 912;
+              kGRa = 512, kGColf = 576, kGBn = 640, kGSafe = 704, kGKeepQ = 705, kGFloats = 720;
+constexpr float kSafeRange = 80.f;  // e^{+-40} factors stay well inside fp32
 constexpr float kKeepQRange = 8.f;  // bf16 only: fp16 would overflow on e^8 (q.k) with raw q and k
 static_assert(kGbuf >= kMisc + 64 && kGbuf + 3 * kGFloats * 4 <= kOutT && kOutT + 16384 == kSmemBytes,
               "shared memory map overlaps");
 static_assert(kXs + 4 * (2 * 16 * 24 + 32 * 40) <= kBars && kMisc + 64 <= kOutT, "scratch / barrier block overlap");
-static_assert(kKQ + kKQStages * kKQStage == kV && kV + 16384 == kTp && kWb + 16384 == kAbuf, "tile block overlap");
+static_assert(kKQ + kKQStages * kKQStage == kV && kV + 16384 == kTp && kTp1 + 8192 == kSpare &&
+                  kSpare + 8192 == kAbuf,
+              "tile block overlap");
 
-// ---- barriers
+// ---- barriers (single ones are safe where no waiter can fall two phases behind; see the roles)
 enum {
     B_KQ_FULL = 0 /* 3 */, B_KQ_EMPTY = 3 /* 3 */, B_V_FULL = 6, B_V_EMPTY = 7, B_D1_FULL = 8, B_D1_EMPTY = 9,
-    B_T_FULL = 10, B_WU_FULL = 11, B_WB_FULL = 12 /* 2 */, B_SB_FULL = 14 /* 2 */, B_DELTA_FULL = 16 /* 2 */,
+    B_T_FULL = 10 /* 2 */, B_U_FULL = 12 /* 2 */, B_SB_FULL = 14 /* 2 */, B_DELTA_FULL = 16 /* 2 */,
     B_DD_FULL = 18 /* 2 */, B_S_FULL = 20 /* 2 */, B_O_EMPTY = 22 /* 2 */, B_GATES_FULL = 24 /* 3 */,
     B_GATES_EMPTY = 27 /* 3 */, B_UNIT_FULL = 30 /* 2 */, B_UNIT_EMPTY = 32 /* 2 */, B_DRAIN_I = 34, B_DRAIN_S = 35,
-    B_COUNT = 36
+    B_XO_FULL = 36, B_XB_FULL = 37, B_O_FULL = 38, B_Q_READY = 39 /* 2 */, B_RM_FULL = 41 /* 3 */, B_COUNT = 44
 };
 
 // ---- TMEM columns
-// S fp32 | Delta 2 x 64 | W | D1 | O (S Q'^T + Delta^T P^T) | S as packed bf16 pairs (A operand)
-constexpr uint32_t kTmS = 0, kTmDelta = 128, kTmW = 256, kTmD1 = 320, kTmO = 384, kTmSbf = 448;
+// S fp32 | Delta 2 x 64 | X = S K^T | O (S Q'^T + Delta^T P^T) | D1 | S as packed bf16 pairs (A operand), which
+// holds X as packed bf16 pairs between the X product and the Delta product (S is not read there)
+constexpr uint32_t kTmS = 0, kTmDelta = 128, kTmX = 256, kTmO = 320, kTmD1 = 384, kTmSbf = 448;
+constexpr uint32_t kTmXbf = kTmSbf;
 constexpr uint32_t kTmCols = 512;
+static_assert(kTmO == kTmX + 64, "X and O are one N = 128 accumulator");
 
 template <bool kF16> constexpr uint32_t kIdescD1 = idesc_16bit_f32(128, 64, false, false, false, kF16);
-template <bool kF16> constexpr uint32_t kIdescWU = idesc_16bit_f32(128, 64, true, false, false, kF16);
-template <bool kF16> constexpr uint32_t kIdescDelta = idesc_16bit_f32(128, 64, false, true, true, kF16);
+template <bool kF16> constexpr uint32_t kIdescU = idesc_16bit_f32(128, 64, true, false, false, kF16);
+template <bool kF16> constexpr uint32_t kIdescXO = idesc_16bit_f32(128, 128, false, false, false, kF16);
+template <bool kF16> constexpr uint32_t kIdescX = idesc_16bit_f32(128, 64, false, false, false, kF16);
+template <bool kF16> constexpr uint32_t kIdescDelta = idesc_16bit_f32(128, 64, false, false, true, kF16);
 template <bool kF16> constexpr uint32_t kIdescO = idesc_16bit_f32(128, 64, false, false, false, kF16);
 template <bool kF16> constexpr uint32_t kIdescS = idesc_16bit_f32(128, 128, false, true, false, kF16);
 
@@ -197,6 +209,12 @@ __device__ __forceinline__ bool wait_bar(const Ctx& cx, int b, uint32_t parity) 
     return wait_bar_slow(cx, b, parity);
 }
 
+// A wait whose outcome is the same for every lane of a converged warp (the
+// single-warp roles use elect.sync and full-mask shuffles after their waits).
+__device__ __forceinline__ bool wait_bar_warp(const Ctx& cx, int b, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait_bar(cx, b, parity));
+}
+
 // Bounded wait used while draining (ignores the abort flag).
 __device__ __forceinline__ void drain_bar(const Ctx& cx, int b, uint32_t parity) {
     if (!mbar_wait(cx.bars + b, parity, kWaitCycles)) atomicOr(cx.status, static_cast<int32_t>(GDN_DEVICE_ERR_TIMEOUT));
@@ -230,8 +248,8 @@ __device__ __forceinline__ UnitInfo read_unit(const uint8_t* sm, int slot) {
 // ===========================================================================
 // Triangular inverse T = (I + A)^-1 of a strictly lower 64 x 64 A (fp32, rows
 // of kLd floats), computed in place by the two intra warpgroups (256 threads),
-// followed by the two bf16 operands of the W and U products,
-// T' = T diag(cw) and T'' = T diag(beta) (K-major [64 i][64 j], 128-byte
+// followed by the two bf16 operands of the Delta and U products,
+// T' = T diag(cw) and T'' = T diag(bn) (K-major [64 i][64 j], 128-byte
 // swizzle; their blocks above the diagonal are never written and stay zero).
 //   stage 1 (warps 0, 1; warp w owns rows and columns 32w..32w+31): the two
 //     16 x 16 diagonal blocks by forward substitution, one column per lane,
@@ -242,7 +260,7 @@ __device__ __forceinline__ UnitInfo read_unit(const uint8_t* sm, int slot) {
 //     two diagonal 32 x 32 blocks are converted from shared memory.
 // The 16- and 32-row products are below the 64-row minimum of tcgen05.mma, so
 // they run as warp-level m16n8k8 tf32 MMAs (fp32 accumulate); T is rounded to
-// bf16 for the W and U products anyway.
+// bf16 for the Delta and U products anyway.
 // ===========================================================================
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
@@ -283,8 +301,8 @@ constexpr int kLdX1 = 24, kLdX2 = 40;  // scratch strides: conflict-free B-fragm
 template <bool kF16>
 __device__ __forceinline__ void tri_inverse_64(float* __restrict__ A, uint8_t* __restrict__ tp,
                                                uint8_t* __restrict__ tpp, const float* __restrict__ cw,
-                                               const float* __restrict__ beta, const float* __restrict__ rn,
-                                               float* __restrict__ X1, float* __restrict__ X2, int t) {
+                                               const float* __restrict__ bn, float* __restrict__ X1,
+                                               float* __restrict__ X2, int t) {
     const int wi = t >> 5, lane = t & 31;  // warp index 0..7 within the intra groups
     if (wi < 2) {
         // ---- stage 1: diagonal 16 x 16 blocks, one column per lane
@@ -350,20 +368,16 @@ __device__ __forceinline__ void tri_inverse_64(float* __restrict__ A, uint8_t* _
         const float4 t1 = *reinterpret_cast<const float4*>(trow + 4);
         const float4 c0 = *reinterpret_cast<const float4*>(cw + j0);
         const float4 c1 = *reinterpret_cast<const float4*>(cw + j0 + 4);
-        const float4 e0 = *reinterpret_cast<const float4*>(beta + j0);
-        const float4 e1 = *reinterpret_cast<const float4*>(beta + j0 + 4);
-        const float4 n0 = *reinterpret_cast<const float4*>(rn + j0);
-        const float4 n1 = *reinterpret_cast<const float4*>(rn + j0 + 4);
+        const float4 e0 = *reinterpret_cast<const float4*>(bn + j0);
+        const float4 e1 = *reinterpret_cast<const float4*>(bn + j0 + 4);
         const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
         const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
         const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-        const float nv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
         float x[8], y[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const float tn = tv[q] * nv[q];
-            x[q] = tn * nv[q] * cv[q];
-            y[q] = tn * ev[q];
+            x[q] = tv[q] * cv[q];
+            y[q] = tv[q] * ev[q];
         }
         st_chunk16<kF16>(tp, i, j0 >> 3, x);
         st_chunk16<kF16>(tpp, i, j0 >> 3, y);
@@ -377,8 +391,7 @@ __device__ __forceinline__ void tri_inverse_64(float* __restrict__ A, uint8_t* _
             mma_tf32_16x8x8(e, A + (32 + mt) * kLd + 32 + k0, kLd, X2 + k0 * kLdX2 + nt, kLdX2, lane);
         const int g = lane >> 2, j = nt + 2 * (lane & 3);
         const int i0 = 32 + mt + g, i1 = i0 + 8;
-        const float n0 = rn[j], n1 = rn[j + 1];
-        const float be0 = beta[j] * n0, be1 = beta[j + 1] * n1, cw0 = cw[j] * n0 * n0, cw1 = cw[j + 1] * n1 * n1;
+        const float be0 = bn[j], be1 = bn[j + 1], cw0 = cw[j], cw1 = cw[j + 1];
         st_pair16<kF16>(tp, i0, j, -e[0] * cw0, -e[1] * cw1);
         st_pair16<kF16>(tp, i1, j, -e[2] * cw0, -e[3] * cw1);
         st_pair16<kF16>(tpp, i0, j, -e[0] * be0, -e[1] * be1);
@@ -411,9 +424,8 @@ __device__ __forceinline__ GatePrefetch load_gates(const ChunkParams& p, int64_t
     return g;
 }
 
-// The vectors of one chunk (see kG*) that need no norm; under the L2 norm the
-// intra warps add rn and q_norms adds rm.  Rows at or past Lc are padding
-// (alpha = 1, beta = 0).
+// The vectors of one chunk (see kG*) with n = m = 1; under the L2 norm qk_norms then rewrites the
+// norm-dependent ones.  Rows at or past Lc are padding (alpha = 1, beta = 0).
 __device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, bool l2norm, float keep_range,
                                               int lane) {
     const int r0 = 2 * lane;
@@ -426,9 +438,8 @@ __device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, 
     }
     const float G1 = incl, G0 = incl - la1;
     const float G63 = __shfl_sync(0xffffffffu, incl, 31);
-    float Gb[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) Gb[b] = __shfl_sync(0xffffffffu, G0, 8 * b);  // G at row 16 b
+    const float Gfirst = __shfl_sync(0xffffffffu, G0, 0);
+    const float Gref = 0.5f * (Gfirst + G63);
     float gmax = fmaxf(G0, G1), gmin = fminf(G0, G1);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -441,44 +452,54 @@ __device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, 
     for (int k = 0; k < 2; ++k) {
         const int r = r0 + k;
         const float e = __expf(Gv[k]);
+        const float rowf = __expf(Gv[k] - Gref);
         gb[kGG + r] = Gv[k];
         gb[kGGam + r] = e;
         gb[kGBeta + r] = bv[k];
         gb[kGRn + r] = 1.f;
         gb[kGCw + r] = bv[k] * e;
+        gb[kGBn + r] = bv[k];
         gb[kGDec + r] = __expf(G63 - Gv[k]);
         if (!l2norm) gb[kGRm + r] = keepq ? e : 1.f;
-        gb[kGRp + r] = keepq ? __expf(-Gv[k]) : 1.f;
-        gb[kGRa + r] = bv[k];
-        gb[kGColf + r] = __expf(Gb[r >> 4] - Gv[k]);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) gb[kGRowf + b * 64 + r] = (r >= 16 * b) ? __expf(Gv[k] - Gb[b]) : 0.f;
+        gb[kGRp + r] = keepq ? rowf / e : rowf;
+        gb[kGRa + r] = bv[k] * rowf;
+        gb[kGColf + r] = __expf(Gref - Gv[k]);
     }
     if (lane == 0) {
-        gb[kGSafe] = (gmax - gmin < 60.f) ? 1.f : 0.f;
+        gb[kGSafe] = (gmax - gmin < kSafeRange) ? 1.f : 0.f;
         gb[kGKeepQ] = keepq ? 1.f : 0.f;
     }
 }
 
 // rm of the chunk's rows lane and lane + 32 under the L2 norm: 1/|q_i| from
 // the Q tile as stored (K-major, 128B-swizzled halves), times gamma_i when the
-// chunk keeps Q; 0 on padded rows.  Runs after compute_gates (reads gamma and
-// keepq back from the same warp's stores).
+// chunk keeps Q; 0 on padded rows.  Runs after compute_gates in the same warp
+// (reads gamma and keepq back from its stores).  The two rows are summed side
+// by side in eight partial sums each, so the dependent chains stay short.
 template <bool kF16>
 __device__ __forceinline__ void q_norms(const uint8_t* q0, float* gb, int32_t Lc, int lane) {
     const bool keepq = gb[kGKeepQ] != 0.f;
-#pragma unroll 1
+    float ss[2][8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ss[h][j] = 0.f;
+#pragma unroll 2
+    for (int cch = 0; cch < 16; ++cch) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float f[8];
+            unpack8<kF16>(*reinterpret_cast<const uint4*>(q0 + (cch >> 3) * 16384 + sw128_offset(lane + 32 * h, cch & 7)),
+                          f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ss[h][j] = fmaf(f[j], f[j], ss[h][j]);
+        }
+    }
+#pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int qr = lane + 32 * h;
-        float ss = 0.f;
-#pragma unroll 4
-        for (int cch = 0; cch < 16; ++cch) {
-            float f[8];
-            unpack8<kF16>(*reinterpret_cast<const uint4*>(q0 + (cch >> 3) * 16384 + sw128_offset(qr, cch & 7)), f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
-        }
-        const float rm = qr < Lc ? rsqrtf(ss + 1e-6f) : 0.f;
+        const float t = ((ss[h][0] + ss[h][1]) + (ss[h][2] + ss[h][3])) + ((ss[h][4] + ss[h][5]) + (ss[h][6] + ss[h][7]));
+        const float rm = qr < Lc ? rsqrtf(t + 1e-6f) : 0.f;
         gb[kGRm + qr] = keepq ? rm * gb[kGGam + qr] : rm;
     }
 }
@@ -505,17 +526,39 @@ __device__ __forceinline__ void lds16(const float* src, float* x) {
 }
 
 // Intermediates for tests (only when requested): this thread's 32 values of W
-// and U (row r = k or v, columns i0..i0+31) and G, in fp32.  Out of line, so
-// the hot loop stays compact in the instruction cache.
+// and U (row r = k or v, columns i0..i0+31) and G, in fp32.  U is read from
+// its TMEM columns before the Delta product accumulates into them; W = T' K is
+// not formed by the kernel (the state pass uses X = S K^T instead), so it is
+// computed here on CUDA cores from the bf16 T' and K tiles the tensor cores
+// read (fp32 sums, the products' own precision).  Out of line, so the hot
+// loop stays compact in the instruction cache.
+template <bool kF16>
 __device__ __noinline__ void dump_intra(float* intra_w, float* intra_u, float* intra_g, size_t dump, size_t gdump,
-                                        uint32_t tm_w, uint32_t tm_u, int r, int i0, int it, const float* G) {
+                                        const uint8_t* tp, const uint8_t* kt, uint32_t tm_u, int r, int i0, int it,
+                                        const float* G) {
     uint32_t rr[32];
-    tmem_ld32_wait(tm_w, rr);
-    if (intra_w)
-        for (int j = 0; j < 32; ++j) intra_w[dump + static_cast<size_t>(i0 + j) * kHead + r] = __uint_as_float(rr[j]);
     tmem_ld32_wait(tm_u, rr);
     if (intra_u)
         for (int j = 0; j < 32; ++j) intra_u[dump + static_cast<size_t>(i0 + j) * kHead + r] = __uint_as_float(rr[j]);
+    if (intra_w) {
+        // K[j][r]: row j of the K tile, column r (halves of 64 columns, 128-byte swizzle)
+        float kc[64];
+        for (int j = 0; j < 64; ++j) {
+            const uint8_t* row = kt + (r >> 6) * 16384;
+            float f[8];
+            unpack8<kF16>(*reinterpret_cast<const uint4*>(row + sw128_offset(j, (r & 63) >> 3)), f);
+            kc[j] = f[r & 7];
+        }
+        for (int i = i0; i < i0 + 32; ++i) {
+            float acc = 0.f;
+            for (int j8 = 0; j8 < 8; ++j8) {
+                float f[8];
+                unpack8<kF16>(*reinterpret_cast<const uint4*>(tp + sw128_offset(i, j8)), f);
+                for (int q = 0; q < 8; ++q) acc += f[q] * kc[8 * j8 + q];
+            }
+            intra_w[dump + static_cast<size_t>(i) * kHead + r] = acc;
+        }
+    }
     if (intra_g && it < 64) intra_g[gdump + it] = G[it];
 }
 
@@ -600,8 +643,9 @@ __device__ __noinline__ void store_final_state(uint32_t tm_s, void* base, int64_
 // E16: the input element type, __nv_bfloat16 or __half.  kTransfer: the context-parallel transfer pass --
 // units [0, N*H) run each sequence (a segment) from a zero state, units [N*H, 2*N*H) run it from the
 // identity with U = 0 (the segment's transfer matrix), into output_state rows seq and N + seq; no output
-// products, epilogue or stores.
-template <typename E16, bool kTransfer>
+// products, epilogue or stores.  kDump: the instance that also writes the intra-chunk intermediates (tests);
+// the other instances carry no code for them.
+template <typename E16, bool kTransfer, bool kDump>
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_chunk_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -637,6 +681,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (uint32_t off = tid * 16; off < 32768; off += kThreads * 16)  // T', T'' and both P buffers
         *reinterpret_cast<uint4*>(sm + kTp + off) = make_uint4(0, 0, 0, 0);
+    for (uint32_t off = tid * 16; off < 8192; off += kThreads * 16)   // the second T' buffer
+        *reinterpret_cast<uint4*>(sm + kTp1 + off) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 3) {
         tmem_alloc(s_tmem, kTmCols);
@@ -721,137 +767,145 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (issued_v >= 0) drain_bar(cx, B_V_FULL, issued_v & 1);
             }
         } else if (warp == 1) {
-            // ================= tcgen05 issue: D1, W, U =================
+            // ================= tcgen05 issue: D1 and U (whole warp; one elected lane issues) =================
             // D1 of the next chunk of the unit needs only the intra side to be done with D1 of this one
-            // (mid-chunk) and its K | Q tiles (three stages), while W and U of this chunk need the full
-            // inverse: D1 goes first, so the intra side finds it computed when it starts the next chunk.
-            if (lane == 0) {
-                uint32_t n = 0, u = 0;
-                bool ok = true;
-                auto next_unit = [&](UnitInfo& info) -> bool {  // next unit with chunks (or the end marker)
-                    for (;;) {
-                        const int slot = u & 1;
-                        if (!wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1)) return false;
-                        info = read_unit(sm, slot);
-                        mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
-                        ++u;
-                        if (!info.valid || info.nC > 0) return true;
+            // (mid-chunk) and its K | Q tiles (three stages), while U of this chunk needs the full inverse: D1
+            // goes first, so the intra side finds it computed when it starts the next chunk.
+            uint32_t n = 0, u = 0;
+            bool ok = true;
+            auto next_unit = [&](UnitInfo& info) -> bool {  // next unit with chunks (or the end marker)
+                for (;;) {
+                    const int slot = u & 1;
+                    if (!wait_bar_warp(cx, B_UNIT_FULL + slot, (u >> 1) & 1)) return false;
+                    info = read_unit(sm, slot);
+                    if (lane == 0) mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
+                    ++u;
+                    if (!info.valid || info.nC > 0) return true;
+                }
+            };
+            auto issue_d1 = [&](uint32_t m) -> bool {  // D1 of global chunk m
+                const uint32_t st = m % kKQStages;
+                if (!wait_bar_warp(cx, B_KQ_FULL + st, (m / kKQStages) & 1)) return false;
+                if (m >= 1 && !wait_bar_warp(cx, B_D1_EMPTY, (m - 1) & 1)) return false;
+                tc_fence_after();
+                const uint32_t kq = smem_u32(sm + kKQ + st * kKQStage);
+#pragma unroll 1
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                    mma_ss_elect(tmem + kTmD1, desc_kmajor_sw128(kq + off), desc_kmajor_sw128(kq + off),
+                                 kIdescD1<kF16>, ks > 0);
+                }
+                mma_commit_elect(cx.bars + B_D1_FULL);
+                return true;
+            };
+            auto issue_u = [&](uint32_t m, bool no_u) -> bool {  // U of global chunk m (U = 0: no product)
+                if (!wait_bar_warp(cx, B_T_FULL + (m & 1), (m >> 1) & 1) || !wait_bar_warp(cx, B_V_FULL, m & 1)) return false;
+                // the Delta slot is free once S of chunk m-2 has read it
+                if (m >= 2 && !wait_bar_warp(cx, B_S_FULL + (m & 1), ((m - 2) >> 1) & 1)) return false;
+                tc_fence_after();
+                const uint32_t vv = smem_u32(sm + kV);
+                const uint32_t tpp = smem_u32(sm + kTpp);
+                const uint32_t dbuf = tmem + kTmDelta + (m & 1) * 64;
+                if (!(kTransfer && no_u)) {
+#pragma unroll 1
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ss_elect(dbuf, desc_mnmajor_sw128(vv + ks * 2048, 8192), desc_kmajor_sw128(tpp + ks * 32),
+                                     kIdescU<kF16>, ks > 0);
+                }
+                mma_commit_elect(cx.bars + B_U_FULL + (m & 1));
+                mma_commit_elect(cx.bars + B_V_EMPTY);
+                return true;
+            };
+            // Look-ahead stays inside a unit: reading the next unit early could wait on a ring slot that the
+            // other roles free only after this unit's last U (two empty units in a row do that).
+            while (ok) {
+                UnitInfo cur;
+                if (!(ok = next_unit(cur)) || !cur.valid) break;
+                ok = issue_d1(n);
+                for (int32_t c = 0; c < cur.nC && ok; ++c, ++n) {
+                    if (c + 1 < cur.nC) ok = issue_d1(n + 1);
+                    if (ok) ok = issue_u(n, kTransfer && cur.valid == 2);
+                }
+            }
+            mma_commit_elect(cx.bars + B_DRAIN_I);
+            drain_bar(cx, B_DRAIN_I, 0);
+        } else if (warp == 2) {
+            // ================= tcgen05 issue: X | S Q'^T, Delta, Delta P^T, S (whole warp, elected lane) =========
+            uint32_t n = 0, u = 0;
+            bool ok = true;
+            for (; ok;) {
+                const int slot = u & 1;
+                if (!(ok = wait_bar_warp(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
+                const UnitInfo info = read_unit(sm, slot);
+                if (lane == 0) mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
+                ++u;
+                if (!info.valid) break;
+                for (int32_t c = 0; c < info.nC; ++c, ++n) {
+                    const int s = n & 1;
+                    const uint32_t ph = (n >> 1) & 1;
+                    const uint32_t st = n % kKQStages;
+                    // [X | O] = S [K; Q']^T: the K and Q rows of a stage half are adjacent, one N = 128 B operand
+                    // (the transfer pass forms X alone).  The O columns are free once the previous output
+                    // epilogue has read them.
+                    if (!(ok = wait_bar_warp(cx, B_SB_FULL + s, ph))) break;
+                    if (!(ok = wait_bar_warp(cx, B_KQ_FULL + st, (n / kKQStages) & 1))) break;
+                    if (!kTransfer) {
+                        if (n >= 1 && !(ok = wait_bar_warp(cx, B_O_EMPTY + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
+                        // a chunk that does not keep Q reads Q' = diag(gamma) Q, written in place by the intra warps
+                        if (!(ok = wait_bar_warp(cx, B_GATES_FULL + n % 3, (n / 3) & 1))) break;
+                        const float keepq = reinterpret_cast<const float*>(sm + kGbuf)[(n % 3) * kGFloats + kGKeepQ];
+                        if (keepq == 0.f && !(ok = wait_bar_warp(cx, B_Q_READY + s, ph))) break;
                     }
-                };
-                auto issue_d1 = [&](uint32_t m) -> bool {  // D1 of global chunk m
-                    const uint32_t st = m % kKQStages;
-                    if (!wait_bar(cx, B_KQ_FULL + st, (m / kKQStages) & 1)) return false;
-                    if (m >= 1 && !wait_bar(cx, B_D1_EMPTY, (m - 1) & 1)) return false;
                     tc_fence_after();
                     const uint32_t kq = smem_u32(sm + kKQ + st * kKQStage);
-    #pragma unroll 1
-                    for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll 1
+                    for (int ks = 0; ks < 8; ++ks) {  // A = S (bf16 pairs in TMEM), k = 16 ks .. 16 ks + 15
                         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_bf16_ss(tmem + kTmD1, desc_kmajor_sw128(kq + off), desc_kmajor_sw128(kq + off),
-                                    kIdescD1<kF16>, ks > 0);
+                        mma_ts_elect(tmem + kTmX, tmem + kTmSbf + ks * 8, desc_kmajor_sw128(kq + off),
+                                     kTransfer ? kIdescX<kF16> : kIdescXO<kF16>, ks > 0);
                     }
-                    mma_commit(cx.bars + B_D1_FULL);
-                    return true;
-                };
-                auto issue_wu = [&](uint32_t m, bool no_u) -> bool {  // W and U of global chunk m (U = 0: no U)
-                    if (!wait_bar(cx, B_T_FULL, m & 1) || !wait_bar(cx, B_V_FULL, m & 1)) return false;
-                    // the W columns are free once the state warps have copied W of chunk m-1
-                    if (m >= 1 && !wait_bar(cx, B_WB_FULL + ((m - 1) & 1), ((m - 1) >> 1) & 1)) return false;
-                    // the Delta slot is free once S of chunk m-2 has read it
-                    if (m >= 2 && !wait_bar(cx, B_S_FULL + (m & 1), ((m - 2) >> 1) & 1)) return false;
+                    mma_commit_elect(cx.bars + B_XO_FULL);
+                    // Delta~^T = U~^T - X T'^T (A = X as bf16 pairs, negated; U = 0 for a transfer-matrix unit)
+                    if (!(ok = wait_bar_warp(cx, B_XB_FULL, n & 1))) break;
+                    if (!(ok = wait_bar_warp(cx, B_T_FULL + s, ph))) break;
+                    if (!(ok = wait_bar_warp(cx, B_U_FULL + s, ph))) break;
                     tc_fence_after();
-                    const uint32_t kq = smem_u32(sm + kKQ + (m % kKQStages) * kKQStage);
-                    const uint32_t vv = smem_u32(sm + kV);
-                    const uint32_t tp = smem_u32(sm + kTp), tpp = smem_u32(sm + kTpp);
-                    const uint32_t dbuf = tmem + kTmDelta + (m & 1) * 64;
-    #pragma unroll 1
-                    for (int ks = 0; ks < 4; ++ks) {
-                        mma_bf16_ss(tmem + kTmW, desc_mnmajor_sw128(kq + ks * 2048, 16384),
-                                    desc_kmajor_sw128(tp + ks * 32), kIdescWU<kF16>, ks > 0);
-                        if (!(kTransfer && no_u))
-                            mma_bf16_ss(dbuf, desc_mnmajor_sw128(vv + ks * 2048, 8192),
-                                        desc_kmajor_sw128(tpp + ks * 32), kIdescWU<kF16>, ks > 0);
-                    }
-                    mma_commit(cx.bars + B_WU_FULL);
-                    mma_commit(cx.bars + B_V_EMPTY);
-                    return true;
-                };
-                // Look-ahead stays inside a unit: reading the next unit early could wait on a ring slot that the
-                // other roles free only after this unit's last W and U (two empty units in a row do that).
-                while (ok) {
-                    UnitInfo cur;
-                    if (!(ok = next_unit(cur)) || !cur.valid) break;
-                    ok = issue_d1(n);
-                    for (int32_t c = 0; c < cur.nC && ok; ++c, ++n) {
-                        if (c + 1 < cur.nC) ok = issue_d1(n + 1);
-                        if (ok) ok = issue_wu(n, kTransfer && cur.valid == 2);
-                    }
-                }
-                mma_commit(cx.bars + B_DRAIN_I);
-                drain_bar(cx, B_DRAIN_I, 0);
-            }
-        } else if (warp == 2) {
-            // ================= tcgen05 issue: Delta, S Q^T, Delta P^T, S =================
-            if (lane == 0) {
-                uint32_t n = 0, u = 0;
-                bool ok = true;
-                for (; ok;) {
-                    const int slot = u & 1;
-                    if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
-                    const UnitInfo info = read_unit(sm, slot);
-                    mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
-                    ++u;
-                    if (!info.valid) break;
-                    for (int32_t c = 0; c < info.nC; ++c, ++n) {
-                        const int s = n & 1;
-                        const uint32_t ph = (n >> 1) & 1;
-                        if (!(ok = wait_bar(cx, B_WB_FULL + s, ph))) break;
-                        if (!(ok = wait_bar(cx, B_SB_FULL + s, ph))) break;
-                        const uint32_t st = n % kKQStages;
-                        if (!(ok = wait_bar(cx, B_KQ_FULL + st, (n / kKQStages) & 1))) break;
-                        tc_fence_after();
-                        const uint32_t kq = smem_u32(sm + kKQ + st * kKQStage);
-                        const uint32_t wb = smem_u32(sm + kWb);
-                        const uint32_t dbuf = tmem + kTmDelta + s * 64;
-    #pragma unroll 1
-                        for (int ks = 0; ks < 8; ++ks)  // A = S (bf16 pairs in TMEM), k = 16 ks .. 16 ks + 15
-                            mma_bf16_ts(dbuf, tmem + kTmSbf + ks * 8, desc_mnmajor_sw128(wb + ks * 2048, 8192),
-                                        kIdescDelta<kF16>, ks > 0 || !(kTransfer && info.valid == 2));  // U = 0
-                        mma_commit(cx.bars + B_DELTA_FULL + s);
-                        if (n >= 1 && !(ok = wait_bar(cx, B_O_EMPTY + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
-                        tc_fence_after();
-    #pragma unroll 1
-                        for (int ks = 0; ks < 8 && !kTransfer; ++ks) {  // O = S Q'^T, Q' = diag(gamma) Q
-                            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                            mma_bf16_ts(tmem + kTmO, tmem + kTmSbf + ks * 8, desc_kmajor_sw128(kq + 8192 + off),
-                                        kIdescO<kF16>, ks > 0);
-                        }
-                        if (!(ok = wait_bar(cx, B_DD_FULL + s, ph))) break;
-                        tc_fence_after();
+                    const uint32_t tp = smem_u32(sm + (s ? kTp1 : kTp));
+                    const uint32_t dbuf = tmem + kTmDelta + s * 64;
+#pragma unroll 1
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ts_elect(dbuf, tmem + kTmXbf + ks * 8, desc_kmajor_sw128(tp + ks * 32), kIdescDelta<kF16>,
+                                     ks > 0 || !(kTransfer && info.valid == 2));
+                    mma_commit_elect(cx.bars + B_DELTA_FULL + s);
+                    // O += Delta^T P^T (its own commit, so the output epilogue overlaps the S product), then
+                    // S += (decayed Delta)^T K
+                    if (!(ok = wait_bar_warp(cx, B_DD_FULL + s, ph))) break;
+                    tc_fence_after();
+                    if (!kTransfer) {
                         const uint32_t pb = smem_u32(sm + kPb + s * 8192);
-    #pragma unroll 1
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint32_t acol = dbuf + 32 * (ks >> 1) + 8 * (ks & 1);  // packed j = 16 ks .. 16 ks + 15
-                            // O += Delta^T P^T, then S += (decayed Delta)^T K
-                            if (!kTransfer)
-                                mma_bf16_ts(tmem + kTmO, acol, desc_kmajor_sw128(pb + ks * 32), kIdescO<kF16>, 1);
-                            mma_bf16_ts(tmem + kTmS, acol + 16, desc_mnmajor_sw128(kq + ks * 2048, 16384),
-                                        kIdescS<kF16>, 1);
-                        }
-                        mma_commit(cx.bars + B_S_FULL + s);
-                        mma_commit(cx.bars + B_KQ_EMPTY + st);
+#pragma unroll 1
+                        for (int ks = 0; ks < 4; ++ks)  // packed j = 16 ks .. 16 ks + 15
+                            mma_ts_elect(tmem + kTmO, dbuf + 32 * (ks >> 1) + 8 * (ks & 1),
+                                         desc_kmajor_sw128(pb + ks * 32), kIdescO<kF16>, 1);
+                        mma_commit_elect(cx.bars + B_O_FULL);
                     }
+#pragma unroll 1
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ts_elect(tmem + kTmS, dbuf + 32 * (ks >> 1) + 8 * (ks & 1) + 16,
+                                     desc_mnmajor_sw128(kq + ks * 2048, 16384), kIdescS<kF16>, 1);
+                    mma_commit_elect(cx.bars + B_S_FULL + s);
+                    mma_commit_elect(cx.bars + B_KQ_EMPTY + st);
                 }
-                mma_commit(cx.bars + B_DRAIN_S);
-                drain_bar(cx, B_DRAIN_S, 0);
             }
+            mma_commit_elect(cx.bars + B_DRAIN_S);
+            drain_bar(cx, B_DRAIN_S, 0);
         } else if (warp == 3) {
             // ================= gates warp: G, gamma, beta and factor vectors per chunk =================
             uint32_t n = 0, u = 0;
             bool ok = true;
             for (; ok;) {
                 const int slot = u & 1;
-                if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
+                if (!(ok = wait_bar_warp(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
                 const UnitInfo info = read_unit(sm, slot);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
@@ -868,20 +922,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         gpf = load_gates(p, info.t0 + static_cast<int64_t>(c + 1) * kChunk,
                                          rem1 < kChunk ? static_cast<int32_t>(rem1) : kChunk, info.h, lane);
                     }
-                    if (n >= 3 && !(ok = wait_bar(cx, B_GATES_EMPTY + gs, ((n - 3) / 3) & 1))) break;
+                    if (n >= 3 && !(ok = wait_bar_warp(cx, B_GATES_EMPTY + gs, ((n - 3) / 3) & 1))) break;
                     float* gbw = reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats;
                     compute_gates(cur, gbw, p.l2norm != 0, kF16 ? 0.f : kKeepQRange, lane);
                     __syncwarp();
-                    if (p.l2norm && !kTransfer) {
-                        // the q norms from the chunk's Q tile (its stage is released only after this chunk's
-                        // products, which wait for these gates)
-                        if (!(ok = wait_bar(cx, B_KQ_FULL + n % kKQStages, (n / kKQStages) & 1))) break;
+                    // The q norms (for the output epilogue only) come from the chunk's Q tile as stored: a chunk
+                    // that keeps Q publishes its gates first and the norms after them (RM_FULL); one that does
+                    // not keep Q computes the norms first, because the intra warps rescale Q in place once they
+                    // have the gates.  (The stage is released only after this chunk's products, and this slot
+                    // only after its output epilogue.)
+                    const bool qn = p.l2norm && !kTransfer;
+                    const bool late = qn && gbw[kGKeepQ] != 0.f;
+                    if (qn) {
+                        if (late && lane == 0) mbar_arrive(cx.bars + B_GATES_FULL + gs);
+                        if (!(ok = wait_bar_warp(cx, B_KQ_FULL + n % kKQStages, (n / kKQStages) & 1))) break;
                         const int64_t rem = info.L - static_cast<int64_t>(c) * kChunk;
                         q_norms<kF16>(sm + kKQ + (n % kKQStages) * kKQStage + 8192, gbw,
-                                rem < kChunk ? static_cast<int32_t>(rem) : kChunk, lane);
+                                      rem < kChunk ? static_cast<int32_t>(rem) : kChunk, lane);
                         __syncwarp();
+                        if (lane == 0) mbar_arrive(cx.bars + B_RM_FULL + gs);
                     }
-                    if (lane == 0) mbar_arrive(cx.bars + B_GATES_FULL + gs);
+                    if (!late && lane == 0) mbar_arrive(cx.bars + B_GATES_FULL + gs);
                 }
             }
         }
@@ -890,19 +951,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int it = tid - 128;                      // 0..255
         const int wq = warp & 3;                       // TMEM lane quarter
         const int hh = (warp - 4) >> 2;                // column half
-        const int r = wq * 32 + lane;                  // TMEM lane: A row r (< 64) or P row r - 64
         const uint32_t tm_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-        const int imax = (wq & 1) * 32 + 31;           // last A or P row of this warp
         float* Abuf = reinterpret_cast<float*>(sm + kAbuf);
         float* X1 = reinterpret_cast<float*>(sm + kXs);
         float* X2 = X1 + 2 * 16 * kLdX1;
         uint32_t n = 0, u = 0;
         bool ok = true;
+        // Every wait's outcome is ANDed over the two warpgroups at their next named barrier
+        // (named_bar_and), and the group leaves its loops only there, all together.
         for (; ok;) {
             const int slot = u & 1;
-            if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
+            ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1);
             const UnitInfo info = read_unit(sm, slot);
-            named_bar_sync(kBarIntra, kIntraThreads);
+            if (!(ok = named_bar_and(kBarIntra, kIntraThreads, ok))) break;
             if (it == 0) mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
             ++u;
             if (!info.valid) break;
@@ -913,67 +974,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t gs = n % 3;
                 float* gb = reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats;
                 uint8_t* kqs = sm + kKQ + (n % kKQStages) * kKQStage;
-                if (!(ok = wait_bar(cx, B_GATES_FULL + gs, (n / 3) & 1))) break;
+                ok = wait_bar(cx, B_GATES_FULL + gs, (n / 3) & 1);
                 // P buffer s is free once O2 of chunk n-2 has completed
-                if (n >= 2 && !(ok = wait_bar(cx, B_S_FULL + s, ((n - 2) >> 1) & 1))) break;
-                if (!(ok = wait_bar(cx, B_D1_FULL, n & 1))) break;
+                if (n >= 2) ok = ok && wait_bar(cx, B_S_FULL + s, ((n - 2) >> 1) & 1);
+                ok = ok && wait_bar(cx, B_D1_FULL, n & 1);
                 tc_fence_after();
-                // A rows (lanes 0..63) and P rows (lanes 64..127), this warp's 32 columns, 16 per step;
-                // blocks entirely above the diagonal are skipped (A's upper part is never read, P's stays zero).
-                // e^{G_i - G_j} = rowf[b][i] colf[j] inside column block b when the chunk's gate range is
-                // moderate, else computed pairwise.
+                // A rows (lanes 0..63: warps with wq < 2) and P rows (lanes 64..127), row i, this warp's 32
+                // columns.  A half that lies entirely above the diagonal is skipped (A's upper part and diagonal
+                // are never read by the inverse, so A needs no mask; P's stays zero).  e^{G_i - G_j} is the row
+                // factor times colf[j] while the chunk's gate range is moderate, else it is computed pairwise.
                 {
-                    const bool arow = r < 64;
-                    const int i = r & 63;
-                    const bool safe = gb[kGSafe] != 0.f;
-                    float rbase = gb[(arow ? kGRa : kGRp) + i];
-                    if (p.l2norm && arow) {
-                        // |k_i|^2 is the diagonal of K K^T: lane l of this warp finds it in column 32 wq + l
-                        uint32_t rr[32];
-                        tmem_ld32_wait(tm_lane + kTmD1 + 32 * wq, rr);
+                    const bool arow = wq < 2;
+                    const int i = 32 * (wq & 1) + lane;
+                    const bool active = !(hh == 1 && (wq & 1) == 0) && !(kTransfer && !arow);  // warp-uniform
+                    float rn = 1.f;
+                    if (arow && p.l2norm) {
+                        // n_i = 1/|k_i|: |k_i|^2 is the diagonal of K K^T, column i of this lane's row (the warps
+                        // whose half holds the diagonal find it in their main load below; warp wq = 1, hh = 0
+                        // loads that half as well)
+                        uint32_t rd[32];
+                        tmem_ld32_wait(tm_lane + kTmD1 + 32 * (wq & 1), rd);
                         float kk = 0.f;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) kk = (j == lane) ? __uint_as_float(rr[j]) : kk;
-                        const float rn = i < Lc ? rsqrtf(kk + 1e-6f) : 0.f;
-                        rbase *= rn * rn;
-                        if (hh == wq) gb[kGRn + i] = rn;
+                        for (int j = 0; j < 32; ++j) kk = (j == lane) ? __uint_as_float(rd[j]) : kk;
+                        rn = i < Lc ? rsqrtf(kk + 1e-6f) : 0.f;
+                        if (hh == (wq & 1)) {  // one writer per row: the factors the inverse reads
+                            gb[kGRn + i] = rn;
+                            gb[kGCw + i] *= rn * rn;
+                            gb[kGBn + i] *= rn;
+                        }
                     }
-                    uint8_t* pb = sm + kPb + s * 8192;
-#pragma unroll 1
-                    for (int jb = 32 * hh; jb < 32 * hh + 32; jb += 16) {
-                        if (jb > imax || (!arow && kTransfer)) break;  // warp-uniform
-                        uint32_t rr[16];
-                        tmem_ld16_wait(tm_lane + kTmD1 + jb, rr);
-                        float x[16];
-                        if (safe) {
-                            float cj[16];
-                            lds16(gb + kGColf + jb, cj);
-                            const float rf = rbase * gb[kGRowf + (jb >> 4) * 64 + i];
+                    if (active) {
+                        uint32_t rr[32];
+                        tmem_ld32_wait(tm_lane + kTmD1 + 32 * hh, rr);
+                        float x[32];
+                        const float rf = arow ? gb[kGRa + i] * rn * rn : gb[kGRp + i];
+                        if (gb[kGSafe] != 0.f) {
 #pragma unroll
-                            for (int q = 0; q < 16; ++q) {
-                                const int j = jb + q;
-                                const bool keep = arow ? (j < i) : (j <= i);
-                                x[q] = keep ? rf * cj[q] * __uint_as_float(rr[q]) : 0.f;
+                            for (int q = 0; q < 32; q += 4) {
+                                const float4 cj = *reinterpret_cast<const float4*>(gb + kGColf + 32 * hh + q);
+                                x[q] = rf * cj.x * __uint_as_float(rr[q]);
+                                x[q + 1] = rf * cj.y * __uint_as_float(rr[q + 1]);
+                                x[q + 2] = rf * cj.z * __uint_as_float(rr[q + 2]);
+                                x[q + 3] = rf * cj.w * __uint_as_float(rr[q + 3]);
                             }
                         } else {
-                            float gj[16];
-                            lds16(gb + kGG + jb, gj);
+                            // pairwise: the row factor without its e^{G_i - Gref}, times e^{G_i - G_j}
                             const float Gi = gb[kGG + i];
+                            const float rb = arow ? gb[kGBeta + i] * rn * rn
+                                                  : (gb[kGKeepQ] != 0.f ? 1.f / gb[kGGam + i] : 1.f);
 #pragma unroll
-                            for (int q = 0; q < 16; ++q) {
-                                const int j = jb + q;
-                                const bool keep = arow ? (j < i) : (j <= i);
-                                x[q] = keep ? rbase * __expf(Gi - gj[q]) * __uint_as_float(rr[q]) : 0.f;
-                            }
+                            for (int q = 0; q < 32; ++q)
+                                x[q] = rb * __expf(Gi - gb[kGG + 32 * hh + q]) * __uint_as_float(rr[q]);
                         }
                         if (arow) {
 #pragma unroll
-                            for (int q = 0; q < 16; q += 4)
-                                *reinterpret_cast<float4*>(Abuf + i * kLd + jb + q) =
+                            for (int q = 0; q < 32; q += 4)
+                                *reinterpret_cast<float4*>(Abuf + i * kLd + 32 * hh + q) =
                                     make_float4(x[q], x[q + 1], x[q + 2], x[q + 3]);
                         } else {
-                            st_chunk16<kF16>(pb, i, jb >> 3, x);
-                            st_chunk16<kF16>(pb, i, (jb >> 3) + 1, x + 8);
+                            uint8_t* pb = sm + kPb + s * 8192;
+                            const int lim = i - 32 * hh;  // keep j <= i
+#pragma unroll
+                            for (int q = 0; q < 32; ++q) x[q] = q <= lim ? x[q] : 0.f;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) st_chunk16<kF16>(pb, i, 4 * hh + q, x + 8 * q);
                         }
                     }
                 }
@@ -996,7 +1061,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // zero the padded rows of the K and V tiles (they hold the next
                 // sequence or TMA zero fill; only exact zeros may meet them)
                 if (Lc < kChunk) {
-                    if (!(ok = wait_bar(cx, B_V_FULL, n & 1))) break;
+                    ok = ok && wait_bar(cx, B_V_FULL, n & 1);
                     const int zr = it & 63;
                     if (it < 128 && zr >= Lc) {
                         const uint4 z = make_uint4(0, 0, 0, 0);
@@ -1007,16 +1072,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<uint4*>(base + (cch >> 3) * hs + sw128_offset(zr, cch & 7)) = z;
                     }
                 }
-                tc_fence_before();  // P and the zeroed tile rows reach the async proxy with the T' and Wb fences
-                named_bar_sync(kBarIntra, kIntraThreads);
-                if (it == 0) mbar_arrive(cx.bars + B_D1_EMPTY);
-                // T = (I + A)^-1 in place, with T' = T diag(cw) and T'' = T diag(beta) in their bf16 tiles
-                // (the W and U products of the previous chunk have read the old ones)
-                if (n >= 1 && !(ok = wait_bar(cx, B_WU_FULL, (n - 1) & 1))) break;
-                tri_inverse_64<kF16>(Abuf, sm + kTp, sm + kTpp, gb + kGCw, gb + kGBeta, gb + kGRn, X1, X2, it);
+                // Q' and the zeroed K / V rows reach the async proxy before Q_READY (the X | O product reads Q')
                 fence_proxy_async_smem();
-                named_bar_sync(kBarIntra, kIntraThreads);
-                if (it == 0) mbar_arrive(cx.bars + B_T_FULL);
+                tc_fence_before();
+                if (!(ok = named_bar_and(kBarIntra, kIntraThreads, ok))) break;
+                if (it == 0) {
+                    mbar_arrive(cx.bars + B_D1_EMPTY);
+                    mbar_arrive(cx.bars + B_Q_READY + s);
+                }
+                // T = (I + A)^-1 in place, with T' = T diag(cw) (buffer s) and T'' = T diag(beta) in their bf16
+                // tiles: U of the previous chunk has read T'', and Delta of chunk n-2 has read T' buffer s
+                if (n >= 1) ok = wait_bar(cx, B_U_FULL + ((n - 1) & 1), ((n - 1) >> 1) & 1);
+                if (n >= 2) ok = ok && wait_bar(cx, B_DELTA_FULL + s, ((n - 2) >> 1) & 1);
+                tri_inverse_64<kF16>(Abuf, sm + (s ? kTp1 : kTp), sm + kTpp, gb + kGCw, gb + kGBn, X1, X2, it);
+                fence_proxy_async_smem();
+                if (!(ok = named_bar_and(kBarIntra, kIntraThreads, ok))) break;
+                if (it == 0) mbar_arrive(cx.bars + B_T_FULL + s);
             }
         }
     } else {
@@ -1030,11 +1101,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         typename E::T* outT = reinterpret_cast<typename E::T*>(sm + kOutT);
         uint32_t n = 0, u = 0;
         bool ok = true;
+        // As in the intra warpgroups: wait outcomes are ANDed over both warpgroups at the next named barrier.
         for (; ok;) {
             const int slot = u & 1;
-            if (!(ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1))) break;
+            ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1);
             const UnitInfo info = read_unit(sm, slot);
-            named_bar_sync(kBarState, kStateThreads);
+            if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
             if (st == 0) mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
             ++u;
             if (!info.valid) break;
@@ -1053,7 +1125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // initial state: S0 -> the bf16 operand columns and gamma_63(first chunk) * S0 -> the accumulator
             // (the previous unit's last products, their readers, completed before its last state epilogue)
             {
-                if (!(ok = wait_bar(cx, B_GATES_FULL + n % 3, (n / 3) & 1))) break;
+                ok = wait_bar(cx, B_GATES_FULL + n % 3, (n / 3) & 1);
                 const float g63 = reinterpret_cast<const float*>(sm + kGbuf)[(n % 3) * kGFloats + kGGam + 63];
                 if (ident)
                     identity_state<kF16>(v - 64 * hh, tm_lane + kTmSbf + 32 * hh, tm_lane + kTmS + 64 * hh, g63,
@@ -1062,31 +1134,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     load_initial_state<kF16>(s0, state_off, p.state.dtype, tm_lane + kTmSbf + 32 * hh,
                                              tm_lane + kTmS + 64 * hh, g63);
                 tc_fence_before();
-                named_bar_sync(kBarState, kStateThreads);
+                if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
                 if (st == 0) mbar_arrive(cx.bars + B_SB_FULL + (n & 1));
             }
-            // W^T of chunk m (unit-local index cm) -> shared memory, the MN-major B operand of -S W^T.  The
-            // reader of the previous copy, Delta of chunk m-1, completed before this warpgroup's Delta epilogue
-            // of that chunk.  The caller publishes it (proxy fence, barrier, WB_FULL).
-            auto copy_w = [&](uint32_t m, int32_t cm) -> bool {
-                if (!wait_bar(cx, B_WU_FULL, m & 1)) return false;
-                tc_fence_after();
-                const int i0 = 32 * hh;
-                uint32_t rr[32];
-                tmem_ld32_wait(tm_lane + kTmW + i0, rr);
-                float w[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(rr[j]);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) st_chunk16<kF16>(sm + kWb, v, (i0 >> 3) + q, w + 8 * q);
-                if (p.intra_w || p.intra_u || p.intra_g)
-                    dump_intra(p.intra_w, p.intra_u, p.intra_g,
-                               (static_cast<size_t>(info.flat0 + cm) * H + info.h) * kChunk * kHead,
-                               (static_cast<size_t>(info.flat0 + cm) * H + info.h) * kChunk, tm_lane + kTmW + i0,
-                               tm_lane + kTmDelta + (m & 1) * 64 + i0, v, i0, st,
-                               reinterpret_cast<const float*>(sm + kGbuf) + (m % 3) * kGFloats + kGG);
-                return true;
-            };
             for (int32_t c = 0; c < info.nC && ok; ++c, ++n) {
                 const int s = n & 1;
                 const uint32_t ph = (n >> 1) & 1;
@@ -1096,17 +1146,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t gs = n % 3;
                 const float* gb = reinterpret_cast<const float*>(sm + kGbuf) + gs * kGFloats;
                 const uint32_t dbuf = tm_lane + kTmDelta + s * 64;
-                // W of the unit's first chunk (the later ones are copied right after the previous chunk's state)
-                if (c == 0) {
-                    if (!(ok = copy_w(n, c))) break;
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    named_bar_sync(kBarState, kStateThreads);
-                    if (st == 0) mbar_arrive(cx.bars + B_WB_FULL + s);
+                // ---- X = S K^T as bf16 pairs (A operand of the Delta product), into the bf16 S columns, which
+                //      the X | O product has finished reading.  This thread: row v, columns 32 hh .. 32 hh + 31.
+                ok = wait_bar(cx, B_XO_FULL, n & 1);
+                tc_fence_after();
+                if constexpr (kDump) {
+                    // test dumps: U before the Delta product accumulates onto it, W from T' and K
+                    ok = ok && wait_bar(cx, B_U_FULL + s, ph) && wait_bar(cx, B_T_FULL + s, ph);
+                    tc_fence_after();
+                    dump_intra<kF16>(p.intra_w, p.intra_u, p.intra_g,
+                                     (static_cast<size_t>(info.flat0 + c) * H + info.h) * kChunk * kHead,
+                                     (static_cast<size_t>(info.flat0 + c) * H + info.h) * kChunk,
+                                     sm + (s ? kTp1 : kTp), sm + kKQ + (n % kKQStages) * kKQStage,
+                                     dbuf + 32 * hh, v, 32 * hh, st,
+                                     reinterpret_cast<const float*>(sm + kGbuf) + gs * kGFloats + kGG);
                 }
+                {
+                    uint32_t rx[32], pk[16];
+                    tmem_ld32_wait(tm_lane + kTmX + 32 * hh, rx);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) pk[q] = E::pack(__uint_as_float(rx[2 * q]), __uint_as_float(rx[2 * q + 1]));
+                    tmem_st16(tm_lane + kTmXbf + 16 * hh, pk);
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
+                if (st == 0) mbar_arrive(cx.bars + B_XB_FULL);
                 // ---- Delta epilogue: this thread's 32 columns j in [32 hh, 32 hh + 32) go back into TMEM as
                 //      16 packed bf16 Delta words followed by 16 packed decayed words (A operands of O2 and S)
-                if (!(ok = wait_bar(cx, B_DELTA_FULL + s, ph))) break;
+                ok = wait_bar(cx, B_DELTA_FULL + s, ph);
                 tc_fence_after();
                 {
                     uint32_t ra[32], pk[16];
@@ -1126,15 +1194,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st16(dbuf + 32 * hh + 16, pk);
                     tmem_wait_st();
                 }
+                if (st == 0) bulk_wait_group_read0();  // the previous chunk's output store has read outT
                 tc_fence_before();
-                named_bar_sync(kBarState, kStateThreads);
+                if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
                 if (st == 0) mbar_arrive(cx.bars + B_DD_FULL + s);
-                // ---- state epilogue: checkpoint / final state, next S operand, prescale (this thread's 64 columns)
-                if (!(ok = wait_bar(cx, B_S_FULL + s, ph))) break;
+                // ---- output, part 1: this thread's 32 tokens i in [32 hh, 32 hh + 32) of O (row v) leave TMEM while
+                //      the S product runs behind the output product; the arithmetic waits until after pass 1, so
+                //      the next X | O product finds its O columns free as soon as the next bf16 S is ready.
+                uint32_t ro[32];
+                if (!kTransfer) {
+                    ok = ok && wait_bar(cx, B_O_FULL, n & 1);
+                    tc_fence_after();
+                    tmem_ld32_wait(tm_lane + kTmO + 32 * hh, ro);
+                }
+                // ---- state epilogue, pass 1: S_n -> the bf16 operand of the next X | O product, checkpoint, final
+                //      state (this thread's 64 columns)
+                ok = ok && wait_bar(cx, B_S_FULL + s, ph);
                 tc_fence_after();
                 const bool last = (c + 1 == info.nC);
                 {
-                    // pass 1: S_n -> the bf16 operand of the next Delta and S Q^T products, checkpoint, final state
                     const int64_t pend = static_cast<int64_t>(c + 1) * kChunk;
                     float* ck = nullptr;
                     if (p.checkpoints && p.ckpt_n > 0 && pend % p.ckpt_n == 0 && pend <= info.L)
@@ -1144,18 +1222,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c0 = 0; c0 < 64; c0 += 16) {
                         uint32_t r[16];
                         tmem_ld16_wait(tm_lane + kTmS + 64 * hh + c0, r);
-                        float x[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(r[j]);
                         if (ck) {
 #pragma unroll
                             for (int j = 0; j < 16; j += 4)
-                                *reinterpret_cast<float4*>(ck + c0 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                                *reinterpret_cast<float4*>(ck + c0 + j) =
+                                    make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                                __uint_as_float(r[j + 3]));
                         }
                         if (!last) {  // bf16 pairs (c, c + 1) in column c / 2 of the operand
                             uint32_t pk[8];
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) pk[q] = E::pack(x[2 * q], x[2 * q + 1]);
+                            for (int q = 0; q < 8; ++q) pk[q] = E::pack(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]));
                             tmem_st8(tm_lane + kTmSbf + 32 * hh + c0 / 2, pk);
                         }
                     }
@@ -1163,78 +1240,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (last && p.output_state) store_final_state(tm_lane + kTmS + 64 * hh, p.output_state, state_off,
                                                                   p.state.dtype);
                 }
-                // W of the next chunk, published with the bf16 state under one barrier: the two are all the next
-                // Delta product waits for, while this chunk's prescale and output epilogue run behind it.
-                if (!last) {
-                    if (!(ok = copy_w(n + 1, c + 1))) break;
-                    fence_proxy_async_smem();
-                }
-                if (st == 0) bulk_wait_group_read0();  // the previous chunk's output store has read outT
                 tc_fence_before();
-                named_bar_sync(kBarState, kStateThreads);
-                if (st == 0 && !last) {
-                    mbar_arrive(cx.bars + B_SB_FULL + ((n + 1) & 1));
-                    mbar_arrive(cx.bars + B_WB_FULL + ((n + 1) & 1));
+                if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
+                if (st == 0) {
+                    if (!last) mbar_arrive(cx.bars + B_SB_FULL + ((n + 1) & 1));
+                    if (!kTransfer) mbar_arrive(cx.bars + B_O_EMPTY + s);
                 }
-                if (!last) {
-                    // pass 2: gamma_63 of the next chunk into the accumulator, before that chunk's S product
-                    const uint32_t gn = (n + 1) % 3;
-                    if (!(ok = wait_bar(cx, B_GATES_FULL + gn, ((n + 1) / 3) & 1))) break;
-                    const float gnext = reinterpret_cast<const float*>(sm + kGbuf)[gn * kGFloats + kGGam + 63];
-#pragma unroll 1
-                    for (int c0 = 0; c0 < 64; c0 += 16) {
-                        uint32_t r[16];
-                        tmem_ld16_wait(tm_lane + kTmS + 64 * hh + c0, r);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gnext);
-                        tmem_st16(tm_lane + kTmS + 64 * hh + c0, r);
-                    }
-                    tmem_wait_st();
-                }
-                // ---- output epilogue: o_i = scale rm_i (S Q'^T + Delta^T P^T)_i, tokens i in [32 hh, 32 hh + 32)
+                // ---- output, part 2: o_i = scale rm_i (S Q'^T + Delta^T P^T)_i into the output tile, then its store
                 if (!kTransfer) {
+                    if (p.l2norm) ok = ok && wait_bar(cx, B_RM_FULL + gs, (n / 3) & 1);
                     const float sc = p.scale;
-#pragma unroll 1
-                    for (int i0 = 32 * hh; i0 < 32 * hh + 32; i0 += 8) {
-                        uint32_t r1[8];
-                        tmem_ld8(tm_lane + kTmO + i0, r1);
-                        const float4 ma = *reinterpret_cast<const float4*>(gb + kGRm + i0);
-                        const float4 mb = *reinterpret_cast<const float4*>(gb + kGRm + i0 + 4);
+#pragma unroll
+                    for (int i0 = 0; i0 < 32; i0 += 8) {
+                        const float4 ma = *reinterpret_cast<const float4*>(gb + kGRm + 32 * hh + i0);
+                        const float4 mb = *reinterpret_cast<const float4*>(gb + kGRm + 32 * hh + i0 + 4);
                         const float rm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-                        tmem_wait_ld();
-                        tmem_regs_ready(r1);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            outT[(i0 + j) * kHead + v] = E::from(sc * rm[j] * __uint_as_float(r1[j]));
+                            outT[(32 * hh + i0 + j) * kHead + v] = E::from(sc * rm[j] * __uint_as_float(ro[i0 + j]));
                     }
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                named_bar_sync(kBarState, kStateThreads);
-                if (st == 0) {
-                    mbar_arrive(cx.bars + B_O_EMPTY + s);
-                    mbar_arrive(cx.bars + B_GATES_EMPTY + gs);
-                }
-                if (kTransfer) {
-                    // a transfer pass writes no output
-                } else if (Lc == kChunk) {
-                    // a full chunk: one TMA store of the 64 x 128 tile (rows all belong to this sequence)
-                    if (st == 0) {
-                        tma_store_3d(&tm_o, sm + kOutT, 0, info.h, static_cast<int32_t>(tc));
-                        bulk_commit_group();
-                    }
-                } else {
-                    // the tail: coalesced copy of the valid rows only, 16 threads per 256-byte row
-                    uint8_t* gout = static_cast<uint8_t*>(p.output);
+                    fence_proxy_async_smem();
+                    if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
+                    if (Lc == kChunk) {
+                        // a full chunk: one TMA store of the 64 x 128 tile (rows all belong to this sequence)
+                        if (st == 0) {
+                            tma_store_3d(&tm_o, sm + kOutT, 0, info.h, static_cast<int32_t>(tc));
+                            bulk_commit_group();
+                        }
+                    } else {
+                        // the tail: coalesced copy of the valid rows only, 16 threads per 256-byte row
+                        uint8_t* gout = static_cast<uint8_t*>(p.output);
 #pragma unroll 1
-                    for (int k = 0; k < 4; ++k) {
-                        const int id = st + 256 * k, row = id >> 4, col = id & 15;
-                        if (row < Lc) {
-                            const uint4 val = *reinterpret_cast<const uint4*>(sm + kOutT + row * 256 + col * 16);
-                            *reinterpret_cast<uint4*>(gout + ((static_cast<size_t>(tc + row) * H + info.h) * kHead) * 2 +
-                                                      col * 16) = val;
+                        for (int k = 0; k < 4; ++k) {
+                            const int id = st + 256 * k, row = id >> 4, col = id & 15;
+                            if (row < Lc) {
+                                const uint4 val = *reinterpret_cast<const uint4*>(sm + kOutT + row * 256 + col * 16);
+                                *reinterpret_cast<uint4*>(gout + ((static_cast<size_t>(tc + row) * H + info.h) * kHead) * 2 +
+                                                          col * 16) = val;
+                            }
                         }
                     }
+                }
+                if (st == 0) mbar_arrive(cx.bars + B_GATES_EMPTY + gs);
+                if (!last) {
+                    // pass 2: gamma_63 of the next chunk into the accumulator, before that chunk's S product (the
+                    // next Delta epilogue's barrier orders it before that product's issue)
+                    const uint32_t gn = (n + 1) % 3;
+                    ok = wait_bar(cx, B_GATES_FULL + gn, ((n + 1) / 3) & 1);
+                    const float gnext = reinterpret_cast<const float*>(sm + kGbuf)[gn * kGFloats + kGGam + 63];
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 64; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_ld32_wait(tm_lane + kTmS + 64 * hh + c0, r);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gnext);
+                        tmem_st32(tm_lane + kTmS + 64 * hh + c0, r);
+                    }
+                    tmem_wait_st();
                 }
             }
         }
@@ -1254,17 +1316,26 @@ size_t chunk_bf16_smem_bytes() { return kSmemAlloc; }
 cudaError_t launch_chunk_16bit(const ChunkParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                const CUtensorMap& tm_v, const CUtensorMap& tm_o, bool f16, bool transfer, int grid,
                                cudaStream_t stream) {
-    static int configured[4] = {-1, -1, -1, -1};
+    // One flag per device and instance: cudaFuncSetAttribute runs once, and concurrent first calls from
+    // several host threads each run it at most once more (the attribute value is the same).
+    constexpr int kMaxDevices = 64;
+    static std::atomic<uint8_t> configured[kMaxDevices][6];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    auto* kernel = f16 ? (transfer ? gdn_chunk_kernel<__half, true> : gdn_chunk_kernel<__half, false>)
-                       : (transfer ? gdn_chunk_kernel<__nv_bfloat16, true> : gdn_chunk_kernel<__nv_bfloat16, false>);
-    const int ki = (f16 ? 2 : 0) + (transfer ? 1 : 0);
-    if (configured[ki] != dev) {
+    const bool dump = p.intra_w || p.intra_u || p.intra_g;
+    if (dump && transfer) return cudaErrorInvalidValue;
+    auto* kernel = f16 ? (transfer ? gdn_chunk_kernel<__half, true, false>
+                                   : (dump ? gdn_chunk_kernel<__half, false, true> : gdn_chunk_kernel<__half, false, false>))
+                       : (transfer ? gdn_chunk_kernel<__nv_bfloat16, true, false>
+                                   : (dump ? gdn_chunk_kernel<__nv_bfloat16, false, true>
+                                           : gdn_chunk_kernel<__nv_bfloat16, false, false>));
+    const int ki = (f16 ? 3 : 0) + (transfer ? 1 : (dump ? 2 : 0));
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!configured[dev][ki].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemAlloc));
         if (e != cudaSuccess) return e;
-        configured[ki] = dev;
+        configured[dev][ki].store(1, std::memory_order_release);
     }
     kernel<<<grid, kThreads, kSmemAlloc, stream>>>(p, tm_q, tm_k, tm_v, tm_o);
     return cudaGetLastError();
