@@ -447,6 +447,7 @@ __device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, 
         gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
     }
     const bool keepq = gmax <= keep_range && gmin >= -keep_range;
+    const float ekeep = __expf(-Gref);
     const float Gv[2] = {G0, G1}, bv[2] = {g.b0, g.b1};
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -461,7 +462,7 @@ __device__ __forceinline__ void compute_gates(const GatePrefetch& g, float* gb, 
         gb[kGBn + r] = bv[k];
         gb[kGDec + r] = __expf(G63 - Gv[k]);
         if (!l2norm) gb[kGRm + r] = keepq ? e : 1.f;
-        gb[kGRp + r] = keepq ? rowf / e : rowf;
+        gb[kGRp + r] = keepq ? ekeep : rowf;  // e^{G_i - Gref} / gamma_i = e^{-Gref}
         gb[kGRa + r] = bv[k] * rowf;
         gb[kGColf + r] = __expf(Gref - Gv[k]);
     }
@@ -847,52 +848,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // [X | O] = S [K; Q']^T: the K and Q rows of a stage half are adjacent, one N = 128 B operand
                     // (the transfer pass forms X alone).  The O columns are free once the previous output
                     // epilogue has read them.
+                    // (the waits on the intra side and the loads come first: they are usually complete; the state
+                    // pass's release comes last, so one wake-up starts the issue)
                     if (!(ok = wait_bar_warp(cx, B_SB_FULL + s, ph))) break;
                     if (!(ok = wait_bar_warp(cx, B_KQ_FULL + st, (n / kKQStages) & 1))) break;
                     if (!kTransfer) {
                         if (n >= 1 && !(ok = wait_bar_warp(cx, B_O_EMPTY + ((n - 1) & 1), ((n - 1) >> 1) & 1))) break;
-                        // a chunk that does not keep Q reads Q' = diag(gamma) Q, written in place by the intra warps
                         if (!(ok = wait_bar_warp(cx, B_GATES_FULL + n % 3, (n / 3) & 1))) break;
                         const float keepq = reinterpret_cast<const float*>(sm + kGbuf)[(n % 3) * kGFloats + kGKeepQ];
                         if (keepq == 0.f && !(ok = wait_bar_warp(cx, B_Q_READY + s, ph))) break;
                     }
                     tc_fence_after();
+                    // descriptors advance by constants (16-byte units of the start address).  The issue loops stay
+                    // rolled: unrolled, the back-to-back products slowed the whole kernel by about a tenth.
                     const uint32_t kq = smem_u32(sm + kKQ + st * kKQStage);
+                    const uint64_t dkq = desc_kmajor_sw128(kq);
 #pragma unroll 1
-                    for (int ks = 0; ks < 8; ++ks) {  // A = S (bf16 pairs in TMEM), k = 16 ks .. 16 ks + 15
-                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_ts_elect(tmem + kTmX, tmem + kTmSbf + ks * 8, desc_kmajor_sw128(kq + off),
+                    for (int ks = 0; ks < 8; ++ks)  // A = S (bf16 pairs in TMEM), k = 16 ks .. 16 ks + 15
+                        mma_ts_elect(tmem + kTmX, tmem + kTmSbf + ks * 8, dkq + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
                                      kTransfer ? kIdescX<kF16> : kIdescXO<kF16>, ks > 0);
-                    }
                     mma_commit_elect(cx.bars + B_XO_FULL);
                     // Delta~^T = U~^T - X T'^T (A = X as bf16 pairs, negated; U = 0 for a transfer-matrix unit)
                     if (!(ok = wait_bar_warp(cx, B_XB_FULL, n & 1))) break;
                     if (!(ok = wait_bar_warp(cx, B_T_FULL + s, ph))) break;
                     if (!(ok = wait_bar_warp(cx, B_U_FULL + s, ph))) break;
                     tc_fence_after();
-                    const uint32_t tp = smem_u32(sm + (s ? kTp1 : kTp));
+                    const uint64_t dtp = desc_kmajor_sw128(smem_u32(sm + (s ? kTp1 : kTp)));
                     const uint32_t dbuf = tmem + kTmDelta + s * 64;
+                    const uint32_t acc0 = !(kTransfer && info.valid == 2);
 #pragma unroll 1
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_ts_elect(dbuf, tmem + kTmXbf + ks * 8, desc_kmajor_sw128(tp + ks * 32), kIdescDelta<kF16>,
-                                     ks > 0 || !(kTransfer && info.valid == 2));
+                        mma_ts_elect(dbuf, tmem + kTmXbf + ks * 8, dtp + ks * 2, kIdescDelta<kF16>, ks > 0 ? 1u : acc0);
                     mma_commit_elect(cx.bars + B_DELTA_FULL + s);
                     // O += Delta^T P^T (its own commit, so the output epilogue overlaps the S product), then
                     // S += (decayed Delta)^T K
                     if (!(ok = wait_bar_warp(cx, B_DD_FULL + s, ph))) break;
                     tc_fence_after();
                     if (!kTransfer) {
-                        const uint32_t pb = smem_u32(sm + kPb + s * 8192);
+                        const uint64_t dpb = desc_kmajor_sw128(smem_u32(sm + kPb + s * 8192));
 #pragma unroll 1
                         for (int ks = 0; ks < 4; ++ks)  // packed j = 16 ks .. 16 ks + 15
-                            mma_ts_elect(tmem + kTmO, dbuf + 32 * (ks >> 1) + 8 * (ks & 1),
-                                         desc_kmajor_sw128(pb + ks * 32), kIdescO<kF16>, 1);
+                            mma_ts_elect(tmem + kTmO, dbuf + 32 * (ks >> 1) + 8 * (ks & 1), dpb + ks * 2, kIdescO<kF16>,
+                                         1);
                         mma_commit_elect(cx.bars + B_O_FULL);
                     }
+                    const uint64_t dks = desc_mnmajor_sw128(kq, 16384);
 #pragma unroll 1
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_ts_elect(tmem + kTmS, dbuf + 32 * (ks >> 1) + 8 * (ks & 1) + 16,
-                                     desc_mnmajor_sw128(kq + ks * 2048, 16384), kIdescS<kF16>, 1);
+                        mma_ts_elect(tmem + kTmS, dbuf + 32 * (ks >> 1) + 8 * (ks & 1) + 16, dks + ks * 128, kIdescS<kF16>,
+                                     1);
                     mma_commit_elect(cx.bars + B_S_FULL + s);
                     mma_commit_elect(cx.bars + B_KQ_EMPTY + st);
                 }
@@ -1099,6 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tm_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         using E = Elem16<kF16>;
         typename E::T* outT = reinterpret_cast<typename E::T*>(sm + kOutT);
+        const int32_t ck_every = (p.checkpoints && p.ckpt_n > 0) ? p.ckpt_n / kChunk : 0;
         uint32_t n = 0, u = 0;
         bool ok = true;
         // As in the intra warpgroups: wait outcomes are ANDed over both warpgroups at the next named barrier.
@@ -1112,6 +1117,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!info.valid) break;
             // element offset of this thread's 64 columns in the initial / output state
             const int64_t state_off = state_offset(p.state, info.srow, info.h, v) + 64 * hh;
+            // checkpoints: every ck_every-th chunk end of the unit (a multiple of 64 tokens), counted down, so the
+            // chunk loop does no division
+            int32_t ck_left = ck_every, ck_row = 0;
             const void* s0 = p.initial_state;
             // a transfer-matrix unit starts from the identity: a 1 in column v - 64 hh of this thread's row v
             const bool ident = kTransfer && info.valid == 2;
@@ -1213,11 +1221,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const bool last = (c + 1 == info.nC);
                 {
-                    const int64_t pend = static_cast<int64_t>(c + 1) * kChunk;
                     float* ck = nullptr;
-                    if (p.checkpoints && p.ckpt_n > 0 && pend % p.ckpt_n == 0 && pend <= info.L)
-                        ck = p.checkpoints + (static_cast<size_t>(info.ckpt_base + pend / p.ckpt_n - 1) * H + info.h) *
-                                                 kHead * kHead + static_cast<size_t>(v) * kHead + 64 * hh;
+                    if (ck_every > 0 && --ck_left == 0) {
+                        ck_left = ck_every;
+                        // the chunk ends at local token 64 (c + 1); a checkpoint only where that is inside the sequence
+                        if (static_cast<int64_t>(c + 1) * kChunk <= info.L)
+                            ck = p.checkpoints + (static_cast<size_t>(info.ckpt_base + ck_row) * H + info.h) * kHead * kHead +
+                                 static_cast<size_t>(v) * kHead + 64 * hh;
+                        ++ck_row;
+                    }
 #pragma unroll 1
                     for (int c0 = 0; c0 < 64; c0 += 16) {
                         uint32_t r[16];
