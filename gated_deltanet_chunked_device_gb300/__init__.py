@@ -45,7 +45,9 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
           4: "GDN_ERR_DEVICE_INPUT", 5: "GDN_ERR_DEVICE_TIMEOUT"}
 DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2
 _QKV_DTYPES = {torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16, torch.float32: DTYPE_F32}
-_STATE_DTYPES = _QKV_DTYPES
+DTYPE_F8E4M3, DTYPE_F8E5M2 = 3, 4
+# states and checkpoints may also be stored in fp8 (widened on load, rounded to nearest and saturated on store)
+_STATE_DTYPES = {**_QKV_DTYPES, torch.float8_e4m3fn: DTYPE_F8E4M3, torch.float8_e5m2: DTYPE_F8E5M2}
 FLAGS = {
     "HAS_G": 1 << 0, "HAS_BETA": 1 << 1, "HAS_SCALE": 1 << 2, "QK_L2NORM": 1 << 3, "HAS_INITIAL_STATE": 1 << 4,
     "OUTPUT_FINAL_STATE": 1 << 5, "HAS_STATE_INDICES": 1 << 6, "CU_SEQLENS_I64": 1 << 7,
@@ -68,7 +70,7 @@ class Desc(ctypes.Structure):
                 ("head_size", ctypes.c_int32), ("qkv_dtype", ctypes.c_int32), ("state_dtype", ctypes.c_int32),
                 ("max_total_tokens", ctypes.c_int64), ("max_num_seqs", ctypes.c_int32),
                 ("max_pool_rows", ctypes.c_int32), ("checkpoint_every_n_tokens", ctypes.c_int32),
-                ("flags", ctypes.c_uint32)]
+                ("flags", ctypes.c_uint32), ("checkpoint_dtype", ctypes.c_int32)]
 
 
 class Args(ctypes.Structure):
@@ -236,8 +238,9 @@ def _pow2_at_least(x: int, lo: int = 1) -> int:
     return 1 << (x - 1).bit_length()
 
 
-def get_plan(hq, hk, hv, qkv_dtype, flags, ckpt_n, total_tokens, num_seqs, pool_rows, state_dtype=DTYPE_F32) -> _Plan:
-    key = (hq, hk, hv, qkv_dtype, flags, ckpt_n, state_dtype)
+def get_plan(hq, hk, hv, qkv_dtype, flags, ckpt_n, total_tokens, num_seqs, pool_rows, state_dtype=DTYPE_F32,
+             checkpoint_dtype=DTYPE_F32) -> _Plan:
+    key = (hq, hk, hv, qkv_dtype, flags, ckpt_n, state_dtype, checkpoint_dtype)
     with _plans_lock:
         p = _plans.get(key)
         d = p.desc if p else None
@@ -245,7 +248,7 @@ def get_plan(hq, hk, hv, qkv_dtype, flags, ckpt_n, total_tokens, num_seqs, pool_
             desc = Desc(num_q_heads=hq, num_k_heads=hk, num_v_heads=hv, head_size=HEAD_SIZE, qkv_dtype=qkv_dtype,
                         state_dtype=state_dtype, max_total_tokens=_pow2_at_least(total_tokens, 64),
                         max_num_seqs=_pow2_at_least(num_seqs), max_pool_rows=_pow2_at_least(pool_rows) if pool_rows else 0,
-                        checkpoint_every_n_tokens=ckpt_n, flags=flags)
+                        checkpoint_every_n_tokens=ckpt_n, flags=flags, checkpoint_dtype=checkpoint_dtype)
             p = _Plan(desc)
             _plans[key] = p
         return p
@@ -371,14 +374,17 @@ def chunk_gated_delta_rule(q, k, v, g=None, beta=None, scale=None, initial_state
     num_ck = 0
     if checkpoint_cu_starts is not None:
         _check_dev("checkpoint_cu_starts", checkpoint_cu_starts, device)
-        _check_dev("state_checkpoints", state_checkpoints, device, torch.float32)
+        _check_dev("state_checkpoints", state_checkpoints, device)
+        if state_checkpoints.dtype not in _STATE_DTYPES:
+            raise ValueError(f"unsupported checkpoint dtype {state_checkpoints.dtype}")
         if checkpoint_cu_starts.dtype == torch.int64:
             flags |= FLAGS["CHECKPOINT_STARTS_I64"]
         num_ck = state_checkpoints.shape[0]
     if output is None:
         output = torch.empty(T, H, D, dtype=q.dtype, device=device)
     _check_dev("output", output, device, q.dtype)
-    plan = get_plan(hq, hk, hv, qkv_dtype, flags, n, T, N, n_pool, state_dtype)
+    ckpt_dtype = _STATE_DTYPES[state_checkpoints.dtype] if state_checkpoints is not None else DTYPE_F32
+    plan = get_plan(hq, hk, hv, qkv_dtype, flags, n, T, N, n_pool, state_dtype, ckpt_dtype)
     ws = plan.workspace(device)
     args = Args(q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
                 scale=float(scale) if scale is not None else 0.0, cu_seqlens=_ptr(cu_seqlens), num_seqs=N,

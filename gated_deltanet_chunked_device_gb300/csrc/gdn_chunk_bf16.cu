@@ -625,8 +625,9 @@ __device__ __noinline__ void identity_state(int ic, uint32_t tm_sbf, uint32_t tm
     if (!dst) tmem_wait_st();
 }
 
-// The final state after a unit's last chunk: this thread's 64 columns of the fp32 accumulator in TMEM
-// (tm_s) to the output state, in the state's type.  Warp-uniform (tcgen05.ld is warp-collective).
+// The final state after a unit's last chunk, or a checkpoint: this thread's 64 columns of the fp32
+// accumulator in TMEM (tm_s) to `base` at element offset `off`, in type dt.  Warp-uniform (tcgen05.ld is
+// warp-collective).
 __device__ __noinline__ void store_final_state(uint32_t tm_s, void* base, int64_t off, int32_t dt) {
 #pragma unroll 1
     for (int c0 = 0; c0 < 64; c0 += 16) {
@@ -639,6 +640,14 @@ __device__ __noinline__ void store_final_state(uint32_t tm_s, void* base, int64_
             state_store4(base, off + c0 + j, dt, f);
         }
     }
+}
+
+// After a unit's last chunk: the checkpoint of that chunk end (ck_off >= 0) and the final state (dst non-null),
+// from this thread's 64 accumulator columns.  One out-of-line call site in the state loop.
+__device__ __noinline__ void finish_unit(uint32_t tm_s, void* ck, int64_t ck_off, int32_t ck_dt, void* dst,
+                                         int64_t off, int32_t dt) {
+    if (ck_off >= 0) store_final_state(tm_s, ck, ck_off, ck_dt);
+    if (dst) store_final_state(tm_s, dst, off, dt);
 }
 
 // E16: the input element type, __nv_bfloat16 or __half.  kTransfer: the context-parallel transfer pass --
@@ -1215,32 +1224,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     tmem_ld32_wait(tm_lane + kTmO + 32 * hh, ro);
                 }
-                // ---- state epilogue, pass 1: S_n -> the bf16 operand of the next X | O product, checkpoint, final
-                //      state (this thread's 64 columns)
+                // ---- state epilogue, pass 1: S_n -> the bf16 operand of the next X | O product (this thread's 64
+                //      columns); the checkpoint and the final state are written later, off the state chain
                 ok = ok && wait_bar(cx, B_S_FULL + s, ph);
                 tc_fence_after();
                 const bool last = (c + 1 == info.nC);
                 {
-                    float* ck = nullptr;
-                    if (ck_every > 0 && --ck_left == 0) {
-                        ck_left = ck_every;
-                        // the chunk ends at local token 64 (c + 1); a checkpoint only where that is inside the sequence
-                        if (static_cast<int64_t>(c + 1) * kChunk <= info.L)
-                            ck = p.checkpoints + (static_cast<size_t>(info.ckpt_base + ck_row) * H + info.h) * kHead * kHead +
-                                 static_cast<size_t>(v) * kHead + 64 * hh;
-                        ++ck_row;
-                    }
 #pragma unroll 1
                     for (int c0 = 0; c0 < 64; c0 += 16) {
                         uint32_t r[16];
                         tmem_ld16_wait(tm_lane + kTmS + 64 * hh + c0, r);
-                        if (ck) {
-#pragma unroll
-                            for (int j = 0; j < 16; j += 4)
-                                *reinterpret_cast<float4*>(ck + c0 + j) =
-                                    make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                                                __uint_as_float(r[j + 3]));
-                        }
                         if (!last) {  // bf16 pairs (c, c + 1) in column c / 2 of the operand
                             uint32_t pk[8];
 #pragma unroll
@@ -1249,8 +1242,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     if (!last) tmem_wait_st();
-                    if (last && p.output_state) store_final_state(tm_lane + kTmS + 64 * hh, p.output_state, state_off,
-                                                                  p.state.dtype);
                 }
                 tc_fence_before();
                 if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
@@ -1294,9 +1285,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (st == 0) mbar_arrive(cx.bars + B_GATES_EMPTY + gs);
+                // a checkpoint where the chunk end, local token 64 (c + 1), is inside the sequence: this thread's 64
+                // columns go to the dense checkpoint row in the checkpoint type
+                int64_t ck_off = -1;
+                if (ck_every > 0 && --ck_left == 0) {
+                    ck_left = ck_every;
+                    if (static_cast<int64_t>(c + 1) * kChunk <= info.L)
+                        ck_off = ((info.ckpt_base + ck_row) * H + info.h) * static_cast<int64_t>(kHead * kHead) +
+                                 static_cast<int64_t>(v) * kHead + 64 * hh;
+                    ++ck_row;
+                }
                 if (!last) {
                     // pass 2: gamma_63 of the next chunk into the accumulator, before that chunk's S product (the
-                    // next Delta epilogue's barrier orders it before that product's issue)
+                    // next Delta epilogue's barrier orders it before that product's issue); S_n on its way through
+                    // is the checkpoint
                     const uint32_t gn = (n + 1) % 3;
                     ok = wait_bar(cx, B_GATES_FULL + gn, ((n + 1) / 3) & 1);
                     const float gnext = reinterpret_cast<const float*>(sm + kGbuf)[gn * kGFloats + kGGam + 63];
@@ -1304,11 +1306,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c0 = 0; c0 < 64; c0 += 32) {
                         uint32_t r[32];
                         tmem_ld32_wait(tm_lane + kTmS + 64 * hh + c0, r);
+                        if (ck_off >= 0) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                const float f[4] = {__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                                    __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])};
+                                state_store4(p.checkpoints, ck_off + c0 + j, p.ckpt_dtype, f);
+                            }
+                        }
 #pragma unroll
                         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gnext);
                         tmem_st32(tm_lane + kTmS + 64 * hh + c0, r);
                     }
                     tmem_wait_st();
+                } else {
+                    // the unit's last chunk: its checkpoint (when due) and the final state, out of line
+                    finish_unit(tm_lane + kTmS + 64 * hh, p.checkpoints, ck_off, p.ckpt_dtype, p.output_state, state_off,
+                                p.state.dtype);
                 }
             }
         }

@@ -16,6 +16,8 @@
 //   Delta = U - W S^T
 //   O_i = scale (gamma_i S q_i + sum_{j<=i} e^{G_i - G_j} (q_i.k_j) Delta_j)
 //   S <- gamma_63 S + sum_j e^{G_63 - G_j} Delta_j k_j^T
+#include <atomic>
+
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -233,9 +235,13 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
         const int64_t pend = (c + 1) * kChunk;
         if (p.checkpoints && p.ckpt_n > 0 && pend % p.ckpt_n == 0 && pend <= L) {
             const int64_t slot = load_index(p.ckpt_cu_starts, p.ckpt_i64, seq) + pend / p.ckpt_n - 1;
-            float* ck = p.checkpoints + (static_cast<size_t>(slot) * H + h) * kHead * kHead;
-            for (int e = tid; e < kVs * kHead; e += kF32Threads)
-                ck[static_cast<size_t>(v0 + e / kHead) * kHead + e % kHead] = Ss[(e / kHead) * kLdK + e % kHead];
+            const int64_t ck = (slot * H + h) * static_cast<int64_t>(kHead * kHead);  // dense row, ckpt_dtype
+            for (int e = 4 * tid; e < kVs * kHead; e += 4 * kF32Threads) {
+                const int vv = e / kHead, kk = e % kHead;
+                const float x[4] = {Ss[vv * kLdK + kk], Ss[vv * kLdK + kk + 1], Ss[vv * kLdK + kk + 2],
+                                    Ss[vv * kLdK + kk + 3]};
+                state_store4(p.checkpoints, ck + static_cast<int64_t>(v0 + vv) * kHead + kk, p.ckpt_dtype, x);
+            }
         }
     }
     if (p.output_state) {
@@ -251,15 +257,19 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
 }  // namespace
 
 cudaError_t launch_chunk_f32(const ChunkParams& p, int grid, cudaStream_t stream) {
-    static int configured = -1;
+    // One flag per device: the attribute is set once, and concurrent first calls from several host threads
+    // each set it at most once more (the same value).
+    constexpr int kMaxDevices = 64;
+    static std::atomic<uint8_t> configured[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured != dev) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!configured[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(gdn_chunk_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kF32Smem));
         if (e != cudaSuccess) return e;
-        configured = dev;
+        configured[dev].store(1, std::memory_order_release);
     }
     gdn_chunk_f32_kernel<<<grid, kF32Threads, kF32Smem, stream>>>(p);
     return cudaGetLastError();

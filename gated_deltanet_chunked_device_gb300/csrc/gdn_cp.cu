@@ -18,6 +18,8 @@
 //      last segment's final state to the caller's output state.
 // The work is about (2 (P-1) + P) / P times a plain pass, spread over
 // P times as many units.
+#include <atomic>
+
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -153,15 +155,19 @@ cudaError_t launch_cp_prepare(const CpParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_cp_fixup(const CpParams& p, cudaStream_t stream) {
-    static int configured = -1;
+    // One flag per device: the attribute is set once, and concurrent first calls from several host threads
+    // each set it at most once more (the same value).
+    constexpr int kMaxDevices = 64;
+    static std::atomic<uint8_t> configured[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured != dev) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!configured[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(cp_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kFixupSmem));
         if (e != cudaSuccess) return e;
-        configured = dev;
+        configured[dev].store(1, std::memory_order_release);
     }
     cp_fixup_kernel<<<p.num_seqs * p.H, kCpThreads, kFixupSmem, stream>>>(p);
     return cudaGetLastError();

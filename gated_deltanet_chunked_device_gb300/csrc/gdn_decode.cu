@@ -62,8 +62,36 @@ __device__ __forceinline__ void load4<__half>(const __half* p, float (&x)[4]) {
     x[3] = fb.y;
 }
 
+// fp8 state elements (storage only): one byte each, converted with the shared fp8 helpers
+struct F8E4M3 {
+    uint8_t bits;
+};
+struct F8E5M2 {
+    uint8_t bits;
+};
+
+template <>
+__device__ __forceinline__ void load4<F8E4M3>(const F8E4M3* p, float (&x)[4]) {
+    state_load4(p, 0, GDN_DTYPE_F8E4M3, x);
+}
+
+template <>
+__device__ __forceinline__ void load4<F8E5M2>(const F8E5M2* p, float (&x)[4]) {
+    state_load4(p, 0, GDN_DTYPE_F8E5M2, x);
+}
+
 template <typename T>
 __device__ __forceinline__ void store4(T* p, const float (&x)[4]);
+
+template <>
+__device__ __forceinline__ void store4<F8E4M3>(F8E4M3* p, const float (&x)[4]) {
+    state_store4(p, 0, GDN_DTYPE_F8E4M3, x);
+}
+
+template <>
+__device__ __forceinline__ void store4<F8E5M2>(F8E5M2* p, const float (&x)[4]) {
+    state_store4(p, 0, GDN_DTYPE_F8E5M2, x);
+}
 
 template <>
 __device__ __forceinline__ void store4<float>(float* p, const float (&x)[4]) {
@@ -221,6 +249,8 @@ template <typename T>
 void launch_decode_t(const DecodeParams& p, unsigned grid, cudaStream_t stream) {
     if (p.state.dtype == GDN_DTYPE_BF16) launch_decode_ts<T, __nv_bfloat16>(p, grid, stream);
     else if (p.state.dtype == GDN_DTYPE_F16) launch_decode_ts<T, __half>(p, grid, stream);
+    else if (p.state.dtype == GDN_DTYPE_F8E4M3) launch_decode_ts<T, F8E4M3>(p, grid, stream);
+    else if (p.state.dtype == GDN_DTYPE_F8E5M2) launch_decode_ts<T, F8E5M2>(p, grid, stream);
     else launch_decode_ts<T, float>(p, grid, stream);
 }
 

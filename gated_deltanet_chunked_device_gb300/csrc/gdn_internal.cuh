@@ -19,9 +19,38 @@ constexpr int kHead = 128;     // head size (K = V = 128)
 // Initial / output state layout: element type and element strides of
 // [row][state head][v]; the 128 k elements of a v row are contiguous.
 struct StateLayout {
-    int32_t dtype;                 // GDN_DTYPE_F32, GDN_DTYPE_BF16 or GDN_DTYPE_F16
+    int32_t dtype;                 // a gdn_dtype: F32, BF16, F16, F8E4M3 or F8E5M2
     int64_t s_row, s_head, s_v;
 };
+
+__host__ __device__ inline int64_t dtype_bytes(int32_t dt) {
+    return dt == GDN_DTYPE_F32 ? 4 : (dt == GDN_DTYPE_BF16 || dt == GDN_DTYPE_F16) ? 2 : 1;
+}
+
+// fp8 pairs <-> fp32 (PTX cvt: widening is exact; narrowing rounds to
+// nearest, ties to even, and saturates to the finite range).  Element 0 is
+// the low byte.
+__device__ __forceinline__ void fp8x2_to_f32(uint16_t b, int32_t dt, float& lo, float& hi) {
+    uint32_t h2;
+    if (dt == GDN_DTYPE_F8E4M3)
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(b));
+    else
+        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(b));
+    __half2 h;
+    memcpy(&h, &h2, 4);
+    const float2 f = __half22float2(h);
+    lo = f.x;
+    hi = f.y;
+}
+
+__device__ __forceinline__ uint16_t f32_to_fp8x2(float lo, float hi, int32_t dt) {
+    uint16_t b;
+    if (dt == GDN_DTYPE_F8E4M3)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(b) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(b) : "f"(hi), "f"(lo));
+    return b;
+}
 
 __host__ __device__ inline int64_t state_offset(StateLayout L, int64_t row, int64_t h, int64_t v) {
     return row * L.s_row + h * L.s_head + v * L.s_v;
@@ -36,6 +65,10 @@ __device__ __forceinline__ void state_load4(const void* base, int64_t off, int32
         x[1] = f.y;
         x[2] = f.z;
         x[3] = f.w;
+    } else if (dt == GDN_DTYPE_F8E4M3 || dt == GDN_DTYPE_F8E5M2) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(base) + off);
+        fp8x2_to_f32(static_cast<uint16_t>(w & 0xffffu), dt, x[0], x[1]);
+        fp8x2_to_f32(static_cast<uint16_t>(w >> 16), dt, x[2], x[3]);
     } else {
         const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + off);
         if (dt == GDN_DTYPE_BF16) {
@@ -59,6 +92,10 @@ __device__ __forceinline__ void state_load4(const void* base, int64_t off, int32
 __device__ __forceinline__ void state_store4(void* base, int64_t off, int32_t dt, const float (&x)[4]) {
     if (dt == GDN_DTYPE_F32) {
         *reinterpret_cast<float4*>(static_cast<float*>(base) + off) = make_float4(x[0], x[1], x[2], x[3]);
+    } else if (dt == GDN_DTYPE_F8E4M3 || dt == GDN_DTYPE_F8E5M2) {
+        const uint32_t w = static_cast<uint32_t>(f32_to_fp8x2(x[0], x[1], dt)) |
+                           (static_cast<uint32_t>(f32_to_fp8x2(x[2], x[3], dt)) << 16);
+        *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(base) + off) = w;
     } else {
         uint2 u;
         if (dt == GDN_DTYPE_BF16) {
@@ -132,7 +169,8 @@ struct ChunkParams {
     StateLayout state;             // type and strides of both
     const void* state_indices;     // nullptr = dense [N, H, V, K]
     int idx_i64;
-    float* checkpoints;            // nullptr = none
+    void* checkpoints;             // nullptr = none; dense [rows][H][128][128] of ckpt_dtype
+    int32_t ckpt_dtype;            // a gdn_dtype
     int32_t ckpt_n;
     const void* ckpt_cu_starts;
     int ckpt_i64;

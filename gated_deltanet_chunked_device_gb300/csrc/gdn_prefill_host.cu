@@ -131,7 +131,7 @@ bool encode_out_map(CUtensorMap* map, void* base, int64_t T, int32_t heads, gdn_
 // stride, each dimension starts past the span of the smaller ones).
 bool make_state_layout(gdn_dtype dt, const int64_t (&st)[3], int64_t rows, int32_t H, gdn::StateLayout* L) {
     L->dtype = dt;
-    const int64_t es = dt == GDN_DTYPE_F32 ? 4 : 2;
+    const int64_t es = gdn::dtype_bytes(dt);
     if (st[0] == 0 && st[1] == 0 && st[2] == 0) {
         L->s_v = gdn::kHead;
         L->s_head = static_cast<int64_t>(gdn::kHead) * gdn::kHead;
@@ -172,6 +172,12 @@ int cp_segments(gdn_prefill_plan_t plan, const gdn_prefill_args& a, int32_t N, i
     return P >= 2 ? static_cast<int>(P) : 0;
 }
 
+// The types a state or a checkpoint may be stored in.
+bool storage_dtype(gdn_dtype t) {
+    return t == GDN_DTYPE_F32 || t == GDN_DTYPE_BF16 || t == GDN_DTYPE_F16 || t == GDN_DTYPE_F8E4M3 ||
+           t == GDN_DTYPE_F8E5M2;
+}
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -197,8 +203,7 @@ gdn_status gdn_prefill_plan(const gdn_prefill_desc* desc, gdn_prefill_plan_t* pl
     if (!gva && !gqa) return GDN_ERR_INVALID_ARG;
     if (d.qkv_dtype != GDN_DTYPE_BF16 && d.qkv_dtype != GDN_DTYPE_F16 && d.qkv_dtype != GDN_DTYPE_F32)
         return GDN_ERR_UNSUPPORTED;
-    if (d.state_dtype != GDN_DTYPE_F32 && d.state_dtype != GDN_DTYPE_BF16 && d.state_dtype != GDN_DTYPE_F16)
-        return GDN_ERR_UNSUPPORTED;
+    if (!storage_dtype(d.state_dtype) || !storage_dtype(d.checkpoint_dtype)) return GDN_ERR_UNSUPPORTED;
     if (d.checkpoint_every_n_tokens < 0 || d.checkpoint_every_n_tokens % gdn::kChunk != 0)
         return GDN_ERR_INVALID_ARG;
     if (d.max_total_tokens < 0 || d.max_num_seqs < 0 || d.max_pool_rows < 0) return GDN_ERR_INVALID_ARG;
@@ -360,6 +365,7 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
     cp.state_indices = pp.state_indices;
     cp.idx_i64 = pp.idx_i64;
     cp.checkpoints = n > 0 ? a.state_checkpoints : nullptr;
+    cp.ckpt_dtype = d.checkpoint_dtype;
     cp.ckpt_n = n;
     cp.ckpt_cu_starts = a.checkpoint_cu_starts;
     cp.ckpt_i64 = pp.ckpt_i64;
@@ -531,6 +537,7 @@ gdn_status gdn_decode_run(gdn_prefill_plan_t plan, const gdn_prefill_args* args,
     if (!make_state_layout(d.state_dtype, a.state_strides, (f & GDN_FLAG_HAS_STATE_INDICES) ? a.n_pool : N, plan->H,
                            &sl))
         return GDN_ERR_INVALID_ARG;
+    if (sl.s_v > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;  // the decode kernel steps v rows with a 32-bit stride
     const int64_t blocks = static_cast<int64_t>(N) * plan->H;
     if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     gdn::DecodeParams p{};

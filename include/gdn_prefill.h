@@ -21,15 +21,17 @@
  *   cu_seqlens       [N+1] int32 or int64, cu_seqlens[0] = 0, cu_seqlens[N] = T;
  *                    equal neighbours are legal zero-length sequences
  *   initial_state    [N, H, 128, 128], or the pool [n_pool, H, 128, 128], in
- *                    the plan's state_dtype (fp32, bf16 or fp16); element
- *                    strides of the row, head and v dims in state_strides
- *                    (all 0: contiguous), the 128 k elements contiguous
+ *                    the plan's state_dtype (fp32, bf16, fp16, fp8 e4m3 or
+ *                    fp8 e5m2); element strides of the row, head and v dims
+ *                    in state_strides (all 0: contiguous), the 128 k
+ *                    elements contiguous
  *   output_state     same shape, type and strides; may be the same buffer
  *   state_indices    [N] int32 or int64: sequence i reads and writes pool row
  *                    state_indices[i] (unique, in [0, n_pool))
- *   state_checkpoints[sum_i floor(L_i / n), H, 128, 128] fp32: the state after
- *                    local token p = j * n of sequence i goes to row
- *                    checkpoint_cu_starts[i] + j - 1
+ *   state_checkpoints[sum_i floor(L_i / n), H, 128, 128] in the plan's
+ *                    checkpoint_dtype (same choices as the state), dense: the
+ *                    state after local token p = j * n of sequence i goes to
+ *                    row checkpoint_cu_starts[i] + j - 1
  *   output           [T, H, 128], dtype of q
  * Head mapping ("FlashInfer GDN Prefill 完全指南", section on the legal CP
  * shapes): either HQ == HK and HV % HQ == 0 (GVA) or HK == HV and HQ % HK == 0
@@ -73,8 +75,21 @@ typedef enum gdn_status {
 
 /* fp16 q/k/v run on fp16 tensor-core operands throughout (the kernel's own
  * 16-bit intermediates take the input type); values must stay inside fp16's
- * range (|x| < 65504), including raw q.k products and the state entries. */
-typedef enum gdn_dtype { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1, GDN_DTYPE_F16 = 2 } gdn_dtype;
+ * range (|x| < 65504), including raw q.k products and the state entries.
+ * The two fp8 types ("FlashInfer GDN Prefill 完全指南": the initial_state row
+ * of the API table and the dtype requirement of "中间状态检查点" list
+ * float8_e4m3fn and float8_e5m2) are storage types of states and
+ * checkpoints only: they are widened to fp32 on load, and on store rounded to
+ * nearest (ties to even) and saturated to the finite range (e4m3: |x| <= 448,
+ * no infinities; e5m2: |x| <= 57344); NaN stays NaN.  The recurrence itself
+ * always runs in fp32. */
+typedef enum gdn_dtype {
+    GDN_DTYPE_F32 = 0,
+    GDN_DTYPE_BF16 = 1,
+    GDN_DTYPE_F16 = 2,
+    GDN_DTYPE_F8E4M3 = 3, /* states and checkpoints only */
+    GDN_DTYPE_F8E5M2 = 4  /* states and checkpoints only */
+} gdn_dtype;
 
 /* gdn_prefill_desc.flags */
 enum {
@@ -116,13 +131,15 @@ typedef struct gdn_prefill_desc {
     int32_t num_q_heads, num_k_heads, num_v_heads; /* HQ, HK, HV */
     int32_t head_size;                             /* must be 128 */
     gdn_dtype qkv_dtype;                           /* q, k, v and output: BF16, F16 or F32 */
-    gdn_dtype state_dtype;                         /* initial / output states: F32, BF16 or F16, widened to fp32
-                                                      on load and rounded to nearest on store (checkpoints: F32) */
+    gdn_dtype state_dtype;                         /* initial / output states: F32, BF16, F16, F8E4M3 or F8E5M2,
+                                                      widened to fp32 on load and rounded to nearest on store */
     int64_t max_total_tokens;                      /* upper bound of T over the plan's runs */
     int32_t max_num_seqs;                          /* upper bound of N */
     int32_t max_pool_rows;                         /* upper bound of n_pool (0 without state_indices) */
     int32_t checkpoint_every_n_tokens;             /* 0, or a multiple of 64 */
     uint32_t flags;                                /* GDN_FLAG_* */
+    gdn_dtype checkpoint_dtype;                    /* state_checkpoints: F32 (0, the default), BF16, F16, F8E4M3
+                                                      or F8E5M2, rounded to nearest on store like the states */
 } gdn_prefill_desc;
 
 typedef struct gdn_prefill_plan_s *gdn_prefill_plan_t;
@@ -142,13 +159,15 @@ typedef struct gdn_prefill_args {
     void *output_state;           /* required with GDN_FLAG_OUTPUT_FINAL_STATE; desc.state_dtype */
     /* Element strides of [row][head][v] of both states; {0, 0, 0} = contiguous
      * (H*128*128, 128*128, 128).  Otherwise each is positive, a multiple of 16
-     * bytes, and the layout does not overlap: sorted by stride, each stride is
-     * at least the extent covered by the smaller ones (128 for the v rows'
-     * own k elements).  Anything else is GDN_ERR_INVALID_ARG. */
+     * bytes (16 elements of an fp8 state), and the layout does not overlap:
+     * sorted by stride, each stride is at least the extent covered by the
+     * smaller ones (128 for the v rows' own k elements).  Anything else is
+     * GDN_ERR_INVALID_ARG.  gdn_decode_run also needs the v stride below
+     * 2^31 elements (else GDN_ERR_UNSUPPORTED). */
     int64_t state_strides[3];
     int32_t n_pool;               /* pool rows, with GDN_FLAG_HAS_STATE_INDICES */
     const void *state_indices;    /* [N], with GDN_FLAG_HAS_STATE_INDICES */
-    float *state_checkpoints;     /* required when checkpoint_every_n_tokens > 0 */
+    void *state_checkpoints;      /* required when checkpoint_every_n_tokens > 0; desc.checkpoint_dtype */
     int64_t num_checkpoints;      /* rows of state_checkpoints (capacity, checked on the device) */
     const void *checkpoint_cu_starts; /* [N+1], required when checkpoint_every_n_tokens > 0 */
     void *output;                 /* [T, H, 128], dtype of q */

@@ -11,6 +11,19 @@ from gated_deltanet_chunked_device_gb300 import workloads as wl
 # fp16 inputs take the 16-bit bound the pages give for bf16 (their only 16-bit figure)
 TOL = {torch.bfloat16: 2e-2, torch.float16: 2e-2, torch.float32: 1e-3}
 
+# Storage of a state or a checkpoint in a narrower type (the reading: the fp32 value is rounded to nearest,
+# ties to even; fp8 saturated to its finite range): mantissa bits m and half the subnormal spacing.  A
+# stored value r of a computed value x obeys |r - x| <= 2^-(m+1) |x| + half_sub, so a stored result carries
+# that much on top of the parity bar.
+STORED = {torch.bfloat16: (7, 2.0 ** -134), torch.float16: (10, 2.0 ** -25), torch.float8_e4m3fn: (3, 2.0 ** -10),
+          torch.float8_e5m2: (2, 2.0 ** -17)}
+
+
+def rounding_bound(x, dtype):
+    """Largest |round(x) - x| of storage type `dtype` at values x (numpy), normal and subnormal ranges."""
+    m, half_sub = STORED[dtype]
+    return 2.0 ** -(m + 1) * np.abs(x) + half_sub
+
 
 def to_device(inp, device="cuda"):
     out = dict(inp)
@@ -20,7 +33,7 @@ def to_device(inp, device="cuda"):
     return out
 
 
-def run_gpu(inp, intermediates=None, return_plan=False, check_status=True, **override):
+def run_gpu(inp, intermediates=None, return_plan=False, check_status=True, ckpt_dtype=torch.float32, **override):
     """Run the CUDA path on device inputs `inp` (from to_device).  With
     check_status the device status word must come back clear: no input flag
     and no timed-out wait inside a kernel."""
@@ -42,7 +55,7 @@ def run_gpu(inp, intermediates=None, return_plan=False, check_status=True, **ove
         nck = wl.num_checkpoints(lens, n)
         kw["checkpoint_every_n_tokens"] = n
         kw["checkpoint_cu_starts"] = inp["checkpoint_cu_starts"]
-        kw["state_checkpoints"] = torch.full((max(nck, 1), H, 128, 128), float("nan"), device=d)
+        kw["state_checkpoints"] = torch.full((max(nck, 1), H, 128, 128), float("nan"), device=d).to(ckpt_dtype)
     kw.update(override)
     res = gdn.chunk_gated_delta_rule(inp["q"], inp["k"], inp["v"], intermediates=intermediates,
                                      return_plan=True, **kw)
@@ -91,14 +104,17 @@ def run_oracle(inp, heads=None, threads=None):
                                  checkpoint_cu_starts=ccs, threads=threads)
 
 
-def compare(name, gpu, ref, tol):
-    """Elementwise |gpu - ref| <= tol + tol*|ref|; returns stats, raises on failure."""
+def compare(name, gpu, ref, tol, stored=None):
+    """Elementwise |gpu - ref| <= tol + tol*|ref| (plus the fp8 rounding bound when the GPU result is stored
+    in a narrower type `stored`: bf16, fp16 or fp8); returns stats, raises on failure."""
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert gpu.shape == ref.shape, f"{name}: shape {gpu.shape} vs {ref.shape}"
     assert np.isfinite(gpu).all(), f"{name}: non-finite values from the CUDA path"
     d = np.abs(gpu - ref)
     bound = tol + tol * np.abs(ref)
+    if stored in STORED:
+        bound = bound + rounding_bound(np.abs(ref) + bound, stored)
     bad = d > bound
     stats = {"max_abs": float(d.max()) if d.size else 0.0,
              "rel_to_max": float(d.max() / max(np.abs(ref).max(), 1e-30)) if d.size else 0.0,
@@ -120,9 +136,10 @@ def check_against_oracle(inp_cpu, gpu_res, heads=None, tol=None):
     stats["output"] = compare("output", _np(gpu_res["output"])[:, hs], ref["output"], tol)
     if inp_cpu["output_final_state"]:
         fin = _np(gpu_res["final_state"])[:, hs]
-        stats["final_state"] = compare("final_state", fin, ref["final_state"], tol)
+        stats["final_state"] = compare("final_state", fin, ref["final_state"], tol,
+                                       stored=gpu_res["final_state"].dtype)
     if inp_cpu.get("checkpoint_every_n_tokens"):
         nck = ref["checkpoints"].shape[0]
         stats["checkpoints"] = compare("checkpoints", _np(gpu_res["checkpoints"])[:nck][:, hs], ref["checkpoints"],
-                                       tol)
+                                       tol, stored=gpu_res["checkpoints"].dtype)
     return stats

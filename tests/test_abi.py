@@ -57,6 +57,15 @@ def _desc(**kw):
     (dict(state_dtype=gdn.DTYPE_BF16), OK),
     (dict(state_dtype=gdn.DTYPE_F16), OK),
     (dict(state_dtype=9), UNSUPPORTED),
+    (dict(state_dtype=gdn.DTYPE_F8E4M3), OK),                          # fp8 states (storage only)
+    (dict(state_dtype=gdn.DTYPE_F8E5M2), OK),
+    (dict(state_dtype=5), UNSUPPORTED),
+    (dict(checkpoint_every_n_tokens=64, checkpoint_dtype=gdn.DTYPE_BF16), OK),
+    (dict(checkpoint_every_n_tokens=64, checkpoint_dtype=gdn.DTYPE_F16), OK),
+    (dict(checkpoint_every_n_tokens=64, checkpoint_dtype=gdn.DTYPE_F8E4M3), OK),
+    (dict(checkpoint_every_n_tokens=64, checkpoint_dtype=gdn.DTYPE_F8E5M2), OK),
+    (dict(checkpoint_every_n_tokens=64, checkpoint_dtype=5), UNSUPPORTED),
+    (dict(qkv_dtype=gdn.DTYPE_F8E4M3), UNSUPPORTED),                   # fp8 is not an input type
     (dict(qkv_dtype=7), UNSUPPORTED),
     (dict(qkv_dtype=gdn.DTYPE_F16), OK),
     (dict(qkv_dtype=gdn.DTYPE_F32), OK),
@@ -149,6 +158,8 @@ def _valid_args(**kw):
     ({}, dict(state_strides=(32 * 128 * 128, 128 * 128, 64)), 1 << 20, INVALID),    # v rows overlap
     ({}, dict(state_strides=(32 * 128 * 128, 127 * 128, 128)), 1 << 20, INVALID),   # heads overlap
     ({}, dict(state_strides=(31 * 128 * 128, 128 * 128, 128)), 1 << 20, INVALID),   # rows overlap
+    # fp8 states: strides are multiples of 16 bytes = 16 elements
+    (dict(state_dtype=gdn.DTYPE_F8E4M3), dict(state_strides=(32 * 128 * 128, 128 * 128, 136)), 1 << 20, INVALID),
 ])
 def test_run_rejects_before_launch(L, desc_kw, args_kw, ws, expect):
     st, plan, nbytes = gdn.gdn_prefill_plan(_desc(**desc_kw))

@@ -67,3 +67,15 @@ def test_cp_full_size_single_long_sequence_sampled_heads():
     assert _cp_segments(res, inp) >= 2
     check_against_oracle(inp, res, heads=[0, 13, 31])
     assert torch.isfinite(res["output"]).all()
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float8_e4m3fn, torch.float8_e5m2])
+def test_cp_fp8_state_pool_and_fp8_checkpoints(state_dtype):
+    # context parallelism reads the fp8 pool into the fp32 scan and writes the last segments' states back in fp8
+    w = wl.custom(seq_lens=[1100, 40], hq=2, hk=2, hv=2, initial_state="pool", n_pool=5, l2norm_in_kernel=True,
+                  qk_prenorm=False, checkpoint_every=128)
+    inp = wl.generate(w, seed=64)
+    inp["initial_state"] = inp["initial_state"].to(state_dtype)
+    res = run_gpu(to_device(inp), use_cp=True, return_plan=True, ckpt_dtype=state_dtype)
+    assert _cp_segments(res, inp) >= 2
+    check_against_oracle(inp, res)

@@ -116,3 +116,73 @@ def test_strided_state_pool(layout, op):
     for r in range(pool.shape[0]):
         if r not in named:
             assert torch.equal(pool[r].cpu(), inp["initial_state"][r])
+
+
+# fp8 states and typed checkpoints ("FlashInfer GDN Prefill 完全指南": the initial_state row of the API table
+# and the dtype requirement of "中间状态检查点" list float8_e4m3fn and float8_e5m2).  The fp8 initial values
+# reach the fp32 recurrence exactly; a stored final state or checkpoint is the fp32 result rounded to nearest
+# (ties to even, saturated), so its check adds the fp8 rounding bound to the parity bar.
+FP8_TYPES = [torch.float8_e4m3fn, torch.float8_e5m2]
+
+
+@pytest.mark.parametrize("state_dtype", FP8_TYPES)
+def test_fp8_state_pool_prefill_with_fp8_checkpoints(state_dtype):
+    w = wl.custom(seq_lens=[300, 0, 90, 64], hq=2, hk=2, hv=4, initial_state="pool", n_pool=10,
+                  l2norm_in_kernel=True, qk_prenorm=False, checkpoint_every=64)
+    inp = wl.generate(w, seed=54)
+    inp["initial_state"] = inp["initial_state"].to(state_dtype)
+    res = run_gpu(to_device(inp), ckpt_dtype=state_dtype)
+    assert res["final_state"].dtype == state_dtype and res["checkpoints"].dtype == state_dtype
+    check_against_oracle(inp, res)
+    named = set(inp["state_indices"].tolist())
+    pool = res["final_state"].cpu()
+    for r in range(pool.shape[0]):
+        if r not in named:  # rows the batch does not name keep their bytes
+            assert torch.equal(pool[r].view(torch.uint8), inp["initial_state"][r].view(torch.uint8))
+
+
+@pytest.mark.parametrize("ckpt_dtype", [torch.bfloat16, torch.float16] + FP8_TYPES)
+def test_checkpoint_types_dense_state(ckpt_dtype):
+    w = wl.custom(seq_lens=[260, 128, 7], hq=4, hk=4, hv=4, initial_state="dense", alpha="exp_softplus16",
+                  checkpoint_every=128)
+    inp = wl.generate(w, seed=55)
+    res = run_gpu(to_device(inp), ckpt_dtype=ckpt_dtype)
+    assert res["checkpoints"].dtype == ckpt_dtype and res["final_state"].dtype == torch.float32
+    check_against_oracle(inp, res)
+
+
+@pytest.mark.parametrize("state_dtype", FP8_TYPES)
+def test_fp8_state_dense_new_output(state_dtype):
+    w = wl.custom(seq_lens=[200, 3, 64], hq=4, hk=2, hv=2, initial_state="dense", alpha="u(0.9,1.0)")
+    inp = wl.generate(w, seed=56)
+    inp["initial_state"] = inp["initial_state"].to(state_dtype)
+    res = run_gpu(to_device(inp))
+    assert res["final_state"].dtype == state_dtype
+    check_against_oracle(inp, res)
+
+
+@pytest.mark.parametrize("state_dtype", FP8_TYPES)
+def test_fp8_state_pool_decode(state_dtype):
+    w = wl.custom(seq_lens=[3] * 24, hq=4, hk=4, hv=8, initial_state="pool", n_pool=32, l2norm_in_kernel=True,
+                  qk_prenorm=False)
+    inp = wl.generate(w, seed=57)
+    inp["initial_state"] = inp["initial_state"].to(state_dtype)
+    d = to_device(inp)
+    pool = d["initial_state"].clone()
+    out, fin = gdn.gated_delta_rule_decode(d["q"], d["k"], d["v"], g=d["g"], beta=d["beta"], scale=inp["scale"],
+                                           initial_state=pool, state_indices=d["state_indices"],
+                                           use_qk_l2norm_in_kernel=True, tokens_per_seq=3)
+    torch.cuda.synchronize()
+    assert fin.dtype == state_dtype and fin.data_ptr() == pool.data_ptr()
+    check_against_oracle(inp, {"output": out, "final_state": fin})
+
+
+def test_fp32_inputs_fp8_state_and_bf16_checkpoints():
+    # the fp32-input kernel shares the typed state and checkpoint stores
+    w = wl.custom(seq_lens=[192, 70], hq=2, hk=2, hv=2, dtype=torch.float32, initial_state="dense",
+                  checkpoint_every=64, qk_prenorm=True)
+    inp = wl.generate(w, seed=58)
+    inp["initial_state"] = inp["initial_state"].to(torch.float8_e4m3fn)
+    res = run_gpu(to_device(inp), ckpt_dtype=torch.bfloat16)
+    assert res["final_state"].dtype == torch.float8_e4m3fn and res["checkpoints"].dtype == torch.bfloat16
+    check_against_oracle(inp, res)  # the fp32 bar, plus each stored type's own rounding
