@@ -79,20 +79,16 @@ constexpr uint32_t kKQ = 0;           // 3 stages x 32 KB: K_h0 | Q_h0 | K_h1 | 
 constexpr uint32_t kKQStage = 32768;
 constexpr uint32_t kKQStages = 3;
 constexpr uint32_t kV = 98304;        // V_h0 | V_h1
-constexpr uint32_t kTp = 114688;      // T' = T diag(beta gamma rn^2) bf16 [64 i][64 j] K-major, chunks n % 2 == 0
-constexpr uint32_t kTpp = 122880;     // T'' = T diag(beta rn)
-constexpr uint32_t kPb = 131072;      // 2 x P bf16 [64 i][64 j] K-major
-constexpr uint32_t kTp1 = 147456;     // T' of chunks n % 2 == 1
-constexpr uint32_t kSpare = 155648;   // 8 KB, unused
-constexpr uint32_t kAbuf = 163840;    // A, then T in place: fp32 [64][kLd]
-constexpr uint32_t kXs = 181248;      // inverse scratch: [2][16][24] then [32][40] fp32
-constexpr uint32_t kBars = 189440;    // up to 64 mbarriers
-constexpr uint32_t kRing = 189952;    // 2 unit descriptors
-constexpr uint32_t kMisc = 190080;    // tmem base, abort flag
-constexpr uint32_t kGbuf = 190144;    // 3 x kGFloats floats of per-row / per-column factors (see kG*)
-constexpr uint32_t kOutT = 205824;    // output tile bf16 [64 i][128 v]
-constexpr uint32_t kSmemBytes = 222208;
-constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
+constexpr uint32_t kTp = 114688;      // T' = T diag(cw) fp32 [64 i][64 j] K-major (halves of 32 j, 8 KB), n % 2 == 0
+constexpr uint32_t kTpp = 131072;     // T'' = T diag(bn) bf16 [64 i][64 j] K-major
+constexpr uint32_t kPb = 139264;      // 2 x P bf16 [64 i][64 j] K-major
+constexpr uint32_t kTp1 = 155648;     // T' of chunks n % 2 == 1
+constexpr uint32_t kAbuf = 172032;    // A, then T in place: fp32 [64][kLd]
+constexpr uint32_t kXs = 189440;      // inverse scratch: [2][16][24] then [32][40] fp32
+constexpr uint32_t kBars = 197632;    // up to 64 mbarriers
+constexpr uint32_t kRing = 198144;    // 2 unit descriptors
+constexpr uint32_t kMisc = 198272;    // tmem base, abort flag
+constexpr uint32_t kGbuf = 198336;    // 3 x kGFloats floats of per-row / per-column factors (see kG*)
 constexpr int kLd = 68;               // fp32 row stride of A and T (bank-conflict free rows)
 
 // gbuf field offsets (floats), one 64-vector each, per chunk (n, m = 1/|k|, 1/|q| under the L2 norm, else 1).
@@ -112,12 +108,15 @@ constexpr int kGG = 0, kGGam = 64, kGBeta = 128, kGRn = 192, kGRm = 256, kGCw = 
               kGRa = 512, kGColf = 576, kGBn = 640, kGSafe = 704, kGKeepQ = 705, kGFloats = 720;
 constexpr float kSafeRange = 80.f;  // e^{+-40} factors stay well inside fp32
 constexpr float kKeepQRange = 8.f;  // bf16 only: fp16 would overflow on e^8 (q.k) with raw q and k
-static_assert(kGbuf >= kMisc + 64 && kGbuf + 3 * kGFloats * 4 <= kOutT && kOutT + 16384 == kSmemBytes,
+constexpr uint32_t kOutT = 207872;    // output tile bf16 [64 i][128 v]
+constexpr uint32_t kSmemBytes = kOutT + 16384;
+constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
+static_assert(kGbuf >= kMisc + 64 && kXs + 4 * (2 * 16 * 24 + 32 * 40) <= kBars && kAbuf + 4 * 64 * kLd <= kXs,
               "shared memory map overlaps");
-static_assert(kXs + 4 * (2 * 16 * 24 + 32 * 40) <= kBars && kMisc + 64 <= kOutT, "scratch / barrier block overlap");
-static_assert(kKQ + kKQStages * kKQStage == kV && kV + 16384 == kTp && kTp1 + 8192 == kSpare &&
-                  kSpare + 8192 == kAbuf,
+static_assert(kKQ + kKQStages * kKQStage == kV && kV + 16384 == kTp && kTp + 16384 == kTpp && kTpp + 8192 == kPb &&
+                  kPb + 16384 == kTp1 && kTp1 + 16384 == kAbuf,
               "tile block overlap");
+static_assert(kSmemAlloc <= 232448, "shared memory above the per-CTA limit");
 
 // ---- barriers (single ones are safe where no waiter can fall two phases behind; see the roles)
 enum {
@@ -129,10 +128,9 @@ enum {
 };
 
 // ---- TMEM columns
-// S fp32 | Delta 2 x 64 | X = S K^T | O (S Q'^T + Delta^T P^T) | D1 | S as packed bf16 pairs (A operand), which
-// holds X as packed bf16 pairs between the X product and the Delta product (S is not read there)
+// S fp32 | Delta 2 x 64 | X = S K^T (fp32, the tf32 A operand of the Delta product) | O (S Q'^T + Delta^T P^T) |
+// D1 | S as packed bf16 pairs (A operand of the X | O product)
 constexpr uint32_t kTmS = 0, kTmDelta = 128, kTmX = 256, kTmO = 320, kTmD1 = 384, kTmSbf = 448;
-constexpr uint32_t kTmXbf = kTmSbf;
 constexpr uint32_t kTmCols = 512;
 static_assert(kTmO == kTmX + 64, "X and O are one N = 128 accumulator");
 
@@ -140,7 +138,7 @@ template <bool kF16> constexpr uint32_t kIdescD1 = idesc_16bit_f32(128, 64, fals
 template <bool kF16> constexpr uint32_t kIdescU = idesc_16bit_f32(128, 64, true, false, false, kF16);
 template <bool kF16> constexpr uint32_t kIdescXO = idesc_16bit_f32(128, 128, false, false, false, kF16);
 template <bool kF16> constexpr uint32_t kIdescX = idesc_16bit_f32(128, 64, false, false, false, kF16);
-template <bool kF16> constexpr uint32_t kIdescDelta = idesc_16bit_f32(128, 64, false, false, true, kF16);
+constexpr uint32_t kIdescDelta = idesc_tf32_f32(128, 64, true);  // X (fp32 in TMEM) times T' (fp32), negated
 template <bool kF16> constexpr uint32_t kIdescO = idesc_16bit_f32(128, 64, false, false, false, kF16);
 template <bool kF16> constexpr uint32_t kIdescS = idesc_16bit_f32(128, 128, false, true, false, kF16);
 
@@ -248,9 +246,10 @@ __device__ __forceinline__ UnitInfo read_unit(const uint8_t* sm, int slot) {
 // ===========================================================================
 // Triangular inverse T = (I + A)^-1 of a strictly lower 64 x 64 A (fp32, rows
 // of kLd floats), computed in place by the two intra warpgroups (256 threads),
-// followed by the two bf16 operands of the Delta and U products,
-// T' = T diag(cw) and T'' = T diag(bn) (K-major [64 i][64 j], 128-byte
-// swizzle; their blocks above the diagonal are never written and stay zero).
+// followed by the operands of the Delta and U products, T' = T diag(cw) in
+// fp32 (tf32 operand) and T'' = T diag(bn) in the 16-bit type (K-major
+// [64 i][64 j], 128-byte swizzle; their blocks above the diagonal are never
+// written and stay zero).
 //   stage 1 (warps 0, 1; warp w owns rows and columns 32w..32w+31): the two
 //     16 x 16 diagonal blocks by forward substitution, one column per lane,
 //     then the block under them, T_10 = -T_11 (A_10 T_00), and a zeroed block
@@ -259,8 +258,8 @@ __device__ __forceinline__ UnitInfo read_unit(const uint8_t* sm, int slot) {
 //     its tiles go from the MMA fragments straight into T' and T'', while the
 //     two diagonal 32 x 32 blocks are converted from shared memory.
 // The 16- and 32-row products are below the 64-row minimum of tcgen05.mma, so
-// they run as warp-level m16n8k8 tf32 MMAs (fp32 accumulate); T is rounded to
-// bf16 for the Delta and U products anyway.
+// they run as warp-level m16n8k8 tf32 MMAs (fp32 accumulate); T feeds the
+// Delta and U products as tf32 and 16-bit operands anyway.
 // ===========================================================================
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
@@ -294,6 +293,20 @@ template <bool kF16>
 __device__ __forceinline__ void st_pair16(uint8_t* tile, int i, int j, float x0, float x1) {
     *reinterpret_cast<uint32_t*>(tile + i * 128 + (((j >> 3) ^ (i & 7)) << 4) + (j & 7) * 2) =
         Elem16<kF16>::pack(x0, x1);
+}
+
+// fp32 elements of a swizzled K-major [64][64] tile stored as two halves of 32 columns (8 KB each, rows of
+// 128 bytes): eight columns j0 .. j0 + 7 (j0 a multiple of 8) of row i, and two columns j, j + 1 (j even).
+__device__ __forceinline__ void st_f32x8(uint8_t* tile, int i, int j0, const float* x) {
+    uint8_t* half = tile + (j0 >> 5) * 8192;
+    const uint32_t c = (j0 & 31) >> 2;
+    *reinterpret_cast<float4*>(half + sw128_offset(i, c)) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(half + sw128_offset(i, c + 1)) = make_float4(x[4], x[5], x[6], x[7]);
+}
+
+__device__ __forceinline__ void st_f32x2(uint8_t* tile, int i, int j, float x0, float x1) {
+    *reinterpret_cast<float2*>(tile + (j >> 5) * 8192 + sw128_offset(i, (j & 31) >> 2) + (j & 3) * 4) =
+        make_float2(x0, x1);
 }
 
 constexpr int kLdX1 = 24, kLdX2 = 40;  // scratch strides: conflict-free B-fragment reads
@@ -379,7 +392,7 @@ __device__ __forceinline__ void tri_inverse_64(float* __restrict__ A, uint8_t* _
             x[q] = tv[q] * cv[q];
             y[q] = tv[q] * ev[q];
         }
-        st_chunk16<kF16>(tp, i, j0 >> 3, x);
+        st_f32x8(tp, i, j0, x);
         st_chunk16<kF16>(tpp, i, j0 >> 3, y);
     }
     named_bar_sync(kBarIntra, kIntraThreads);
@@ -392,8 +405,8 @@ __device__ __forceinline__ void tri_inverse_64(float* __restrict__ A, uint8_t* _
         const int g = lane >> 2, j = nt + 2 * (lane & 3);
         const int i0 = 32 + mt + g, i1 = i0 + 8;
         const float be0 = bn[j], be1 = bn[j + 1], cw0 = cw[j], cw1 = cw[j + 1];
-        st_pair16<kF16>(tp, i0, j, -e[0] * cw0, -e[1] * cw1);
-        st_pair16<kF16>(tp, i1, j, -e[2] * cw0, -e[3] * cw1);
+        st_f32x2(tp, i0, j, -e[0] * cw0, -e[1] * cw1);
+        st_f32x2(tp, i1, j, -e[2] * cw0, -e[3] * cw1);
         st_pair16<kF16>(tpp, i0, j, -e[0] * be0, -e[1] * be1);
         st_pair16<kF16>(tpp, i1, j, -e[2] * be0, -e[3] * be1);
     }
@@ -530,8 +543,8 @@ __device__ __forceinline__ void lds16(const float* src, float* x) {
 // and U (row r = k or v, columns i0..i0+31) and G, in fp32.  U is read from
 // its TMEM columns before the Delta product accumulates into them; W = T' K is
 // not formed by the kernel (the state pass uses X = S K^T instead), so it is
-// computed here on CUDA cores from the bf16 T' and K tiles the tensor cores
-// read (fp32 sums, the products' own precision).  Out of line, so the hot
+// computed here on CUDA cores from the fp32 T' and the K tile the tensor cores
+// read (fp32 sums).  Out of line, so the hot
 // loop stays compact in the instruction cache.
 template <bool kF16>
 __device__ __noinline__ void dump_intra(float* intra_w, float* intra_u, float* intra_g, size_t dump, size_t gdump,
@@ -550,12 +563,11 @@ __device__ __noinline__ void dump_intra(float* intra_w, float* intra_u, float* i
             unpack8<kF16>(*reinterpret_cast<const uint4*>(row + sw128_offset(j, (r & 63) >> 3)), f);
             kc[j] = f[r & 7];
         }
-        for (int i = i0; i < i0 + 32; ++i) {
+        for (int i = i0; i < i0 + 32; ++i) {  // T' row i: fp32, halves of 32 j, 128-byte swizzle
             float acc = 0.f;
-            for (int j8 = 0; j8 < 8; ++j8) {
-                float f[8];
-                unpack8<kF16>(*reinterpret_cast<const uint4*>(tp + sw128_offset(i, j8)), f);
-                for (int q = 0; q < 8; ++q) acc += f[q] * kc[8 * j8 + q];
+            for (int j4 = 0; j4 < 16; ++j4) {
+                const float4 t4 = *reinterpret_cast<const float4*>(tp + (j4 >> 3) * 8192 + sw128_offset(i, j4 & 7));
+                acc += t4.x * kc[4 * j4] + t4.y * kc[4 * j4 + 1] + t4.z * kc[4 * j4 + 2] + t4.w * kc[4 * j4 + 3];
             }
             intra_w[dump + static_cast<size_t>(i) * kHead + r] = acc;
         }
@@ -681,18 +693,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < B_COUNT; ++b) mbar_init(cx.bars + b, 1);
         mbar_init(cx.bars + B_UNIT_EMPTY + 0, 5);
         mbar_init(cx.bars + B_UNIT_EMPTY + 1, 5);
+        for (int b = 0; b < 3; ++b) mbar_init(cx.bars + B_GATES_EMPTY + b, 8);  // one arrival per state warp
         fence_mbar_init();
         if (p.has_tokens) {
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
-            prefetch_tensormap(&tm_o);
         }
     }
-    for (uint32_t off = tid * 16; off < 32768; off += kThreads * 16)  // T', T'' and both P buffers
+    for (uint32_t off = tid * 16; off < kAbuf - kTp; off += kThreads * 16)  // both T', T'' and both P buffers
         *reinterpret_cast<uint4*>(sm + kTp + off) = make_uint4(0, 0, 0, 0);
-    for (uint32_t off = tid * 16; off < 8192; off += kThreads * 16)   // the second T' buffer
-        *reinterpret_cast<uint4*>(sm + kTp1 + off) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 3) {
         tmem_alloc(s_tmem, kTmCols);
@@ -877,8 +887,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_ts_elect(tmem + kTmX, tmem + kTmSbf + ks * 8, dkq + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
                                      kTransfer ? kIdescX<kF16> : kIdescXO<kF16>, ks > 0);
                     mma_commit_elect(cx.bars + B_XO_FULL);
-                    // Delta~^T = U~^T - X T'^T (A = X as bf16 pairs, negated; U = 0 for a transfer-matrix unit)
-                    if (!(ok = wait_bar_warp(cx, B_XB_FULL, n & 1))) break;
+                    // Delta~^T = U~^T - X T'^T: tf32 products with A = X read as fp32 straight from TMEM (negated)
+                    // and T' in fp32, once X is complete (U = 0 for a transfer-matrix unit).  The test instance
+                    // also waits for the state warps to have read U (XB_FULL).
+                    if (!(ok = wait_bar_warp(cx, B_XO_FULL, n & 1))) break;
+                    if (kDump && !(ok = wait_bar_warp(cx, B_XB_FULL, n & 1))) break;
                     if (!(ok = wait_bar_warp(cx, B_T_FULL + s, ph))) break;
                     if (!(ok = wait_bar_warp(cx, B_U_FULL + s, ph))) break;
                     tc_fence_after();
@@ -886,8 +899,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t dbuf = tmem + kTmDelta + s * 64;
                     const uint32_t acc0 = !(kTransfer && info.valid == 2);
 #pragma unroll 1
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_ts_elect(dbuf, tmem + kTmXbf + ks * 8, dtp + ks * 2, kIdescDelta<kF16>, ks > 0 ? 1u : acc0);
+                    for (int ks = 0; ks < 8; ++ks)  // j = 8 ks .. 8 ks + 7: 32 bytes of a T' row, halves of 32 j
+                        mma_ts_tf32_elect(dbuf, tmem + kTmX + ks * 8, dtp + ((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4),
+                                          kIdescDelta, ks > 0 ? 1u : acc0);
                     mma_commit_elect(cx.bars + B_DELTA_FULL + s);
                     // O += Delta^T P^T (its own commit, so the output epilogue overlaps the S product), then
                     // S += (decayed Delta)^T K
@@ -1163,12 +1177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t gs = n % 3;
                 const float* gb = reinterpret_cast<const float*>(sm + kGbuf) + gs * kGFloats;
                 const uint32_t dbuf = tm_lane + kTmDelta + s * 64;
-                // ---- X = S K^T as bf16 pairs (A operand of the Delta product), into the bf16 S columns, which
-                //      the X | O product has finished reading.  This thread: row v, columns 32 hh .. 32 hh + 31.
-                ok = wait_bar(cx, B_XO_FULL, n & 1);
-                tc_fence_after();
                 if constexpr (kDump) {
-                    // test dumps: U before the Delta product accumulates onto it, W from T' and K
+                    // test dumps: U before the Delta product accumulates onto it (the issuer waits for XB_FULL in
+                    // this instance), W from T' and K
+                    ok = wait_bar(cx, B_XO_FULL, n & 1);
                     ok = ok && wait_bar(cx, B_U_FULL + s, ph) && wait_bar(cx, B_T_FULL + s, ph);
                     tc_fence_after();
                     dump_intra<kF16>(p.intra_w, p.intra_u, p.intra_g,
@@ -1177,21 +1189,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      sm + (s ? kTp1 : kTp), sm + kKQ + (n % kKQStages) * kKQStage,
                                      dbuf + 32 * hh, v, 32 * hh, st,
                                      reinterpret_cast<const float*>(sm + kGbuf) + gs * kGFloats + kGG);
+                    tc_fence_before();
+                    if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
+                    if (st == 0) mbar_arrive(cx.bars + B_XB_FULL);
                 }
-                {
-                    uint32_t rx[32], pk[16];
-                    tmem_ld32_wait(tm_lane + kTmX + 32 * hh, rx);
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) pk[q] = E::pack(__uint_as_float(rx[2 * q]), __uint_as_float(rx[2 * q + 1]));
-                    tmem_st16(tm_lane + kTmXbf + 16 * hh, pk);
-                    tmem_wait_st();
-                }
-                tc_fence_before();
-                if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
-                if (st == 0) mbar_arrive(cx.bars + B_XB_FULL);
                 // ---- Delta epilogue: this thread's 32 columns j in [32 hh, 32 hh + 32) go back into TMEM as
                 //      16 packed bf16 Delta words followed by 16 packed decayed words (A operands of O2 and S)
-                ok = wait_bar(cx, B_DELTA_FULL + s, ph);
+                ok = ok && wait_bar(cx, B_DELTA_FULL + s, ph);
                 tc_fence_after();
                 {
                     uint32_t ra[32], pk[16];
@@ -1211,7 +1215,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st16(dbuf + 32 * hh + 16, pk);
                     tmem_wait_st();
                 }
-                if (st == 0) bulk_wait_group_read0();  // the previous chunk's output store has read outT
                 tc_fence_before();
                 if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
                 if (st == 0) mbar_arrive(cx.bars + B_DD_FULL + s);
@@ -1249,9 +1252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!last) mbar_arrive(cx.bars + B_SB_FULL + ((n + 1) & 1));
                     if (!kTransfer) mbar_arrive(cx.bars + B_O_EMPTY + s);
                 }
-                // ---- output, part 2: o_i = scale rm_i (S Q'^T + Delta^T P^T)_i into the output tile, then its store
+                // ---- output, part 2: o_i = scale rm_i (S Q'^T + Delta^T P^T)_i into the output tile (once the previous
+                //      chunk's store has read it), then one TMA store of a full chunk, or the valid rows of a tail.
+                //      (Stores straight from registers were measured slower than the tile and its bulk store.)
                 if (!kTransfer) {
                     if (p.l2norm) ok = ok && wait_bar(cx, B_RM_FULL + gs, (n / 3) & 1);
+                    if (st == 0) bulk_wait_group_read0();
+                    ok = named_bar_and(kBarState, kStateThreads, ok);
                     const float sc = p.scale;
 #pragma unroll
                     for (int i0 = 0; i0 < 32; i0 += 8) {
@@ -1265,13 +1272,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                     if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
                     if (Lc == kChunk) {
-                        // a full chunk: one TMA store of the 64 x 128 tile (rows all belong to this sequence)
                         if (st == 0) {
                             tma_store_3d(&tm_o, sm + kOutT, 0, info.h, static_cast<int32_t>(tc));
                             bulk_commit_group();
                         }
                     } else {
-                        // the tail: coalesced copy of the valid rows only, 16 threads per 256-byte row
                         uint8_t* gout = static_cast<uint8_t*>(p.output);
 #pragma unroll 1
                         for (int k = 0; k < 4; ++k) {
@@ -1284,7 +1289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (st == 0) mbar_arrive(cx.bars + B_GATES_EMPTY + gs);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cx.bars + B_GATES_EMPTY + gs);  // one arrival per state warp
                 // a checkpoint where the chunk end, local token 64 (c + 1), is inside the sequence: this thread's 64
                 // columns go to the dense checkpoint row in the checkpoint type
                 int64_t ck_off = -1;

@@ -109,20 +109,16 @@ bool encode_qkv_map(CUtensorMap* map, const void* base, int64_t T, int32_t heads
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Output [T, H, 128] (dtype of q) as a 3-D TMA map with 128 x 1 x 64 boxes, no
-// swizzle (the kernel stages a 64 x 128 row-major tile).
 bool encode_out_map(CUtensorMap* map, void* base, int64_t T, int32_t heads, gdn_dtype t) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(gdn::kHead), static_cast<cuuint64_t>(heads),
-                          static_cast<cuuint64_t>(T)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(gdn::kHead) * 2,
-                             static_cast<cuuint64_t>(heads) * gdn::kHead * 2};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(gdn::kHead), 1, static_cast<cuuint32_t>(gdn::kChunk)};
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(gdn::kHead), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(T)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(gdn::kHead) * 2, static_cast<cuuint64_t>(heads) * gdn::kHead * 2};
+    cuuint32_t box[3] = {128, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(map, tma_type(t), 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
 }
 
 // The state layout of a run: the plan's state type and the args' strides
@@ -387,10 +383,10 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
         return GDN_OK;
     }
     CUtensorMap tq, tk, tv, to;
+    std::memset(&to, 0, sizeof(to));
     std::memset(&tq, 0, sizeof(tq));
     std::memset(&tk, 0, sizeof(tk));
     std::memset(&tv, 0, sizeof(tv));
-    std::memset(&to, 0, sizeof(to));
     if (T > 0) {
         const gdn_dtype t = d.qkv_dtype;
         if (!encode_qkv_map(&tq, a.q, T, d.num_q_heads, t) || !encode_qkv_map(&tk, a.k, T, d.num_k_heads, t) ||

@@ -322,6 +322,16 @@ __host__ __device__ constexpr uint32_t idesc_16bit_f32(uint32_t M, uint32_t N, b
            | ((M >> 4) << 24);              // M / 16
 }
 
+// Instruction descriptor for kind::tf32 with fp32 accumulate (A and B formats: tf32 = 2), K-major B.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(uint32_t M, uint32_t N, bool neg_a) {
+    return (1u << 4)                        // D format: f32
+           | (2u << 7)                      // A format: tf32
+           | (2u << 10)                     // B format: tf32
+           | ((neg_a ? 1u : 0u) << 13)      // negate A
+           | ((N >> 3) << 17)               // N / 8
+           | ((M >> 4) << 24);              // M / 16
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn = false, bool b_mn = false,
                                                       bool neg_a = false) {
     return idesc_16bit_f32(M, N, a_mn, b_mn, neg_a, false);
@@ -377,6 +387,19 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
         "setp.ne.b32 p, %4, 0;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T with tf32 operands (.kind::tf32: K = 8 per instruction; A is fp32 in TMEM,
+// one element per 32-bit column; B is fp32 in shared memory), from a converged warp.
+__device__ __forceinline__ void mma_ts_tf32_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
