@@ -261,19 +261,19 @@ __device__ __forceinline__ UnitInfo read_unit(const uint8_t* sm, int slot) {
 // they run as warp-level m16n8k8 tf32 MMAs (fp32 accumulate); T feeds the
 // Delta and U products as tf32 and 16-bit operands anyway.
 // ===========================================================================
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
 
-// D (16 x 8) += A (16 x 8, row-major, stride lda) * B (8 x 8, row-major K x N, stride ldb)
+// D (16 x 8) += A (16 x 8, row-major, stride lda) * B (8 x 8, row-major K x N, stride ldb).  The operands
+// go to the tensor core as fp32 bits, which it reads as tf32 (the low mantissa bits dropped): a conversion
+// with rounding per fragment element cost more time than the bit it saves (T is rounded to tf32 and bf16
+// for the Delta and U products anyway).  A comes in with one ldmatrix (rows 16-byte aligned).
 __device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const float* A, int lda, const float* B, int ldb,
                                                 int lane) {
     const int g = lane >> 2, t = lane & 3;
-    const uint32_t a0 = to_tf32(A[g * lda + t]), a1 = to_tf32(A[(g + 8) * lda + t]);
-    const uint32_t a2 = to_tf32(A[g * lda + t + 4]), a3 = to_tf32(A[(g + 8) * lda + t + 4]);
-    const uint32_t b0 = to_tf32(B[t * ldb + g]), b1 = to_tf32(B[(t + 4) * ldb + g]);
+    uint32_t a0, a1, a2, a3;  // ldmatrix: row (lane & 15), columns 4 (lane >> 4) .. + 3 of the 16 x 8 tile
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(smem_u32(A + (lane & 15) * lda + (lane >> 4) * 4)));
+    const uint32_t b0 = __float_as_uint(B[t * ldb + g]), b1 = __float_as_uint(B[(t + 4) * ldb + g]);
     asm volatile(
         "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
