@@ -24,21 +24,55 @@ namespace {
 static __device__ __align__(256) uint8_t g_static_workspace[GDN_PREFILL_STATIC_WORKSPACE_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_static_workspace_addr[kMaxDevices] = {};
+struct CachedAddress {
+    unsigned long long context_id;  // the context the address belongs to (0: none yet)
+    void* addr;
+};
+CachedAddress g_static_workspace_addr[kMaxDevices] = {};
 std::mutex g_static_lock;
 
-// Device address of the array on the current device, looked up once per
-// device (host code only sees a stand-in symbol, never the device address).
+// The driver's cuCtxGetCurrent and cuCtxGetId, through the runtime's entry-point query (no link-time
+// dependency on the driver library).  A context id is unique for the life of the process, so a context that
+// a device reset re-creates gets a fresh look-up of the array's address.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of the array on the current device (host code only sees a stand-in symbol, never the device
+// address), looked up once per device and context.
 gdn_status static_workspace(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
     std::lock_guard<std::mutex> guard(g_static_lock);
-    if (!g_static_workspace_addr[dev]) {
+    CachedAddress& c = g_static_workspace_addr[dev];
+    const unsigned long long id = current_context_id();
+    if (!c.addr || id == 0 || id != c.context_id) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess || !ptr) return GDN_ERR_CUDA;
-        g_static_workspace_addr[dev] = ptr;
+        c.addr = ptr;
+        c.context_id = current_context_id();  // after the look-up, which makes the device's context current
     }
-    *out = g_static_workspace_addr[dev];
+    *out = c.addr;
     return GDN_OK;
 }
 

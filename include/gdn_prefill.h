@@ -245,7 +245,9 @@ gdn_status gdn_prefill_workspace_layout(gdn_prefill_plan_t plan, gdn_prefill_lay
  *     sequences and 6 million tokens).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept per device and
+ *     context: after a device reset the first call on the new context looks
+ *     it up again (and must again come before any capture).
  *   - All calls share the array, and the prepare kernel resets what must start
  *     at zero on every call.  Calls whose kernels overlap on the GPU (other
  *     streams, or host threads without ordering between them) race on it.

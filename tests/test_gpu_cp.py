@@ -79,3 +79,15 @@ def test_cp_fp8_state_pool_and_fp8_checkpoints(state_dtype):
     res = run_gpu(to_device(inp), use_cp=True, return_plan=True, ckpt_dtype=state_dtype)
     assert _cp_segments(res, inp) >= 2
     check_against_oracle(inp, res)
+
+
+def test_cp_eight_segments_long_sequence():
+    # one sequence, two state heads: N * H = 2 on a 152-SM GPU gives the plan's maximum of eight segments,
+    # whose start states come from seven chained transfers (each rounded through the 16-bit state operand)
+    w = wl.custom(seq_lens=[4096], hq=2, hk=2, hv=2, initial_state="dense", l2norm_in_kernel=True,
+                  qk_prenorm=False, alpha="u(0.95,1.0)", checkpoint_every=256)
+    inp = wl.generate(w, seed=65)
+    res = run_gpu(to_device(inp), use_cp=True, return_plan=True)
+    if torch.cuda.get_device_properties(0).multi_processor_count >= 30:
+        assert _cp_segments(res, inp) == 8
+    check_against_oracle(inp, res)

@@ -5,13 +5,17 @@ synchronisation and no host read of device memory, so a serving loop can
 capture them once and replay them with new data in the same buffers.  These
 tests capture each call into a graph, refill the inputs in place, replay, and
 require the replay to equal an eager call on the new inputs bit for bit (each
-(sequence, head) unit is computed the same way whichever CTA takes it)."""
+(sequence, head) unit is computed the same way whichever CTA takes it), and
+the replayed results to match the fp64 oracle on those inputs.  The
+context-parallel path (transfer pass, scan, segment pass, final copy) is
+captured the same way ("FlashInfer GDN Prefill 完全指南", the section on plan
+caching, address rebinding and CUDA Graph replay)."""
 import pytest
 import torch
 
 import gated_deltanet_chunked_device_gb300 as gdn
 from gated_deltanet_chunked_device_gb300 import workloads as wl
-from gdn_testlib import to_device
+from gdn_testlib import check_against_oracle, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -32,7 +36,8 @@ def _refill(dst, src):
 def test_prefill_graph_replay_matches_eager():
     w = wl.custom(seq_lens=[300, 0, 77, 130], hq=4, hk=4, hv=8, initial_state="dense", l2norm_in_kernel=True,
                   qk_prenorm=False, checkpoint_every=64)
-    a, b = (to_device(wl.generate(w, seed=s)) for s in (40, 41))
+    b_cpu = wl.generate(w, seed=41)
+    a, b = to_device(wl.generate(w, seed=40)), to_device(b_cpu)
     ck = torch.zeros(wl.num_checkpoints(a["seq_lens"], 64), a["H"], 128, 128, device="cuda")
     out = torch.empty(a["T"], a["H"], 128, dtype=a["q"].dtype, device="cuda")
     fin = torch.empty_like(a["initial_state"])
@@ -60,12 +65,49 @@ def test_prefill_graph_replay_matches_eager():
     assert torch.equal(out, out_e)
     assert torch.equal(fin, fin_e)
     assert torch.equal(ck, ck_e)
+    check_against_oracle(b_cpu, {"output": out, "final_state": fin, "checkpoints": ck})
+
+
+def test_context_parallel_graph_replay_matches_eager_and_oracle():
+    # few (sequence, head) units: the run takes segments; all its launches go into one graph
+    w = wl.custom(seq_lens=[1500, 70], hq=2, hk=2, hv=2, initial_state="dense", l2norm_in_kernel=True,
+                  qk_prenorm=False, checkpoint_every=128)
+    b_cpu = wl.generate(w, seed=48)
+    a, b = to_device(wl.generate(w, seed=47)), to_device(b_cpu)
+    ck = torch.zeros(wl.num_checkpoints(a["seq_lens"], 128), a["H"], 128, 128, device="cuda")
+    out = torch.empty(a["T"], a["H"], 128, dtype=a["q"].dtype, device="cuda")
+    fin = torch.empty_like(a["initial_state"])
+
+    def call(d, out_, fin_, ck_, return_plan=False):
+        return gdn.chunk_gated_delta_rule(
+            d["q"], d["k"], d["v"], g=d["g"], beta=d["beta"], scale=d["scale"], initial_state=d["initial_state"],
+            output_final_state=True, cu_seqlens=d["cu_seqlens"], use_qk_l2norm_in_kernel=True, output=out_,
+            output_state=fin_, state_checkpoints=ck_, checkpoint_cu_starts=d["checkpoint_cu_starts"],
+            checkpoint_every_n_tokens=128, use_cp=True, return_plan=return_plan)
+
+    live = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in a.items()}
+    _, plan, _ = call(live, out, fin, ck, return_plan=True)  # eager: plan, workspace, kernel attributes
+    assert gdn.lib().gdn_prefill_cp_segments(plan.handle, 2, a["T"], 0) >= 2
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(live, out, fin, ck)
+    _refill(live, b)
+    live["initial_state"].copy_(b["initial_state"])
+    g.replay()
+    torch.cuda.synchronize()
+    out_e, fin_e, ck_e = torch.empty_like(out), torch.empty_like(fin), torch.zeros_like(ck)
+    call(b, out_e, fin_e, ck_e)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_e) and torch.equal(fin, fin_e) and torch.equal(ck, ck_e)
+    check_against_oracle(b_cpu, {"output": out, "final_state": fin, "checkpoints": ck})
 
 
 def test_decode_graph_replay_matches_eager():
     w = wl.custom(seq_lens=[1] * 40, hq=8, hk=8, hv=16, initial_state="pool", n_pool=64, l2norm_in_kernel=True,
                   qk_prenorm=False)
-    a, b = (to_device(wl.generate(w, seed=s)) for s in (42, 43))
+    b_cpu = wl.generate(w, seed=43)
+    a, b = to_device(wl.generate(w, seed=42)), to_device(b_cpu)
     pool = a["initial_state"].clone()
     out = torch.empty(a["T"], a["H"], 128, dtype=a["q"].dtype, device="cuda")
     live = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in a.items()}
@@ -89,6 +131,7 @@ def test_decode_graph_replay_matches_eager():
     torch.cuda.synchronize()
     assert torch.equal(out, out_e)
     assert torch.equal(pool, pool_e)
+    check_against_oracle(b_cpu, {"output": out, "final_state": pool})
 
 
 def test_one_plan_serves_rotating_buffers_and_smaller_batches():
