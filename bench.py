@@ -51,6 +51,11 @@ from gated_deltanet_chunked_device_gb300 import workloads as wl  # noqa: E402
 METRIC = "GDN prefill tokens/s and TFLOP/s as % of GB300 dense BF16 roofline, 1 GPU"
 FLOP_DENSE = 180224       # per token per state head: 10*C*D + 6*D^2, dense 64/128 tiles
 FLOP_TRI = 140630         # per token per state head: triangular-aware count
+# the arithmetic type each input type computes in, and the chunk kernel instance that runs it
+DTYPE_NAMES = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}
+CHUNK_KERNEL_NAMES = {torch.bfloat16: "gdn_chunk_kernel<__nv_bfloat16, false, false>",
+                      torch.float16: "gdn_chunk_kernel<__half, false, false>",
+                      torch.float32: "gdn_chunk_f32_kernel"}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
@@ -79,10 +84,43 @@ def max_over_ranks(x, dist=None, device=None):
     return float(t.item())
 
 
-def job_tokens_per_s(world, tokens_per_rank, ms):
-    """Whole-job throughput: every rank prefills its own copy of the workload
-    (units are independent), so the job processes world x tokens per step."""
-    return world * tokens_per_rank / (ms / 1e3)
+def job_tokens_per_s(copies, tokens_per_copy, ms):
+    """Whole-job throughput: the job processes `copies` whole batches per step (replicas: every rank prefills its
+    own copy, so copies = world; a head-split batch is one copy spread over the ranks)."""
+    return copies * tokens_per_copy / (ms / 1e3)
+
+
+def head_shard(H, hq, hk, hv, rank, world):
+    """The heads rank `rank` of `world` takes when one batch is split by state head (the (sequence, head) units
+    are independent: no exchange).  State heads [a, b) with b - a = H / world, and the q, k and v heads those
+    read under the grouped head mapping (state head h reads q head h / (H / hq), and so on): each a contiguous
+    range, so every rank runs the same problem shape with hq, hk, hv and H divided by `world`.  Raises when the
+    head counts do not divide."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("bad rank / world")
+    for name, n in (("state", H), ("q", hq), ("k", hk), ("v", hv)):
+        if n % world:
+            raise ValueError(f"{n} {name} heads do not split over {world} ranks")
+    per = {"h": H // world, "q": hq // world, "k": hk // world, "v": hv // world}
+    return {key: (rank * n, (rank + 1) * n) for key, n in per.items()}
+
+
+def shard_heads(w, inp, rank, world):
+    """This rank's part of a head-split batch: the workload with its head counts divided and the inputs sliced
+    (contiguous copies) to this rank's heads."""
+    import dataclasses
+    r = head_shard(inp["H"], w.hq, w.hk, w.hv, rank, world)
+    out = dict(inp)
+    for key, hk_ in (("q", "q"), ("k", "k"), ("v", "v")):
+        a, b = r[hk_]
+        out[key] = inp[key][:, a:b].contiguous()
+    a, b = r["h"]
+    out["g"] = inp["g"][:, a:b].contiguous()
+    out["beta"] = inp["beta"][:, a:b].contiguous()
+    if inp.get("initial_state") is not None:
+        out["initial_state"] = inp["initial_state"][:, a:b].contiguous()
+    out["H"] = b - a
+    return dataclasses.replace(w, hq=w.hq // world, hk=w.hk // world, hv=w.hv // world), out
 
 
 def algorithmic_bytes(w, inp):
@@ -430,12 +468,19 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--op", choices=["prefill", "decode"], default="prefill")
     ap.add_argument("--cp", action="store_true", help="allow context parallelism (few (sequence, head) units)")
+    ap.add_argument("--shard", choices=["replica", "heads"], default="replica",
+                    help="multi-GPU: every rank runs its own copy of the batch (weak scaling), or the ranks split "
+                         "one batch's state heads (strong scaling); no data-path collective either way")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.op == "decode" and args.workload == wl.BENCH_WORKLOAD:
         args.workload = "decode_gva_512seq_bf16"
     w = wl.WORKLOADS[args.workload]
     inp = wl.generate(w, seed=args.seed)
+    full_batches = world if args.shard == "replica" else 1  # copies of the whole batch the job runs per step
+    tokens_batch = inp["T"]
+    if args.shard == "heads" and world > 1 and args.impl == "ours":
+        w, inp = shard_heads(w, inp, rank, world)
 
     if args.impl == "reference":
         if rank == 0:
@@ -517,52 +562,73 @@ def main():
     torch.cuda.synchronize(device)
     unflushed_ms = sum(evu[i][0].elapsed_time(evu[i][2]) for i in range(Ku)) / Ku
 
-    # ---- end to end through the public API, host buffers
+    # ---- end to end through the public API, host buffers: every step copies its inputs in from pinned host
+    #      memory and its results out.  Two sets of device buffers and three streams (copy in, compute, copy
+    #      out) let step i's copy-in and step i-1's copy-out run while step i-1 / step i compute: the two
+    #      directions and the compute overlap, the computes stay in order on one stream (one workspace).
     e2e = None
     if not args.no_e2e:
-        host_in = {k: inp[k].pin_memory() for k in ("q", "k", "v", "g", "beta", "cu_seqlens")}
-        if inp.get("checkpoint_cu_starts") is not None:
-            host_in["checkpoint_cu_starts"] = inp["checkpoint_cu_starts"].pin_memory()
-        if inp.get("initial_state") is not None:
-            host_in["initial_state"] = inp["initial_state"].pin_memory()
-        if inp.get("state_indices") is not None:
-            host_in["state_indices"] = inp["state_indices"].pin_memory()
-        host_out = {"output": torch.empty_like(call["out"], device="cpu").pin_memory()}
-        if call["ck"] is not None:
-            host_out["checkpoints"] = torch.empty_like(call["ck"], device="cpu").pin_memory()
-        if call["fin"] is not None or inp.get("state_indices") is not None:
-            src = call["kw"]["output_state"]
-            host_out["final_state"] = torch.empty_like(src, device="cpu").pin_memory()
-        dev_in = {k: call["dev"][k] for k in host_in}
+        sets = [call, make_call(inp, device, use_cp=args.cp)]
+        in_keys = [k for k in ("q", "k", "v", "g", "beta", "cu_seqlens", "checkpoint_cu_starts", "initial_state",
+                               "state_indices") if inp.get(k) is not None]
+        host_in = {k: inp[k].pin_memory() for k in in_keys}
+
+        def outs(c):
+            o = {"output": c["out"]}
+            if c["ck"] is not None:
+                o["checkpoints"] = c["ck"]
+            if c["fin"] is not None or inp.get("state_indices") is not None:
+                o["final_state"] = c["kw"]["output_state"]
+            return o
+
+        host_out = {k: torch.empty_like(t, device="cpu").pin_memory() for k, t in outs(call).items()}
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+        ev_in = [torch.cuda.Event() for _ in sets]
+        ev_done = [torch.cuda.Event() for _ in sets]
+        ev_free = [torch.cuda.Event() for _ in sets]
+        for e in ev_free:
+            e.record(stream)
         Ke = max(3, min(K, 50))
 
-        def e2e_step():
-            for k2, t in host_in.items():
-                dev_in[k2].copy_(t, non_blocking=True)
-            step()
-            host_out["output"].copy_(call["out"], non_blocking=True)
-            if "checkpoints" in host_out:
-                host_out["checkpoints"].copy_(call["ck"], non_blocking=True)
-            if "final_state" in host_out:
-                host_out["final_state"].copy_(call["kw"]["output_state"], non_blocking=True)
+        def e2e_step(i):
+            b = i % 2
+            c = sets[b]
+            s_in.wait_event(ev_free[b])                 # set b's previous results have been copied out
+            with torch.cuda.stream(s_in):
+                for k2, t in host_in.items():
+                    c["dev"][k2].copy_(t, non_blocking=True)
+            ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            st = gdn.gdn_prefill_prepare(c["plan"].handle, c["args"], c["ws"].data_ptr(),
+                                         c["plan"].workspace_bytes, sp)
+            st |= gdn.gdn_prefill_chunks(c["plan"].handle, c["args"], c["ws"].data_ptr(),
+                                         c["plan"].workspace_bytes, sp)
+            if st:
+                raise RuntimeError(f"gdn_prefill returned {st}")
+            ev_done[b].record(stream)
+            s_out.wait_event(ev_done[b])
+            with torch.cuda.stream(s_out):
+                for k2, t in outs(c).items():
+                    host_out[k2].copy_(t, non_blocking=True)
+            ev_free[b].record(s_out)
 
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                e2e_step()
+        for i in range(3):
+            e2e_step(i)
         torch.cuda.synchronize(device)
         es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            es.record(stream)
-            for _ in range(Ke):
-                e2e_step()
-            ee.record(stream)
+        es.record(s_in)
+        for i in range(Ke):
+            e2e_step(i)
+        ee.record(s_out)
         torch.cuda.synchronize(device)
         e2e_ms = es.elapsed_time(ee) / Ke
         e2e_ms = max_over_ranks(e2e_ms, pg, device)
-        e2e = {"value": job_tokens_per_s(world, inp["T"], e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+        e2e = {"value": job_tokens_per_s(full_batches, tokens_batch, e2e_ms), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "link_gb_per_s": (h2d + d2h) / (e2e_ms / 1e3) / 1e9,
+               "pipelined": "two buffer sets; copy-in, compute and copy-out streams overlap"}
 
     clocks = sampler.stop() if sampler else None
     if rank != 0:
@@ -578,15 +644,18 @@ def main():
     tflops_tri = T * H * FLOP_TRI / (ms_per_step / 1e3) / 1e12
     roof_time = max(abytes / (hbm * 1e9), T * H * FLOP_DENSE / (bf16 * 1e12))
     line = {
-        "metric": METRIC, "value": job_tokens_per_s(world, T, ms_per_step), "unit": "tokens/s", "n_gpus": world,
-        "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_config(w, inp, args), context_parallel_segments=cp_segments),
+        "metric": METRIC, "value": job_tokens_per_s(full_batches, tokens_batch, ms_per_step), "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak" if args.shard == "replica" else "strong",
+        "vs_baseline": None, "dtype": DTYPE_NAMES[w.dtype], "data": "synthetic",
+        "config": dict(workload_config(w, inp, args), context_parallel_segments=cp_segments,
+                       parallelism=(f"replicas{world}" if args.shard == "replica" else f"heads{world}")),
         "tflops": {"dense_tile_count": tflops_dense, "triangular_aware": tflops_tri,
                    "pct_of_bf16_peak": 100 * tflops_dense / bf16, "peak_tflops": bf16, "peak_source": src},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": traffic if not cp_segments else None,
-                     "kernel": ("gdn_chunk_kernel<__nv_bfloat16, false>" if not cp_segments
+                     "kernel": (CHUNK_KERNEL_NAMES[w.dtype] if not cp_segments
                                 else "chunk stage with context parallelism (transfer pass, scan, segment pass)"),
                      "kernel_ms": chunk_avg_ms,
                      "algorithmic_bytes": abytes, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
