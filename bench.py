@@ -503,7 +503,12 @@ def main():
         return
     call = make_call(inp, device, use_cp=args.cp)
     plan, ws, cargs = call["plan"], call["ws"], call["args"]
-    cp_segments = int(gdn.lib().gdn_prefill_cp_segments(plan.handle, len(inp["seq_lens"]), inp["T"], 0)) if args.cp else 0
+    cp_segments = gdn.gdn_prefill_cp_segments(plan.handle, inp["seq_lens"], 0)[0] if args.cp else 0
+    # the context-parallel launches run whenever the plan allows them, unless max_seqlen (passed by make_call)
+    # already rules out any gain: 0.85 ceil(max_seqlen / 64) <= H T / (64 S), as the header states
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    cmax = -(-max(inp["seq_lens"]) // 64) if inp["seq_lens"] else 0
+    cp_route = bool(args.cp and w.dtype != torch.float32 and 85 * cmax * 64 * sms > 100 * inp["H"] * inp["T"])
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.Stream(device)
     sp = stream.cuda_stream
@@ -661,9 +666,9 @@ def main():
                      "algorithmic_bytes": abytes, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
                      if src == "measured" else "fallback 6800 GB/s",
                      "step_frac_of_roofline_time": roof_time / (ms_per_step / 1e3)},
-        # prepare + chunk kernel; with context parallelism the chunk stage is cp_prepare, the transfer
+        # prepare + chunk kernel; on the context-parallel route the chunk stage is cp_prepare, the transfer
         # pass, the scan, the segment prepare, the segment pass and (with a final state) the state copy
-        "gpu_launches": K * ((6 + (1 if inp["output_final_state"] else 0)) if cp_segments else 2),
+        "gpu_launches": K * ((6 + (1 if inp["output_final_state"] else 0)) if cp_route else 2),
         "wall_s_timed_region": wall,
         "step_ms_stats": {"mean": sum(step_ms) / K, "median": statistics.median(step_ms), "min": min(step_ms),
                           "max": max(step_ms), "unflushed_mean": unflushed_ms, "unflushed_steps": Ku},

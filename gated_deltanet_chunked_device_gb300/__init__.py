@@ -18,9 +18,10 @@ section "chunk_gated_delta_rule API 全参数解析"):
                            max_seqlen=None)
 
 returning ``output`` or ``(output, final_state)``; with ``state_indices`` the
-final state is the pool itself.  The pages' ``use_cp``, ``_cp_chunk_len`` and
-``backend`` arguments select among other libraries' kernels and have no
-counterpart here.
+final state is the pool itself.  ``use_cp`` allows context parallelism inside
+the GPU (long sequences cut into segments chosen on the device); the pages'
+``_cp_chunk_len`` and ``backend`` arguments select among other libraries'
+kernels and have no counterpart here.
 """
 from __future__ import annotations
 
@@ -129,7 +130,8 @@ def lib():
                 L.gdn_prefill_workspace_layout.argtypes = [ctypes.c_void_p, ctypes.POINTER(Layout)]
                 L.gdn_prefill_workspace_layout.restype = ctypes.c_int
                 L.gdn_prefill_plan_destroy.argtypes = [ctypes.c_void_p]
-                L.gdn_prefill_cp_segments.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32]
+                L.gdn_prefill_cp_segments.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.c_int32,
+                                                      ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
                 L.gdn_prefill_cp_segments.restype = ctypes.c_int32
                 L.gdn_prefill_plan_destroy.restype = None
                 L.gdn_status_string.argtypes = [ctypes.c_int]
@@ -189,6 +191,16 @@ def gdn_prefill_workspace_layout(plan) -> Layout:
     if st != 0:
         raise GdnError(st, "gdn_prefill_workspace_layout")
     return lay
+
+
+def gdn_prefill_cp_segments(plan, seq_lens, sm_count_hint: int = 0):
+    """Returns (largest segment count or 0, per-sequence counts): the
+    context-parallel choice a run of this plan makes for these host lengths."""
+    n = len(seq_lens)
+    lens = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in seq_lens])
+    segs = (ctypes.c_int32 * max(n, 1))()
+    most = lib().gdn_prefill_cp_segments(plan, lens, n, int(sm_count_hint), segs)
+    return int(most), [int(segs[i]) for i in range(n)]
 
 
 def gdn_prefill_plan_destroy(plan) -> None:
@@ -304,9 +316,9 @@ def chunk_gated_delta_rule(q, k, v, g=None, beta=None, scale=None, initial_state
     (it is its length minus one).  ``intermediates``, when a dict, receives
     the intra-chunk outputs G, W and U per flat chunk (fp32).  With
     ``return_plan`` the plan and workspace are returned as well (for status
-    and chunk-map reads).  ``use_cp`` allows context parallelism: batches
-    with few (sequence, head) units run each sequence as segments on more
-    SMs (a larger workspace; the same results within rounding).
+    and chunk-map reads).  ``use_cp`` allows context parallelism: the
+    sequences that set the run's time run as segments on more SMs, chosen on
+    the device (a larger workspace; the same results within rounding).
     """
     if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
         raise ValueError("q, k, v must be [total_tokens, heads, head_size]")
@@ -338,7 +350,7 @@ def chunk_gated_delta_rule(q, k, v, g=None, beta=None, scale=None, initial_state
         flags |= FLAGS["HAS_SCALE"]
     if use_qk_l2norm_in_kernel:
         flags |= FLAGS["QK_L2NORM"]
-    if use_cp:  # the library uses it when the batch has few (sequence, head) units
+    if use_cp:  # the library segments the sequences that its load model says gain from it
         flags |= FLAGS["CONTEXT_PARALLEL"]
     if cu_seqlens.dtype == torch.int64:
         flags |= FLAGS["CU_SEQLENS_I64"]

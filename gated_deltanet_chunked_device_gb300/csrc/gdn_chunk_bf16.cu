@@ -169,7 +169,8 @@ struct Elem16<true> {
 constexpr long long kWaitCycles = 2000000000LL;  // about one second
 
 struct UnitInfo {
-    int32_t valid, seq, h, nC;  // valid: 0 = no more units, 1 = a unit, 2 = a transfer-matrix unit (identity, U = 0)
+    int32_t valid, seq, h, nC;  // valid: 0 = no more units, 1 = a unit, 2 = a transfer-matrix unit (identity, U = 0),
+                                // 3 = a unit on the caller's own state (segment pass of context parallelism)
     int32_t qh, kh, vh, flat0;
     int64_t t0, L, srow, ckpt_base;
 };
@@ -683,8 +684,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     cx.status = p.status;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kMisc);
 
-    // Bad input flagged by the prepare kernel: every thread sees one copy of the word.
-    if (tid == 0) *cx.abort = *reinterpret_cast<volatile int32_t*>(p.status);
+    // Bad input flagged by the prepare kernel: every thread sees one copy of the word.  A run whose
+    // device-side sequence count is zero (a transfer pass with no segments) has nothing to do either.
+    if (tid == 0)
+        *cx.abort = *reinterpret_cast<volatile int32_t*>(p.status) != 0 || (p.num_seqs_dev && *p.num_seqs_dev <= 0);
     __syncthreads();
     if (*cx.abort != 0) return;
     __syncthreads();
@@ -713,14 +716,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const int32_t H = p.H;
-    const int64_t units1 = static_cast<int64_t>(p.num_seqs) * H;
-    const int64_t units = kTransfer ? 2 * units1 : units1;
 
     if (warp < 4) {
         // the scheduling warpgroup: TMA producer, two MMA issuers, gates warp
         if (warp == 0) {
             // ================= TMA producer and unit scheduler =================
             if (lane == 0) {
+                const int64_t units1 = static_cast<int64_t>(p.num_seqs_dev ? *p.num_seqs_dev : p.num_seqs) * H;
+                const int64_t units = kTransfer ? 2 * units1 : units1;
                 uint32_t n = 0, u = 0;
                 int64_t issued_kq[kKQStages] = {-1, -1, -1};
                 int issued_v = -1;
@@ -753,6 +756,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         info.flat0 = kTransfer ? 0 : p.chunk_offsets[seq];
                         info.srow = (p.state_indices ? load_index(p.state_indices, p.idx_i64, seq) : seq) +
                                     (second ? p.num_seqs : 0);
+                        if (!kTransfer && p.split_state && info.srow < 0) {  // a row of the caller's own state
+                            info.srow = -1 - info.srow;
+                            info.valid = 3;
+                        }
                         info.ckpt_base = p.ckpt_n > 0 ? load_index(p.ckpt_cu_starts, p.ckpt_i64, seq) : 0;
                     }
                     *reinterpret_cast<UnitInfo*>(sm + kRing + slot * 64) = info;
@@ -1138,19 +1145,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (st == 0) mbar_arrive(cx.bars + B_UNIT_EMPTY + slot);
             ++u;
             if (!info.valid) break;
-            // element offset of this thread's 64 columns in the initial / output state
-            const int64_t state_off = state_offset(p.state, info.srow, info.h, v) + 64 * hh;
+            // element offset of this thread's 64 columns in the initial / output state (the caller's own, for a
+            // whole sequence in the segment pass of context parallelism)
+            const bool own = !kTransfer && info.valid == 3;
+            const int64_t state_off = state_offset(own ? p.state2 : p.state, info.srow, info.h, v) + 64 * hh;
+            const int32_t sdt = own ? p.state2.dtype : p.state.dtype;
             // checkpoints: every ck_every-th chunk end of the unit (a multiple of 64 tokens), counted down, so the
             // chunk loop does no division
             int32_t ck_left = ck_every, ck_row = 0;
-            const void* s0 = p.initial_state;
+            const void* s0 = own ? p.initial_state2 : p.initial_state;
             // a transfer-matrix unit starts from the identity: a 1 in column v - 64 hh of this thread's row v
             const bool ident = kTransfer && info.valid == 2;
             if (info.nC == 0) {
                 if (ident)  // the transfer output is dense fp32
                     identity_state<kF16>(v - 64 * hh, 0, 0, 1.f, static_cast<float*>(p.output_state) + state_off);
-                else if (p.output_state)
-                    pass_state_through(s0, p.output_state, state_off, p.state.dtype);
+                else if (void* const s_out = own ? p.output_state2 : p.output_state)
+                    pass_state_through(s0, s_out, state_off, sdt);
                 continue;
             }
             // initial state: S0 -> the bf16 operand columns and gamma_63(first chunk) * S0 -> the accumulator
@@ -1162,7 +1172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     identity_state<kF16>(v - 64 * hh, tm_lane + kTmSbf + 32 * hh, tm_lane + kTmS + 64 * hh, g63,
                                          nullptr);
                 else
-                    load_initial_state<kF16>(s0, state_off, p.state.dtype, tm_lane + kTmSbf + 32 * hh,
+                    load_initial_state<kF16>(s0, state_off, sdt, tm_lane + kTmSbf + 32 * hh,
                                              tm_lane + kTmS + 64 * hh, g63);
                 tc_fence_before();
                 if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
@@ -1327,8 +1337,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_wait_st();
                 } else {
                     // the unit's last chunk: its checkpoint (when due) and the final state, out of line
-                    finish_unit(tm_lane + kTmS + 64 * hh, p.checkpoints, ck_off, p.ckpt_dtype, p.output_state, state_off,
-                                p.state.dtype);
+                    finish_unit(tm_lane + kTmS + 64 * hh, p.checkpoints, ck_off, p.ckpt_dtype,
+                                own ? p.output_state2 : p.output_state, state_off,
+                                own ? p.state2.dtype : p.state.dtype);
                 }
             }
         }

@@ -1,23 +1,30 @@
-// gdn_cp.cu -- context parallelism inside one GPU for batches with few
-// (sequence, head) units ("FlashInfer GDN Prefill 完全指南", the CP routing and
-// max_seqlen rows of the API table; "GDN与线性注意力GPU并行实现", the
-// per-block transfer (M, N) and the scan over the blocks of section 3.3).
+// gdn_cp.cu -- context parallelism inside one GPU ("FlashInfer GDN Prefill
+// 完全指南", the CP routing and max_seqlen rows of the API table and the CP
+// backend's routing rules; "GDN与线性注意力GPU并行实现", the per-block transfer
+// (M, N) and the scan over the blocks of section 3.3).
 //
-// Each sequence is cut into P segments of Ls tokens (Ls a multiple of 64, or
-// of the checkpoint interval).  Over one segment the chunk recurrence is
-// affine in the state it starts from, S_end = S_start M + N, because every
+// Sequences long enough to dominate the run are cut into segments of tau
+// chunks (tau a multiple of the checkpoint interval); the others run whole.
+// The choice is made on the device from cu_seqlens (cp_prepare_kernel, with
+// the load model of gdn_internal.cuh).  Over one segment the chunk recurrence
+// is affine in the state it starts from, S_end = S_start M + N, because every
 // chunk maps S to S (gamma_63 I - W~^T D K) + U~^T D K.  So:
 //   1. a transfer pass (the chunk kernel's kTransfer instance) runs segments
-//      0 .. P-2 of every sequence twice: from zero (N) and from the identity
-//      with U = 0 (M); the units are independent, so they fill the GPU;
+//      0 .. P_i-2 of every segmented sequence twice: from zero (N) and from
+//      the identity with U = 0 (M); the units are independent;
 //   2. cp_fixup_kernel scans the segments in order on CUDA cores in fp32:
-//      S_start(0) = the initial state, S_start(s+1) = S_start(s) M_s + N_s;
-//   3. the ordinary chunk kernel runs all P segments as separate sequences
-//      from those start states (outputs and checkpoints land where the whole
-//      sequence would put them), and cp_final_kernel copies each sequence's
-//      last segment's final state to the caller's output state.
-// The work is about (2 (P-1) + P) / P times a plain pass, spread over
-// P times as many units.
+//      S_start(0) = the initial state, S_start(s+1) = S_start(s) M_s + N_s
+//      (rows of S are independent, so four CTAs share one (sequence, head));
+//   3. the ordinary chunk kernel runs every segment, and every whole
+//      sequence, as sequences of one batch: segments from their start states
+//      in a scratch buffer (in place), whole sequences straight from and to
+//      the caller's state; outputs and checkpoints land where one pass over
+//      the whole sequences puts them;
+//   4. cp_final_kernel copies each segmented sequence's last segment's final
+//      state to the caller's output state.
+// A segmented sequence costs about (2 (P-1) + P) / P times its plain work,
+// spread over P times as many units; when the model finds no gain every
+// sequence runs whole and steps 1, 2 and 4 have nothing to do.
 #include <atomic>
 
 #include "gdn_internal.cuh"
@@ -26,126 +33,259 @@ namespace gdn {
 namespace {
 
 constexpr int kCpThreads = 256;
-constexpr int kLdS = kHead + 1;  // padded rows of the running state in shared memory
+constexpr int kCand = kCpMaxSegments - 1;  // candidates P = 2 .. kCpMaxSegments
+constexpr int kFixRows = 32;                // rows of S per fixup CTA
+constexpr int kFixSplit = kHead / kFixRows; // fixup CTAs per (sequence, head)
+constexpr int kLdS = kHead + 1;             // padded rows of the running state in shared memory
 
-// Segments of every sequence, the segment pass's cu_seqlens and checkpoint
-// starts, and the transfer pass's work order.  One CTA (N <= 256 here).
-__global__ void __launch_bounds__(kCpThreads) cp_prepare_kernel(const CpParams p) {
-    const int P = p.P;
-    for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) {
-        const int64_t t0 = load_index(p.cu_seqlens, p.cu_i64, i);
-        int64_t L = load_index(p.cu_seqlens, p.cu_i64, i + 1) - t0;
-        if (L < 0) L = 0;  // a bad cu_seqlens is flagged by the prepare kernel; keep the segments sane
-        const int64_t per = (L + P - 1) / P;
-        const int64_t Ls = (per + p.align - 1) / p.align * p.align;
-        const int64_t c0 = p.ckpt_n > 0 ? load_index(p.ckpt_cu_starts, p.ckpt_i64, i) : 0;
-        for (int s = 0; s < P; ++s) {
-            const int64_t a = s * Ls < L ? s * Ls : L;
-            const int64_t b = (s + 1) * Ls < L ? (s + 1) * Ls : L;
-            if (s < P - 1) {
-                const int j = i * (P - 1) + s;
-                p.seg_a[2 * j] = t0 + a;
-                p.seg_a[2 * j + 1] = b - a;
-                p.order_a[j] = j;
-            }
-            p.cu_c[i * P + s] = static_cast<int32_t>(t0 + a);
-            p.ckpt_c[i * P + s] = p.ckpt_n > 0 ? c0 + a / p.ckpt_n : 0;
+__device__ __forceinline__ int64_t seq_chunks(const CpParams& p, int32_t i, int64_t& t0, int64_t& L) {
+    t0 = load_index(p.cu_seqlens, p.cu_i64, i);
+    L = load_index(p.cu_seqlens, p.cu_i64, i + 1) - t0;
+    if (L < 0) L = 0;  // a bad cu_seqlens is flagged by the prepare kernel; keep the segments sane
+    return (L + kChunk - 1) / kChunk;
+}
+
+// Exclusive scan of one value per thread over the CTA; *total gets the sum.
+__device__ int32_t cp_excl_scan(int32_t x, int32_t* warp_sums, int32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t inc = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) warp_sums[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const int32_t w = lane < kCpThreads / 32 ? warp_sums[lane] : 0;
+        int32_t wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
         }
+        if (lane < kCpThreads / 32) warp_sums[lane] = wi - w;
+        if (lane == 31) *total = wi;
     }
-    if (threadIdx.x == 0) {
-        p.cu_c[p.num_seqs * P] = static_cast<int32_t>(load_index(p.cu_seqlens, p.cu_i64, p.num_seqs));
-        p.ckpt_c[p.num_seqs * P] = p.ckpt_n > 0 ? load_index(p.ckpt_cu_starts, p.ckpt_i64, p.num_seqs) : 0;
-        *p.counter_a = 0;
-    }
+    __syncthreads();
+    const int32_t r = warp_sums[warp] + inc - x;
+    __syncthreads();
+    return r;
 }
 
 __device__ __forceinline__ int64_t real_row(const CpParams& p, int32_t i) {
     return p.state_indices ? load_index(p.state_indices, p.idx_i64, i) : i;
 }
 
-// One CTA per (sequence, state head): the start states of its P segments, in
-// fp32.  Thread t owns row v = t / 2, columns 64 (t % 2) .. + 63 of S.
-__global__ void __launch_bounds__(kCpThreads) cp_fixup_kernel(const CpParams p) {
-    extern __shared__ float cp_smem[];
-    float* S = cp_smem;                 // [128][kLdS]
-    float* M = cp_smem + kHead * kLdS;  // [128][128]
-    if (*reinterpret_cast<volatile int32_t*>(p.status)) return;
-    const int32_t i = blockIdx.x / p.H, h = blockIdx.x % p.H;
-    const int P = p.P;
-    const int64_t nA = static_cast<int64_t>(p.num_seqs) * (P - 1);  // transfer rows per kind
-    const size_t plane = static_cast<size_t>(kHead) * kHead;
-    const int t = threadIdx.x, v = t >> 1, c0 = (t & 1) * 64;
-    // S_start(0): the caller's initial state (or zeros), in any layout and type
-    const int64_t srow = real_row(p, i);
-    float* out0 = p.start + (static_cast<size_t>(i) * P * p.H + h) * plane;
-    for (int e = 4 * t; e < kHead * kHead; e += 4 * kCpThreads) {
-        const int r = e / kHead, k = e % kHead;
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (p.initial_state) state_load4(p.initial_state, state_offset(p.state, srow, h, r) + k, p.state.dtype, x);
+// The segmentation, the transfer pass's segments and order, the fixup's list
+// of segmented sequences and the segment pass's batch.  One CTA.
+__global__ void __launch_bounds__(kCpThreads) cp_prepare_kernel(const CpParams p) {
+    __shared__ unsigned long long s_sum[kCand][2];  // nA, nS
+    __shared__ long long s_max[kCand][2];           // longest whole sequence, largest P
+    __shared__ long long s_cmax;
+    __shared__ unsigned long long s_sumc;
+    __shared__ long long s_tau;
+    __shared__ int32_t warp_sums[kCpThreads / 32];
+    __shared__ int32_t tile_total;
+    const int tid = threadIdx.x;
+    const int32_t N = p.num_seqs;
+    if (tid < kCand) {
+        s_sum[tid][0] = s_sum[tid][1] = 0;
+        s_max[tid][0] = s_max[tid][1] = 0;
+    }
+    if (tid == 0) {
+        s_cmax = 0;
+        s_sumc = 0;
+    }
+    __syncthreads();
+    // ---- chunk counts: longest and total
+    {
+        long long cmax = 0;
+        unsigned long long sumc = 0;
+        for (int32_t i = tid; i < N; i += kCpThreads) {
+            int64_t t0, L;
+            const int64_t c = seq_chunks(p, i, t0, L);
+            if (c > cmax) cmax = c;
+            sumc += static_cast<unsigned long long>(c);
+        }
+        atomicMax(&s_cmax, cmax);
+        atomicAdd(&s_sumc, sumc);
+    }
+    __syncthreads();
+    const int64_t c_max = s_cmax, sum_c = static_cast<int64_t>(s_sumc);
+    // ---- every candidate's sums
+    {
+        CpSums loc[kCand];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            S[r * kLdS + k + j] = x[j];
-            out0[static_cast<size_t>(r) * kHead + k + j] = x[j];
+        for (int j = 0; j < kCand; ++j) loc[j] = CpSums{0, 0, 0, 0};
+        for (int32_t i = tid; i < N; i += kCpThreads) {
+            int64_t t0, L;
+            const int64_t c = seq_chunks(p, i, t0, L);
+#pragma unroll
+            for (int j = 0; j < kCand; ++j) cp_add_sequence(loc[j], c, cp_tau(c_max, j + 2, p.align_chunks));
+        }
+#pragma unroll
+        for (int j = 0; j < kCand; ++j) {
+            atomicAdd(&s_sum[j][0], static_cast<unsigned long long>(loc[j].nA));
+            atomicAdd(&s_sum[j][1], static_cast<unsigned long long>(loc[j].nS));
+            atomicMax(&s_max[j][0], static_cast<long long>(loc[j].max_whole));
+            atomicMax(&s_max[j][1], static_cast<long long>(loc[j].max_p));
         }
     }
     __syncthreads();
+    if (tid == 0) {
+        CpSums s[kCand];
+        for (int j = 0; j < kCand; ++j)
+            s[j] = CpSums{static_cast<int64_t>(s_sum[j][0]), static_cast<int64_t>(s_sum[j][1]), s_max[j][0],
+                          s_max[j][1]};
+        s_tau = (p.nA_max > 0 && p.sms > 0) ? cp_pick_tau(s, c_max, sum_c, p.H, p.sms, p.align_chunks) : 0;
+    }
+    __syncthreads();
+    const int64_t tau = s_tau, tau_tok = tau * kChunk;
+    // ---- per sequence: segments, offsets (exclusive scans), lists
+    int32_t carry_a = 0, carry_k = 0, carry_s = 0;
+    for (int32_t base = 0; base < N; base += kCpThreads) {
+        const int32_t i = base + tid;
+        int64_t t0 = 0, L = 0;
+        int32_t P = 1;
+        if (i < N) P = cp_seq_segments(seq_chunks(p, i, t0, L), tau);
+        const int32_t segd = P >= 2 ? 1 : 0;
+        const int32_t ta = carry_a + cp_excl_scan(P - 1, warp_sums, &tile_total);
+        carry_a += tile_total;
+        const int32_t k = carry_k + cp_excl_scan(segd, warp_sums, &tile_total);
+        carry_k += tile_total;
+        const int32_t sb = carry_s + cp_excl_scan(segd ? P : 0, warp_sums, &tile_total);
+        carry_s += tile_total;
+        if (i < N) {
+            const int64_t c0 = p.ckpt_n > 0 ? load_index(p.ckpt_cu_starts, p.ckpt_i64, i) : 0;
+            if (segd) {
+                p.seg_seq[4 * k] = i;
+                p.seg_seq[4 * k + 1] = P;
+                p.seg_seq[4 * k + 2] = ta;
+                p.seg_seq[4 * k + 3] = sb;
+                for (int32_t s = 0; s + 1 < P; ++s) {
+                    p.seg_a[2 * (ta + s)] = t0 + s * tau_tok;
+                    p.seg_a[2 * (ta + s) + 1] = tau_tok;
+                }
+            }
+            const int32_t v = i + ta;  // first entry of this sequence in the segment pass's batch
+            const int64_t row = segd ? 0 : real_row(p, i);
+            for (int32_t s = 0; s < P; ++s) {
+                const int64_t a = segd ? (s * tau_tok < L ? s * tau_tok : L) : 0;
+                p.cu_c[v + s] = static_cast<int32_t>(t0 + a);
+                p.ckpt_c[v + s] = p.ckpt_n > 0 ? c0 + a / p.ckpt_n : 0;
+                p.vrow[v + s] = segd ? static_cast<int64_t>(sb + s) : -1 - row;
+            }
+        }
+    }
+    // ---- the batch's tail of empty entries, the transfer order, the counts
+    const int32_t V = N + carry_a;
+    const int32_t end = static_cast<int32_t>(load_index(p.cu_seqlens, p.cu_i64, N));
+    const int64_t ck_end = p.ckpt_n > 0 ? load_index(p.ckpt_cu_starts, p.ckpt_i64, N) : 0;
+    for (int32_t v = V + tid; v <= p.V_max; v += kCpThreads) {
+        p.cu_c[v] = end;
+        p.ckpt_c[v] = ck_end;
+        if (v < p.V_max) p.vrow[v] = 0;
+    }
+    for (int32_t j = tid; j < p.nA_max; j += kCpThreads) p.order_a[j] = j;
+    if (tid == 0) {
+        p.counts[0] = carry_a;
+        p.counts[1] = V;
+        p.counts[2] = carry_k;
+        *p.counter_a = 0;
+    }
+}
+
+// Four CTAs per (segmented sequence, state head), 32 rows of S each: the
+// start states of its P segments, in fp32.  Thread t owns row v = t / 8 of
+// the CTA's rows and columns 4 (t % 8) + 32 q + j (q, j < 4), so that eight
+// neighbouring threads read 128 contiguous bytes of M and N.
+__global__ void __launch_bounds__(kCpThreads) cp_fixup_kernel(const CpParams p) {
+    extern __shared__ float cp_smem[];
+    float* S = cp_smem;                     // [32][kLdS]
+    float* M = cp_smem + kFixRows * kLdS;   // [128][128]
+    if (*reinterpret_cast<volatile int32_t*>(p.status)) return;
+    const int32_t part = blockIdx.x % kFixSplit, uh = blockIdx.x / kFixSplit;
+    const int32_t k = uh / p.H, h = uh % p.H;
+    if (k >= p.counts[2]) return;
+    const int32_t i = p.seg_seq[4 * k], P = p.seg_seq[4 * k + 1], ta = p.seg_seq[4 * k + 2], sb = p.seg_seq[4 * k + 3];
+    const size_t plane = static_cast<size_t>(kHead) * kHead;
+    const int r0 = part * kFixRows;
+    const int t = threadIdx.x, v = t >> 3, cl = 4 * (t & 7);
+    // S_start(0): the caller's initial state (or zeros), in any layout and type
+    const int64_t srow = real_row(p, i);
+    float* out0 = p.start + (static_cast<size_t>(sb) * p.H + h) * plane;
+    for (int e = 4 * t; e < kFixRows * kHead; e += 4 * kCpThreads) {
+        const int r = e / kHead, c = e % kHead;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (p.initial_state) state_load4(p.initial_state, state_offset(p.state, srow, h, r0 + r) + c, p.state.dtype, x);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) S[r * kLdS + c + j] = x[j];
+        *reinterpret_cast<float4*>(out0 + static_cast<size_t>(r0 + r) * kHead + c) = make_float4(x[0], x[1], x[2], x[3]);
+    }
+    __syncthreads();
     for (int s = 0; s + 1 < P; ++s) {
-        const int64_t j = static_cast<int64_t>(i) * (P - 1) + s;
-        const float* Nm = p.trans + (static_cast<size_t>(j) * p.H + h) * plane;
-        const float* Mm = p.trans + (static_cast<size_t>(nA + j) * p.H + h) * plane;
+        const float* Nm = p.trans + (static_cast<size_t>(ta + s) * p.H + h) * plane;
+        const float* Mm = p.trans + (static_cast<size_t>(p.nA_max + ta + s) * p.H + h) * plane;
         for (int e = 4 * t; e < kHead * kHead; e += 4 * kCpThreads)
             *reinterpret_cast<float4*>(M + e) = *reinterpret_cast<const float4*>(Mm + e);
         __syncthreads();
-        float acc[64];
+        float acc[16];
+        const float* nrow = Nm + static_cast<size_t>(r0 + v) * kHead + cl;
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-            const float4 n4 = *reinterpret_cast<const float4*>(Nm + static_cast<size_t>(v) * kHead + c0 + c);
-            acc[c] = n4.x;
-            acc[c + 1] = n4.y;
-            acc[c + 2] = n4.z;
-            acc[c + 3] = n4.w;
+        for (int q = 0; q < 4; ++q) {
+            const float4 n4 = *reinterpret_cast<const float4*>(nrow + 32 * q);
+            acc[4 * q] = n4.x;
+            acc[4 * q + 1] = n4.y;
+            acc[4 * q + 2] = n4.z;
+            acc[4 * q + 3] = n4.w;
         }
-#pragma unroll 2
-        for (int k = 0; k < kHead; ++k) {
-            const float sv = S[v * kLdS + k];
-            const float4* mr = reinterpret_cast<const float4*>(M + k * kHead + c0);
+#pragma unroll 4
+        for (int c = 0; c < kHead; ++c) {
+            const float sv = S[v * kLdS + c];
+            const float* mr = M + c * kHead + cl;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const float4 m4 = mr[c];
-                acc[4 * c] = fmaf(sv, m4.x, acc[4 * c]);
-                acc[4 * c + 1] = fmaf(sv, m4.y, acc[4 * c + 1]);
-                acc[4 * c + 2] = fmaf(sv, m4.z, acc[4 * c + 2]);
-                acc[4 * c + 3] = fmaf(sv, m4.w, acc[4 * c + 3]);
+            for (int q = 0; q < 4; ++q) {
+                const float4 m4 = *reinterpret_cast<const float4*>(mr + 32 * q);
+                acc[4 * q] = fmaf(sv, m4.x, acc[4 * q]);
+                acc[4 * q + 1] = fmaf(sv, m4.y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(sv, m4.z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(sv, m4.w, acc[4 * q + 3]);
             }
         }
-        __syncthreads();  // every row of S has been read
-        float* outs = p.start + ((static_cast<size_t>(i) * P + s + 1) * p.H + h) * plane + static_cast<size_t>(v) * kHead;
+        __syncthreads();  // every row of S and all of M have been read
+        float* outs = p.start + (static_cast<size_t>(sb + s + 1) * p.H + h) * plane +
+                      static_cast<size_t>(r0 + v) * kHead + cl;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) S[v * kLdS + c0 + c] = acc[c];
+        for (int q = 0; q < 4; ++q) {
 #pragma unroll
-        for (int c = 0; c < 64; c += 4)
-            *reinterpret_cast<float4*>(outs + c0 + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+            for (int j = 0; j < 4; ++j) S[v * kLdS + cl + 32 * q + j] = acc[4 * q + j];
+            *reinterpret_cast<float4*>(outs + 32 * q) =
+                make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+        }
         __syncthreads();
     }
 }
 
-// One CTA per (sequence, state head): the last segment's final state (left in
-// place by the segment pass) to the caller's output state.
+// One CTA per (segmented sequence, state head): the last segment's final
+// state (left in place by the segment pass) to the caller's output state.
 __global__ void __launch_bounds__(kCpThreads) cp_final_kernel(const CpParams p) {
     if (*reinterpret_cast<volatile int32_t*>(p.status)) return;
-    const int32_t i = blockIdx.x / p.H, h = blockIdx.x % p.H;
+    const int32_t k = blockIdx.x / p.H, h = blockIdx.x % p.H;
+    if (k >= p.counts[2]) return;
+    const int32_t i = p.seg_seq[4 * k], P = p.seg_seq[4 * k + 1], sb = p.seg_seq[4 * k + 3];
     const size_t plane = static_cast<size_t>(kHead) * kHead;
-    const float* src = p.start + ((static_cast<size_t>(i) * p.P + p.P - 1) * p.H + h) * plane;
+    const float* src = p.start + (static_cast<size_t>(sb + P - 1) * p.H + h) * plane;
     const int64_t srow = real_row(p, i);
     for (int e = 4 * threadIdx.x; e < kHead * kHead; e += 4 * kCpThreads) {
-        const int r = e / kHead, k = e % kHead;
+        const int r = e / kHead, c = e % kHead;
         const float4 f = *reinterpret_cast<const float4*>(src + e);
         const float x[4] = {f.x, f.y, f.z, f.w};
-        state_store4(p.output_state, state_offset(p.state, srow, h, r) + k, p.state.dtype, x);
+        state_store4(p.output_state, state_offset(p.state, srow, h, r) + c, p.state.dtype, x);
     }
 }
 
-constexpr size_t kFixupSmem = sizeof(float) * (kHead * kLdS + kHead * kHead);
+constexpr size_t kFixupSmem = sizeof(float) * (kFixRows * kLdS + kHead * kHead);
 
 }  // namespace
 
@@ -169,13 +309,14 @@ cudaError_t launch_cp_fixup(const CpParams& p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev].store(1, std::memory_order_release);
     }
-    cp_fixup_kernel<<<p.num_seqs * p.H, kCpThreads, kFixupSmem, stream>>>(p);
+    if (p.nA_max <= 0) return cudaSuccess;
+    cp_fixup_kernel<<<p.nA_max * p.H * kFixSplit, kCpThreads, kFixupSmem, stream>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_cp_final(const CpParams& p, cudaStream_t stream) {
-    if (!p.output_state) return cudaSuccess;
-    cp_final_kernel<<<p.num_seqs * p.H, kCpThreads, 0, stream>>>(p);
+    if (!p.output_state || p.nA_max <= 0) return cudaSuccess;
+    cp_final_kernel<<<p.nA_max * p.H, kCpThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

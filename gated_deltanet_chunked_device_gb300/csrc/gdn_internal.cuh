@@ -184,27 +184,116 @@ struct ChunkParams {
     float* intra_u;
     int has_tokens;                // 0: the TMA maps are blank (T == 0) and never used
     const int64_t* seg;            // transfer pass: [num_seqs][2] segment start token and length (else null)
+    const int32_t* num_seqs_dev;   // non-null: the run's sequence count, read on the device (<= num_seqs)
+    // Segment pass of context parallelism: a negative row r of state_indices names row -1 - r of the
+    // caller's own state (initial_state2 / output_state2 in layout state2) instead of the start buffer.
+    int split_state;
+    const void* initial_state2;
+    void* output_state2;
+    StateLayout state2;
 };
 
-// Context-parallel arguments: the real batch, its P segments per sequence and
-// the scratch buffers of the transfer pass (A) and the segment pass (C).
+// Context parallelism with a segment count per sequence.  Sequence i of c_i
+// chunks is cut into P_i segments of tau chunks (the last one shorter) when
+// c_i > tau, else it runs whole (P_i = 1).  One tau serves the whole batch;
+// it is chosen from a load model in chunk periods (one chunk of one
+// (sequence, head) unit on one SM) over the three launches:
+//   transfer pass  ceil(2 H nA / S) tau                 nA = sum (P_i - 1)
+//   segment pass   max(ceil(H nS / S) tau, ceil(H sum c_i / S), longest whole c_i)
+//                                                       nS = sum of P_i over segmented sequences
+//   fixup + launches  (max P_i - 1) + 4
+// against one pass, max(c_max, ceil(H sum c_i / S)); the segments are taken
+// only when they cost at most 85 % of it.  Candidates: tau = c_max / P
+// rounded up to the segment granularity, P = 2 .. kCpMaxSegments; ties go to
+// the smaller P.  The device (cp_prepare_kernel) and the host query
+// (gdn_prefill_cp_segments) both evaluate it with these functions.
+constexpr int32_t kCpMaxSegments = 8;
+constexpr int64_t kCpMaxPlanes = 256;  // 128 x 128 fp32 planes of transfer output, and of start states
+
+__host__ __device__ inline int64_t cp_tau(int64_t c_max, int32_t P, int64_t align_chunks) {
+    const int64_t t = (c_max + P - 1) / P;
+    return (t + align_chunks - 1) / align_chunks * align_chunks;
+}
+
+__host__ __device__ inline int32_t cp_seq_segments(int64_t c, int64_t tau) {
+    return (tau > 0 && c > tau) ? static_cast<int32_t>((c + tau - 1) / tau) : 1;
+}
+
+// Per-candidate sums over the batch (one per P = 2 .. kCpMaxSegments).
+struct CpSums {
+    int64_t nA, nS, max_whole, max_p;
+};
+
+__host__ __device__ inline void cp_add_sequence(CpSums& s, int64_t c, int64_t tau) {
+    const int32_t P = cp_seq_segments(c, tau);
+    if (P >= 2) {
+        s.nA += P - 1;
+        s.nS += P;
+    } else if (c > s.max_whole) {
+        s.max_whole = c;
+    }
+    if (P > s.max_p) s.max_p = P;
+}
+
+__host__ __device__ inline int64_t cp_ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Cost of a candidate in chunk periods, or -1 when it does not fit the scratch planes.
+__host__ __device__ inline int64_t cp_cost(const CpSums& s, int64_t tau, int64_t sum_c, int32_t H, int32_t sms) {
+    if (2 * H * s.nA > kCpMaxPlanes || H * s.nS > kCpMaxPlanes) return -1;
+    const int64_t ta = cp_ceil_div(2 * H * s.nA, sms) * tau;
+    int64_t tc = cp_ceil_div(H * s.nS, sms) * tau;
+    const int64_t bal = cp_ceil_div(H * sum_c, sms);
+    if (bal > tc) tc = bal;
+    if (s.max_whole > tc) tc = s.max_whole;
+    return ta + tc + (s.max_p - 1) + 4;
+}
+
+__host__ __device__ inline int64_t cp_one_pass_cost(int64_t c_max, int64_t sum_c, int32_t H, int32_t sms) {
+    const int64_t bal = cp_ceil_div(H * sum_c, sms);
+    return c_max > bal ? c_max : bal;
+}
+
+// The chosen tau from the candidates' sums (0: one pass).
+__host__ __device__ inline int64_t cp_pick_tau(const CpSums (&s)[kCpMaxSegments - 1], int64_t c_max, int64_t sum_c,
+                                               int32_t H, int32_t sms, int64_t align_chunks) {
+    const int64_t one = cp_one_pass_cost(c_max, sum_c, H, sms);
+    int64_t best = -1, tau = 0;
+    for (int32_t P = 2; P <= kCpMaxSegments; ++P) {
+        const int64_t t = cp_tau(c_max, P, align_chunks);
+        const int64_t c = cp_cost(s[P - 2], t, sum_c, H, sms);
+        if (c < 0 || s[P - 2].max_p < 2) continue;
+        if (best < 0 || c < best) {
+            best = c;
+            tau = t;
+        }
+    }
+    return (best >= 0 && 100 * best <= 85 * one) ? tau : 0;
+}
+
+// Context-parallel arguments: the real batch, its segments and the scratch
+// buffers of the transfer pass (A), the fp32 scan and the segment pass (C).
 struct CpParams {
     const void* cu_seqlens;        // real [N+1]
     int cu_i64;
     int32_t num_seqs;              // N
     int32_t H;
-    int32_t P;                     // segments per sequence
-    int32_t align;                 // segment length granularity (64, or the checkpoint interval)
+    int32_t sms;                   // SMs of the device (the load model's S)
+    int32_t align_chunks;          // segment length granularity in chunks (1, or the checkpoint interval / 64)
+    int32_t nA_max;                // bound of transfer segments: rows per kind of the transfer output
+    int32_t V_max;                 // bound of the segment pass's sequences (N + nA_max)
     int32_t ckpt_n;                // 0 = no checkpoints
     const void* ckpt_cu_starts;    // real [N+1]
     int ckpt_i64;
-    int64_t* seg_a;                // [N*(P-1)][2] segments 0..P-2 (start, length)
-    int32_t* order_a;              // [N*(P-1)] identity work order of the transfer pass
+    int64_t* seg_a;                // [nA_max][2] transfer segments (start token, length)
+    int32_t* order_a;              // [nA_max] identity work order of the transfer pass
     int32_t* counter_a;            // work counter of the transfer pass
-    int32_t* cu_c;                 // [N*P+1] segment cu_seqlens of the segment pass
-    int64_t* ckpt_c;               // [N*P+1] segment checkpoint starts
-    const float* trans;            // transfer pass output [2*N*(P-1)][H][128][128]: N_s rows, then M_s rows
-    float* start;                  // segment start states [N*P][H][128][128] (the segment pass runs in place)
+    int32_t* counts;               // [0] transfer segments nA, [1] segment-pass sequences V, [2] segmented sequences
+    int32_t* seg_seq;              // [nA_max][4] per segmented sequence: index, P, first transfer row, first start row
+    int32_t* cu_c;                 // [V_max+1] cu_seqlens of the segment pass (a tail of empty entries)
+    int64_t* ckpt_c;               // [V_max+1] its checkpoint starts
+    int64_t* vrow;                 // [V_max] its state rows: start plane row, or -1 - row of the caller's state
+    const float* trans;            // transfer output [2*nA_max][H][128][128]: N_s rows, then M_s rows
+    float* start;                  // segment start states [nS][H][128][128] (the segment pass runs in place)
     const void* initial_state;     // real initial state (null: zeros)
     void* output_state;            // real output state (null: none)
     StateLayout state;             // its layout

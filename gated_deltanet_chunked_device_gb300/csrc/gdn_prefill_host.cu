@@ -8,6 +8,7 @@
 // a multiple of 64; checkpoints and their starts given together; an output
 // state pool is required with state_indices; max_seqlen within
 // [ceil(T/N), T]).
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -21,8 +22,9 @@
 // Context-parallel scratch (plans with GDN_FLAG_CONTEXT_PARALLEL): byte offsets
 // in the workspace, after the main layout.
 struct CpLayout {
-    size_t trans, start, seg_a, order_a, counter_a, cu_c, ckpt_c, prep;  // prep: the segment pass's prepare
-    gdn::WorkspaceLayout wc;                                             // its layout, relative to prep
+    size_t trans, start, seg_a, order_a, counter_a, seg_seq, cu_c, ckpt_c, vrow;
+    size_t prep;              // the segment pass's prepare
+    gdn::WorkspaceLayout wc;  // its layout, relative to prep
 };
 
 struct gdn_prefill_plan_s {
@@ -41,11 +43,9 @@ constexpr uint32_t kKnownFlags = GDN_FLAG_HAS_G | GDN_FLAG_HAS_BETA | GDN_FLAG_H
                                  GDN_FLAG_HAS_STATE_INDICES | GDN_FLAG_CU_SEQLENS_I64 | GDN_FLAG_STATE_INDICES_I64 |
                                  GDN_FLAG_CHECKPOINT_STARTS_I64 | GDN_FLAG_CONTEXT_PARALLEL;
 
-// Context-parallel bounds: (sequence, head) rows of the transfer pass and of
-// the segment pass, and virtual sequences (segments) of either.
-constexpr int64_t kCpMaxRows = 256;
-constexpr int32_t kCpMaxSeqs = 256;
-constexpr int32_t kCpMaxSegments = 8;
+// Context-parallel bound: transfer segments per run (each takes 2 H planes
+// of the transfer output, so at most kCpMaxPlanes / 2 with one head).
+constexpr int32_t kCpMaxTransfer = static_cast<int32_t>(gdn::kCpMaxPlanes / 2);
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -154,18 +154,27 @@ bool make_state_layout(gdn_dtype dt, const int64_t (&st)[3], int64_t rows, int32
     return true;
 }
 
-// Segments per sequence for context parallelism, or 0: only for plans that
-// allow it, 16-bit inputs, no intra-chunk dumps, and at most half as many
-// (sequence, head) units as SMs.  P fills the SMs with the transfer pass
-// (2 (P-1) N H units) within the plan's scratch bounds.
-int cp_segments(gdn_prefill_plan_t plan, const gdn_prefill_args& a, int32_t N, int64_t T, int sms) {
-    if (!plan->cp || plan->desc.qkv_dtype == GDN_DTYPE_F32 || a.intra_g || a.intra_w || a.intra_u) return 0;
-    const int64_t nh = static_cast<int64_t>(N) * plan->H;
-    if (N <= 0 || T <= 0 || 2 * nh > sms) return 0;
-    int64_t P = sms / (2 * nh) + 1;
-    if (P > kCpMaxSegments) P = kCpMaxSegments;
-    while (P >= 2 && (2 * (P - 1) * nh > kCpMaxRows || P * nh > kCpMaxRows || N * P > kCpMaxSeqs)) --P;
-    return P >= 2 ? static_cast<int>(P) : 0;
+// Whether a run takes the context-parallel route (the device then chooses the
+// segments, possibly none): plans that allow it, 16-bit inputs, no intra-chunk
+// dumps, room for one transfer segment, and -- when max_seqlen is given -- a
+// longest sequence that the load model could shorten at all: with
+// 0.85 ceil(max_seqlen / 64) <= H T / (64 S) the segment pass alone already
+// costs 85 % of one pass (see cp_pick_tau), so one pass it is.
+bool cp_route(gdn_prefill_plan_t plan, const gdn_prefill_args& a, int32_t N, int64_t T, int sms) {
+    if (!plan->cp || plan->desc.qkv_dtype == GDN_DTYPE_F32 || a.intra_g || a.intra_w || a.intra_u) return false;
+    if (N <= 0 || T <= 0 || sms <= 0 || 2 * static_cast<int64_t>(plan->H) > gdn::kCpMaxPlanes) return false;
+    if (a.max_seqlen > 0) {
+        const int64_t c_bound = (a.max_seqlen + gdn::kChunk - 1) / gdn::kChunk;
+        if (85 * c_bound * gdn::kChunk * sms <= 100 * static_cast<int64_t>(plan->H) * T) return false;
+    }
+    return true;
+}
+
+// Bound of the transfer segments of a run of N sequences.
+int32_t cp_transfer_bound(gdn_prefill_plan_t plan, int32_t N) {
+    const int64_t by_planes = gdn::kCpMaxPlanes / (2 * static_cast<int64_t>(plan->H));
+    const int64_t by_seqs = static_cast<int64_t>(N) * (gdn::kCpMaxSegments - 1);
+    return static_cast<int32_t>(by_planes < by_seqs ? by_planes : by_seqs);
 }
 
 // The types a state or a checkpoint may be stored in.
@@ -216,21 +225,30 @@ gdn_status gdn_prefill_plan(const gdn_prefill_desc* desc, gdn_prefill_plan_t* pl
         const size_t plane = sizeof(float) * gdn::kHead * gdn::kHead;
         CpLayout& c = p->cpl;
         c.trans = total;
-        total = align_up(total + plane * kCpMaxRows, 256);
+        total = align_up(total + plane * gdn::kCpMaxPlanes, 256);
         c.start = total;
-        total = align_up(total + plane * kCpMaxRows, 256);
+        total = align_up(total + plane * gdn::kCpMaxPlanes, 256);
+        const int64_t vmax = static_cast<int64_t>(d.max_num_seqs) + kCpMaxTransfer;  // segment-pass batch bound
+        if (vmax > 0x7fffffffLL) {
+            delete p;
+            return GDN_ERR_UNSUPPORTED;
+        }
         c.seg_a = total;
-        total = align_up(total + sizeof(int64_t) * 2 * kCpMaxSeqs, 256);
+        total = align_up(total + sizeof(int64_t) * 2 * kCpMaxTransfer, 256);
         c.order_a = total;
-        total = align_up(total + sizeof(int32_t) * kCpMaxSeqs, 256);
-        c.counter_a = total;
+        total = align_up(total + sizeof(int32_t) * kCpMaxTransfer, 256);
+        c.counter_a = total;  // the work counter, then the three counts
         total = align_up(total + 16, 256);
+        c.seg_seq = total;
+        total = align_up(total + sizeof(int32_t) * 4 * kCpMaxTransfer, 256);
         c.cu_c = total;
-        total = align_up(total + sizeof(int32_t) * (kCpMaxSeqs + 1), 256);
+        total = align_up(total + sizeof(int32_t) * (vmax + 1), 256);
         c.ckpt_c = total;
-        total = align_up(total + sizeof(int64_t) * (kCpMaxSeqs + 1), 256);
+        total = align_up(total + sizeof(int64_t) * (vmax + 1), 256);
+        c.vrow = total;
+        total = align_up(total + sizeof(int64_t) * vmax, 256);
         gdn_prefill_desc dc = d;
-        dc.max_num_seqs = kCpMaxSeqs;
+        dc.max_num_seqs = static_cast<int32_t>(vmax);
         dc.max_pool_rows = 0;
         c.wc = make_layout(dc);
         c.prep = total;
@@ -244,13 +262,38 @@ gdn_status gdn_prefill_plan(const gdn_prefill_desc* desc, gdn_prefill_plan_t* pl
 
 void gdn_prefill_plan_destroy(gdn_prefill_plan_t plan) { delete plan; }
 
-int32_t gdn_prefill_cp_segments(gdn_prefill_plan_t plan, int32_t num_seqs, int64_t total_tokens,
-                                int32_t sm_count_hint) {
-    if (!plan) return 0;
+int32_t gdn_prefill_cp_segments(gdn_prefill_plan_t plan, const int64_t* seq_lens, int32_t num_seqs,
+                                int32_t sm_count_hint, int32_t* segments) {
+    if (!plan || num_seqs < 0 || (num_seqs > 0 && !seq_lens)) return 0;
+    for (int32_t i = 0; i < num_seqs && segments; ++i) segments[i] = 1;
     const int sms = sm_count_hint > 0 ? sm_count_hint : sm_count();
-    if (sms <= 0) return 0;
+    int64_t T = 0, c_max = 0, sum_c = 0;
+    for (int32_t i = 0; i < num_seqs; ++i) {
+        const int64_t L = seq_lens[i] > 0 ? seq_lens[i] : 0;
+        const int64_t c = (L + gdn::kChunk - 1) / gdn::kChunk;
+        T += L;
+        sum_c += c;
+        if (c > c_max) c_max = c;
+    }
     gdn_prefill_args a{};
-    return cp_segments(plan, a, num_seqs, total_tokens, sms);
+    if (!cp_route(plan, a, num_seqs, T, sms)) return 0;
+    const int32_t n = plan->desc.checkpoint_every_n_tokens;
+    const int64_t align = n > 0 ? n / gdn::kChunk : 1;
+    gdn::CpSums s[gdn::kCpMaxSegments - 1];
+    for (int32_t P = 2; P <= gdn::kCpMaxSegments; ++P) {
+        s[P - 2] = gdn::CpSums{0, 0, 0, 0};
+        const int64_t tau = gdn::cp_tau(c_max, P, align);
+        for (int32_t i = 0; i < num_seqs; ++i)
+            gdn::cp_add_sequence(s[P - 2], (std::max<int64_t>(seq_lens[i], 0) + gdn::kChunk - 1) / gdn::kChunk, tau);
+    }
+    const int64_t tau = gdn::cp_pick_tau(s, c_max, sum_c, plan->H, sms, align);
+    int32_t most = 0;
+    for (int32_t i = 0; tau > 0 && i < num_seqs; ++i) {
+        const int32_t P = gdn::cp_seq_segments((std::max<int64_t>(seq_lens[i], 0) + gdn::kChunk - 1) / gdn::kChunk, tau);
+        if (segments) segments[i] = P;
+        if (P > most) most = P;
+    }
+    return most >= 2 ? most : 0;
 }
 
 gdn_status gdn_prefill_workspace_layout(gdn_prefill_plan_t plan, gdn_prefill_layout* layout) {
@@ -398,30 +441,36 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
     const bool f16 = d.qkv_dtype == GDN_DTYPE_F16;
     const int32_t H = plan->H;
     const int64_t units = static_cast<int64_t>(N) * H;
-    const int P = cp_segments(plan, a, N, T, sms);
-    if (P < 2) {
+    if (!cp_route(plan, a, N, T, sms)) {
         const int grid = static_cast<int>(units < sms ? units : sms);
         if (gdn::launch_chunk_16bit(cp, tq, tk, tv, to, f16, false, grid, stream) != cudaSuccess) return GDN_ERR_CUDA;
         return GDN_OK;
     }
 
-    // ---- context parallelism: segments, transfer pass, fp32 scan, segment pass, final states
+    // ---- context parallelism: segmentation on the device, transfer pass, fp32 scan, one pass over the
+    //      segments and the whole sequences, final states of the segmented sequences
     const CpLayout& c = plan->cpl;
+    const int32_t nA_max = cp_transfer_bound(plan, N);
     gdn::CpParams q{};
     q.cu_seqlens = a.cu_seqlens;
     q.cu_i64 = pp.cu_i64;
     q.num_seqs = N;
     q.H = H;
-    q.P = P;
-    q.align = n > 0 ? n : gdn::kChunk;
+    q.sms = sms;
+    q.align_chunks = n > 0 ? n / gdn::kChunk : 1;
+    q.nA_max = nA_max;
+    q.V_max = N + nA_max;
     q.ckpt_n = n;
     q.ckpt_cu_starts = a.checkpoint_cu_starts;
     q.ckpt_i64 = pp.ckpt_i64;
     q.seg_a = reinterpret_cast<int64_t*>(ws + c.seg_a);
     q.order_a = reinterpret_cast<int32_t*>(ws + c.order_a);
     q.counter_a = reinterpret_cast<int32_t*>(ws + c.counter_a);
+    q.counts = q.counter_a + 1;
+    q.seg_seq = reinterpret_cast<int32_t*>(ws + c.seg_seq);
     q.cu_c = reinterpret_cast<int32_t*>(ws + c.cu_c);
     q.ckpt_c = reinterpret_cast<int64_t*>(ws + c.ckpt_c);
+    q.vrow = reinterpret_cast<int64_t*>(ws + c.vrow);
     q.trans = reinterpret_cast<const float*>(ws + c.trans);
     q.start = reinterpret_cast<float*>(ws + c.start);
     q.initial_state = cp.initial_state;
@@ -438,8 +487,9 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
     dense.s_head = static_cast<int64_t>(gdn::kHead) * gdn::kHead;
     dense.s_row = dense.s_head * H;
 
-    gdn::ChunkParams ta = cp;  // transfer pass over segments 0 .. P-2
-    ta.num_seqs = N * (P - 1);
+    gdn::ChunkParams ta = cp;  // transfer pass over segments 0 .. P_i-2 of the segmented sequences
+    ta.num_seqs = nA_max;
+    ta.num_seqs_dev = q.counts;
     ta.seg = q.seg_a;
     ta.seq_order = q.order_a;
     ta.counter = q.counter_a;
@@ -451,14 +501,14 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
     ta.checkpoints = nullptr;
     ta.ckpt_n = 0;
     ta.intra_g = ta.intra_w = ta.intra_u = nullptr;
-    const int64_t units_a = 2 * static_cast<int64_t>(ta.num_seqs) * H;
+    const int64_t units_a = 2 * static_cast<int64_t>(nA_max) * H;
     if (gdn::launch_chunk_16bit(ta, tq, tk, tv, to, f16, true, static_cast<int>(units_a < sms ? units_a : sms),
                                 stream) != cudaSuccess)
         return GDN_ERR_CUDA;
     if (gdn::launch_cp_fixup(q, stream) != cudaSuccess) return GDN_ERR_CUDA;
 
-    uint8_t* wsc = ws + c.prep;  // the segment pass: P segments per sequence as sequences of their own
-    const int32_t nc = N * P;
+    uint8_t* wsc = ws + c.prep;  // the segment pass: segments and whole sequences as one batch
+    const int32_t nc = q.V_max;
     gdn::PrepareParams pc{};
     pc.cu_seqlens = q.cu_c;
     pc.cu_i64 = 0;
@@ -484,10 +534,16 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
     sc.cu_seqlens = q.cu_c;
     sc.cu_i64 = 0;
     sc.num_seqs = nc;
+    sc.num_seqs_dev = q.counts + 1;
     sc.initial_state = q.start;
     sc.output_state = q.start;
     sc.state = dense;
-    sc.state_indices = nullptr;
+    sc.state_indices = q.vrow;
+    sc.idx_i64 = 1;
+    sc.split_state = 1;
+    sc.initial_state2 = cp.initial_state;
+    sc.output_state2 = cp.output_state;
+    sc.state2 = sl;
     sc.ckpt_cu_starts = q.ckpt_c;
     sc.ckpt_i64 = 1;
     sc.counter = pc.counter;

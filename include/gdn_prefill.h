@@ -104,14 +104,17 @@ enum {
     GDN_FLAG_STATE_INDICES_I64 = 1u << 8,  /* state_indices is int64 (else int32) */
     GDN_FLAG_CHECKPOINT_STARTS_I64 = 1u << 9, /* checkpoint_cu_starts is int64 (else int32) */
     /* Context parallelism inside the GPU ("FlashInfer GDN Prefill 完全指南",
-     * the use_cp row of the API table; the per-segment transfer and boundary
-     * scan of "GDN与线性注意力GPU并行实现", section 3.3): when a run has few
-     * (sequence, head) units (N*H at most half the SM count) the sequences
-     * are cut into segments whose start states come from a transfer pass and
-     * an fp32 scan, so that more SMs share each sequence.  Same results
-     * within rounding; the plan's workspace grows by about 32 MiB.  Not used
-     * with fp32 q/k/v or when intra-chunk outputs are requested
-     * (gdn_prefill_cp_segments reports the choice). */
+     * the use_cp row of the API table and the CP backend's routing rules; the
+     * per-segment transfer and boundary scan of "GDN与线性注意力GPU并行实现",
+     * section 3.3): sequences long enough to set the run's time are cut into
+     * segments whose start states come from a transfer pass and an fp32 scan,
+     * so that more SMs share them, while the rest of the batch runs whole in
+     * the same launches.  The device picks the segments from cu_seqlens with
+     * a load model (no host sync), and picks none when they would not pay;
+     * gdn_prefill_cp_segments gives the same choice on the host.  Same
+     * results within rounding; the plan's workspace grows by about 32 MiB.
+     * Not used with fp32 q/k/v, when intra-chunk outputs are requested, or
+     * when args.max_seqlen shows that no sequence is long enough to gain. */
     GDN_FLAG_CONTEXT_PARALLEL = 1u << 10
 };
 
@@ -182,12 +185,16 @@ typedef struct gdn_prefill_args {
     float *intra_g, *intra_w, *intra_u;
 } gdn_prefill_args;
 
-/* Segments per sequence that a gdn_prefill_run of this plan uses for N
- * sequences and T tokens (context parallelism; 0 = none, one pass over whole
- * sequences) on a GPU with sm_count_hint SMs, or on the current device when
- * sm_count_hint <= 0 (then it queries the device).  No launch. */
-int32_t gdn_prefill_cp_segments(gdn_prefill_plan_t plan, int32_t num_seqs, int64_t total_tokens,
-                                int32_t sm_count_hint);
+/* The context-parallel choice a gdn_prefill_run of this plan makes for a
+ * batch of sequences with the host lengths seq_lens[num_seqs], on a GPU with
+ * sm_count_hint SMs (or the current device's count when sm_count_hint <= 0):
+ * the largest number of segments any sequence is cut into, 0 when every
+ * sequence runs whole (also for plans without GDN_FLAG_CONTEXT_PARALLEL or
+ * with fp32 q/k/v).  segments, when not NULL, receives each sequence's count
+ * (1 = whole).  No launch; the device evaluates the same model from
+ * cu_seqlens. */
+int32_t gdn_prefill_cp_segments(gdn_prefill_plan_t plan, const int64_t *seq_lens, int32_t num_seqs,
+                                int32_t sm_count_hint, int32_t *segments);
 
 /* Validate `desc` and create a plan.  *workspace_bytes receives the device
  * workspace size gdn_prefill_run needs (16-byte aligned, caller allocated).

@@ -90,22 +90,46 @@ def test_plan_validation(L, kw, expect):
 _CP = gdn.FLAGS["CONTEXT_PARALLEL"]
 
 
-@pytest.mark.parametrize("desc_kw,N,T,sms,expect", [
-    (dict(flags=_CP), 1, 32768, 152, 3),                                  # 32 state heads: 3 segments fill 152 SMs
-    (dict(flags=_CP), 8, 33408, 152, 0),                                  # 256 units: one pass
-    (dict(flags=_CP, num_q_heads=1, num_k_heads=1, num_v_heads=1), 1, 5000, 152, 8),  # capped at 8 segments
-    (dict(flags=_CP, num_q_heads=4, num_k_heads=4, num_v_heads=4), 2, 1000, 152, 8),
-    (dict(flags=_CP, num_q_heads=64, num_k_heads=16, num_v_heads=16), 1, 1000, 152, 2),
-    (dict(flags=_CP, num_q_heads=128, num_k_heads=16, num_v_heads=16), 1, 1000, 1024, 2),  # scratch bound
-    ({}, 1, 32768, 152, 0),                                               # the plan does not allow it
-    (dict(flags=_CP, qkv_dtype=gdn.DTYPE_F32), 1, 1000, 152, 0),          # fp32 inputs: one pass
-    (dict(flags=_CP), 1, 0, 152, 0),                                      # no tokens
+_H64 = dict(num_q_heads=64, num_k_heads=16, num_v_heads=16)
+_H128 = dict(num_q_heads=128, num_k_heads=16, num_v_heads=16)
+_H1 = dict(num_q_heads=1, num_k_heads=1, num_v_heads=1)
+_H2 = dict(num_q_heads=2, num_k_heads=2, num_v_heads=2)
+
+
+# Expected choices worked by hand from the load model (chunk periods; S SMs, H state heads, c_i chunks):
+# transfer ceil(2 H nA / S) tau + segment pass max(ceil(H nS / S) tau, ceil(H sum c / S), longest whole)
+# + (P - 1) + 4, taken when at most 85 % of one pass max(c_max, ceil(H sum c / S)).
+@pytest.mark.parametrize("desc_kw,lens,sms,expect,per_seq", [
+    # 512 chunks, 32 heads: P = 3 costs 171 + 171 + 6 = 348 of 512; P = 4 needs two waves of transfers (391)
+    (dict(flags=_CP), [32768], 152, 3, [3]),
+    # the same sequence beside four short ones: they run whole in the segment pass
+    (dict(flags=_CP), [32768, 1024, 1024, 1024, 1024], 152, 3, [3, 1, 1, 1, 1]),
+    # ... beside 64 of them: the batch alone fills 324 periods of the 512, CP would cost 501 > 435
+    (dict(flags=_CP), [32768] + [1024] * 64, 152, 0, None),
+    # eight sequences up to 118 chunks on 32 heads: P = 2 already needs two transfer waves (118); P >= 3 does
+    # not fit the 256 transfer planes
+    (dict(flags=_CP), [7528, 6000, 5000, 4000, 3000, 2000, 1000, 500], 152, 0, None),
+    # one head, 79 chunks: eight segments of 10 chunks cost 10 + 10 + 11 = 31
+    (dict(flags=_CP, **_H1), [5000], 152, 8, [8]),
+    # checkpoints every 1024 tokens: segments are multiples of 16 chunks, so 4 x 16 (39) beats 2 x 32 (69)
+    (dict(flags=_CP, checkpoint_every_n_tokens=1024, **_H2), [4096], 152, 4, [4]),
+    (dict(flags=_CP, checkpoint_every_n_tokens=512, **_H2), [4096], 152, 8, [8]),
+    # 64 heads: two transfer segments fill the 256 planes, so at most three segments (53 + 53 + 6 of 157)
+    (dict(flags=_CP, **_H64), [10000], 1024, 3, [3]),
+    (dict(flags=_CP, **_H64), [10000], 152, 0, None),     # ... but on 152 SMs two waves each: 218 > 157
+    (dict(flags=_CP, **_H128), [10000], 1024, 0, None),   # 128 heads: three segments do not fit, two cannot gain
+    ({}, [32768], 152, 0, None),                          # the plan does not allow it
+    (dict(flags=_CP, qkv_dtype=gdn.DTYPE_F32), [32768], 152, 0, None),  # fp32 inputs: one pass
+    (dict(flags=_CP), [0], 152, 0, None),                 # no tokens
+    (dict(flags=_CP), [0, 32768, 0], 152, 3, [1, 3, 1]),  # empty sequences run whole (their state passes through)
 ])
-def test_context_parallel_segment_choice(L, desc_kw, N, T, sms, expect):
+def test_context_parallel_segment_choice(L, desc_kw, lens, sms, expect, per_seq):
     st, plan, nbytes = gdn.gdn_prefill_plan(_desc(**desc_kw))
     assert st == OK
     try:
-        assert L.gdn_prefill_cp_segments(plan, N, T, sms) == expect
+        most, segs = gdn.gdn_prefill_cp_segments(plan, lens, sms)
+        assert most == expect
+        assert segs == (per_seq if per_seq is not None else [1] * len(lens))
     finally:
         gdn.gdn_prefill_plan_destroy(plan)
 

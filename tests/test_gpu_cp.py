@@ -1,11 +1,14 @@
-"""GPU parity of context parallelism inside the GPU (use_cp): a batch with few
-(sequence, head) units is cut into segments whose start states come from a
+"""GPU parity of context parallelism inside the GPU (use_cp): the sequences
+that set a run's time are cut into segments whose start states come from a
 transfer pass (each segment run from zero and, with U = 0, from the
-identity) and an fp32 scan, then the segments run as sequences of their own
-("FlashInfer GDN Prefill 完全指南", the CP routing of the API table).  Every
-case is checked against the fp64 sequential oracle: outputs, final states
-(pool rows in place, 16-bit states) and checkpoints, which must land where
-the unsegmented sequence puts them."""
+identity) and an fp32 scan; then the segments and the sequences left whole
+run as one batch ("FlashInfer GDN Prefill 完全指南", the CP routing of the
+API table).  The device picks the segments from cu_seqlens; each case first
+asks the host mirror of that choice which sequences it cuts, so that the
+case covers what it names.  Every case is checked against the fp64
+sequential oracle: outputs, final states (pool rows in place, 16-bit and
+fp8 states) and checkpoints, which must land where the unsegmented sequence
+puts them."""
 import pytest
 import torch
 
@@ -24,7 +27,11 @@ def _built():
 
 
 def _cp_segments(res, inp):
-    return gdn.lib().gdn_prefill_cp_segments(res["plan"].handle, len(inp["seq_lens"]), inp["T"], 0)
+    return gdn.gdn_prefill_cp_segments(res["plan"].handle, inp["seq_lens"], 0)[0]
+
+
+def _cp_per_seq(res, inp):
+    return gdn.gdn_prefill_cp_segments(res["plan"].handle, inp["seq_lens"], 0)[1]
 
 
 def test_cp_one_long_sequence_with_checkpoints():
@@ -37,26 +44,61 @@ def test_cp_one_long_sequence_with_checkpoints():
 
 
 def test_cp_pool_zero_length_and_short_sequences():
-    w = wl.custom(seq_lens=[700, 0, 5, 64, 333], hq=2, hk=2, hv=2, initial_state="pool", n_pool=9,
+    # a mixed batch on a pool: the long sequence runs as segments; the empty and short ones run whole, in the
+    # same launch, reading and writing their own pool rows in place
+    w = wl.custom(seq_lens=[2800, 0, 5, 64, 333], hq=2, hk=2, hv=2, initial_state="pool", n_pool=9,
                   l2norm_in_kernel=True, qk_prenorm=False, checkpoint_every=64)
     inp = wl.generate(w, seed=61)
-    check_against_oracle(inp, run_gpu(to_device(inp), use_cp=True))
+    res = run_gpu(to_device(inp), use_cp=True, return_plan=True)
+    segs = _cp_per_seq(res, inp)
+    assert segs[0] >= 2 and segs[1:] == [1, 1, 1, 1]
+    check_against_oracle(inp, res)
 
 
 @pytest.mark.parametrize("dtype,state_dtype", [(torch.float16, torch.float32), (torch.bfloat16, torch.bfloat16)])
 def test_cp_input_and_state_types(dtype, state_dtype):
-    w = wl.custom(seq_lens=[900, 260], hq=4, hk=2, hv=2, dtype=dtype, initial_state="dense", alpha="exp_softplus16")
+    # the 16-bit state is read by the fp32 scan (segmented sequence) and by the chunk kernel (whole sequence)
+    w = wl.custom(seq_lens=[3000, 260], hq=4, hk=2, hv=2, dtype=dtype, initial_state="dense", alpha="exp_softplus16")
     inp = wl.generate(w, seed=62)
     inp["initial_state"] = inp["initial_state"].to(state_dtype)
-    check_against_oracle(inp, run_gpu(to_device(inp), use_cp=True))
+    res = run_gpu(to_device(inp), use_cp=True, return_plan=True)
+    segs = _cp_per_seq(res, inp)
+    assert segs[0] >= 2 and segs[1] == 1
+    check_against_oracle(inp, res)
 
 
 def test_cp_steep_gates_and_zero_initial_state():
     # strong decay: the segment transfers are close to zero and the pairwise decay path runs
-    w = wl.custom(seq_lens=[640, 130], hq=1, hk=1, hv=2, alpha="u(0.05,0.3)", l2norm_in_kernel=True,
+    w = wl.custom(seq_lens=[2560, 130], hq=1, hk=1, hv=2, alpha="u(0.05,0.3)", l2norm_in_kernel=True,
                   qk_prenorm=False)
     inp = wl.generate(w, seed=63)
-    check_against_oracle(inp, run_gpu(to_device(inp), use_cp=True))
+    res = run_gpu(to_device(inp), use_cp=True, return_plan=True)
+    assert _cp_segments(res, inp) >= 2
+    check_against_oracle(inp, res)
+
+
+def test_cp_several_segmented_sequences_among_whole_ones():
+    # two long sequences cut (one of them into fewer segments), five short ones whole, a pool with gaps,
+    # checkpoints every 128 tokens: segment starts, transfer rows and start rows of two sequences interleave
+    w = wl.custom(seq_lens=[150, 2600, 40, 1400, 0, 300, 90], hq=2, hk=2, hv=2, initial_state="pool", n_pool=12,
+                  l2norm_in_kernel=True, qk_prenorm=False, checkpoint_every=128)
+    inp = wl.generate(w, seed=66)
+    res = run_gpu(to_device(inp), use_cp=True, return_plan=True)
+    segs = _cp_per_seq(res, inp)
+    assert segs[1] >= 2 and segs[3] >= 2 and segs[3] < segs[1]
+    assert [segs[i] for i in (0, 2, 4, 5, 6)] == [1] * 5
+    check_against_oracle(inp, res)
+
+
+def test_cp_declined_runs_every_sequence_whole():
+    # a balanced batch: the load model takes no segments, and the context-parallel launches still give the
+    # one-pass results (every unit on the caller's state in the segment pass, nothing to scan or copy)
+    w = wl.custom(seq_lens=[400, 380, 410, 350], hq=2, hk=2, hv=2, initial_state="dense", l2norm_in_kernel=True,
+                  qk_prenorm=False, checkpoint_every=64)
+    inp = wl.generate(w, seed=67)
+    res = run_gpu(to_device(inp), use_cp=True, return_plan=True)
+    assert _cp_segments(res, inp) == 0
+    check_against_oracle(inp, res)
 
 
 def test_cp_full_size_single_long_sequence_sampled_heads():
@@ -72,7 +114,7 @@ def test_cp_full_size_single_long_sequence_sampled_heads():
 @pytest.mark.parametrize("state_dtype", [torch.float8_e4m3fn, torch.float8_e5m2])
 def test_cp_fp8_state_pool_and_fp8_checkpoints(state_dtype):
     # context parallelism reads the fp8 pool into the fp32 scan and writes the last segments' states back in fp8
-    w = wl.custom(seq_lens=[1100, 40], hq=2, hk=2, hv=2, initial_state="pool", n_pool=5, l2norm_in_kernel=True,
+    w = wl.custom(seq_lens=[3000, 40], hq=2, hk=2, hv=2, initial_state="pool", n_pool=5, l2norm_in_kernel=True,
                   qk_prenorm=False, checkpoint_every=128)
     inp = wl.generate(w, seed=64)
     inp["initial_state"] = inp["initial_state"].to(state_dtype)
@@ -82,8 +124,9 @@ def test_cp_fp8_state_pool_and_fp8_checkpoints(state_dtype):
 
 
 def test_cp_eight_segments_long_sequence():
-    # one sequence, two state heads: N * H = 2 on a 152-SM GPU gives the plan's maximum of eight segments,
-    # whose start states come from seven chained transfers (each rounded through the 16-bit state operand)
+    # one sequence of 64 chunks, two state heads: eight segments of 8 chunks (27 chunk periods against 64 for
+    # one pass) -- the plan's maximum, whose start states come from seven chained transfers, each rounded
+    # through the 16-bit state operand
     w = wl.custom(seq_lens=[4096], hq=2, hk=2, hv=2, initial_state="dense", l2norm_in_kernel=True,
                   qk_prenorm=False, alpha="u(0.95,1.0)", checkpoint_every=256)
     inp = wl.generate(w, seed=65)

@@ -69,10 +69,14 @@ def test_prefill_graph_replay_matches_eager():
 
 
 def test_context_parallel_graph_replay_matches_eager_and_oracle():
-    # few (sequence, head) units: the run takes segments; all its launches go into one graph
+    # one long sequence beside a short one: the long one runs as segments, the short one whole, and all the
+    # launches go into one graph.  The replay swaps the two lengths (same total): the segments are cut on the
+    # device from cu_seqlens, so the captured graph follows the new batch without being captured again.
     w = wl.custom(seq_lens=[1500, 70], hq=2, hk=2, hv=2, initial_state="dense", l2norm_in_kernel=True,
                   qk_prenorm=False, checkpoint_every=128)
-    b_cpu = wl.generate(w, seed=48)
+    w2 = wl.custom(seq_lens=[70, 1500], hq=2, hk=2, hv=2, initial_state="dense", l2norm_in_kernel=True,
+                   qk_prenorm=False, checkpoint_every=128)
+    b_cpu = wl.generate(w2, seed=48)
     a, b = to_device(wl.generate(w, seed=47)), to_device(b_cpu)
     ck = torch.zeros(wl.num_checkpoints(a["seq_lens"], 128), a["H"], 128, 128, device="cuda")
     out = torch.empty(a["T"], a["H"], 128, dtype=a["q"].dtype, device="cuda")
@@ -87,13 +91,16 @@ def test_context_parallel_graph_replay_matches_eager_and_oracle():
 
     live = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in a.items()}
     _, plan, _ = call(live, out, fin, ck, return_plan=True)  # eager: plan, workspace, kernel attributes
-    assert gdn.lib().gdn_prefill_cp_segments(plan.handle, 2, a["T"], 0) >= 2
+    assert gdn.gdn_prefill_cp_segments(plan.handle, a["seq_lens"], 0)[1][1] == 1
+    assert gdn.gdn_prefill_cp_segments(plan.handle, a["seq_lens"], 0)[1][0] >= 2
+    assert gdn.gdn_prefill_cp_segments(plan.handle, b["seq_lens"], 0)[1][0] == 1
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         call(live, out, fin, ck)
     _refill(live, b)
-    live["initial_state"].copy_(b["initial_state"])
+    for key in ("initial_state", "cu_seqlens", "checkpoint_cu_starts"):
+        live[key].copy_(b[key])
     g.replay()
     torch.cuda.synchronize()
     out_e, fin_e, ck_e = torch.empty_like(out), torch.empty_like(fin), torch.zeros_like(ck)
