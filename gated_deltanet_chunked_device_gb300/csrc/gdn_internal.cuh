@@ -321,6 +321,8 @@ struct DecodeParams {
     int32_t N, H, hq, hk, hv;
     int32_t m;                     // tokens per sequence
     int l2norm;
+    int32_t stages;                // shared-memory stages of the unit ring (set by the launcher)
+    int32_t stage_bytes;           // bytes of one stage: state rows, then the unit's tokens
 };
 
 __host__ __device__ inline int64_t load_index(const void* p, int i64, int64_t i) {

@@ -589,9 +589,9 @@ gdn_status gdn_decode_run(gdn_prefill_plan_t plan, const gdn_prefill_args* args,
     if (!make_state_layout(d.state_dtype, a.state_strides, (f & GDN_FLAG_HAS_STATE_INDICES) ? a.n_pool : N, plan->H,
                            &sl))
         return GDN_ERR_INVALID_ARG;
-    if (sl.s_v > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;  // the decode kernel steps v rows with a 32-bit stride
-    const int64_t blocks = static_cast<int64_t>(N) * plan->H;
-    if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    // (sequence, head) units in 32 bits, with room for the kernel's look-ahead of a few grid strides
+    const int64_t units = static_cast<int64_t>(N) * plan->H;
+    if (units > 0x7fffffffLL - (1 << 20)) return GDN_ERR_UNSUPPORTED;
     gdn::DecodeParams p{};
     p.q = a.q;
     p.k = a.k;

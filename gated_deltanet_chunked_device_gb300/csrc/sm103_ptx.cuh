@@ -100,6 +100,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     return true;
 }
 
+// Plain bulk copy (no tensor map) of `bytes` bytes, a multiple of 16, from global to shared memory, both
+// addresses 16-byte aligned; completes on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Proxy fences
 // ---------------------------------------------------------------------------

@@ -165,8 +165,7 @@ typedef struct gdn_prefill_args {
      * bytes (16 elements of an fp8 state), and the layout does not overlap:
      * sorted by stride, each stride is at least the extent covered by the
      * smaller ones (128 for the v rows' own k elements).  Anything else is
-     * GDN_ERR_INVALID_ARG.  gdn_decode_run also needs the v stride below
-     * 2^31 elements (else GDN_ERR_UNSUPPORTED). */
+     * GDN_ERR_INVALID_ARG. */
     int64_t state_strides[3];
     int32_t n_pool;               /* pool rows, with GDN_FLAG_HAS_STATE_INDICES */
     const void *state_indices;    /* [N], with GDN_FLAG_HAS_STATE_INDICES */
