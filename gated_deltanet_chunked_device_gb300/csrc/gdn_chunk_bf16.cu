@@ -1136,8 +1136,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t ck_every = (p.checkpoints && p.ckpt_n > 0) ? p.ckpt_n / kChunk : 0;
         uint32_t n = 0, u = 0;
         bool ok = true;
-        // As in the intra warpgroups: wait outcomes are ANDed over both warpgroups at the next named barrier.
-        for (; ok;) {
+        // As in the intra warpgroups: wait outcomes are ANDed over both warpgroups at the next named barrier,
+        // and the loops are left only there.  (The pre-scale pass ends an iteration with a wait, so neither
+        // loop condition may test `ok`: a thread whose wait ran out carries it to the next AND barrier, which
+        // every thread reaches, instead of leaving alone.)
+        for (;;) {
             const int slot = u & 1;
             ok = wait_bar(cx, B_UNIT_FULL + slot, (u >> 1) & 1);
             const UnitInfo info = read_unit(sm, slot);
@@ -1178,7 +1181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
                 if (st == 0) mbar_arrive(cx.bars + B_SB_FULL + (n & 1));
             }
-            for (int32_t c = 0; c < info.nC && ok; ++c, ++n) {
+            for (int32_t c = 0; c < info.nC; ++c, ++n) {
                 const int s = n & 1;
                 const uint32_t ph = (n >> 1) & 1;
                 const int64_t tc = info.t0 + static_cast<int64_t>(c) * kChunk;
