@@ -63,6 +63,7 @@ KERNEL_SOURCES = ["gated_deltanet_chunked_device_gb300/csrc/gdn_chunk_bf16.cu",
                   "gated_deltanet_chunked_device_gb300/csrc/sm103_ptx.cuh",
                   "gated_deltanet_chunked_device_gb300/csrc/gdn_internal.cuh"]
 DECODE_SOURCES = ["gated_deltanet_chunked_device_gb300/csrc/gdn_decode.cu",
+                  "gated_deltanet_chunked_device_gb300/csrc/sm103_ptx.cuh",
                   "gated_deltanet_chunked_device_gb300/csrc/gdn_internal.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
