@@ -2,9 +2,9 @@
 // fp32 state, on sm_103a: tcgen05 tensor cores with TMEM accumulators,
 // TMA-fed operands, warp-specialised and pipelined across chunks.  The two
 // input types share one kernel template (gdn_chunk_kernel<__nv_bfloat16> and
-// gdn_chunk_kernel<__half>): every 16-bit operand the kernel writes itself (P, T',
-// T'', W^T, S, Delta) takes the input type, because A and B of one tcgen05
-// kind::f16 product have the same type.
+// gdn_chunk_kernel<__half>): every 16-bit operand the kernel writes itself (P,
+// T'', the TMEM copy of S, Delta) takes the input type, because A and B of one
+// tcgen05 kind::f16 product have the same type.
 //
 // Per chunk of C = 64 tokens (G_r = sum_{m<=r} log alpha_m inside the chunk,
 // gamma_r = e^{G_r}; n_j, m_i = 1/|k_j|, 1/|q_i| when the L2 norm is on, else
@@ -16,11 +16,14 @@
 //     A~_ij = beta_i n_i^2 e^{G_i-G_j} (k_i.k_j), j < i      (n_i from diag D1)
 //     P_ij = e^{G_i-G_j} (q_i.k_j),                j <= i
 //     T~ = (I + A~)^-1                              blocked substitution + tf32 mma.sync
-//     W~^T = K^T (T~ diag(beta gamma n^2))^T,  U~^T = V^T (T~ diag(beta n))^T   tcgen05
+//     T' = T~ diag(beta gamma n^2) (fp32),  T'' = T~ diag(beta n) (16-bit)
+//     U~^T = V^T T''^T                              tcgen05, into the Delta slot
 //   state pass ("块内 state 和块间 final state": only the chunk's last state
 //   crosses the boundary):
-//     Delta~^T = U~^T - S W~^T                      tcgen05, A (bf16 S) from TMEM, negated
+//     [X | O] = S [K; Q']^T                         tcgen05, one N = 128 product, A (16-bit S) from TMEM
+//     Delta~^T = U~^T - X T'^T                      tcgen05 kind::tf32, A = X (fp32) from TMEM, negated
 //     S <- gamma_63 S + (Delta~^T diag(e^{G_63-G_j})) K          tcgen05, in TMEM
+//   (S W~^T with W~^T = K^T T'^T is computed as X T'^T: no W~ tile exists.)
 //   output ("GDN与线性注意力GPU并行实现" section 3.3: O_init = Q S plus a
 //   triangular-masked product):
 //     O^T = scale (S Q'^T + Delta~^T P^T) diag(m),  Q' = diag(gamma) Q     tcgen05, one accumulator
@@ -35,27 +38,28 @@
 // the rows first, without re-rounding them to bf16.  With the normalised
 // matrix A = diag(beta n) M diag(n) (M_ij = e^{G_i-G_j} k_i.k_j), the
 // similarity diag(n) (I + A) diag(n)^-1 = I + A~ gives T = diag(1/n) T~ diag(n);
-// so W~ = diag(n) W, U~ = diag(n) U, Delta~ = diag(n) Delta, and n cancels
-// from the state update and from P: every norm factor is a row factor of the
-// matrix that uses it, known to the thread that holds that row.
+// so U~ = diag(n) U, Delta~ = diag(n) Delta, and n cancels from the state
+// update and from P: every norm factor is a row factor of the matrix that uses
+// it, known to the thread that holds that row.
 //
 // Roles (640 threads in five warpgroups, one work unit = (sequence, state
 // head) at a time, units taken longest first from an atomic counter):
 //   warp 0       TMA: K, Q tiles (3 stages) and V tile; unit scheduler
-//   warp 1       tcgen05 issue for the intra-chunk products (D1, W, U)
-//   warp 2       tcgen05 issue for the state chain (Delta, S Q^T, Delta P^T, S)
+//   warp 1       tcgen05 issue for the intra-chunk products (D1, U)
+//   warp 2       tcgen05 issue for the state chain (X | O, Delta, Delta P^T, S)
 //   warp 3       TMEM allocation; gates: G, gamma, beta, the per-row /
 //                per-column factor vectors and the q norms
 //   warps 4-11   two intra warpgroups (TMEM lane quarter x column half):
 //                A and P, Q' = diag(gamma) Q where needed, T in place
 //                with T' and T'', one chunk ahead of the state warpgroups
-//   warps 12-19  two state warpgroups (lane quarter x column half): W to
-//                shared memory, Delta epilogue, state epilogue (next bf16 S
-//                operand in TMEM, checkpoints, final state, prescale),
-//                output epilogue
+//   warps 12-19  two state warpgroups (lane quarter x column half): Delta
+//                epilogue, state epilogue (next 16-bit S operand in TMEM,
+//                checkpoints, final state, prescale), output epilogue
 // Every wait is bounded; a timeout sets GDN_DEVICE_ERR_TIMEOUT, raises a
 // shared abort flag that every other wait polls, drains the CTA's in-flight
-// copies and tensor-core work, frees TMEM and returns.
+// copies and tensor-core work, frees TMEM and returns.  The intra and state
+// warpgroups carry each wait's outcome to their next named barrier, which ANDs
+// it over the group (bar.red.and), and leave their loops only there.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 

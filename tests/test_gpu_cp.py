@@ -134,3 +134,17 @@ def test_cp_eight_segments_long_sequence():
     if torch.cuda.get_device_properties(0).multi_processor_count >= 30:
         assert _cp_segments(res, inp) == 8
     check_against_oracle(inp, res)
+
+
+def test_cp_state_carried_across_segments():
+    # gates near one and small beta: a segment's transfer M stays close to the identity (alpha^512 ~ 0.77,
+    # the erasure (I - beta k k^T) weak), so the start state of every segment -- the fp32 scan S M + N over up
+    # to seven transfers -- shows in that segment's outputs and in the final state instead of decaying away
+    w = wl.custom(seq_lens=[4096, 300], hq=2, hk=2, hv=2, initial_state="dense", l2norm_in_kernel=True,
+                  qk_prenorm=False, alpha="u(0.999,1.0)", checkpoint_every=256)
+    inp = wl.generate(w, seed=68)
+    inp["beta"] = inp["beta"] * 0.02
+    res = run_gpu(to_device(inp), use_cp=True, return_plan=True)
+    segs = _cp_per_seq(res, inp)
+    assert segs[0] >= 4 and segs[1] == 1
+    check_against_oracle(inp, res)
