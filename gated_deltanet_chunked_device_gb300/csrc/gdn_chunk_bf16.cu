@@ -667,6 +667,62 @@ __device__ __noinline__ void finish_unit(uint32_t tm_s, void* ck, int64_t ck_off
     if (dst) store_final_state(tm_s, dst, off, dt);
 }
 
+// Cold paths of the per-chunk loops, out of line so that the code every chunk runs stays small in the
+// instruction caches (every SM sub-partition runs intra, state and scheduler code at once).
+
+// A / P row i, this warp's 32 columns, with e^{G_i - G_j} taken pairwise (a chunk whose gate range is too
+// wide for row and column factors): rb times the exponential times the D1 value, into x.
+__device__ __noinline__ void pairwise_decay_row(float* x, uint32_t tm_d1, const float* gb, int i, int hh, float rb) {
+    uint32_t rr[32];
+    tmem_ld32_wait(tm_d1, rr);
+    const float Gi = gb[kGG + i];
+#pragma unroll
+    for (int q = 0; q < 32; ++q) x[q] = rb * __expf(Gi - gb[kGG + 32 * hh + q]) * __uint_as_float(rr[q]);
+}
+
+// Q' = diag(gamma) Q in place (a chunk that does not keep Q as stored): row it / 4, 32 values per thread.
+template <bool kF16>
+__device__ __noinline__ void scale_q_rows(uint8_t* kqs, int it, const float* gb) {
+    const int qr = it >> 2, qq = it & 3;
+    const float gam = gb[kGGam + qr];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int cch = 4 * qq + k;  // 16-byte column of the 256-byte row
+        uint8_t* half = kqs + 8192 + (cch >> 3) * 16384;
+        float f[8];
+        unpack8<kF16>(*reinterpret_cast<const uint4*>(half + sw128_offset(qr, cch & 7)), f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] *= gam;
+        st_chunk16<kF16>(half, qr, cch & 7, f);
+    }
+}
+
+// The padded rows (>= Lc) of a tail chunk's K tile (threads 0..63) and V tile (64..127) are zeroed.
+__device__ __noinline__ void zero_tail_rows(uint8_t* kqs, uint8_t* vt, int it, int Lc) {
+    const int zr = it & 63;
+    if (it < 128 && zr >= Lc) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        uint8_t* base = (it < 64) ? kqs : vt;
+        const uint32_t hs = (it < 64) ? 16384 : 8192;
+#pragma unroll 1
+        for (int cch = 0; cch < 16; ++cch)
+            *reinterpret_cast<uint4*>(base + (cch >> 3) * hs + sw128_offset(zr, cch & 7)) = z;
+    }
+}
+
+// The valid rows of a tail chunk's output tile, by coalesced 16-byte stores (a full chunk goes by TMA).
+__device__ __noinline__ void store_output_tail(const uint8_t* tile, uint8_t* gout, int st, int Lc, int64_t tc,
+                                              int H, int h) {
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+        const int id = st + 256 * k, row = id >> 4, col = id & 15;
+        if (row < Lc) {
+            const uint4 val = *reinterpret_cast<const uint4*>(tile + row * 256 + col * 16);
+            *reinterpret_cast<uint4*>(gout + ((static_cast<size_t>(tc + row) * H + h) * kHead) * 2 + col * 16) = val;
+        }
+    }
+}
+
 // E16: the input element type, __nv_bfloat16 or __half.  kTransfer: the context-parallel transfer pass --
 // units [0, N*H) run each sequence (a segment) from a zero state, units [N*H, 2*N*H) run it from the
 // identity with U = 0 (the segment's transfer matrix), into output_state rows seq and N + seq; no output
@@ -1058,12 +1114,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         } else {
                             // pairwise: the row factor without its e^{G_i - Gref}, times e^{G_i - G_j}
-                            const float Gi = gb[kGG + i];
                             const float rb = arow ? gb[kGBeta + i] * rn * rn
                                                   : (gb[kGKeepQ] != 0.f ? 1.f / gb[kGGam + i] : 1.f);
+                            float xp[32];
+                            pairwise_decay_row(xp, tm_lane + kTmD1 + 32 * hh, gb, i, hh, rb);
 #pragma unroll
-                            for (int q = 0; q < 32; ++q)
-                                x[q] = rb * __expf(Gi - gb[kGG + 32 * hh + q]) * __uint_as_float(rr[q]);
+                            for (int q = 0; q < 32; ++q) x[q] = xp[q];
                         }
                         if (arow) {
 #pragma unroll
@@ -1082,33 +1138,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // Q' = diag(gamma) Q in place, for the S Q'^T product (D1 has read Q already), unless the chunk
                 // keeps Q as stored.  Four threads per row, 32 values each.
-                if (gb[kGKeepQ] == 0.f && !kTransfer) {
-                    const int qr = it >> 2, qq = it & 3;
-                    const float gam = gb[kGGam + qr];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int cch = 4 * qq + k;  // 16-byte column of the 256-byte row
-                        uint8_t* half = kqs + 8192 + (cch >> 3) * 16384;
-                        float f[8];
-                        unpack8<kF16>(*reinterpret_cast<const uint4*>(half + sw128_offset(qr, cch & 7)), f);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) f[j] *= gam;
-                        st_chunk16<kF16>(half, qr, cch & 7, f);
-                    }
-                }
+                if (gb[kGKeepQ] == 0.f && !kTransfer) scale_q_rows<kF16>(kqs, it, gb);
                 // zero the padded rows of the K and V tiles (they hold the next
                 // sequence or TMA zero fill; only exact zeros may meet them)
                 if (Lc < kChunk) {
                     ok = ok && wait_bar(cx, B_V_FULL, n & 1);
-                    const int zr = it & 63;
-                    if (it < 128 && zr >= Lc) {
-                        const uint4 z = make_uint4(0, 0, 0, 0);
-                        uint8_t* base = (it < 64) ? kqs : sm + kV;
-                        const uint32_t hs = (it < 64) ? 16384 : 8192;
-#pragma unroll 1
-                        for (int cch = 0; cch < 16; ++cch)
-                            *reinterpret_cast<uint4*>(base + (cch >> 3) * hs + sw128_offset(zr, cch & 7)) = z;
-                    }
+                    zero_tail_rows(kqs, sm + kV, it, Lc);
                 }
                 // Q' and the zeroed K / V rows reach the async proxy before Q_READY (the X | O product reads Q')
                 fence_proxy_async_smem();
@@ -1294,16 +1329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             bulk_commit_group();
                         }
                     } else {
-                        uint8_t* gout = static_cast<uint8_t*>(p.output);
-#pragma unroll 1
-                        for (int k = 0; k < 4; ++k) {
-                            const int id = st + 256 * k, row = id >> 4, col = id & 15;
-                            if (row < Lc) {
-                                const uint4 val = *reinterpret_cast<const uint4*>(sm + kOutT + row * 256 + col * 16);
-                                *reinterpret_cast<uint4*>(gout + ((static_cast<size_t>(tc + row) * H + info.h) * kHead) * 2 +
-                                                          col * 16) = val;
-                            }
-                        }
+                        store_output_tail(sm + kOutT, static_cast<uint8_t*>(p.output), st, Lc, tc, H, info.h);
                     }
                 }
                 __syncwarp();
@@ -1325,18 +1351,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t gn = (n + 1) % 3;
                     ok = wait_bar(cx, B_GATES_FULL + gn, ((n + 1) / 3) & 1);
                     const float gnext = reinterpret_cast<const float*>(sm + kGbuf)[gn * kGFloats + kGGam + 63];
+                    // the checkpoint (S_n, before the scale) by the out-of-line store that also writes final states
+                    if (ck_off >= 0) store_final_state(tm_lane + kTmS + 64 * hh, p.checkpoints, ck_off, p.ckpt_dtype);
 #pragma unroll 1
                     for (int c0 = 0; c0 < 64; c0 += 32) {
                         uint32_t r[32];
                         tmem_ld32_wait(tm_lane + kTmS + 64 * hh + c0, r);
-                        if (ck_off >= 0) {
-#pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
-                                const float f[4] = {__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                                    __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])};
-                                state_store4(p.checkpoints, ck_off + c0 + j, p.ckpt_dtype, f);
-                            }
-                        }
 #pragma unroll
                         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gnext);
                         tmem_st32(tm_lane + kTmS + 64 * hh + c0, r);
