@@ -212,10 +212,26 @@ __device__ __forceinline__ bool wait_bar(const Ctx& cx, int b, uint32_t parity) 
     return wait_bar_slow(cx, b, parity);
 }
 
+// The single-warp roles' slow path: the same bounded loop with a 100 ns suspend hint (measured a little
+// faster for the issuers and the producer than the warpgroups' 2 us).
+__device__ __noinline__ bool wait_bar_warp_slow(const Ctx& cx, int b, uint32_t parity) {
+    uint64_t* bar = cx.bars + b;
+    const long long t0 = clock64();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 100)) return true;
+        if (*cx.abort) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            atomicOr(cx.status, static_cast<int32_t>(GDN_DEVICE_ERR_TIMEOUT));
+            *cx.abort = 1;
+            return false;
+        }
+    }
+}
+
 // A wait whose outcome is the same for every lane of a converged warp (the
 // single-warp roles use elect.sync and full-mask shuffles after their waits).
 __device__ __forceinline__ bool wait_bar_warp(const Ctx& cx, int b, uint32_t parity) {
-    return __all_sync(0xffffffffu, wait_bar(cx, b, parity));
+    return __all_sync(0xffffffffu, mbar_try_wait(cx.bars + b, parity) || wait_bar_warp_slow(cx, b, parity));
 }
 
 // Bounded wait used while draining (ignores the abort flag).
