@@ -35,9 +35,10 @@ constexpr int kOffW = kOffQ + 64 * kLdK;       // W  [64][kLdK]
 constexpr int kOffS = kOffW + 64 * kLdK;       // S slice [64 v][kLdK]
 constexpr int kOffV = kOffS + kVs * kLdK;      // V slice [64 j][kLdV]
 constexpr int kOffX = kOffV + 64 * kLdV;       // U, then Delta [64 j][kLdV]
-constexpr int kOffA = kOffX + 64 * kLdV;       // A, then T, then P [64][kLdV]
-constexpr int kOffG = kOffA + 64 * kLdV;       // G[64], gamma[64], beta[64]
-constexpr int kF32SmemFloats = kOffG + 3 * 64;
+constexpr int kOffA = kOffX + 64 * kLdV;       // A, then P [64][kLdV]
+constexpr int kOffT = kOffA + 64 * kLdV;       // T = (I + A)^-1 [64][kLdV]
+constexpr int kOffG = kOffT + 64 * kLdV;       // G[64], gamma[64], beta[64], dec[64], beta gamma[64]
+constexpr int kF32SmemFloats = kOffG + 5 * 64;
 constexpr size_t kF32Smem = sizeof(float) * kF32SmemFloats;
 
 __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkParams p) {
@@ -70,9 +71,12 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
     float* Vs = sf + kOffV;
     float* Xs = sf + kOffX;
     float* Am = sf + kOffA;
+    float* Ts = sf + kOffT;
     float* sG = sf + kOffG;
     float* sGam = sG + 64;
     float* sBeta = sG + 128;
+    float* sDec = sG + 192;   // e^{G_63 - G_j}
+    float* sWc = sG + 256;    // beta_j gamma_j
 
     // state slice: rows v0..v0+63 of [V][K]
     for (int e = 4 * tid; e < kVs * kHead; e += 4 * kF32Threads) {
@@ -126,12 +130,17 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
                 const float y = __shfl_up_sync(0xffffffffu, incl, o);
                 if (tid >= o) incl += y;
             }
+            const float g63 = __shfl_sync(0xffffffffu, incl, 31);
             sG[r0] = incl - la1;
             sG[r1] = incl;
             sGam[r0] = expf(incl - la1);
             sGam[r1] = expf(incl);
             sBeta[r0] = b0;
             sBeta[r1] = b1;
+            sDec[r0] = expf(g63 - (incl - la1));
+            sDec[r1] = expf(g63 - incl);
+            sWc[r0] = b0 * sGam[r0];
+            sWc[r1] = b1 * sGam[r1];
         }
         __syncthreads();
         // ---- A (strictly lower)
@@ -146,34 +155,35 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
             Am[i * kLdV + j] = a;
         }
         __syncthreads();
-        // ---- T = (I + A)^-1, one column per thread, in registers, then written over A
-        {
-            float x[kChunk];
+        // ---- T = (I + A)^-1 by forward substitution, column j on thread j, into its own buffer (two
+        //      accumulators per row; the column lives in shared memory, not in a run-time indexed array)
+        if (tid < kChunk) {
             const int j = tid;
-            if (j < kChunk) {
-                for (int i = 0; i < kChunk; ++i) {
-                    float acc = (i == j) ? 1.f : 0.f;
-                    if (i > j)
-                        for (int m = j; m < i; ++m) acc -= Am[i * kLdV + m] * x[m];
-                    x[i] = (i < j) ? 0.f : acc;
+            for (int i = 0; i < kChunk; ++i) {
+                float a0 = (i == j) ? 1.f : 0.f, a1 = 0.f;
+                if (i > j) {
+                    int m = j;
+                    for (; m + 1 < i; m += 2) {
+                        a0 -= Am[i * kLdV + m] * Ts[m * kLdV + j];
+                        a1 -= Am[i * kLdV + m + 1] * Ts[(m + 1) * kLdV + j];
+                    }
+                    if (m < i) a0 -= Am[i * kLdV + m] * Ts[m * kLdV + j];
                 }
+                Ts[i * kLdV + j] = (i < j) ? 0.f : a0 + a1;
             }
-            __syncthreads();
-            if (j < kChunk)
-                for (int i = 0; i < kChunk; ++i) Am[i * kLdV + j] = x[i];
         }
         __syncthreads();
         // ---- W = T diag(beta gamma) K,  U = T diag(beta) V_slice
         for (int e = tid; e < kChunk * kHead; e += kF32Threads) {
             const int i = e / kHead, d = e % kHead;
             float acc = 0.f;
-            for (int j = 0; j <= i; ++j) acc += Am[i * kLdV + j] * sBeta[j] * sGam[j] * Ks[j * kLdK + d];
+            for (int j = 0; j <= i; ++j) acc += Ts[i * kLdV + j] * sWc[j] * Ks[j * kLdK + d];
             Ws[i * kLdK + d] = acc;
         }
         for (int e = tid; e < kChunk * kVs; e += kF32Threads) {
             const int i = e / kVs, d = e % kVs;
             float acc = 0.f;
-            for (int j = 0; j <= i; ++j) acc += Am[i * kLdV + j] * sBeta[j] * Vs[j * kLdV + d];
+            for (int j = 0; j <= i; ++j) acc += Ts[i * kLdV + j] * sBeta[j] * Vs[j * kLdV + d];
             Xs[i * kLdV + d] = acc;
         }
         __syncthreads();
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
             Xs[i * kLdV + vv] -= acc;
         }
         __syncthreads();
-        // ---- P_ij = e^{G_i - G_j} (q_i . k_j) for j <= i, over T (done with it)
+        // ---- P_ij = e^{G_i - G_j} (q_i . k_j) for j <= i, over A
         for (int e = tid; e < kChunk * kChunk; e += kF32Threads) {
             const int i = e / kChunk, j = e % kChunk;
             float pv = 0.f;
@@ -222,11 +232,11 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
         __syncthreads();
         // ---- state: S <- gamma_63 S + sum_j e^{G_63 - G_j} Delta_j k_j^T
         {
-            const float g63 = sG[kChunk - 1];
+            const float eg63 = sGam[kChunk - 1];
             for (int e = tid; e < kVs * kHead; e += kF32Threads) {
                 const int vv = e / kHead, d = e % kHead;
-                float acc = expf(g63) * Ss[vv * kLdK + d];
-                for (int j = 0; j < kChunk; ++j) acc += expf(g63 - sG[j]) * Xs[j * kLdV + vv] * Ks[j * kLdK + d];
+                float acc = eg63 * Ss[vv * kLdK + d];
+                for (int j = 0; j < kChunk; ++j) acc += sDec[j] * Xs[j * kLdV + vv] * Ks[j * kLdK + d];
                 Ss[vv * kLdK + d] = acc;
             }
         }
