@@ -684,17 +684,9 @@ __device__ __noinline__ void finish_unit(uint32_t tm_s, void* ck, int64_t ck_off
 }
 
 // Cold paths of the per-chunk loops, out of line so that the code every chunk runs stays small in the
-// instruction caches (every SM sub-partition runs intra, state and scheduler code at once).
-
-// A / P row i, this warp's 32 columns, with e^{G_i - G_j} taken pairwise (a chunk whose gate range is too
-// wide for row and column factors): rb times the exponential times the D1 value, into x.
-__device__ __noinline__ void pairwise_decay_row(float* x, uint32_t tm_d1, const float* gb, int i, int hh, float rb) {
-    uint32_t rr[32];
-    tmem_ld32_wait(tm_d1, rr);
-    const float Gi = gb[kGG + i];
-#pragma unroll
-    for (int q = 0; q < 32; ++q) x[q] = rb * __expf(Gi - gb[kGG + 32 * hh + q]) * __uint_as_float(rr[q]);
-}
+// instruction caches (every SM sub-partition runs intra, state and scheduler code at once).  The pairwise
+// decay of A / P and the checkpoint rows stay inline: out of line (an array handed to the call, a second
+// TMEM read) they cost registers and spills in the hot loops, and measured slower.
 
 // Q' = diag(gamma) Q in place (a chunk that does not keep Q as stored): row it / 4, 32 values per thread.
 template <bool kF16>
@@ -1132,10 +1124,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // pairwise: the row factor without its e^{G_i - Gref}, times e^{G_i - G_j}
                             const float rb = arow ? gb[kGBeta + i] * rn * rn
                                                   : (gb[kGKeepQ] != 0.f ? 1.f / gb[kGGam + i] : 1.f);
-                            float xp[32];
-                            pairwise_decay_row(xp, tm_lane + kTmD1 + 32 * hh, gb, i, hh, rb);
+                            const float Gi = gb[kGG + i];
 #pragma unroll
-                            for (int q = 0; q < 32; ++q) x[q] = xp[q];
+                            for (int q = 0; q < 32; ++q)
+                                x[q] = rb * __expf(Gi - gb[kGG + 32 * hh + q]) * __uint_as_float(rr[q]);
                         }
                         if (arow) {
 #pragma unroll
@@ -1368,11 +1360,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = wait_bar(cx, B_GATES_FULL + gn, ((n + 1) / 3) & 1);
                     const float gnext = reinterpret_cast<const float*>(sm + kGbuf)[gn * kGFloats + kGGam + 63];
                     // the checkpoint (S_n, before the scale) by the out-of-line store that also writes final states
-                    if (ck_off >= 0) store_final_state(tm_lane + kTmS + 64 * hh, p.checkpoints, ck_off, p.ckpt_dtype);
 #pragma unroll 1
                     for (int c0 = 0; c0 < 64; c0 += 32) {
                         uint32_t r[32];
                         tmem_ld32_wait(tm_lane + kTmS + 64 * hh + c0, r);
+                        if (ck_off >= 0) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                const float f[4] = {__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                                    __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])};
+                                state_store4(p.checkpoints, ck_off + c0 + j, p.ckpt_dtype, f);
+                            }
+                        }
 #pragma unroll
                         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gnext);
                         tmem_st32(tm_lane + kTmS + 64 * hh + c0, r);

@@ -134,6 +134,22 @@ def test_context_parallel_segment_choice(L, desc_kw, lens, sms, expect, per_seq)
         gdn.gdn_prefill_plan_destroy(plan)
 
 
+def test_context_parallel_choice_on_large_batches(L):
+    # the host query walks any number of sequences; a batch of many short ones never segments, and one long
+    # sequence among them is cut while the rest stay whole
+    st, plan, _ = gdn.gdn_prefill_plan(_desc(flags=_CP, max_num_seqs=5000, **_H1))
+    assert st == OK
+    try:
+        most, segs = gdn.gdn_prefill_cp_segments(plan, [100] * 3000, 152)
+        assert most == 0 and set(segs) == {1}
+        lens = [30] * 3000
+        lens[1234] = 20000
+        most, segs = gdn.gdn_prefill_cp_segments(plan, lens, 152)
+        assert most >= 2 and segs[1234] == most and segs.count(1) == 2999
+    finally:
+        gdn.gdn_prefill_plan_destroy(plan)
+
+
 def test_context_parallel_plan_reserves_its_scratch(L):
     st, p0, base = gdn.gdn_prefill_plan(_desc())
     st1, p1, with_cp = gdn.gdn_prefill_plan(_desc(flags=_CP))

@@ -148,3 +148,19 @@ def test_cp_state_carried_across_segments():
     segs = _cp_per_seq(res, inp)
     assert segs[0] >= 4 and segs[1] == 1
     check_against_oracle(inp, res)
+
+
+def test_cp_many_sequences_cross_the_segmentation_tiles():
+    # 600 sequences: the segmentation's block scans run over three tiles of 256; one long sequence early and
+    # one late are cut, the others run whole, and every offset after the first cut shifts
+    lens = [5 + (37 * i) % 90 for i in range(600)]
+    lens[3] = 5000
+    lens[520] = 4000
+    w = wl.custom(seq_lens=lens, hq=1, hk=1, hv=1, initial_state="pool", n_pool=640, l2norm_in_kernel=True,
+                  qk_prenorm=False, checkpoint_every=64)
+    inp = wl.generate(w, seed=69)
+    res = run_gpu(to_device(inp), use_cp=True, return_plan=True)
+    segs = _cp_per_seq(res, inp)
+    assert segs[3] >= 2 and segs[520] >= 2
+    assert sum(1 for x in segs if x > 1) == 2
+    check_against_oracle(inp, res, heads=[0])
