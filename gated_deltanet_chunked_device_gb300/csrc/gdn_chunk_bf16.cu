@@ -54,7 +54,9 @@
 //                with T' and T'', one chunk ahead of the state warpgroups
 //   warps 12-19  two state warpgroups (lane quarter x column half): Delta
 //                epilogue, state epilogue (next 16-bit S operand in TMEM,
-//                checkpoints, final state, prescale), output epilogue
+//                checkpoints, final state, prescale), output epilogue;
+//                checkpoints and final states leave through the output
+//                tile's buffer, so that their stores are coalesced
 // Every wait is bounded; a timeout sets GDN_DEVICE_ERR_TIMEOUT, raises a
 // shared abort flag that every other wait polls, drains the CTA's in-flight
 // copies and tensor-core work, frees TMEM and returns.  The intra and state
@@ -328,6 +330,33 @@ __device__ __forceinline__ void st_f32x8(uint8_t* tile, int i, int j0, const flo
 __device__ __forceinline__ void st_f32x2(uint8_t* tile, int i, int j, float x0, float x1) {
     *reinterpret_cast<float2*>(tile + (j >> 5) * 8192 + sw128_offset(i, (j & 31) >> 2) + (j & 3) * 4) =
         make_float2(x0, x1);
+}
+
+// Columns c0 .. c0 + 15 of this warp's 32 state rows (row = lane, values r) to a checkpoint or an output state,
+// staged through the warp's 2 KB slice of shared memory: written row by row (float4 j of row i at slot
+// j ^ ((i >> 1) & 3), so that neither the writes nor the reads meet a bank conflict) and read back with four lanes
+// per row, so that each store instruction covers 64 contiguous bytes of eight rows.  Stored straight from the
+// registers, each instruction would touch 32 rows a full row apart.  warp_off is the element offset of the warp's
+// row 0 at column 0 of its half, ld the element stride between rows.  kStoreUnroll unrolls the store loop (four
+// instructions of eight rows): fully on the per-chunk path, not at all on the once-per-unit one (whose registers
+// the caller pays for across the call).
+template <int kStoreUnroll>
+__device__ __forceinline__ void stage_rows16(const uint32_t (&r)[16], float* slice, void* dst, int64_t warp_off,
+                                             int64_t ld, int c0, int32_t dt, int lane) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<float4*>(slice + lane * 16 + 4 * (j ^ ((lane >> 1) & 3))) =
+            make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
+                        __uint_as_float(r[4 * j + 3]));
+    __syncwarp();
+#pragma unroll kStoreUnroll
+    for (int q = 0; q < 4; ++q) {
+        const int i = 8 * q + (lane >> 2), j = lane & 3;
+        const float4 f4 = *reinterpret_cast<const float4*>(slice + i * 16 + 4 * (j ^ ((i >> 1) & 3)));
+        const float f[4] = {f4.x, f4.y, f4.z, f4.w};
+        state_store4(dst, warp_off + static_cast<int64_t>(i) * ld + c0 + 4 * j, dt, f);
+    }
+    __syncwarp();
 }
 
 constexpr int kLdX1 = 24, kLdX2 = 40;  // scratch strides: conflict-free B-fragment reads
@@ -658,35 +687,36 @@ __device__ __noinline__ void identity_state(int ic, uint32_t tm_sbf, uint32_t tm
     if (!dst) tmem_wait_st();
 }
 
-// The final state after a unit's last chunk, or a checkpoint: this thread's 64 columns of the fp32
-// accumulator in TMEM (tm_s) to `base` at element offset `off`, in type dt.  Warp-uniform (tcgen05.ld is
-// warp-collective).
-__device__ __noinline__ void store_final_state(uint32_t tm_s, void* base, int64_t off, int32_t dt) {
+// The final state after a unit's last chunk, or its checkpoint: the warp's 32 rows of accumulator columns
+// (tm_s: this thread's 64 columns) to `base` in type dt, this thread's row at element offset `off` and the rows
+// ld elements apart, staged through the warp's slice of the output tile's buffer (free: the chunk's output
+// store has read it).  Warp-uniform (tcgen05.ld is warp-collective).
+__device__ __noinline__ void store_state_rows(uint32_t tm_s, void* base, int64_t off, int64_t ld, int32_t dt) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int lane = threadIdx.x & 31;
+    float* slice = reinterpret_cast<float*>(sm + kOutT) + ((threadIdx.x >> 5) & 7) * 512;
+    const int64_t warp_off = off - static_cast<int64_t>(lane) * ld;
 #pragma unroll 1
     for (int c0 = 0; c0 < 64; c0 += 16) {
         uint32_t r[16];
         tmem_ld16_wait(tm_s + c0, r);
-#pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-            const float f[4] = {__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                                __uint_as_float(r[j + 3])};
-            state_store4(base, off + c0 + j, dt, f);
-        }
+        stage_rows16<1>(r, slice, base, warp_off, ld, c0, dt, lane);
     }
 }
 
 // After a unit's last chunk: the checkpoint of that chunk end (ck_off >= 0) and the final state (dst non-null),
 // from this thread's 64 accumulator columns.  One out-of-line call site in the state loop.
 __device__ __noinline__ void finish_unit(uint32_t tm_s, void* ck, int64_t ck_off, int32_t ck_dt, void* dst,
-                                         int64_t off, int32_t dt) {
-    if (ck_off >= 0) store_final_state(tm_s, ck, ck_off, ck_dt);
-    if (dst) store_final_state(tm_s, dst, off, dt);
+                                         int64_t off, int64_t s_v, int32_t dt) {
+    if (ck_off >= 0) store_state_rows(tm_s, ck, ck_off, kHead, ck_dt);
+    if (dst) store_state_rows(tm_s, dst, off, s_v, dt);
 }
 
 // Cold paths of the per-chunk loops, out of line so that the code every chunk runs stays small in the
 // instruction caches (every SM sub-partition runs intra, state and scheduler code at once).  The pairwise
-// decay of A / P and the checkpoint rows stay inline: out of line (an array handed to the call, a second
-// TMEM read) they cost registers and spills in the hot loops, and measured slower.
+// decay of A / P and the checkpoint rows of a unit's inner chunks stay inline: out of line (an array handed to
+// the call, a second TMEM read) they cost registers and spills in the hot loops, and measured slower.
 
 // Q' = diag(gamma) Q in place (a chunk that does not keep Q as stored): row it / 4, 32 values per thread.
 template <bool kF16>
@@ -894,9 +924,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             auto issue_u = [&](uint32_t m, bool no_u) -> bool {  // U of global chunk m (U = 0: no product)
-                if (!wait_bar_warp(cx, B_T_FULL + (m & 1), (m >> 1) & 1) || !wait_bar_warp(cx, B_V_FULL, m & 1)) return false;
-                // the Delta slot is free once S of chunk m-2 has read it
+                // the Delta slot is free once S of chunk m-2 has read it; T comes last (usually the last to complete)
+                if (!wait_bar_warp(cx, B_V_FULL, m & 1)) return false;
                 if (m >= 2 && !wait_bar_warp(cx, B_S_FULL + (m & 1), ((m - 2) >> 1) & 1)) return false;
+                if (!wait_bar_warp(cx, B_T_FULL + (m & 1), (m >> 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t vv = smem_u32(sm + kV);
                 const uint32_t tpp = smem_u32(sm + kTpp);
@@ -1077,8 +1108,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* gb = reinterpret_cast<float*>(sm + kGbuf) + gs * kGFloats;
                 uint8_t* kqs = sm + kKQ + (n % kKQStages) * kKQStage;
                 ok = wait_bar(cx, B_GATES_FULL + gs, (n / 3) & 1);
-                // P buffer s is free once O2 of chunk n-2 has completed
-                if (n >= 2) ok = ok && wait_bar(cx, B_S_FULL + s, ((n - 2) >> 1) & 1);
+                // P buffer s is free once O2 of chunk n-2 has completed (only the P-row warps write it)
+                if (n >= 2 && wq >= 2) ok = ok && wait_bar(cx, B_S_FULL + s, ((n - 2) >> 1) & 1);
                 ok = ok && wait_bar(cx, B_D1_FULL, n & 1);
                 tc_fence_after();
                 // A rows (lanes 0..63: warps with wq < 2) and P rows (lanes 64..127), row i, this warp's 32
@@ -1090,7 +1121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int i = 32 * (wq & 1) + lane;
                     const bool active = !(hh == 1 && (wq & 1) == 0) && !(kTransfer && !arow);  // warp-uniform
                     float rn = 1.f;
-                    if (arow && p.l2norm) {
+                    if (arow && active && p.l2norm) {
                         // n_i = 1/|k_i|: |k_i|^2 is the diagonal of K K^T, column i of this lane's row (the warps
                         // whose half holds the diagonal find it in their main load below; warp wq = 1, hh = 0
                         // loads that half as well)
@@ -1157,18 +1188,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 if (!(ok = named_bar_and(kBarIntra, kIntraThreads, ok))) break;
-                if (it == 0) {
-                    mbar_arrive(cx.bars + B_D1_EMPTY);
-                    mbar_arrive(cx.bars + B_Q_READY + s);
-                }
                 // T = (I + A)^-1 in place, with T' = T diag(cw) (buffer s) and T'' = T diag(beta) in their bf16
-                // tiles: U of the previous chunk has read T'', and Delta of chunk n-2 has read T' buffer s
-                if (n >= 1) ok = wait_bar(cx, B_U_FULL + ((n - 1) & 1), ((n - 1) >> 1) & 1);
-                if (n >= 2) ok = ok && wait_bar(cx, B_DELTA_FULL + s, ((n - 2) >> 1) & 1);
+                // tiles: U of the previous chunk has read T'', and Delta of chunk n-2 has read T' buffer s.  Only
+                // the inverse's second stage writes those tiles, two group barriers later, so the hand-offs and
+                // these waits run on warps 8..11, which have no work in its first stage, and warps 4 and 5 start
+                // the forward substitution at once.
+                if (it >= 128) {
+                    if (it == 192) {
+                        mbar_arrive(cx.bars + B_D1_EMPTY);
+                        mbar_arrive(cx.bars + B_Q_READY + s);
+                    }
+                    if (n >= 1) ok = wait_bar(cx, B_U_FULL + ((n - 1) & 1), ((n - 1) >> 1) & 1);
+                    if (n >= 2) ok = ok && wait_bar(cx, B_DELTA_FULL + s, ((n - 2) >> 1) & 1);
+                }
                 tri_inverse_64<kF16>(Abuf, sm + (s ? kTp1 : kTp), sm + kTpp, gb + kGCw, gb + kGBn, X1, X2, it);
                 fence_proxy_async_smem();
                 if (!(ok = named_bar_and(kBarIntra, kIntraThreads, ok))) break;
-                if (it == 0) mbar_arrive(cx.bars + B_T_FULL + s);
+                if (it == 192) mbar_arrive(cx.bars + B_T_FULL + s);
             }
         }
     } else {
@@ -1359,29 +1395,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t gn = (n + 1) % 3;
                     ok = wait_bar(cx, B_GATES_FULL + gn, ((n + 1) / 3) & 1);
                     const float gnext = reinterpret_cast<const float*>(sm + kGbuf)[gn * kGFloats + kGGam + 63];
-                    // the checkpoint (S_n, before the scale) by the out-of-line store that also writes final states
+                    // the checkpoint (S_n, before the scale), staged through the output tile's buffer once the
+                    // output store has read it (not the unit's last chunk, so that store is a TMA store)
+                    if (ck_off >= 0) {
+                        if (st == 0) bulk_wait_group_read0();
+                        ok = named_bar_and(kBarState, kStateThreads, ok);
+                        float* slice = reinterpret_cast<float*>(sm + kOutT) + (st >> 5) * 512;
+                        const int64_t warp_off = ck_off - static_cast<int64_t>(lane) * kHead;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < 64; c0 += 32) {
-                        uint32_t r[32];
-                        tmem_ld32_wait(tm_lane + kTmS + 64 * hh + c0, r);
-                        if (ck_off >= 0) {
+                        for (int c0 = 0; c0 < 64; c0 += 16) {
+                            uint32_t r[16];
+                            tmem_ld16_wait(tm_lane + kTmS + 64 * hh + c0, r);
+                            stage_rows16<4>(r, slice, p.checkpoints, warp_off, kHead, c0, p.ckpt_dtype, lane);
 #pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
-                                const float f[4] = {__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                                    __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])};
-                                state_store4(p.checkpoints, ck_off + c0 + j, p.ckpt_dtype, f);
-                            }
+                            for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gnext);
+                            tmem_st16(tm_lane + kTmS + 64 * hh + c0, r);
                         }
+                    } else {
+#pragma unroll 1
+                        for (int c0 = 0; c0 < 64; c0 += 32) {
+                            uint32_t r[32];
+                            tmem_ld32_wait(tm_lane + kTmS + 64 * hh + c0, r);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gnext);
-                        tmem_st32(tm_lane + kTmS + 64 * hh + c0, r);
+                            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gnext);
+                            tmem_st32(tm_lane + kTmS + 64 * hh + c0, r);
+                        }
                     }
                     tmem_wait_st();
                 } else {
-                    // the unit's last chunk: its checkpoint (when due) and the final state, out of line
+                    // the unit's last chunk: its checkpoint (when due) and the final state, out of line, staged
+                    // through the output tile's buffer once this chunk's output (its TMA store or the tail rows)
+                    // has left it
+                    if (st == 0) bulk_wait_group_read0();
+                    ok = named_bar_and(kBarState, kStateThreads, ok);
                     finish_unit(tm_lane + kTmS + 64 * hh, p.checkpoints, ck_off, p.ckpt_dtype,
                                 own ? p.output_state2 : p.output_state, state_off,
-                                own ? p.state2.dtype : p.state.dtype);
+                                own ? p.state2.s_v : p.state.s_v, own ? p.state2.dtype : p.state.dtype);
                 }
             }
         }
