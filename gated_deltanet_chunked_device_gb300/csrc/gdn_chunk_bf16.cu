@@ -114,7 +114,7 @@ constexpr int kGG = 0, kGGam = 64, kGBeta = 128, kGRn = 192, kGRm = 256, kGCw = 
               kGRa = 512, kGColf = 576, kGBn = 640, kGSafe = 704, kGKeepQ = 705, kGFloats = 720;
 constexpr float kSafeRange = 80.f;  // e^{+-40} factors stay well inside fp32
 constexpr float kKeepQRange = 8.f;  // bf16 only: fp16 would overflow on e^8 (q.k) with raw q and k
-constexpr uint32_t kOutT = 207872;    // output tile bf16 [64 i][128 v]
+constexpr uint32_t kOutT = 207872;    // output tile: two halves [64 i][64 v] 16-bit, 128-byte swizzle
 constexpr uint32_t kSmemBytes = kOutT + 16384;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 static_assert(kGbuf >= kMisc + 64 && kXs + 4 * (2 * 16 * 24 + 32 * 40) <= kBars && kAbuf + 4 * 64 * kLd <= kXs,
@@ -748,14 +748,16 @@ __device__ __noinline__ void zero_tail_rows(uint8_t* kqs, uint8_t* vt, int it, i
     }
 }
 
-// The valid rows of a tail chunk's output tile, by coalesced 16-byte stores (a full chunk goes by TMA).
+// The valid rows of a tail chunk's output tile (two swizzled halves of 64 v, as the TMA store reads them), by
+// coalesced 16-byte stores (a full chunk goes by TMA).
 __device__ __noinline__ void store_output_tail(const uint8_t* tile, uint8_t* gout, int st, int Lc, int64_t tc,
                                               int H, int h) {
 #pragma unroll 1
     for (int k = 0; k < 4; ++k) {
-        const int id = st + 256 * k, row = id >> 4, col = id & 15;
+        const int id = st + 256 * k, row = id >> 4, col = id & 15;  // col: 16-byte column (8 v) of the row
         if (row < Lc) {
-            const uint4 val = *reinterpret_cast<const uint4*>(tile + row * 256 + col * 16);
+            const uint4 val =
+                *reinterpret_cast<const uint4*>(tile + (col >> 3) * 8192 + row * 128 + (((col & 7) ^ (row & 7)) << 4));
             *reinterpret_cast<uint4*>(gout + ((static_cast<size_t>(tc + row) * H + h) * kHead) * 2 + col * 16) = val;
         }
     }
@@ -1215,7 +1217,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int v = wq * 32 + lane;                  // TMEM lane = state row v
         const uint32_t tm_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         using E = Elem16<kF16>;
-        typename E::T* outT = reinterpret_cast<typename E::T*>(sm + kOutT);
         const int32_t ck_every = (p.checkpoints && p.ckpt_n > 0) ? p.ckpt_n / kChunk : 0;
         uint32_t n = 0, u = 0;
         bool ok = true;
@@ -1314,14 +1315,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
                 if (st == 0) mbar_arrive(cx.bars + B_DD_FULL + s);
-                // ---- output, part 1: this thread's 32 tokens i in [32 hh, 32 hh + 32) of O (row v) leave TMEM while
-                //      the S product runs behind the output product; the arithmetic waits until after pass 1, so
-                //      the next X | O product finds its O columns free as soon as the next bf16 S is ready.
-                uint32_t ro[32];
+                // ---- output, part 1: tokens i in [32 hh, 32 hh + 32) of O for this warp's 32 rows v leave TMEM, in
+                //      the accumulator-fragment layout of two 16-row blocks (ro0, ro1), while the S product runs
+                //      behind the output product; the arithmetic waits until after pass 1, so the next X | O
+                //      product finds its O columns free as soon as the next bf16 S is ready.
+                uint32_t ro0[16], ro1[16];
                 if (!kTransfer) {
                     ok = ok && wait_bar(cx, B_O_FULL, n & 1);
                     tc_fence_after();
-                    tmem_ld32_wait(tm_lane + kTmO + 32 * hh, ro);
+                    tmem_ld16x256_x4_pair_wait(tm_lane + kTmO + 32 * hh, tm_lane + (16u << 16) + kTmO + 32 * hh, ro0, ro1);
                 }
                 // ---- state epilogue, pass 1: S_n -> the bf16 operand of the next X | O product (this thread's 64
                 //      columns); the checkpoint and the final state are written later, off the state chain
@@ -1355,21 +1357,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p.l2norm) ok = ok && wait_bar(cx, B_RM_FULL + gs, (n / 3) & 1);
                     if (st == 0) bulk_wait_group_read0();
                     ok = named_bar_and(kBarState, kStateThreads, ok);
-                    const float sc = p.scale;
+                    // the tile is two halves of 64 v (8 KB, rows i of 128 bytes, 16-byte chunk c of row i at
+                    // c ^ (i % 8): the TMA 128-byte swizzle).  Each stmatrix writes four 8 x 8 blocks transposed:
+                    // block (token group k, row block vb) of fragment block b, rows i = 32 hh + 8 k + j of 8 v.
+                    const int fq = lane & 3, fm = lane >> 3, fj = lane & 7;
+                    float2 fac[4];  // scale rm_i for this thread's tokens 32 hh + 8 k + 2 fq (+ 1)
 #pragma unroll
-                    for (int i0 = 0; i0 < 32; i0 += 8) {
-                        const float4 ma = *reinterpret_cast<const float4*>(gb + kGRm + 32 * hh + i0);
-                        const float4 mb = *reinterpret_cast<const float4*>(gb + kGRm + 32 * hh + i0 + 4);
-                        const float rm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 rm = *reinterpret_cast<const float2*>(gb + kGRm + 32 * hh + 8 * k + 2 * fq);
+                        fac[k] = make_float2(p.scale * rm.x, p.scale * rm.y);
+                    }
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            outT[(32 * hh + i0 + j) * kHead + v] = E::from(sc * rm[j] * __uint_as_float(ro[i0 + j]));
+                    for (int b = 0; b < 2; ++b) {
+                        const uint32_t(&rb)[16] = b ? ro1 : ro0;
+#pragma unroll
+                        for (int kp = 0; kp < 2; ++kp) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int mm = 0; mm < 4; ++mm) {
+                                const int k = 2 * kp + (mm >> 1), vb = mm & 1;
+                                w[mm] = E::pack(fac[k].x * __uint_as_float(rb[4 * k + 2 * vb]),
+                                                fac[k].y * __uint_as_float(rb[4 * k + 2 * vb + 1]));
+                            }
+                            const int k = 2 * kp + (fm >> 1), i = 32 * hh + 8 * k + fj;
+                            const int v0 = 32 * wq + 16 * b + 8 * (fm & 1);
+                            stmatrix_x4_trans(smem_u32(sm + kOutT) + (v0 >> 6) * 8192 + i * 128 +
+                                                  ((((v0 & 63) >> 3) ^ fj) << 4),
+                                              w[0], w[1], w[2], w[3]);
+                        }
                     }
                     fence_proxy_async_smem();
                     if (!(ok = named_bar_and(kBarState, kStateThreads, ok))) break;
                     if (Lc == kChunk) {
                         if (st == 0) {
                             tma_store_3d(&tm_o, sm + kOutT, 0, info.h, static_cast<int32_t>(tc));
+                            tma_store_3d(&tm_o, sm + kOutT + 8192, 64, info.h, static_cast<int32_t>(tc));
                             bulk_commit_group();
                         }
                     } else {

@@ -109,15 +109,17 @@ bool encode_qkv_map(CUtensorMap* map, const void* base, int64_t T, int32_t heads
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The output [T, heads, 128] as a 3-D TMA map for stores: 64 x 1 x 64 boxes (half a chunk's v columns) and the
+// 128-byte swizzle, the layout the chunk kernel writes its output tile in.
 bool encode_out_map(CUtensorMap* map, void* base, int64_t T, int32_t heads, gdn_dtype t) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(gdn::kHead), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(T)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(gdn::kHead) * 2, static_cast<cuuint64_t>(heads) * gdn::kHead * 2};
-    cuuint32_t box[3] = {128, 1, 64};
+    cuuint32_t box[3] = {64, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(map, tma_type(t), 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
 

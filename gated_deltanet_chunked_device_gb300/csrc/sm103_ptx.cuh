@@ -244,6 +244,36 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
         : "memory");
 }
 
+// Two 16-lane blocks (taddr0, taddr1) x 256 bits, four repetitions each (32 columns), followed by the wait.
+// Thread t receives, for repetition k (columns col + 8k .. col + 8k + 7) of block b, r_b[4k] and r_b[4k + 1] =
+// columns 2 (t % 4) and 2 (t % 4) + 1 of lane lane_base + t / 4, r_b[4k + 2] and r_b[4k + 3] = the same columns
+// of lane lane_base + t / 4 + 8: the layout of an MMA accumulator fragment.
+__device__ __forceinline__ void tmem_ld16x256_x4_pair_wait(uint32_t taddr0, uint32_t taddr1, uint32_t (&a)[16],
+                                                           uint32_t (&b)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+          "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
+          "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]),
+          "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15])
+        : "r"(taddr0), "r"(taddr1)
+        : "memory");
+}
+
+// Four 8 x 8 matrices of 16-bit elements, each thread holding a pair (row t / 4, columns 2 (t % 4) and
+// 2 (t % 4) + 1) of every matrix (m0 .. m3), stored transposed: row j of stored matrix m (column j of the held
+// one) goes to the 16 bytes at the address that thread 8 m + j gives.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t m0, uint32_t m1, uint32_t m2,
+                                                  uint32_t m3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(m0),
+                 "r"(m1), "r"(m2), "r"(m3)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
