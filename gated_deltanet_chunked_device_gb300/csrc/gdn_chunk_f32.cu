@@ -4,9 +4,9 @@
 // fp32 inputs are held to a 1e-3 bar; tf32 tensor-core operands (10-bit
 // mantissa) would sit close to it, and 4-byte operand tiles of the fused
 // tensor-core kernel do not fit in shared memory.  This kernel keeps every
-// product in fp32.  One CTA owns (sequence, state head, 64-row slice of V):
+// product in fp32.  One CTA owns (sequence, state head, a slice of the V rows):
 // rows of the state are independent (S[v,:] only meets v_t[v] and Delta[:,v]),
-// so the two slices of a head run in parallel and each recomputes the
+// so the slices of a head run in parallel and each recomputes the
 // slice-independent parts (A, T, W, P).
 //
 // Per chunk ("GDN 与 Chunked Prefill": cumsum, triangular solve, recompute):
@@ -23,25 +23,30 @@
 namespace gdn {
 namespace {
 
-constexpr int kF32Threads = 256;
-constexpr int kVs = 64;          // rows of V (and of the state) per CTA
+constexpr int kF32Threads = 512;
 constexpr int kLdK = 129;        // padded row stride for 128-wide rows
-constexpr int kLdV = 65;         // padded row stride for 64-wide rows
+constexpr int kLdV = 65;         // padded row stride for rows of up to 64
 
-// shared memory layout (floats)
-constexpr int kOffK = 0;                       // K  [64][kLdK]
-constexpr int kOffQ = kOffK + 64 * kLdK;       // Q  [64][kLdK]
-constexpr int kOffW = kOffQ + 64 * kLdK;       // W  [64][kLdK]
-constexpr int kOffS = kOffW + 64 * kLdK;       // S slice [64 v][kLdK]
-constexpr int kOffV = kOffS + kVs * kLdK;      // V slice [64 j][kLdV]
-constexpr int kOffX = kOffV + 64 * kLdV;       // U, then Delta [64 j][kLdV]
-constexpr int kOffA = kOffX + 64 * kLdV;       // A, then P [64][kLdV]
-constexpr int kOffT = kOffA + 64 * kLdV;       // T = (I + A)^-1 [64][kLdV]
-constexpr int kOffG = kOffT + 64 * kLdV;       // G[64], gamma[64], beta[64], dec[64], beta gamma[64]
-constexpr int kF32SmemFloats = kOffG + 5 * 64;
-constexpr size_t kF32Smem = sizeof(float) * kF32SmemFloats;
+// shared memory layout (floats) for kVs rows of V (and of the state) per CTA
+template <int kVs>
+struct F32Layout {
+    static constexpr int kOffK = 0;                       // K  [64][kLdK]
+    static constexpr int kOffQ = kOffK + 64 * kLdK;       // Q  [64][kLdK]
+    static constexpr int kOffW = kOffQ + 64 * kLdK;       // W  [64][kLdK]
+    static constexpr int kOffS = kOffW + 64 * kLdK;       // S slice [kVs v][kLdK]
+    static constexpr int kOffV = kOffS + kVs * kLdK;      // V slice [64 j][kLdV]
+    static constexpr int kOffX = kOffV + 64 * kLdV;       // U, then Delta [64 j][kLdV]
+    static constexpr int kOffA = kOffX + 64 * kLdV;       // A, then P [64][kLdV]
+    static constexpr int kOffT = kOffA + 64 * kLdV;       // T = (I + A)^-1 [64][kLdV]
+    static constexpr int kOffG = kOffT + 64 * kLdV;       // G[64], gamma[64], beta[64], dec[64], beta gamma[64]
+    static constexpr size_t kBytes = sizeof(float) * (kOffG + 5 * 64);
+};
 
-__global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkParams p) {
+// kSlices CTAs per (sequence, state head), each owning kHead / kSlices rows of the state.
+template <int kSlices>
+__global__ void __launch_bounds__(kF32Threads, 1) gdn_chunk_f32_kernel(const ChunkParams p) {
+    constexpr int kVs = kHead / kSlices;
+    using Lay = F32Layout<kVs>;
     extern __shared__ float sf[];
     __shared__ int s_bad;
     const int tid = threadIdx.x;
@@ -50,8 +55,8 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
     if (s_bad) return;
 
     const int32_t H = p.H;
-    const int64_t unit = blockIdx.x / 2;
-    const int v0 = (blockIdx.x & 1) * kVs;
+    const int64_t unit = blockIdx.x / kSlices;
+    const int v0 = static_cast<int>(blockIdx.x % kSlices) * kVs;
     const int32_t seq = static_cast<int32_t>(unit / H);
     const int32_t h = static_cast<int32_t>(unit % H);
     const int qh = h / (H / p.hq), kh = h / (H / p.hk), vh = h / (H / p.hv);
@@ -64,15 +69,15 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
     const float* vg = static_cast<const float*>(p.v);
     float* og = static_cast<float*>(p.output);
 
-    float* Ks = sf + kOffK;
-    float* Qs = sf + kOffQ;
-    float* Ws = sf + kOffW;
-    float* Ss = sf + kOffS;
-    float* Vs = sf + kOffV;
-    float* Xs = sf + kOffX;
-    float* Am = sf + kOffA;
-    float* Ts = sf + kOffT;
-    float* sG = sf + kOffG;
+    float* Ks = sf + Lay::kOffK;
+    float* Qs = sf + Lay::kOffQ;
+    float* Ws = sf + Lay::kOffW;
+    float* Ss = sf + Lay::kOffS;
+    float* Vs = sf + Lay::kOffV;
+    float* Xs = sf + Lay::kOffX;
+    float* Am = sf + Lay::kOffA;
+    float* Ts = sf + Lay::kOffT;
+    float* sG = sf + Lay::kOffG;
     float* sGam = sG + 64;
     float* sBeta = sG + 128;
     float* sDec = sG + 192;   // e^{G_63 - G_j}
@@ -149,7 +154,8 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
             float a = 0.f;
             if (j < i) {
                 float dot = 0.f;
-                for (int d = 0; d < kHead; ++d) dot += Ks[i * kLdK + d] * Ks[j * kLdK + d];
+                #pragma unroll 4
+for (int d = 0; d < kHead; ++d) dot += Ks[i * kLdK + d] * Ks[j * kLdK + d];
                 a = sBeta[i] * expf(sG[i] - sG[j]) * dot;
             }
             Am[i * kLdV + j] = a;
@@ -177,13 +183,15 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
         for (int e = tid; e < kChunk * kHead; e += kF32Threads) {
             const int i = e / kHead, d = e % kHead;
             float acc = 0.f;
-            for (int j = 0; j <= i; ++j) acc += Ts[i * kLdV + j] * sWc[j] * Ks[j * kLdK + d];
+            #pragma unroll 4
+for (int j = 0; j <= i; ++j) acc += Ts[i * kLdV + j] * sWc[j] * Ks[j * kLdK + d];
             Ws[i * kLdK + d] = acc;
         }
         for (int e = tid; e < kChunk * kVs; e += kF32Threads) {
             const int i = e / kVs, d = e % kVs;
             float acc = 0.f;
-            for (int j = 0; j <= i; ++j) acc += Ts[i * kLdV + j] * sBeta[j] * Vs[j * kLdV + d];
+            #pragma unroll 4
+for (int j = 0; j <= i; ++j) acc += Ts[i * kLdV + j] * sBeta[j] * Vs[j * kLdV + d];
             Xs[i * kLdV + d] = acc;
         }
         __syncthreads();
@@ -203,7 +211,8 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
         for (int e = tid; e < kChunk * kVs; e += kF32Threads) {
             const int i = e / kVs, vv = e % kVs;
             float acc = 0.f;
-            for (int d = 0; d < kHead; ++d) acc += Ws[i * kLdK + d] * Ss[vv * kLdK + d];
+            #pragma unroll 4
+for (int d = 0; d < kHead; ++d) acc += Ws[i * kLdK + d] * Ss[vv * kLdK + d];
             Xs[i * kLdV + vv] -= acc;
         }
         __syncthreads();
@@ -213,7 +222,8 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
             float pv = 0.f;
             if (j <= i) {
                 float dot = 0.f;
-                for (int d = 0; d < kHead; ++d) dot += Qs[i * kLdK + d] * Ks[j * kLdK + d];
+                #pragma unroll 4
+for (int d = 0; d < kHead; ++d) dot += Qs[i * kLdK + d] * Ks[j * kLdK + d];
                 pv = expf(sG[i] - sG[j]) * dot;
             }
             Am[i * kLdV + j] = pv;
@@ -224,9 +234,11 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
             const int i = e / kVs, vv = e % kVs;
             if (i >= Lc) continue;
             float sq = 0.f;
-            for (int d = 0; d < kHead; ++d) sq += Ss[vv * kLdK + d] * Qs[i * kLdK + d];
+            #pragma unroll 4
+for (int d = 0; d < kHead; ++d) sq += Ss[vv * kLdK + d] * Qs[i * kLdK + d];
             float acc = sGam[i] * sq;
-            for (int j = 0; j <= i; ++j) acc += Am[i * kLdV + j] * Xs[j * kLdV + vv];
+            #pragma unroll 4
+for (int j = 0; j <= i; ++j) acc += Am[i * kLdV + j] * Xs[j * kLdV + vv];
             og[(static_cast<size_t>(tc + i) * H + h) * kHead + v0 + vv] = p.scale * acc;
         }
         __syncthreads();
@@ -236,7 +248,8 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
             for (int e = tid; e < kVs * kHead; e += kF32Threads) {
                 const int vv = e / kHead, d = e % kHead;
                 float acc = eg63 * Ss[vv * kLdK + d];
-                for (int j = 0; j < kChunk; ++j) acc += sDec[j] * Xs[j * kLdV + vv] * Ks[j * kLdK + d];
+                #pragma unroll 4
+for (int j = 0; j < kChunk; ++j) acc += sDec[j] * Xs[j * kLdV + vv] * Ks[j * kLdK + d];
                 Ss[vv * kLdK + d] = acc;
             }
         }
@@ -264,25 +277,38 @@ __global__ void __launch_bounds__(kF32Threads) gdn_chunk_f32_kernel(const ChunkP
     }
 }
 
-}  // namespace
-
-cudaError_t launch_chunk_f32(const ChunkParams& p, int grid, cudaStream_t stream) {
-    // One flag per device: the attribute is set once, and concurrent first calls from several host threads
-    // each set it at most once more (the same value).
+template <int kSlices>
+cudaError_t launch_slices(const ChunkParams& p, int64_t units, cudaStream_t stream) {
+    // One flag per device and instance: the attribute is set once, and concurrent first calls from several host
+    // threads each set it at most once more (the same value).
     constexpr int kMaxDevices = 64;
+    constexpr size_t kSmem = F32Layout<kHead / kSlices>::kBytes;
     static std::atomic<uint8_t> configured[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (!configured[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(gdn_chunk_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kF32Smem));
+        e = cudaFuncSetAttribute(gdn_chunk_f32_kernel<kSlices>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmem));
         if (e != cudaSuccess) return e;
         configured[dev].store(1, std::memory_order_release);
     }
-    gdn_chunk_f32_kernel<<<grid, kF32Threads, kF32Smem, stream>>>(p);
+    if (units * kSlices > 0x7fffffffLL) return cudaErrorInvalidValue;
+    gdn_chunk_f32_kernel<kSlices><<<static_cast<int>(units * kSlices), kF32Threads, kSmem, stream>>>(p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_f32(const ChunkParams& p, int64_t units, int slices, cudaStream_t stream) {
+    switch (slices) {
+        case 2: return launch_slices<2>(p, units, stream);
+        case 4: return launch_slices<4>(p, units, stream);
+        case 8: return launch_slices<8>(p, units, stream);
+        case 16: return launch_slices<16>(p, units, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace gdn

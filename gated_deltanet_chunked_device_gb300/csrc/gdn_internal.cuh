@@ -334,7 +334,9 @@ cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t stream);
 cudaError_t launch_chunk_16bit(const ChunkParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                const CUtensorMap& tm_v, const CUtensorMap& tm_o, bool f16, bool transfer, int grid,
                                cudaStream_t stream);
-cudaError_t launch_chunk_f32(const ChunkParams& p, int grid, cudaStream_t stream);
+// fp32 inputs: `slices` (2, 4, 8 or 16) CTAs per (sequence, state head) unit, each owning kHead / slices rows of
+// the state (the rows are independent; every slice recomputes the slice-independent parts).
+cudaError_t launch_chunk_f32(const ChunkParams& p, int64_t units, int slices, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, gdn_dtype dtype, cudaStream_t stream);
 cudaError_t launch_cp_prepare(const CpParams& p, cudaStream_t stream);
 cudaError_t launch_cp_fixup(const CpParams& p, cudaStream_t stream);

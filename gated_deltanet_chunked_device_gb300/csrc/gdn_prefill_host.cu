@@ -421,10 +421,14 @@ gdn_status run_stages(gdn_prefill_plan_t plan, const gdn_prefill_args* args, voi
     cp.has_tokens = T > 0 ? 1 : 0;
 
     if (d.qkv_dtype == GDN_DTYPE_F32) {
-        // fp32 inputs: CUDA-core kernel, one CTA per (sequence, state head, half of the V rows)
-        const int64_t blocks = static_cast<int64_t>(N) * plan->H * 2;
-        if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
-        if (gdn::launch_chunk_f32(cp, static_cast<int>(blocks), stream) != cudaSuccess) return GDN_ERR_CUDA;
+        // fp32 inputs: CUDA-core kernel, one CTA per (sequence, state head, slice of the V rows): the most slices
+        // (up to 16) that keep the grid within about four CTAs per SM, since every slice repeats the
+        // slice-independent work
+        const int64_t units = static_cast<int64_t>(N) * plan->H;
+        if (units * 2 > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+        int slices = 16;
+        while (slices > 2 && units * slices > 4LL * std::max(sm_count(), 1)) slices /= 2;
+        if (gdn::launch_chunk_f32(cp, units, slices, stream) != cudaSuccess) return GDN_ERR_CUDA;
         return GDN_OK;
     }
     CUtensorMap tq, tk, tv, to;

@@ -219,6 +219,20 @@ def test_fp32_inputs_tails_heads_pool_checkpoints(l2):
     check_against_oracle(inp, run_gpu(to_device(inp)))
 
 
+@pytest.mark.parametrize("per_sm", [0.25, 0.5, 1.0, 1.2])
+def test_fp32_inputs_every_slice_count(per_sm):
+    # the fp32 kernel cuts each (sequence, head) unit into 16, 8, 4 or 2 slices of the state rows, the most that
+    # keep the grid within about four CTAs per SM: a quarter, a half, one and 1.2 times the SM count in units take
+    # each instance once (rows of every slice, tails, checkpoints and the final state against the oracle)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = max(1, int(sms * per_sm) // 4)
+    lens = [70 + (13 * i) % 60 for i in range(n)]
+    w = wl.custom(seq_lens=lens, hq=2, hk=2, hv=4, dtype=torch.float32, l2norm_in_kernel=True, qk_prenorm=False,
+                  initial_state="dense", checkpoint_every=64)
+    inp = wl.generate(w, seed=70)
+    check_against_oracle(inp, run_gpu(to_device(inp)))
+
+
 def test_steep_gates_take_the_pairwise_decay_path():
     # alpha ~ U(0.05, 0.3): log alpha ~ -1.2 .. -3 per token, so a chunk's gate range is far above the
     # limit of the row x column factorisation and every A / P entry takes e^{G_i - G_j} pairwise
