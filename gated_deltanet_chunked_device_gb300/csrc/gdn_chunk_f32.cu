@@ -24,7 +24,9 @@ namespace gdn {
 namespace {
 
 constexpr int kF32Threads = 512;
-constexpr int kLdK = 129;        // padded row stride for 128-wide rows
+static_assert(kF32Threads == 2 * 64 * 4, "the q/k norms take four threads for each of the 2 x 64 rows");
+constexpr int kLdK = 132;        // padded row stride for 128-wide rows: 16-byte aligned, and eight rows of a
+                                 // 16-byte column fall in eight different bank groups
 constexpr int kLdV = 65;         // padded row stride for rows of up to 64
 
 // shared memory layout (floats) for kVs rows of V (and of the state) per CTA
@@ -41,6 +43,23 @@ struct F32Layout {
     static constexpr int kOffG = kOffT + 64 * kLdV;       // G[64], gamma[64], beta[64], dec[64], beta gamma[64]
     static constexpr size_t kBytes = sizeof(float) * (kOffG + 5 * 64);
 };
+
+// dot[a] = X[i0 + a] . Y[j] over the kHead elements of rows of stride kLdK (zero when `live` is false): the four
+// X rows are the same for the whole warp (broadcast loads), the Y row is the lane's own, 16 bytes per load.
+__device__ __forceinline__ void row4_dots(const float* X, int i0, const float* Y, int j, bool live, float (&dot)[4]) {
+#pragma unroll
+    for (int a = 0; a < 4; ++a) dot[a] = 0.f;
+    if (!live) return;
+#pragma unroll 2
+    for (int d = 0; d < kHead; d += 4) {
+        const float4 y = *reinterpret_cast<const float4*>(Y + j * kLdK + d);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const float4 x = *reinterpret_cast<const float4*>(X + (i0 + a) * kLdK + d);
+            dot[a] += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+        }
+    }
+}
 
 // kSlices CTAs per (sequence, state head), each owning kHead / kSlices rows of the state.
 template <int kSlices>
@@ -98,23 +117,42 @@ __global__ void __launch_bounds__(kF32Threads, 1) gdn_chunk_f32_kernel(const Chu
         const int64_t tc = t0 + c * kChunk;
         const int Lc = static_cast<int>(L - c * kChunk < kChunk ? L - c * kChunk : kChunk);
         // ---- load the chunk (padded rows: zeros), L2-normalise q and k rows when asked
-        for (int e = tid; e < kChunk * kHead; e += kF32Threads) {
-            const int r = e / kHead, d = e % kHead;
-            const bool ok = r < Lc;
-            Ks[r * kLdK + d] = ok ? kg[(static_cast<size_t>(tc + r) * p.hk + kh) * kHead + d] : 0.f;
-            Qs[r * kLdK + d] = ok ? qg[(static_cast<size_t>(tc + r) * p.hq + qh) * kHead + d] : 0.f;
+        {   // 16 bytes per load, every load of the thread issued before its stores
+            constexpr int kPer = kChunk * kHead / 4 / kF32Threads;
+            float4 kv[kPer], qv[kPer];
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int e = 4 * (tid + u * kF32Threads), r = e / kHead, d = e % kHead;
+                const bool ok = r < Lc;
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                kv[u] = ok ? *reinterpret_cast<const float4*>(kg + (static_cast<size_t>(tc + r) * p.hk + kh) * kHead + d) : z;
+                qv[u] = ok ? *reinterpret_cast<const float4*>(qg + (static_cast<size_t>(tc + r) * p.hq + qh) * kHead + d) : z;
+            }
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int e = 4 * (tid + u * kF32Threads), r = e / kHead, d = e % kHead;
+                *reinterpret_cast<float4*>(Ks + r * kLdK + d) = kv[u];
+                *reinterpret_cast<float4*>(Qs + r * kLdK + d) = qv[u];
+            }
         }
         for (int e = tid; e < kChunk * kVs; e += kF32Threads) {
             const int r = e / kVs, d = e % kVs;
             Vs[r * kLdV + d] = r < Lc ? vg[(static_cast<size_t>(tc + r) * p.hv + vh) * kHead + v0 + d] : 0.f;
         }
         __syncthreads();
-        if (p.l2norm && tid < 2 * kChunk) {
-            float* row = (tid < kChunk ? Ks : Qs) + (tid & 63) * kLdK;
+        if (p.l2norm) {
+            // four threads per row (elements d = part, part + 4, ...: the rows' 4-float stride offset keeps the
+            // 32 lanes of a load in 32 banks), combined by shuffles
+            const int row = tid >> 2, part = tid & 3;
+            float* r = (row < kChunk ? Ks : Qs) + (row & 63) * kLdK + part;
             float ss = 0.f;
-            for (int d = 0; d < kHead; ++d) ss += row[d] * row[d];
+#pragma unroll 8
+            for (int d = 0; d < kHead; d += 4) ss += r[d] * r[d];
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
             const float inv = 1.0f / sqrtf(ss + 1e-6f);
-            for (int d = 0; d < kHead; ++d) row[d] *= inv;
+#pragma unroll 8
+            for (int d = 0; d < kHead; d += 4) r[d] *= inv;
         }
         // ---- gates (warp 0: two rows per lane, shuffle scan of log alpha)
         if (tid < 32) {
@@ -148,17 +186,16 @@ __global__ void __launch_bounds__(kF32Threads, 1) gdn_chunk_f32_kernel(const Chu
             sWc[r1] = b1 * sGam[r1];
         }
         __syncthreads();
-        // ---- A (strictly lower)
-        for (int e = tid; e < kChunk * kChunk; e += kF32Threads) {
-            const int i = e / kChunk, j = e % kChunk;
-            float a = 0.f;
-            if (j < i) {
-                float dot = 0.f;
-                #pragma unroll 4
-for (int d = 0; d < kHead; ++d) dot += Ks[i * kLdK + d] * Ks[j * kLdK + d];
-                a = sBeta[i] * expf(sG[i] - sG[j]) * dot;
+        // ---- A (strictly lower): rows i0 .. i0 + 3 against row j per thread, four k elements per load
+        for (int e = tid; e < kChunk * kChunk / 4; e += kF32Threads) {
+            const int i0 = 4 * (e / kChunk), j = e % kChunk;
+            float dot[4];
+            row4_dots(Ks, i0, Ks, j, j < i0 + 3, dot);
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int i = i0 + a;
+                Am[i * kLdV + j] = j < i ? sBeta[i] * expf(sG[i] - sG[j]) * dot[a] : 0.f;
             }
-            Am[i * kLdV + j] = a;
         }
         __syncthreads();
         // ---- T = (I + A)^-1 by forward substitution, column j on thread j, into its own buffer (two
@@ -179,19 +216,26 @@ for (int d = 0; d < kHead; ++d) dot += Ks[i * kLdK + d] * Ks[j * kLdK + d];
             }
         }
         __syncthreads();
-        // ---- W = T diag(beta gamma) K,  U = T diag(beta) V_slice
-        for (int e = tid; e < kChunk * kHead; e += kF32Threads) {
-            const int i = e / kHead, d = e % kHead;
-            float acc = 0.f;
-            #pragma unroll 4
-for (int j = 0; j <= i; ++j) acc += Ts[i * kLdV + j] * sWc[j] * Ks[j * kLdK + d];
-            Ws[i * kLdK + d] = acc;
+        // ---- W = T diag(beta gamma) K (four k elements per thread),  U = T diag(beta) V_slice
+        for (int e = tid; e < kChunk * kHead / 4; e += kF32Threads) {
+            const int i = e / (kHead / 4), d = 4 * (e % (kHead / 4));
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int j = 0; j <= i; ++j) {
+                const float t = Ts[i * kLdV + j] * sWc[j];
+                const float4 kj = *reinterpret_cast<const float4*>(Ks + j * kLdK + d);
+                acc.x += t * kj.x;
+                acc.y += t * kj.y;
+                acc.z += t * kj.z;
+                acc.w += t * kj.w;
+            }
+            *reinterpret_cast<float4*>(Ws + i * kLdK + d) = acc;
         }
         for (int e = tid; e < kChunk * kVs; e += kF32Threads) {
             const int i = e / kVs, d = e % kVs;
             float acc = 0.f;
-            #pragma unroll 4
-for (int j = 0; j <= i; ++j) acc += Ts[i * kLdV + j] * sBeta[j] * Vs[j * kLdV + d];
+#pragma unroll 4
+            for (int j = 0; j <= i; ++j) acc += Ts[i * kLdV + j] * sBeta[j] * Vs[j * kLdV + d];
             Xs[i * kLdV + d] = acc;
         }
         __syncthreads();
@@ -211,22 +255,21 @@ for (int j = 0; j <= i; ++j) acc += Ts[i * kLdV + j] * sBeta[j] * Vs[j * kLdV + 
         for (int e = tid; e < kChunk * kVs; e += kF32Threads) {
             const int i = e / kVs, vv = e % kVs;
             float acc = 0.f;
-            #pragma unroll 4
-for (int d = 0; d < kHead; ++d) acc += Ws[i * kLdK + d] * Ss[vv * kLdK + d];
+#pragma unroll 4
+            for (int d = 0; d < kHead; ++d) acc += Ws[i * kLdK + d] * Ss[vv * kLdK + d];
             Xs[i * kLdV + vv] -= acc;
         }
         __syncthreads();
-        // ---- P_ij = e^{G_i - G_j} (q_i . k_j) for j <= i, over A
-        for (int e = tid; e < kChunk * kChunk; e += kF32Threads) {
-            const int i = e / kChunk, j = e % kChunk;
-            float pv = 0.f;
-            if (j <= i) {
-                float dot = 0.f;
-                #pragma unroll 4
-for (int d = 0; d < kHead; ++d) dot += Qs[i * kLdK + d] * Ks[j * kLdK + d];
-                pv = expf(sG[i] - sG[j]) * dot;
+        // ---- P_ij = e^{G_i - G_j} (q_i . k_j) for j <= i, over A: rows i0 .. i0 + 3 per thread
+        for (int e = tid; e < kChunk * kChunk / 4; e += kF32Threads) {
+            const int i0 = 4 * (e / kChunk), j = e % kChunk;
+            float dot[4];
+            row4_dots(Qs, i0, Ks, j, j <= i0 + 3, dot);
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int i = i0 + a;
+                Am[i * kLdV + j] = j <= i ? expf(sG[i] - sG[j]) * dot[a] : 0.f;
             }
-            Am[i * kLdV + j] = pv;
         }
         __syncthreads();
         // ---- output rows of the slice
@@ -234,11 +277,11 @@ for (int d = 0; d < kHead; ++d) dot += Qs[i * kLdK + d] * Ks[j * kLdK + d];
             const int i = e / kVs, vv = e % kVs;
             if (i >= Lc) continue;
             float sq = 0.f;
-            #pragma unroll 4
-for (int d = 0; d < kHead; ++d) sq += Ss[vv * kLdK + d] * Qs[i * kLdK + d];
+#pragma unroll 4
+            for (int d = 0; d < kHead; ++d) sq += Ss[vv * kLdK + d] * Qs[i * kLdK + d];
             float acc = sGam[i] * sq;
-            #pragma unroll 4
-for (int j = 0; j <= i; ++j) acc += Am[i * kLdV + j] * Xs[j * kLdV + vv];
+#pragma unroll 4
+            for (int j = 0; j <= i; ++j) acc += Am[i * kLdV + j] * Xs[j * kLdV + vv];
             og[(static_cast<size_t>(tc + i) * H + h) * kHead + v0 + vv] = p.scale * acc;
         }
         __syncthreads();
@@ -248,8 +291,8 @@ for (int j = 0; j <= i; ++j) acc += Am[i * kLdV + j] * Xs[j * kLdV + vv];
             for (int e = tid; e < kVs * kHead; e += kF32Threads) {
                 const int vv = e / kHead, d = e % kHead;
                 float acc = eg63 * Ss[vv * kLdK + d];
-                #pragma unroll 4
-for (int j = 0; j < kChunk; ++j) acc += sDec[j] * Xs[j * kLdV + vv] * Ks[j * kLdK + d];
+#pragma unroll 4
+                for (int j = 0; j < kChunk; ++j) acc += sDec[j] * Xs[j * kLdV + vv] * Ks[j * kLdK + d];
                 Ss[vv * kLdK + d] = acc;
             }
         }
