@@ -198,22 +198,25 @@ __global__ void __launch_bounds__(kF32Threads, 1) gdn_chunk_f32_kernel(const Chu
             }
         }
         __syncthreads();
-        // ---- T = (I + A)^-1 by forward substitution, column j on thread j, into its own buffer (two
-        //      accumulators per row; the column lives in shared memory, not in a run-time indexed array)
+        // ---- T = (I + A)^-1 by forward substitution, column j on thread j, held in registers (the loops are
+        //      unrolled, so the row's A entries, the same for every thread, load ahead of the running sums; the
+        //      terms above the diagonal are exact zeros)
         if (tid < kChunk) {
             const int j = tid;
+            float t[kChunk];
+#pragma unroll
             for (int i = 0; i < kChunk; ++i) {
                 float a0 = (i == j) ? 1.f : 0.f, a1 = 0.f;
-                if (i > j) {
-                    int m = j;
-                    for (; m + 1 < i; m += 2) {
-                        a0 -= Am[i * kLdV + m] * Ts[m * kLdV + j];
-                        a1 -= Am[i * kLdV + m + 1] * Ts[(m + 1) * kLdV + j];
-                    }
-                    if (m < i) a0 -= Am[i * kLdV + m] * Ts[m * kLdV + j];
+#pragma unroll
+                for (int m = 0; m + 1 < i; m += 2) {
+                    a0 -= Am[i * kLdV + m] * t[m];
+                    a1 -= Am[i * kLdV + m + 1] * t[m + 1];
                 }
-                Ts[i * kLdV + j] = (i < j) ? 0.f : a0 + a1;
+                if (i & 1) a0 -= Am[i * kLdV + i - 1] * t[i - 1];
+                t[i] = (i < j) ? 0.f : a0 + a1;
             }
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) Ts[i * kLdV + j] = t[i];
         }
         __syncthreads();
         // ---- W = T diag(beta gamma) K (four k elements per thread),  U = T diag(beta) V_slice
