@@ -44,6 +44,19 @@ struct F32Layout {
     static constexpr size_t kBytes = sizeof(float) * (kOffG + 5 * 64);
 };
 
+// x . y over the kHead elements of two rows (16-byte aligned), four elements per load.
+__device__ __forceinline__ float dot_rows(const float* x, const float* y) {
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+    for (int d = 0; d < kHead; d += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(x + d);
+        const float4 b = *reinterpret_cast<const float4*>(y + d);
+        s0 += a.x * b.x + a.y * b.y;
+        s1 += a.z * b.z + a.w * b.w;
+    }
+    return s0 + s1;
+}
+
 // dot[a] = X[i0 + a] . Y[j] over the kHead elements of rows of stride kLdK (zero when `live` is false): the four
 // X rows are the same for the whole warp (broadcast loads), the Y row is the lane's own, 16 bytes per load.
 __device__ __forceinline__ void row4_dots(const float* X, int i0, const float* Y, int j, bool live, float (&dot)[4]) {
@@ -219,20 +232,28 @@ __global__ void __launch_bounds__(kF32Threads, 1) gdn_chunk_f32_kernel(const Chu
             for (int i = 0; i < kChunk; ++i) Ts[i * kLdV + j] = t[i];
         }
         __syncthreads();
-        // ---- W = T diag(beta gamma) K (four k elements per thread),  U = T diag(beta) V_slice
-        for (int e = tid; e < kChunk * kHead / 4; e += kF32Threads) {
-            const int i = e / (kHead / 4), d = 4 * (e % (kHead / 4));
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int j = 0; j <= i; ++j) {
-                const float t = Ts[i * kLdV + j] * sWc[j];
+        // ---- W = T diag(beta gamma) K: rows i0 .. i0 + 3 and four k elements per thread (T is zero above its
+        //      diagonal, so every row of the group runs to i0 + 3),  U = T diag(beta) V_slice
+        for (int e = tid; e < kChunk * kHead / 16; e += kF32Threads) {
+            const int i0 = 4 * (e / (kHead / 4)), d = 4 * (e % (kHead / 4));
+            float4 acc[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) acc[a] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+            for (int j = 0; j <= i0 + 3; ++j) {
+                const float wc = sWc[j];
                 const float4 kj = *reinterpret_cast<const float4*>(Ks + j * kLdK + d);
-                acc.x += t * kj.x;
-                acc.y += t * kj.y;
-                acc.z += t * kj.z;
-                acc.w += t * kj.w;
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const float t = Ts[(i0 + a) * kLdV + j] * wc;
+                    acc[a].x += t * kj.x;
+                    acc[a].y += t * kj.y;
+                    acc[a].z += t * kj.z;
+                    acc[a].w += t * kj.w;
+                }
             }
-            *reinterpret_cast<float4*>(Ws + i * kLdK + d) = acc;
+#pragma unroll
+            for (int a = 0; a < 4; ++a) *reinterpret_cast<float4*>(Ws + (i0 + a) * kLdK + d) = acc[a];
         }
         for (int e = tid; e < kChunk * kVs; e += kF32Threads) {
             const int i = e / kVs, d = e % kVs;
@@ -254,13 +275,10 @@ __global__ void __launch_bounds__(kF32Threads, 1) gdn_chunk_f32_kernel(const Chu
         }
         if (p.intra_g && v0 == 0 && tid < kChunk)
             p.intra_g[(static_cast<size_t>(p.chunk_offsets[seq] + c) * H + h) * kChunk + tid] = sG[tid];
-        // ---- Delta = U - W S^T (slice columns), in place over U
+        // ---- Delta = U - W S^T (slice columns), in place over U; four k elements per load
         for (int e = tid; e < kChunk * kVs; e += kF32Threads) {
             const int i = e / kVs, vv = e % kVs;
-            float acc = 0.f;
-#pragma unroll 4
-            for (int d = 0; d < kHead; ++d) acc += Ws[i * kLdK + d] * Ss[vv * kLdK + d];
-            Xs[i * kLdV + vv] -= acc;
+            Xs[i * kLdV + vv] -= dot_rows(Ws + i * kLdK, Ss + vv * kLdK);
         }
         __syncthreads();
         // ---- P_ij = e^{G_i - G_j} (q_i . k_j) for j <= i, over A: rows i0 .. i0 + 3 per thread
@@ -279,24 +297,29 @@ __global__ void __launch_bounds__(kF32Threads, 1) gdn_chunk_f32_kernel(const Chu
         for (int e = tid; e < kChunk * kVs; e += kF32Threads) {
             const int i = e / kVs, vv = e % kVs;
             if (i >= Lc) continue;
-            float sq = 0.f;
-#pragma unroll 4
-            for (int d = 0; d < kHead; ++d) sq += Ss[vv * kLdK + d] * Qs[i * kLdK + d];
-            float acc = sGam[i] * sq;
+            float acc = sGam[i] * dot_rows(Ss + vv * kLdK, Qs + i * kLdK);
 #pragma unroll 4
             for (int j = 0; j <= i; ++j) acc += Am[i * kLdV + j] * Xs[j * kLdV + vv];
             og[(static_cast<size_t>(tc + i) * H + h) * kHead + v0 + vv] = p.scale * acc;
         }
         __syncthreads();
-        // ---- state: S <- gamma_63 S + sum_j e^{G_63 - G_j} Delta_j k_j^T
+        // ---- state: S <- gamma_63 S + sum_j e^{G_63 - G_j} Delta_j k_j^T, four k elements per thread
         {
             const float eg63 = sGam[kChunk - 1];
-            for (int e = tid; e < kVs * kHead; e += kF32Threads) {
-                const int vv = e / kHead, d = e % kHead;
-                float acc = eg63 * Ss[vv * kLdK + d];
+            for (int e = tid; e < kVs * kHead / 4; e += kF32Threads) {
+                const int vv = e / (kHead / 4), d = 4 * (e % (kHead / 4));
+                float4 acc = *reinterpret_cast<const float4*>(Ss + vv * kLdK + d);
+                acc = make_float4(eg63 * acc.x, eg63 * acc.y, eg63 * acc.z, eg63 * acc.w);
 #pragma unroll 4
-                for (int j = 0; j < kChunk; ++j) acc += sDec[j] * Xs[j * kLdV + vv] * Ks[j * kLdK + d];
-                Ss[vv * kLdK + d] = acc;
+                for (int j = 0; j < kChunk; ++j) {
+                    const float x = sDec[j] * Xs[j * kLdV + vv];
+                    const float4 kj = *reinterpret_cast<const float4*>(Ks + j * kLdK + d);
+                    acc.x += x * kj.x;
+                    acc.y += x * kj.y;
+                    acc.z += x * kj.z;
+                    acc.w += x * kj.w;
+                }
+                *reinterpret_cast<float4*>(Ss + vv * kLdK + d) = acc;
             }
         }
         __syncthreads();
