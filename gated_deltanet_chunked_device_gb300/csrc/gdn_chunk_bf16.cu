@@ -785,7 +785,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kMisc);
 
     // Bad input flagged by the prepare kernel: every thread sees one copy of the word.  A run whose
-    // device-side sequence count is zero (a transfer pass with no segments) has nothing to do either.
+    // device-side sequence count is zero (a transfer pass with no segments) has nothing to do either.  With a
+    // programmatic launch the CTAs are resident while the prepare step finishes; griddep_wait orders every
+    // read after it.
+    griddep_wait();
     if (tid == 0)
         *cx.abort = *reinterpret_cast<volatile int32_t*>(p.status) != 0 || (p.num_seqs_dev && *p.num_seqs_dev <= 0);
     __syncthreads();
@@ -1493,8 +1496,18 @@ cudaError_t launch_chunk_16bit(const ChunkParams& p, const CUtensorMap& tm_q, co
         if (e != cudaSuccess) return e;
         configured[dev][ki].store(1, std::memory_order_release);
     }
-    kernel<<<grid, kThreads, kSmemAlloc, stream>>>(p, tm_q, tm_k, tm_v, tm_o);
-    return cudaGetLastError();
+    // a programmatic launch: the CTAs start while the previous kernel on the stream finishes (see griddep_wait)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p, tm_q, tm_k, tm_v, tm_o);
 }
 
 }  // namespace gdn

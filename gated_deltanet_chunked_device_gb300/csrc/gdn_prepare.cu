@@ -13,6 +13,7 @@
 //  * orders sequences longest first (LPT) for the persistent chunk kernel;
 //  * resets the chunk kernel's work counter.
 #include "gdn_internal.cuh"
+#include "sm103_ptx.cuh"
 
 namespace gdn {
 namespace {
@@ -55,6 +56,8 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prepare_kernel(PrepareParams
     __shared__ int32_t s_err;
     const int tid = threadIdx.x;
     const int32_t N = p.num_seqs;
+    // the chunk kernel may start its set-up now; it reads what this kernel writes only after it completes
+    griddep_launch_dependents();
 
     if (tid == 0) {
         s_err = 0;

@@ -286,6 +286,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the previous kernel on the stream ends;
+// griddep_wait returns once that kernel has completed and its memory is visible
+// (at once when there is no such kernel).  griddep_launch_dependents lets the
+// next kernel start.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // Named barrier over `nthreads` threads (a multiple of 32); id 0 is __syncthreads.
 // Per-warpgroup register budgets (every warp of a warpgroup executes the same one).
 template <uint32_t N>
