@@ -56,6 +56,11 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prepare_kernel(PrepareParams
     __shared__ int32_t s_err;
     const int tid = threadIdx.x;
     const int32_t N = p.num_seqs;
+    // up to kSortMax sequences, the chunk offsets also live in shared memory, after the sort keys
+    const bool on_chip = N <= kSortMax;
+    int32_t n2 = 1;
+    while (n2 < N) n2 <<= 1;
+    int32_t* s_off = reinterpret_cast<int32_t*>(sort_keys + (on_chip ? n2 : 0));
     // the chunk kernel may start its set-up now; it reads what this kernel writes only after it completes
     griddep_launch_dependents();
 
@@ -105,12 +110,16 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prepare_kernel(PrepareParams
             }
         }
         const int32_t ex = block_excl_scan(nc, warp_sums, &tile_total);
-        if (i < N) p.chunk_offsets[i] = carry + ex;
+        if (i < N) {
+            p.chunk_offsets[i] = carry + ex;
+            if (on_chip) s_off[i] = carry + ex;
+        }
         carry += tile_total;  // every thread reads the same total
         __syncthreads();
     }
     if (tid == 0) {
         p.chunk_offsets[N] = carry;
+        if (on_chip) s_off[N] = carry;
         *p.n_chunks = carry;
     }
     if (err) atomicOr(&s_err, err);
@@ -118,6 +127,7 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prepare_kernel(PrepareParams
     if (tid == 0 && s_err) atomicOr(p.status, s_err);
 
     // ---- flat chunk map: chunk f belongs to the last sequence whose offset is <= f
+    const int32_t* offs = on_chip ? s_off : p.chunk_offsets;
     const int32_t total = carry < p.max_chunks ? carry : static_cast<int32_t>(p.max_chunks);
     for (int64_t f = tid; f < p.max_chunks; f += kPrepThreads) {
         int32_t seq = -1, c = -1;
@@ -125,24 +135,22 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prepare_kernel(PrepareParams
             int32_t lo = 0, hi = N;  // invariant: offsets[lo] <= f < offsets[hi]
             while (hi - lo > 1) {
                 const int32_t mid = (lo + hi) >> 1;
-                if (p.chunk_offsets[mid] <= f) lo = mid;
+                if (offs[mid] <= f) lo = mid;
                 else hi = mid;
             }
             seq = lo;
-            c = static_cast<int32_t>(f) - p.chunk_offsets[lo];
+            c = static_cast<int32_t>(f) - offs[lo];
         }
         p.chunk_map[2 * f] = seq;
         p.chunk_map[2 * f + 1] = c;
     }
 
     // ---- longest-first order of sequences (bitonic sort of (chunks desc, index asc))
-    if (N <= kSortMax) {
-        int32_t n2 = 1;
-        while (n2 < N) n2 <<= 1;
+    if (on_chip) {
         for (int32_t i = tid; i < n2; i += kPrepThreads) {
             uint64_t key = ~0ull;
             if (i < N) {
-                const uint32_t nc = static_cast<uint32_t>(p.chunk_offsets[i + 1] - p.chunk_offsets[i]);
+                const uint32_t nc = static_cast<uint32_t>(s_off[i + 1] - s_off[i]);
                 key = (static_cast<uint64_t>(0x7fffffffu - nc) << 32) | static_cast<uint32_t>(i);
             }
             sort_keys[i] = key;
@@ -176,7 +184,9 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prepare_kernel(PrepareParams
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t stream) {
     int32_t n2 = 1;
     while (n2 < p.num_seqs && n2 < kSortMax) n2 <<= 1;
-    const size_t smem = (p.num_seqs <= kSortMax) ? static_cast<size_t>(n2) * sizeof(uint64_t) : 16;
+    const size_t smem = (p.num_seqs <= kSortMax)
+                            ? static_cast<size_t>(n2) * sizeof(uint64_t) + static_cast<size_t>(p.num_seqs + 1) * sizeof(int32_t)
+                            : 16;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(gdn_prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
