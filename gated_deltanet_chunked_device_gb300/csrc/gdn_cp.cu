@@ -28,15 +28,21 @@
 #include <atomic>
 
 #include "gdn_internal.cuh"
+#include "sm103_ptx.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kCpThreads = 256;
+constexpr int kCpWarps = kCpThreads / 32;
 constexpr int kCand = kCpMaxSegments - 1;  // candidates P = 2 .. kCpMaxSegments
-constexpr int kFixRows = 32;                // rows of S per fixup CTA
-constexpr int kFixSplit = kHead / kFixRows; // fixup CTAs per (sequence, head)
+constexpr int kSlots = 8;                   // candidate slots per group of eight threads (the last: one pass)
+static_assert(kCand < kSlots && kCpThreads % kSlots == 0, "one candidate per thread of a group of eight");
+constexpr int kFixRows = 32;                // rows of S per fixup or final CTA
+constexpr int kFixSplit = kHead / kFixRows; // fixup or final CTAs per (sequence, head)
 constexpr int kLdS = kHead + 1;             // padded rows of the running state in shared memory
+constexpr int kPlaneVec = kHead * kHead / (4 * kCpThreads);   // float4 per thread of a 128 x 128 plane
+constexpr int kRowsVec = kFixRows * kHead / (4 * kCpThreads); // float4 per thread of a CTA's 32 rows
 
 __device__ __forceinline__ int64_t seq_chunks(const CpParams& p, int32_t i, int64_t& t0, int64_t& L) {
     t0 = load_index(p.cu_seqlens, p.cu_i64, i);
@@ -77,78 +83,107 @@ __device__ __forceinline__ int64_t real_row(const CpParams& p, int32_t i) {
     return p.state_indices ? load_index(p.state_indices, p.idx_i64, i) : i;
 }
 
+__device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
 // The segmentation, the transfer pass's segments and order, the fixup's list
-// of segmented sequences and the segment pass's batch.  One CTA.
+// of segmented sequences and the segment pass's batch.  One CTA.  The load
+// model's candidates are evaluated side by side: thread t scores candidate
+// P = 2 + t % 8 on every 32nd sequence, and eight threads cost the candidates
+// and one pass, so that no thread runs the 64-bit divisions of all of them.
 __global__ void __launch_bounds__(kCpThreads) cp_prepare_kernel(const CpParams p) {
-    __shared__ unsigned long long s_sum[kCand][2];  // nA, nS
-    __shared__ long long s_max[kCand][2];           // longest whole sequence, largest P
-    __shared__ long long s_cmax;
-    __shared__ unsigned long long s_sumc;
-    __shared__ long long s_tau;
-    __shared__ int32_t warp_sums[kCpThreads / 32];
+    __shared__ int64_t s_red[kCpWarps][2];             // per warp: longest sequence, total chunks
+    __shared__ int64_t s_cand[kCpWarps][kSlots][4];    // per warp and slot: nA, nS, longest whole, largest P
+    __shared__ int64_t s_cost[kSlots], s_tauc[kSlots]; // per candidate (slot 7: one pass)
+    __shared__ int64_t s_tau;
+    __shared__ int32_t warp_sums[kCpWarps];
     __shared__ int32_t tile_total;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t N = p.num_seqs;
-    if (tid < kCand) {
-        s_sum[tid][0] = s_sum[tid][1] = 0;
-        s_max[tid][0] = s_max[tid][1] = 0;
-    }
-    if (tid == 0) {
-        s_cmax = 0;
-        s_sumc = 0;
-    }
-    __syncthreads();
+    // the batch's ends, which the tail of the segment pass's batch repeats
+    const int32_t end = static_cast<int32_t>(load_index(p.cu_seqlens, p.cu_i64, N));
+    const int64_t ck_end = p.ckpt_n > 0 ? load_index(p.ckpt_cu_starts, p.ckpt_i64, N) : 0;
     // ---- chunk counts: longest and total
     {
-        long long cmax = 0;
-        unsigned long long sumc = 0;
+        int64_t cmax = 0, sumc = 0;
         for (int32_t i = tid; i < N; i += kCpThreads) {
             int64_t t0, L;
             const int64_t c = seq_chunks(p, i, t0, L);
-            if (c > cmax) cmax = c;
-            sumc += static_cast<unsigned long long>(c);
+            cmax = max64(cmax, c);
+            sumc += c;
         }
-        atomicMax(&s_cmax, cmax);
-        atomicAdd(&s_sumc, sumc);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            cmax = max64(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+            sumc += __shfl_xor_sync(0xffffffffu, sumc, o);
+        }
+        if (lane == 0) {
+            s_red[warp][0] = cmax;
+            s_red[warp][1] = sumc;
+        }
     }
     __syncthreads();
-    const int64_t c_max = s_cmax, sum_c = static_cast<int64_t>(s_sumc);
-    // ---- every candidate's sums
+    int64_t c_max = 0, sum_c = 0;
+#pragma unroll
+    for (int w = 0; w < kCpWarps; ++w) {
+        c_max = max64(c_max, s_red[w][0]);
+        sum_c += s_red[w][1];
+    }
+    // ---- every candidate's sums: slot j = t % 8 is candidate P = j + 2
     {
-        CpSums loc[kCand];
+        const int j = tid % kSlots;
+        const int64_t tau_j = j < kCand ? cp_tau(c_max, j + 2, p.align_chunks) : 0;
+        CpSums loc{0, 0, 0, 0};
+        if (j < kCand)
+            for (int32_t i = tid / kSlots; i < N; i += kCpThreads / kSlots) {
+                int64_t t0, L;
+                cp_add_sequence(loc, seq_chunks(p, i, t0, L), tau_j);
+            }
 #pragma unroll
-        for (int j = 0; j < kCand; ++j) loc[j] = CpSums{0, 0, 0, 0};
-        for (int32_t i = tid; i < N; i += kCpThreads) {
-            int64_t t0, L;
-            const int64_t c = seq_chunks(p, i, t0, L);
-#pragma unroll
-            for (int j = 0; j < kCand; ++j) cp_add_sequence(loc[j], c, cp_tau(c_max, j + 2, p.align_chunks));
+        for (int o = kSlots; o < 32; o <<= 1) {  // lanes of one slot: lane % 8 equal
+            loc.nA += __shfl_xor_sync(0xffffffffu, loc.nA, o);
+            loc.nS += __shfl_xor_sync(0xffffffffu, loc.nS, o);
+            loc.max_whole = max64(loc.max_whole, __shfl_xor_sync(0xffffffffu, loc.max_whole, o));
+            loc.max_p = max64(loc.max_p, __shfl_xor_sync(0xffffffffu, loc.max_p, o));
         }
-#pragma unroll
-        for (int j = 0; j < kCand; ++j) {
-            atomicAdd(&s_sum[j][0], static_cast<unsigned long long>(loc[j].nA));
-            atomicAdd(&s_sum[j][1], static_cast<unsigned long long>(loc[j].nS));
-            atomicMax(&s_max[j][0], static_cast<long long>(loc[j].max_whole));
-            atomicMax(&s_max[j][1], static_cast<long long>(loc[j].max_p));
+        if (lane < kSlots) {
+            s_cand[warp][lane][0] = loc.nA;
+            s_cand[warp][lane][1] = loc.nS;
+            s_cand[warp][lane][2] = loc.max_whole;
+            s_cand[warp][lane][3] = loc.max_p;
         }
+        __syncthreads();
+        if (tid < kSlots) {
+            CpSums s{0, 0, 0, 0};
+#pragma unroll
+            for (int w = 0; w < kCpWarps; ++w) {
+                s.nA += s_cand[w][tid][0];
+                s.nS += s_cand[w][tid][1];
+                s.max_whole = max64(s.max_whole, s_cand[w][tid][2]);
+                s.max_p = max64(s.max_p, s_cand[w][tid][3]);
+            }
+            s_tauc[tid] = tau_j;
+            s_cost[tid] = tid < kCand ? cp_candidate_cost(s, tau_j, sum_c, p.H, p.sms)
+                                      : cp_one_pass_cost(c_max, sum_c, p.H, p.sms);
+        }
+        __syncthreads();
+        if (tid == 0) s_tau = (p.nA_max > 0 && p.sms > 0) ? cp_choose_tau(s_cost, s_tauc, s_cost[kCand]) : 0;
+        __syncthreads();
     }
-    __syncthreads();
-    if (tid == 0) {
-        CpSums s[kCand];
-        for (int j = 0; j < kCand; ++j)
-            s[j] = CpSums{static_cast<int64_t>(s_sum[j][0]), static_cast<int64_t>(s_sum[j][1]), s_max[j][0],
-                          s_max[j][1]};
-        s_tau = (p.nA_max > 0 && p.sms > 0) ? cp_pick_tau(s, c_max, sum_c, p.H, p.sms, p.align_chunks) : 0;
-    }
-    __syncthreads();
     const int64_t tau = s_tau, tau_tok = tau * kChunk;
+    // Segment s of a cut sequence starts s tau_tok tokens in (that is inside
+    // the sequence: (P - 1) tau < c), a whole multiple of the checkpoint interval.
+    const int64_t ck_step = p.ckpt_n > 0 ? tau_tok / p.ckpt_n : 0;
     // ---- per sequence: segments, offsets (exclusive scans), lists
     int32_t carry_a = 0, carry_k = 0, carry_s = 0;
     for (int32_t base = 0; base < N; base += kCpThreads) {
         const int32_t i = base + tid;
-        int64_t t0 = 0, L = 0;
+        int64_t t0 = 0, L = 0, c0 = 0, row = 0;
         int32_t P = 1;
-        if (i < N) P = cp_seq_segments(seq_chunks(p, i, t0, L), tau);
+        if (i < N) {
+            P = cp_seq_segments(seq_chunks(p, i, t0, L), tau);
+            if (p.ckpt_n > 0) c0 = load_index(p.ckpt_cu_starts, p.ckpt_i64, i);
+            row = real_row(p, i);
+        }
         const int32_t segd = P >= 2 ? 1 : 0;
         const int32_t ta = carry_a + cp_excl_scan(P - 1, warp_sums, &tile_total);
         carry_a += tile_total;
@@ -157,7 +192,6 @@ __global__ void __launch_bounds__(kCpThreads) cp_prepare_kernel(const CpParams p
         const int32_t sb = carry_s + cp_excl_scan(segd ? P : 0, warp_sums, &tile_total);
         carry_s += tile_total;
         if (i < N) {
-            const int64_t c0 = p.ckpt_n > 0 ? load_index(p.ckpt_cu_starts, p.ckpt_i64, i) : 0;
             if (segd) {
                 p.seg_seq[4 * k] = i;
                 p.seg_seq[4 * k + 1] = P;
@@ -169,19 +203,15 @@ __global__ void __launch_bounds__(kCpThreads) cp_prepare_kernel(const CpParams p
                 }
             }
             const int32_t v = i + ta;  // first entry of this sequence in the segment pass's batch
-            const int64_t row = segd ? 0 : real_row(p, i);
             for (int32_t s = 0; s < P; ++s) {
-                const int64_t a = segd ? (s * tau_tok < L ? s * tau_tok : L) : 0;
-                p.cu_c[v + s] = static_cast<int32_t>(t0 + a);
-                p.ckpt_c[v + s] = p.ckpt_n > 0 ? c0 + a / p.ckpt_n : 0;
+                p.cu_c[v + s] = static_cast<int32_t>(t0 + s * tau_tok);
+                p.ckpt_c[v + s] = p.ckpt_n > 0 ? c0 + s * ck_step : 0;
                 p.vrow[v + s] = segd ? static_cast<int64_t>(sb + s) : -1 - row;
             }
         }
     }
     // ---- the batch's tail of empty entries, the transfer order, the counts
     const int32_t V = N + carry_a;
-    const int32_t end = static_cast<int32_t>(load_index(p.cu_seqlens, p.cu_i64, N));
-    const int64_t ck_end = p.ckpt_n > 0 ? load_index(p.ckpt_cu_starts, p.ckpt_i64, N) : 0;
     for (int32_t v = V + tid; v <= p.V_max; v += kCpThreads) {
         p.cu_c[v] = end;
         p.ckpt_c[v] = ck_end;
@@ -199,11 +229,13 @@ __global__ void __launch_bounds__(kCpThreads) cp_prepare_kernel(const CpParams p
 // Four CTAs per (segmented sequence, state head), 32 rows of S each: the
 // start states of its P segments, in fp32.  Thread t owns row v = t / 8 of
 // the CTA's rows and columns 4 (t % 8) + 32 q + j (q, j < 4), so that eight
-// neighbouring threads read 128 contiguous bytes of M and N.
+// neighbouring threads read 128 contiguous bytes of M and N.  The M planes
+// arrive by asynchronous copies into two buffers: M_{s+1} is in flight while
+// step s multiplies by M_s.
 __global__ void __launch_bounds__(kCpThreads) cp_fixup_kernel(const CpParams p) {
-    extern __shared__ float cp_smem[];
-    float* S = cp_smem;                     // [32][kLdS]
-    float* M = cp_smem + kFixRows * kLdS;   // [128][128]
+    extern __shared__ __align__(16) float cp_smem[];
+    float* S = cp_smem;                            // [32][kLdS]
+    float* Mbuf = cp_smem + kFixRows * kLdS;       // two [128][128] planes
     if (*reinterpret_cast<volatile int32_t*>(p.status)) return;
     const int32_t part = blockIdx.x % kFixSplit, uh = blockIdx.x / kFixSplit;
     const int32_t k = uh / p.H, h = uh % p.H;
@@ -212,24 +244,46 @@ __global__ void __launch_bounds__(kCpThreads) cp_fixup_kernel(const CpParams p) 
     const size_t plane = static_cast<size_t>(kHead) * kHead;
     const int r0 = part * kFixRows;
     const int t = threadIdx.x, v = t >> 3, cl = 4 * (t & 7);
+    // One commit group per step (empty past the last M), so that waiting for
+    // all but the newest group always means "M_s has landed".
+    auto copy_m = [&](int32_t s) {
+        if (s + 1 < P) {
+            const float* Mm = p.trans + (static_cast<size_t>(p.nA_max + ta + s) * p.H + h) * plane;
+            float* dst = Mbuf + (s & 1) * plane;
+#pragma unroll
+            for (int it = 0; it < kPlaneVec; ++it) {
+                const int e = 4 * (t + it * kCpThreads);
+                cp_async16(dst + e, Mm + e);
+            }
+        }
+        cp_async_commit();
+    };
+    copy_m(0);
+    copy_m(1);
     // S_start(0): the caller's initial state (or zeros), in any layout and type
     const int64_t srow = real_row(p, i);
     float* out0 = p.start + (static_cast<size_t>(sb) * p.H + h) * plane;
-    for (int e = 4 * t; e < kFixRows * kHead; e += 4 * kCpThreads) {
-        const int r = e / kHead, c = e % kHead;
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (p.initial_state) state_load4(p.initial_state, state_offset(p.state, srow, h, r0 + r) + c, p.state.dtype, x);
+    {
+        float x[kRowsVec][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) S[r * kLdS + c + j] = x[j];
-        *reinterpret_cast<float4*>(out0 + static_cast<size_t>(r0 + r) * kHead + c) = make_float4(x[0], x[1], x[2], x[3]);
+        for (int it = 0; it < kRowsVec; ++it) {
+            const int e = 4 * (t + it * kCpThreads), r = e / kHead, c = e % kHead;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[it][j] = 0.f;
+            if (p.initial_state)
+                state_load4(p.initial_state, state_offset(p.state, srow, h, r0 + r) + c, p.state.dtype, x[it]);
+        }
+#pragma unroll
+        for (int it = 0; it < kRowsVec; ++it) {
+            const int e = 4 * (t + it * kCpThreads), r = e / kHead, c = e % kHead;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) S[r * kLdS + c + j] = x[it][j];
+            *reinterpret_cast<float4*>(out0 + static_cast<size_t>(r0 + r) * kHead + c) =
+                make_float4(x[it][0], x[it][1], x[it][2], x[it][3]);
+        }
     }
-    __syncthreads();
-    for (int s = 0; s + 1 < P; ++s) {
+    for (int32_t s = 0; s + 1 < P; ++s) {
         const float* Nm = p.trans + (static_cast<size_t>(ta + s) * p.H + h) * plane;
-        const float* Mm = p.trans + (static_cast<size_t>(p.nA_max + ta + s) * p.H + h) * plane;
-        for (int e = 4 * t; e < kHead * kHead; e += 4 * kCpThreads)
-            *reinterpret_cast<float4*>(M + e) = *reinterpret_cast<const float4*>(Mm + e);
-        __syncthreads();
         float acc[16];
         const float* nrow = Nm + static_cast<size_t>(r0 + v) * kHead + cl;
 #pragma unroll
@@ -240,6 +294,9 @@ __global__ void __launch_bounds__(kCpThreads) cp_fixup_kernel(const CpParams p) 
             acc[4 * q + 2] = n4.z;
             acc[4 * q + 3] = n4.w;
         }
+        cp_async_wait<1>();  // this thread's pieces of M_s
+        __syncthreads();     // everyone's pieces, and S
+        const float* M = Mbuf + (s & 1) * plane;
 #pragma unroll 4
         for (int c = 0; c < kHead; ++c) {
             const float sv = S[v * kLdS + c];
@@ -253,7 +310,8 @@ __global__ void __launch_bounds__(kCpThreads) cp_fixup_kernel(const CpParams p) 
                 acc[4 * q + 3] = fmaf(sv, m4.w, acc[4 * q + 3]);
             }
         }
-        __syncthreads();  // every row of S and all of M have been read
+        __syncthreads();  // every row of S and all of M_s have been read
+        copy_m(s + 2);    // into the buffer M_s leaves
         float* outs = p.start + (static_cast<size_t>(sb + s + 1) * p.H + h) * plane +
                       static_cast<size_t>(r0 + v) * kHead + cl;
 #pragma unroll
@@ -263,29 +321,37 @@ __global__ void __launch_bounds__(kCpThreads) cp_fixup_kernel(const CpParams p) 
             *reinterpret_cast<float4*>(outs + 32 * q) =
                 make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
         }
-        __syncthreads();
     }
+    cp_async_wait<0>();  // nothing is left in flight when the CTA ends (the groups past the last M are empty)
 }
 
-// One CTA per (segmented sequence, state head): the last segment's final
-// state (left in place by the segment pass) to the caller's output state.
+// Four CTAs per (segmented sequence, state head), 32 rows each: the last
+// segment's final state (left in place by the segment pass) to the caller's
+// output state.  Every load is issued before the first store.
 __global__ void __launch_bounds__(kCpThreads) cp_final_kernel(const CpParams p) {
     if (*reinterpret_cast<volatile int32_t*>(p.status)) return;
-    const int32_t k = blockIdx.x / p.H, h = blockIdx.x % p.H;
+    const int32_t part = blockIdx.x % kFixSplit, uh = blockIdx.x / kFixSplit;
+    const int32_t k = uh / p.H, h = uh % p.H;
     if (k >= p.counts[2]) return;
     const int32_t i = p.seg_seq[4 * k], P = p.seg_seq[4 * k + 1], sb = p.seg_seq[4 * k + 3];
     const size_t plane = static_cast<size_t>(kHead) * kHead;
-    const float* src = p.start + (static_cast<size_t>(sb + P - 1) * p.H + h) * plane;
+    const int r0 = part * kFixRows;
+    const float* src = p.start + (static_cast<size_t>(sb + P - 1) * p.H + h) * plane + static_cast<size_t>(r0) * kHead;
     const int64_t srow = real_row(p, i);
-    for (int e = 4 * threadIdx.x; e < kHead * kHead; e += 4 * kCpThreads) {
-        const int r = e / kHead, c = e % kHead;
-        const float4 f = *reinterpret_cast<const float4*>(src + e);
-        const float x[4] = {f.x, f.y, f.z, f.w};
-        state_store4(p.output_state, state_offset(p.state, srow, h, r) + c, p.state.dtype, x);
+    float4 f[kRowsVec];
+#pragma unroll
+    for (int it = 0; it < kRowsVec; ++it)
+        f[it] = *reinterpret_cast<const float4*>(src + 4 * (threadIdx.x + it * kCpThreads));
+#pragma unroll
+    for (int it = 0; it < kRowsVec; ++it) {
+        const int e = 4 * (threadIdx.x + it * kCpThreads), r = e / kHead, c = e % kHead;
+        const float x[4] = {f[it].x, f[it].y, f[it].z, f[it].w};
+        state_store4(p.output_state, state_offset(p.state, srow, h, r0 + r) + c, p.state.dtype, x);
     }
 }
 
-constexpr size_t kFixupSmem = sizeof(float) * (kFixRows * kLdS + kHead * kHead);
+constexpr size_t kFixupSmem = sizeof(float) * (kFixRows * kLdS + 2 * kHead * kHead);
+static_assert(kFixRows * kLdS % 4 == 0, "the M planes start on a 16-byte boundary");
 
 }  // namespace
 
@@ -316,7 +382,7 @@ cudaError_t launch_cp_fixup(const CpParams& p, cudaStream_t stream) {
 
 cudaError_t launch_cp_final(const CpParams& p, cudaStream_t stream) {
     if (!p.output_state || p.nA_max <= 0) return cudaSuccess;
-    cp_final_kernel<<<p.nA_max * p.H, kCpThreads, 0, stream>>>(p);
+    cp_final_kernel<<<p.nA_max * p.H * kFixSplit, kCpThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -253,21 +253,38 @@ __host__ __device__ inline int64_t cp_one_pass_cost(int64_t c_max, int64_t sum_c
     return c_max > bal ? c_max : bal;
 }
 
+// Cost of candidate P (its tau from cp_tau) from its sums, or -1 when it cuts no
+// sequence or does not fit the scratch planes.
+__host__ __device__ inline int64_t cp_candidate_cost(const CpSums& s, int64_t tau, int64_t sum_c, int32_t H,
+                                                     int32_t sms) {
+    if (s.max_p < 2) return -1;
+    return cp_cost(s, tau, sum_c, H, sms);
+}
+
+// The chosen tau from the candidates' costs and taus (index P - 2) and the
+// cost of one pass: the cheapest feasible candidate (ties to the smaller P)
+// when it costs at most 85 % of one pass, else 0 (one pass).
+__host__ __device__ inline int64_t cp_choose_tau(const int64_t* cost, const int64_t* tau, int64_t one) {
+    int64_t best = -1, t = 0;
+    for (int32_t j = 0; j < kCpMaxSegments - 1; ++j) {
+        if (cost[j] < 0) continue;
+        if (best < 0 || cost[j] < best) {
+            best = cost[j];
+            t = tau[j];
+        }
+    }
+    return (best >= 0 && 100 * best <= 85 * one) ? t : 0;
+}
+
 // The chosen tau from the candidates' sums (0: one pass).
 __host__ __device__ inline int64_t cp_pick_tau(const CpSums (&s)[kCpMaxSegments - 1], int64_t c_max, int64_t sum_c,
                                                int32_t H, int32_t sms, int64_t align_chunks) {
-    const int64_t one = cp_one_pass_cost(c_max, sum_c, H, sms);
-    int64_t best = -1, tau = 0;
-    for (int32_t P = 2; P <= kCpMaxSegments; ++P) {
-        const int64_t t = cp_tau(c_max, P, align_chunks);
-        const int64_t c = cp_cost(s[P - 2], t, sum_c, H, sms);
-        if (c < 0 || s[P - 2].max_p < 2) continue;
-        if (best < 0 || c < best) {
-            best = c;
-            tau = t;
-        }
+    int64_t cost[kCpMaxSegments - 1], tau[kCpMaxSegments - 1];
+    for (int32_t j = 0; j < kCpMaxSegments - 1; ++j) {
+        tau[j] = cp_tau(c_max, j + 2, align_chunks);
+        cost[j] = cp_candidate_cost(s[j], tau[j], sum_c, H, sms);
     }
-    return (best >= 0 && 100 * best <= 85 * one) ? tau : 0;
+    return cp_choose_tau(cost, tau, cp_one_pass_cost(c_max, sum_c, H, sms));
 }
 
 // Context-parallel arguments: the real batch, its segments and the scratch
