@@ -133,15 +133,37 @@ def algorithmic_bytes(w, inp):
     b += T * H * 4 * 2                          # g, beta (fp32)
     b += T * H * D * esz                        # output
     N = len(inp["seq_lens"])
-    state = H * D * D * 4
+    state = H * D * D * storage_bytes(inp, "state_dtype")
     if inp.get("initial_state") is not None:
         b += N * state                          # rows read (pool: only the indexed rows)
     if inp["output_final_state"]:
         b += N * state
     n = inp.get("checkpoint_every_n_tokens") or 0
     if n:
-        b += wl.num_checkpoints(inp["seq_lens"], n) * state
+        b += wl.num_checkpoints(inp["seq_lens"], n) * H * D * D * storage_bytes(inp, "checkpoint_dtype")
     return b
+
+
+STORAGE_DTYPES = {"float32": torch.float32, "bfloat16": torch.bfloat16, "float16": torch.float16,
+                  "float8_e4m3fn": torch.float8_e4m3fn, "float8_e5m2": torch.float8_e5m2}
+
+
+def storage_bytes(inp, key):
+    """Bytes per element of the states or checkpoints as stored (fp32 unless the run chose another type)."""
+    return torch.empty(0, dtype=inp.get(key, torch.float32)).element_size()
+
+
+def with_storage_types(inp, state_dtype=None, checkpoint_dtype=None):
+    """The workload with its initial state (or pool) rounded to `state_dtype` and the final states and
+    checkpoints to be stored in the given types; the oracle then reads the same rounded state."""
+    inp = dict(inp)
+    if state_dtype is not None:
+        inp["state_dtype"] = STORAGE_DTYPES[state_dtype]
+        if inp.get("initial_state") is not None:
+            inp["initial_state"] = inp["initial_state"].to(inp["state_dtype"])
+    if checkpoint_dtype is not None:
+        inp["checkpoint_dtype"] = STORAGE_DTYPES[checkpoint_dtype]
+    return inp
 
 
 def measured_peaks():
@@ -245,10 +267,11 @@ def make_call(inp, device, use_cp=False):
     T, H = inp["T"], inp["H"]
     N = len(inp["seq_lens"])
     out = torch.empty(T, H, 128, dtype=d["q"].dtype, device=device)
-    fin = torch.empty(N, H, 128, 128, dtype=torch.float32, device=device) if inp["output_final_state"] else None
+    fin = (torch.empty(N, H, 128, 128, dtype=inp.get("state_dtype", torch.float32), device=device)
+           if inp["output_final_state"] else None)
     n = inp.get("checkpoint_every_n_tokens") or 0
-    ck = torch.empty(max(wl.num_checkpoints(inp["seq_lens"], n), 1), H, 128, 128, dtype=torch.float32,
-                     device=device) if n else None
+    ck = torch.empty(max(wl.num_checkpoints(inp["seq_lens"], n), 1), H, 128, 128,
+                     dtype=inp.get("checkpoint_dtype", torch.float32), device=device) if n else None
     kw = dict(g=d["g"], beta=d["beta"], scale=inp["scale"], cu_seqlens=d["cu_seqlens"],
               use_qk_l2norm_in_kernel=inp["use_qk_l2norm_in_kernel"], output=out,
               initial_state=d.get("initial_state"), output_final_state=inp["output_final_state"], output_state=fin,
@@ -371,7 +394,8 @@ def decode_bytes(w, inp):
     T, H, D = inp["T"], inp["H"], 128
     N = len(inp["seq_lens"])
     esz = inp["q"].element_size()
-    return (2 * N * H * D * D * 4 + T * (w.hq + w.hk + w.hv) * D * esz + T * H * 8 + T * H * D * esz
+    return (2 * N * H * D * D * storage_bytes(inp, "state_dtype") + T * (w.hq + w.hk + w.hv) * D * esz
+            + T * H * 8 + T * H * D * esz
             + (N * 4 if inp.get("state_indices") is not None else 0))
 
 
@@ -394,7 +418,8 @@ def run_decode_bench(args, w, inp, device):
                         gdn.FLAGS["HAS_G"] | gdn.FLAGS["HAS_BETA"] | gdn.FLAGS["HAS_SCALE"] |
                         (gdn.FLAGS["QK_L2NORM"] if inp["use_qk_l2norm_in_kernel"] else 0) |
                         gdn.FLAGS["HAS_INITIAL_STATE"] | gdn.FLAGS["OUTPUT_FINAL_STATE"] |
-                        gdn.FLAGS["HAS_STATE_INDICES"], 0, T, N, pool.shape[0])
+                        gdn.FLAGS["HAS_STATE_INDICES"], 0, T, N, pool.shape[0],
+                        state_dtype=gdn._STATE_DTYPES[pool.dtype])
     cargs = gdn.Args(q=d["q"].data_ptr(), k=d["k"].data_ptr(), v=d["v"].data_ptr(), g=d["g"].data_ptr(),
                      beta=d["beta"].data_ptr(), scale=float(inp["scale"]), num_seqs=N, total_tokens=T,
                      initial_state=pool.data_ptr(), output_state=pool.data_ptr(), n_pool=pool.shape[0],
@@ -435,9 +460,12 @@ def run_decode_bench(args, w, inp, device):
             "config": {"workload": w.name, "op": "decode", "num_seqs": N, "tokens_per_seq": m,
                        "num_q_heads": w.hq, "num_k_heads": w.hk, "num_v_heads": w.hv, "state_heads": H,
                        "pool_rows": pool.shape[0], "qk_l2norm_in_kernel": w.l2norm_in_kernel,
+                       **storage_config(inp),
                        "l2": f"inputs larger than L2 ({abytes / 2**20:.0f} MiB moved per step), no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": recorded_traffic(w.name, DECODE_SOURCES)[0], "kernel": "gdn_decode_kernel",
+                         "traffic": (None if "state_dtype" in inp
+                                     else recorded_traffic(w.name, DECODE_SOURCES)[0]),
+                         "kernel": "gdn_decode_kernel",
                          "kernel_ms": ms,
                          "algorithmic_bytes": abytes, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"},
             "gpu_launches": K}
@@ -448,13 +476,18 @@ def run_decode_bench(args, w, inp, device):
     print(json.dumps(line), flush=True)
 
 
+def storage_config(inp):
+    """Config keys for storage types other than the default fp32 (absent otherwise)."""
+    return {k: str(inp[k]).replace("torch.", "") for k in ("state_dtype", "checkpoint_dtype") if k in inp}
+
+
 def workload_config(w, inp, args):
     return {"workload": w.name, "total_tokens": inp["T"], "num_seqs": len(inp["seq_lens"]),
             "seq_lens": inp["seq_lens"] if len(inp["seq_lens"]) <= 16 else f"{len(inp['seq_lens'])} sequences",
             "num_q_heads": w.hq, "num_k_heads": w.hk, "num_v_heads": w.hv, "state_heads": inp["H"],
             "head_size": 128, "chunk": 64, "checkpoint_every_n_tokens": w.checkpoint_every,
             "qk_l2norm_in_kernel": w.l2norm_in_kernel, "seed": args.seed,
-            "l2": "flushed between steps (256 MiB write outside the timed events)"}
+            "l2": "flushed between steps (256 MiB write outside the timed events)", **storage_config(inp)}
 
 
 def main():
@@ -472,12 +505,16 @@ def main():
     ap.add_argument("--shard", choices=["replica", "heads"], default="replica",
                     help="multi-GPU: every rank runs its own copy of the batch (weak scaling), or the ranks split "
                          "one batch's state heads (strong scaling); no data-path collective either way")
+    ap.add_argument("--state-dtype", choices=sorted(STORAGE_DTYPES), default=None,
+                    help="store the initial / final states (or the pool) in this type (default fp32)")
+    ap.add_argument("--checkpoint-dtype", choices=sorted(STORAGE_DTYPES), default=None,
+                    help="store the checkpoints in this type (default fp32)")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.op == "decode" and args.workload == wl.BENCH_WORKLOAD:
         args.workload = "decode_gva_512seq_bf16"
     w = wl.WORKLOADS[args.workload]
-    inp = wl.generate(w, seed=args.seed)
+    inp = with_storage_types(wl.generate(w, seed=args.seed), args.state_dtype, args.checkpoint_dtype)
     full_batches = world if args.shard == "replica" else 1  # copies of the whole batch the job runs per step
     tokens_batch = inp["T"]
     if args.shard == "heads" and world > 1 and args.impl == "ours":
@@ -645,7 +682,7 @@ def main():
     hbm, bf16, src = measured_peaks()
     abytes = algorithmic_bytes(w, inp)
     achieved = abytes / (chunk_avg_ms / 1e3) / 1e9
-    traffic, tnote = recorded_traffic(w.name)
+    traffic, tnote = recorded_traffic(w.name) if not storage_config(inp) else (None, None)
     tflops_dense = T * H * FLOP_DENSE / (ms_per_step / 1e3) / 1e12
     tflops_tri = T * H * FLOP_TRI / (ms_per_step / 1e3) / 1e12
     roof_time = max(abytes / (hbm * 1e9), T * H * FLOP_DENSE / (bf16 * 1e12))
