@@ -196,7 +196,7 @@ __device__ __forceinline__ bool dec_wait(uint64_t* bar, uint32_t parity, const v
 // released it) by bulk copies -- the whole (row, head) plane when its v rows are contiguous, else row by
 // row; a bare arrival without an initial state or for a pool row out of range -- then the token part: q, k,
 // v rows by bulk copies (lane 0) and g, beta by plain loads (all lanes), every lane arriving once.
-template <typename T, typename SD>
+template <typename T, typename SD, bool kAhead>
 __device__ void decode_producer(const DecodeParams& p, DecodeShared& sh, uint8_t* dsm, UnitPos x, int32_t units,
                                 int32_t grid, int32_t gseq, int32_t gh) {
     const int lane = threadIdx.x & 31, m = p.m, stages = p.stages;
@@ -205,12 +205,40 @@ __device__ void decode_producer(const DecodeParams& p, DecodeShared& sh, uint8_t
     uint32_t use = 0;  // how many times stage s has been filled before
     int32_t issued = 0;
     bool ok_run = true;
+    // The pool row (lane 0) and the first 32 gate values (one per lane) of a unit are read one unit ahead, so
+    // that their global-memory latency overlaps the previous unit's waits and copies instead of sitting between
+    // a stage turning free and its state copy.  Not for one token on fp32 states: that step runs at the HBM
+    // roofline, and there the earlier copies measured slower (0.322 -> 0.346 ms on 512 sequences x 32 heads):
+    // that case runs the instance without the lookahead (kAhead false).
+    constexpr bool ahead = kAhead;
+    auto row_of = [&](const UnitPos& y) -> int64_t {
+        return p.state_indices ? load_index(p.state_indices, p.idx_i64, y.seq) : y.seq;
+    };
+    auto gate_of = [&](const UnitPos& y, int i) -> float {  // i < m: g of token i, else beta of token i - m
+        const float* src = i < m ? p.g : p.beta;
+        const int t = i < m ? i : i - m;
+        return src ? src[(static_cast<int64_t>(y.seq) * m + t) * p.H + y.h] : 1.f;
+    };
+    int64_t row_next = 0;
+    float gate_next = 1.f;
+    if (ahead && x.u < units) {
+        if (lane == 0) row_next = row_of(x);
+        if (lane < 2 * m) gate_next = gate_of(x, lane);
+    }
     for (; x.u < units; ++issued) {
+        const int64_t row_pre = row_next;
+        const float gate_pre = gate_next;
+        UnitPos nx = x;
+        nx.advance(grid, gseq, gh, p.H);
+        if (ahead && nx.u < units) {
+            if (lane == 0) row_next = row_of(nx);
+            if (lane < 2 * m) gate_next = gate_of(nx, lane);
+        }
         uint8_t* st = dsm + static_cast<size_t>(s) * p.stage_bytes;
         if (use > 0) ok_run = dec_wait(&sh.empty_s[s], (use - 1) & 1, &sh.abort);
         if (!__all_sync(0xffffffffu, ok_run)) break;
         if (lane == 0) {
-            const int64_t srow = p.state_indices ? load_index(p.state_indices, p.idx_i64, x.seq) : x.seq;
+            const int64_t srow = ahead ? row_pre : row_of(x);
             const bool ok = !p.state_indices || (srow >= 0 && srow < p.n_pool);
             sh.row[s] = srow;
             sh.ok[s] = ok ? 1 : 0;
@@ -235,11 +263,7 @@ __device__ void decode_producer(const DecodeParams& p, DecodeShared& sh, uint8_t
         if (!__all_sync(0xffffffffu, ok_run)) break;
         uint8_t* tk = st + kHead * kRowBytes;
         float* gb = reinterpret_cast<float*>(tk + 3 * m * kVecBytes);  // g [m], then beta [m]
-        for (int i = lane; i < 2 * m; i += 32) {
-            const int t = i < m ? i : i - m;
-            const float* src = i < m ? p.g : p.beta;
-            gb[i] = src ? src[(static_cast<int64_t>(x.seq) * m + t) * p.H + x.h] : 1.f;
-        }
+        for (int i = lane; i < 2 * m; i += 32) gb[i] = ahead && i < 32 ? gate_pre : gate_of(x, i);
         if (lane == 0) {
             mbar_arrive_expect_tx(&sh.full_t[s], 3 * m * kVecBytes);
             for (int which = 0; which < 3; ++which) {
@@ -300,7 +324,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) gdn_decode_kernel(const Decode
     }
     __syncthreads();
     if (warp == kDecConsumers / 32) {
-        decode_producer<T, SD>(p, sh, dsm, first, units, grid, gseq, gh);
+        if (sizeof(SD) < 4 || m > 1)
+            decode_producer<T, SD, true>(p, sh, dsm, first, units, grid, gseq, gh);
+        else
+            decode_producer<T, SD, false>(p, sh, dsm, first, units, grid, gseq, gh);
         return;
     }
 
